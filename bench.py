@@ -1,0 +1,435 @@
+"""Benchmark of the CSA2 decode step: 1M-token context, 20-layer stack.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+               [--workload 1m|128k|group3|prefill|tiny] [--no-graph]
+
+Workload (default "1m"): batch 8, N = 262144 compressed entries per
+sequence (1M tokens at 4 tokens per entry), layer schedule (Full, Reindex,
+Reuse, Reuse) x 5, indexer 64 heads x 128 (E4M3 keys, bf16 queries), top-512,
+64 heads x 512 FP4-E2M1 main KV, 128-row bf16 window; seeded synthetic data.
+A step is one decode step through all 20 layers (csa2_layer_stack), replayed
+from a CUDA graph.  One JSON line is printed by rank 0.
+
+N > 1 (torchrun): every rank runs its own replica of the workload (decode
+sequences are independent; no data-path collective), so per-GPU work is
+fixed ("weak" scaling); value = tokens of all ranks / max-over-ranks time.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode µs/layer & tokens/s at 1M ctx; HBM GB/s vs ~8 TB/s peak"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world, device="cpu"):
+    """Max of a float over all ranks (the slowest rank sets the job time)."""
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world, device="cpu"):
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- peaks, clocks
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), "measured"
+    return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        sm = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def launches_per_step(modes, q_per_seq):
+    """Kernels of this library per step: Full = new-row quantiser + indexer-Q
+    quantiser + score + 3 top-k + 2 attention; Reindex = the same without the
+    new rows; Reuse = 2 attention kernels.  (A prefill chunk with several new
+    rows per sequence still quantises them in one launch when B = 1.)"""
+    n = 0
+    for m in modes:
+        n += {0: 8, 1: 7, 2: 2}[m]
+    return n
+
+
+def time_index_kernel(csa2, W, flush, reps=20):
+    """Average device time of one launch of the FP8 indexer kernel on the
+    workload's first Full layer (already-quantised queries, so the launch
+    holds only that kernel), with L2 flushed before each launch."""
+    L0 = W.layers[0]
+    q8, c = csa2.quantize_index_q(L0["idx_q"], L0["idx_w"])
+    scores = torch.empty(W.wl.nq, W.wl.N, dtype=torch.float32, device=q8.device)
+    for _ in range(3):
+        csa2.index_score(q8, c, L0["idxk"], W.wl.q_per_seq, W.n_valid, scores)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        csa2.index_score(q8, c, L0["idxk"], W.wl.q_per_seq, W.n_valid, scores)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / reps * 1e-3  # seconds
+
+
+def run_ours(args, world, rank, local):
+    from long_context_sparse_27_b300 import csa2, synth
+    from long_context_sparse_27_b300.workload import StackWorkload
+
+    torch.cuda.set_device(local)
+    wl = synth.WORKLOADS[args.workload]
+    W = StackWorkload(wl, seed=100 + rank, gen_device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # warm-up (also sets kernel attributes before any capture)
+    for _ in range(max(args.warmup, 3)):
+        W.run()
+    torch.cuda.synchronize()
+    assert int(W.dev_status.item()) == 0, "device status set during warm-up"
+
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            W.run()
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    def step():
+        if graph is not None:
+            graph.replay()
+        else:
+            W.run()
+
+    # ---- device-timed steps (L2 flushed before each, outside the events)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    dev_s = sum(a.elapsed_time(b) for a, b in ev) * 1e-3
+    assert int(W.dev_status.item()) == 0, "device status set during the timed steps"
+    t_max = max_over_ranks(dev_s, world, "cuda")
+
+    # ---- end to end: pinned host inputs -> device, step, outputs -> host
+    h2d_pairs, d2h_pairs = [], []
+    for L in W.layers:
+        for key in ("new_kv", "new_idxk", "idx_q", "idx_w", "attn_q"):
+            if key in L:
+                h = torch.empty(L[key].shape, dtype=L[key].dtype, pin_memory=True)
+                h.copy_(L[key])
+                h2d_pairs.append((h, L[key]))
+        h = torch.empty(L["out"].shape, dtype=L["out"].dtype, pin_memory=True)
+        d2h_pairs.append((L["out"], h))
+    h2d_bytes = sum(h.numel() * h.element_size() for h, _ in h2d_pairs)
+    d2h_bytes = sum(d.numel() * d.element_size() for d, _ in d2h_pairs)
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for a, b in e_ev:
+        flush.zero_()
+        a.record(stream)
+        for h, d in h2d_pairs:
+            d.copy_(h, non_blocking=True)
+        step()
+        for d, h in d2h_pairs:
+            h.copy_(d, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_ev) * 1e-3, world, "cuda")
+
+    # ---- dominant kernel, timed live (roofline)
+    k_s = time_index_kernel(csa2, W, flush)
+    peak, peak_kind = measured_peaks()
+    k_bytes = W.indexer_bytes_per_layer() + wl.nq * wl.Hi * (wl.Di + 4)
+
+    tokens = wl.nq * args.steps * world
+    value = tokens / t_max
+    ms_per_step = t_max / args.steps * 1e3
+    n_layers = len(wl.modes)
+    alg = W.algorithmic_bytes()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "us_per_layer": round(ms_per_step * 1e3 / n_layers, 3),
+        "hbm_gbs_algorithmic": round(alg / (t_max / args.steps) / 1e9, 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic (seeded N(0,1); planted indexer keys)",
+        "config": {
+            "workload": f"{wl.name}: B={wl.B}, N={wl.N}, layers={n_layers} "
+                        f"{''.join('FIU'[m] for m in wl.modes)}, indexer {wl.Hi}x{wl.Di} E4M3, "
+                        f"top-{wl.k}, {wl.Hq} heads x {wl.D} FP4 KV, window {wl.W} bf16",
+            "l2": "inputs larger than L2 (%.2f GB per step) and L2 flushed before every step"
+                  % (alg / 1e9),
+            "graph": graph is not None,
+            "parallelism": f"replicas x{world}",
+        },
+        "algorithmic_bytes_per_step": alg,
+        "roofline": {
+            "kernel": "idx_score_tc_kernel",
+            "bound": "hbm",
+            "achieved": round(k_bytes / k_s / 1e9, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(k_bytes / k_s / 1e9 / peak, 4),
+            "traffic": None,
+            "avg_launch_us": round(k_s * 1e6, 3),
+            "bytes_per_launch": k_bytes,
+        },
+        "e2e": {
+            "value": round(wl.nq * args.steps * world / e2e_s, 1),
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d_bytes,
+            "d2h_bytes_per_step": d2h_bytes,
+        },
+        "gpu_launches": launches_per_step(wl.modes, wl.q_per_seq) * args.steps,
+        "clocks": clk.summary(),
+    }
+    traffic = os.path.join(ROOT, "profiles", "idx_score_tc_traffic.json")
+    if os.path.exists(traffic):
+        with open(traffic) as f:
+            t = json.load(f)
+        if t.get("workload") == wl.name:
+            line["roofline"]["traffic"] = t.get("bytes_per_launch")
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
+    return line
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def cpu_baseline(wl, budget_s):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload:
+    whole sequences through the first group of layers (Full, Reindex,
+    Reuse, Reuse), one sequence at a time until `budget_s` is spent.  Inputs
+    are prepared outside the timed region (the oracle's own E4M3 / FP4
+    casts of the seeded bf16 rows); timed: scores, top-k and attention."""
+    import numpy as np
+    from oracle import oracle as orc
+    from long_context_sparse_27_b300 import synth
+    orc.lib()
+    cores = len(os.sched_getaffinity(0))
+    group = list(wl.modes[:4]) if len(wl.modes) >= 4 else list(wl.modes)
+    scale = 1.0 / math.sqrt(wl.D)
+    one = synth.scaled(wl, B=1)
+    elapsed = 0.0
+    seqs = 0
+    table = orc.e4m3_table()
+    while elapsed < budget_s and seqs < wl.B:
+        s = 9000 + seqs
+        kk = synth.index_k_rows(one, s + 1)
+        k8 = orc.cast_e4m3(kk.double().numpy())
+        kd = table[k8]
+        kv = synth.kv_rows(one, s + 2)
+        layers = []
+        for l, m in enumerate(group):
+            layers.append({"q": synth.index_q(one, s + 10 + l).double().numpy(),
+                           "w": synth.index_w(one, s + 20 + l).double().numpy(),
+                           "aq": synth.attn_q(one, s + 30 + l).double().numpy(),
+                           "win": synth.window_rows(one, s + 40 + l).double().numpy()})
+        q8c = [orc.quantize_index_q(L["q"], L["w"]) for L in layers]
+        t0 = time.perf_counter()
+        idx = None
+        for l, m in enumerate(group):
+            L = layers[l]
+            if m in (0, 1):
+                q8, c = q8c[l]
+                sc = orc.index_score(table[q8], c, kd[None])
+                idx = orc.topk(sc, wl.k)
+            sel = idx[0][idx[0] >= 0]
+            c_rows, s_rows = orc.quantize_fp4(
+                kv[0][torch.from_numpy(sel.astype(np.int64))].double().numpy())
+            codes = np.zeros((1, wl.N, wl.D // 2), np.uint8)
+            scl = np.zeros((1, wl.N, wl.D // 32), np.uint8)
+            codes[0, sel], scl[0, sel] = c_rows, s_rows
+            orc.sparse_attn(L["aq"], codes, scl, idx, L["win"], scale)
+        elapsed += time.perf_counter() - t0
+        seqs += 1
+    token_steps = seqs * len(group) / len(wl.modes)
+    return {"value": round(token_steps / elapsed, 4), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{seqs} of {wl.B} sequences through layers 0-{len(group) - 1} "
+                      f"({''.join('FIU'[m] for m in group)}) of {len(wl.modes)}, N={wl.N}; "
+                      f"{elapsed:.1f} s of oracle time",
+            "seconds": round(elapsed, 2)}
+
+
+def run_reference(args, world, rank):
+    from long_context_sparse_27_b300 import synth
+    if rank != 0:
+        return None
+    wl = synth.WORKLOADS[args.workload]
+    budget = max(2.0, args.cpu_budget_s / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        cpu_baseline(wl, budget)
+    vals = [cpu_baseline(wl, budget) for _ in range(args.steps)]
+    v = statistics.median(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = v
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": v,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1); planted indexer keys)",
+        "config": {"workload": f"{wl.name}: B={wl.B}, N={wl.N}, layers={len(wl.modes)}",
+                   "sample": cb["sample"]},
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="1m")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    init_dist(world, "nccl")
+    line = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,496 @@
+// api.cu -- the C ABI of libcsa2 (declared in include/csa2.h): argument
+// checks, workspace sizing, status codes, host-side fault injection and the
+// static Full / Reindex / Reuse layer schedule.
+//
+// The three layer modes are those of "Unlocking Extreme Context Scaling with
+// DeepSeek-V4.1-Flash", section "Compressed Sparse Attention 2 (CSA2)": Full
+// computes main KV and indexer K afresh and selects new top-k entries;
+// Reindex uses the main KV and indexer K of the last Full layer with a new
+// indexer Q; Reuse takes both the main KV and the top-k indices of an
+// earlier layer.  The modes are fixed per layer ("static layer modes",
+// aiany.app DeepSeek-V4.1-Flash page, "What Sets It Apart").
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+
+namespace csa2 {
+
+static thread_local int32_t g_last_cuda_error = 0;
+
+csa2_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int32_t)e;
+  return CSA2_ERR_CUDA;
+}
+
+csa2_status check_launch() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e);
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// CSA2_FAULT_INJECT="<call>:<status>" makes the named entry point return
+// <status> before it enqueues anything (host-side failure injection for
+// tests of the callers' error paths).  <call> is the entry point's name
+// without the "csa2_" prefix, e.g. "topk:4".
+csa2_status injected(const char* call) {
+  const char* env = std::getenv("CSA2_FAULT_INJECT");
+  if (!env || !*env) return CSA2_OK;
+  const char* colon = std::strchr(env, ':');
+  if (!colon) return CSA2_OK;
+  const size_t len = (size_t)(colon - env);
+  if (std::strlen(call) != len || std::strncmp(env, call, len) != 0) return CSA2_OK;
+  const int v = std::atoi(colon + 1);
+  return (v > 0 && v <= CSA2_ERR_DEVICE_BOUNDS) ? (csa2_status)v : CSA2_OK;
+}
+
+csa2_status check_quant(const csa2_quant_args* a) {
+  if (!a || a->rows < 0 || a->d <= 0 || a->d % 32 != 0) return CSA2_ERR_INVALID_ARG;
+  if (a->rows == 0) return CSA2_OK;
+  if (!a->x || !a->codes || !a->scales) return CSA2_ERR_INVALID_ARG;
+  if (a->x_ld < a->d || a->codes_ld < a->d / 2 || a->scales_ld < a->d / 32)
+    return CSA2_ERR_INVALID_ARG;
+  if (!aligned(a->x, 16) || a->x_ld % 8 != 0 || !aligned(a->codes, 4) || a->codes_ld % 4 != 0)
+    return CSA2_ERR_ALIGNMENT;
+  if ((a->idxk == nullptr) != (a->idxk_e4m3 == nullptr)) return CSA2_ERR_INVALID_ARG;
+  if (a->idxk) {
+    if (a->di <= 0 || a->di % 8 != 0 || a->idxk_ld < a->di || a->idxk_e4m3_ld < a->di)
+      return CSA2_ERR_INVALID_ARG;
+    if (!aligned(a->idxk, 16) || a->idxk_ld % 8 != 0 || !aligned(a->idxk_e4m3, 8) ||
+        a->idxk_e4m3_ld % 8 != 0)
+      return CSA2_ERR_ALIGNMENT;
+  }
+  return CSA2_OK;
+}
+
+csa2_status check_index_q(const void* q, const float* w, int64_t nq, int32_t hi, int32_t di,
+                          const uint8_t* q8, const float* c) {
+  if (nq < 0 || hi < 1) return CSA2_ERR_INVALID_ARG;
+  if (di != 32 && di != 64 && di != 128 && di != 256) return CSA2_ERR_INVALID_ARG;
+  if (nq == 0) return CSA2_OK;
+  if (!q || !w || !q8 || !c) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(q8, 16)) return CSA2_ERR_ALIGNMENT;
+  return CSA2_OK;
+}
+
+bool fp8_path(const csa2_index_args* a) {
+  return (a->q_dtype == CSA2_BF16 || a->q_dtype == CSA2_E4M3) && a->k_dtype == CSA2_E4M3;
+}
+
+size_t index_ws(const csa2_index_args* a) {
+  if (!fp8_path(a) || a->q_dtype == CSA2_E4M3) return 0;
+  const int64_t nq = a->B * a->q_per_seq;
+  return align256((size_t)nq * a->hi * a->di) + align256((size_t)nq * a->hi * sizeof(float));
+}
+
+csa2_status check_index(const csa2_index_args* a) {
+  if (!a || a->B < 0 || a->q_per_seq < 1 || a->n < 0 || a->hi < 1 || a->di < 1)
+    return CSA2_ERR_INVALID_ARG;
+  const int64_t nq = a->B * a->q_per_seq;
+  if (nq == 0 || a->n == 0) return CSA2_OK;
+  if (!a->q || !a->w || !a->k || !a->scores) return CSA2_ERR_INVALID_ARG;
+  if (a->k_ld < a->di || a->k_seq_stride < 0 || a->scores_ld < a->n) return CSA2_ERR_INVALID_ARG;
+  if (a->B > 1 && a->k_seq_stride < a->k_ld * a->n) return CSA2_ERR_INVALID_ARG;
+  if (fp8_path(a)) {
+    if (a->hi != 64 || a->di != 128) return CSA2_ERR_UNSUPPORTED;
+    if (!aligned(a->k, 16) || a->k_ld % 16 != 0 || a->k_seq_stride % 16 != 0)
+      return CSA2_ERR_ALIGNMENT;
+    if (!aligned(a->q, 16)) return CSA2_ERR_ALIGNMENT;
+    if (a->n > (int64_t)1 << 31 || nq * a->hi > (int64_t)1 << 31) return CSA2_ERR_UNSUPPORTED;
+    if (a->q_dtype == CSA2_E4M3) return CSA2_OK;
+    if (!a->workspace || a->workspace_bytes < index_ws(a)) return CSA2_ERR_WORKSPACE;
+    if (!aligned(a->workspace, 256)) return CSA2_ERR_ALIGNMENT;
+    return CSA2_OK;
+  }
+  if (a->q_dtype == CSA2_F32 && a->k_dtype == CSA2_F32) {
+    if (a->hi > 64 || a->di > 256) return CSA2_ERR_UNSUPPORTED;
+    return CSA2_OK;
+  }
+  return CSA2_ERR_UNSUPPORTED;
+}
+
+csa2_status run_index(const csa2_index_args& a, cudaStream_t s) {
+  if (a.B * a.q_per_seq == 0 || a.n == 0) return CSA2_OK;
+  if (!fp8_path(&a)) return launch_index_score_f32(a, s);
+  if (a.q_dtype == CSA2_E4M3)
+    return launch_index_score_fp8(a, static_cast<const uint8_t*>(a.q), a.w, s);
+  const int64_t nq = a.B * a.q_per_seq;
+  uint8_t* q8 = static_cast<uint8_t*>(a.workspace);
+  float* c = reinterpret_cast<float*>(q8 + align256((size_t)nq * a.hi * a.di));
+  csa2_status st = launch_quantize_index_q(a.q, a.w, nq, a.hi, a.di, q8, c, s);
+  if (st != CSA2_OK) return st;
+  return launch_index_score_fp8(a, q8, c, s);
+}
+
+csa2_status check_topk(const float* scores, int64_t rows, int64_t n, int64_t ld, int32_t k,
+                       int32_t* idx_out, int64_t idx_ld, void* ws, size_t ws_bytes) {
+  if (rows < 0 || n < 0 || k < 1 || idx_ld < k || ld < n) return CSA2_ERR_INVALID_ARG;
+  if (k > 2048) return CSA2_ERR_UNSUPPORTED;
+  if (n >= ((int64_t)1 << 31)) return CSA2_ERR_UNSUPPORTED;
+  if (rows == 0) return CSA2_OK;
+  if (!idx_out || (n > 0 && !scores)) return CSA2_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < topk_workspace_bytes(rows, n, k)) return CSA2_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return CSA2_ERR_ALIGNMENT;
+  return CSA2_OK;
+}
+
+csa2_status check_attn(const csa2_attn_args* a) {
+  if (!a || a->nq < 0 || a->q_per_seq < 1 || a->hq < 1 || a->d < 32 || a->d % 32 != 0 ||
+      a->n < 0 || a->k < 0 || a->w_rows < 0 || a->win_max < 0)
+    return CSA2_ERR_INVALID_ARG;
+  if (a->nq == 0) return CSA2_OK;
+  if (!a->q || !a->out) return CSA2_ERR_INVALID_ARG;
+  if (a->k > 0 && (!a->idx || !a->codes || !a->scales || a->idx_ld < a->k))
+    return CSA2_ERR_INVALID_ARG;
+  if (a->w_rows > 0 && !a->window) return CSA2_ERR_INVALID_ARG;
+  if (a->codes_ld < a->d / 2 || a->scales_ld < a->d / 32) return CSA2_ERR_INVALID_ARG;
+  if (a->window && a->win_ld < a->d) return CSA2_ERR_INVALID_ARG;
+  if (a->q_dtype == CSA2_F32) {
+    if (a->hq > 65535 || a->d > 256) return CSA2_ERR_UNSUPPORTED;
+    const int64_t wm = a->win_max > 0 ? a->win_max : a->w_rows;
+    if (sizeof(float) * ((size_t)a->d + a->k + wm) > 48 * 1024) return CSA2_ERR_UNSUPPORTED;
+    return CSA2_OK;
+  }
+  if (a->q_dtype != CSA2_BF16) return CSA2_ERR_UNSUPPORTED;
+  if (a->d != 512 || a->hq % 16 != 0) return CSA2_ERR_UNSUPPORTED;
+  if (a->nq > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (!aligned(a->q, 16)) return CSA2_ERR_ALIGNMENT;
+  if (a->k > 0 && (!aligned(a->codes, 16) || a->codes_ld % 16 != 0 ||
+                   a->codes_seq_stride % 16 != 0))
+    return CSA2_ERR_ALIGNMENT;
+  if (a->window && (!aligned(a->window, 16) || a->win_ld % 8 != 0 || a->win_seq_stride % 8 != 0))
+    return CSA2_ERR_ALIGNMENT;
+  const size_t need = attn_workspace_bytes(*a);
+  if (need > 0 && (!a->workspace || a->workspace_bytes < need)) return CSA2_ERR_WORKSPACE;
+  if (need > 0 && !aligned(a->workspace, 16)) return CSA2_ERR_ALIGNMENT;
+  return CSA2_OK;
+}
+
+// ---- layer stack ----
+
+struct StackPieces {
+  size_t scores, ix, tk, at;
+};
+
+csa2_index_args stack_index_args(const csa2_stack_args& s, const csa2_layer_desc& L,
+                                 const csa2_layer_desc& src, float* scores, void* ws,
+                                 size_t ws_bytes) {
+  csa2_index_args a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = L.idx_q;
+  a.q_dtype = s.idx_q_dtype;
+  a.w = L.idx_w;
+  a.k = src.idxk;
+  a.k_dtype = s.idx_k_dtype;
+  a.B = s.B;
+  a.q_per_seq = s.q_per_seq;
+  a.hi = s.hi;
+  a.di = s.di;
+  a.n = s.n;
+  a.k_ld = s.di;
+  a.k_seq_stride = s.n * s.di;
+  a.n_valid = s.n_valid;
+  a.scores = scores;
+  a.scores_ld = s.n;
+  a.workspace = ws;
+  a.workspace_bytes = ws_bytes;
+  a.dev_status = s.dev_status;
+  return a;
+}
+
+csa2_attn_args stack_attn_args(const csa2_stack_args& s, const csa2_layer_desc& L,
+                               const csa2_layer_desc& kv, const int32_t* idx, void* ws,
+                               size_t ws_bytes) {
+  csa2_attn_args a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = L.attn_q;
+  a.q_dtype = s.attn_q_dtype;
+  a.nq = s.B * s.q_per_seq;
+  a.q_per_seq = s.q_per_seq;
+  a.hq = s.hq;
+  a.d = s.d;
+  a.codes = kv.codes;
+  a.scales = kv.scales;
+  a.n = s.n;
+  a.codes_ld = s.d / 2;
+  a.codes_seq_stride = s.n * (s.d / 2);
+  a.scales_ld = s.d / 32;
+  a.scales_seq_stride = s.n * (s.d / 32);
+  a.idx = idx;
+  a.k = s.k;
+  a.idx_ld = s.k;
+  a.window = L.window;
+  a.w_rows = s.w_rows;
+  a.win_ld = s.d;
+  a.win_seq_stride = (int64_t)s.w_rows * s.d;
+  a.win_start = s.win_start;
+  a.win_len = s.win_len;
+  a.win_max = 0;
+  a.softmax_scale = s.softmax_scale;
+  a.out = L.out;
+  a.workspace = ws;
+  a.workspace_bytes = ws_bytes;
+  a.dev_status = s.dev_status;
+  return a;
+}
+
+// Quantise a Full layer's new rows into its caches: new_kv [B, nr, d] goes
+// to rows new_row .. new_row + nr - 1 of every sequence.  With one new row
+// per sequence a single launch covers all sequences (the sequence stride is
+// the row stride); otherwise one launch per sequence.
+csa2_status quantize_new_rows(const csa2_stack_args& s, const csa2_layer_desc& d,
+                              cudaStream_t cs) {
+  const int64_t nr = d.new_rows > 0 ? d.new_rows : 1;
+  const bool e4m3 = s.idx_k_dtype == CSA2_E4M3;
+  const int64_t per_call = nr == 1 ? 1 : s.B;  // number of calls
+  for (int64_t b = 0; b < per_call; ++b) {
+    csa2_quant_args q;
+    std::memset(&q, 0, sizeof(q));
+    const int64_t row0 = b * s.n + d.new_row;  // in rows of the [B, n] cache
+    q.x = static_cast<const uint16_t*>(d.new_kv) + b * nr * s.d;
+    q.rows = nr == 1 ? s.B : nr;
+    q.d = s.d;
+    q.x_ld = s.d;
+    q.codes = d.codes + row0 * (s.d / 2);
+    q.codes_ld = nr == 1 ? s.n * (s.d / 2) : s.d / 2;
+    q.scales = d.scales + row0 * (s.d / 32);
+    q.scales_ld = nr == 1 ? s.n * (s.d / 32) : s.d / 32;
+    if (e4m3) {
+      q.idxk = static_cast<const uint16_t*>(d.new_idxk) + b * nr * s.di;
+      q.di = s.di;
+      q.idxk_ld = s.di;
+      q.idxk_e4m3 = static_cast<uint8_t*>(d.idxk) + row0 * s.di;
+      q.idxk_e4m3_ld = nr == 1 ? s.n * s.di : s.di;
+    }
+    csa2_status st = check_quant(&q);
+    if (st != CSA2_OK) return st;
+    if ((st = launch_quantize_fp4(q, cs)) != CSA2_OK) return st;
+    if (!e4m3) {
+      // fp32 indexer keys are stored as given
+      const size_t row_bytes = (size_t)s.di * sizeof(float);
+      cudaError_t e = cudaMemcpy2DAsync(
+          static_cast<float*>(d.idxk) + row0 * s.di, nr == 1 ? (size_t)s.n * row_bytes : row_bytes,
+          static_cast<const float*>(d.new_idxk) + b * nr * s.di, row_bytes, row_bytes,
+          (size_t)q.rows, cudaMemcpyDeviceToDevice, cs);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+  }
+  return CSA2_OK;
+}
+
+StackPieces stack_pieces(const csa2_stack_args& s) {
+  StackPieces p;
+  const int64_t nq = s.B * s.q_per_seq;
+  p.scores = align256((size_t)nq * s.n * sizeof(float));
+  csa2_layer_desc dummy;
+  std::memset(&dummy, 0, sizeof(dummy));
+  csa2_index_args ia = stack_index_args(s, dummy, dummy, nullptr, nullptr, 0);
+  p.ix = align256(index_ws(&ia));
+  p.tk = align256(topk_workspace_bytes(nq, s.n, s.k));
+  csa2_attn_args aa = stack_attn_args(s, dummy, dummy, nullptr, nullptr, 0);
+  p.at = align256(attn_workspace_bytes(aa));
+  return p;
+}
+
+}  // namespace
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+const char* csa2_version(void) { return "0.1.0"; }
+
+const char* csa2_status_string(int32_t st) {
+  switch (st) {
+    case CSA2_OK: return "CSA2_OK";
+    case CSA2_ERR_INVALID_ARG: return "CSA2_ERR_INVALID_ARG";
+    case CSA2_ERR_UNSUPPORTED: return "CSA2_ERR_UNSUPPORTED";
+    case CSA2_ERR_ALIGNMENT: return "CSA2_ERR_ALIGNMENT";
+    case CSA2_ERR_CUDA: return "CSA2_ERR_CUDA";
+    case CSA2_ERR_WORKSPACE: return "CSA2_ERR_WORKSPACE";
+    case CSA2_ERR_DEVICE_TIMEOUT: return "CSA2_ERR_DEVICE_TIMEOUT";
+    case CSA2_ERR_DEVICE_BOUNDS: return "CSA2_ERR_DEVICE_BOUNDS";
+    default: return "CSA2_ERR_UNKNOWN";
+  }
+}
+
+int32_t csa2_last_cuda_error(void) { return g_last_cuda_error; }
+
+csa2_status csa2_status_from_device(int32_t w) {
+  if (w & CSA2_DEVFLAG_TIMEOUT) return CSA2_ERR_DEVICE_TIMEOUT;
+  if (w & CSA2_DEVFLAG_BOUNDS) return CSA2_ERR_DEVICE_BOUNDS;
+  return CSA2_OK;
+}
+
+csa2_status csa2_quantize_fp4(const csa2_quant_args* args, csa2_stream_t stream) {
+  csa2_status st = check_quant(args);
+  if (st != CSA2_OK) return st;
+  if ((st = injected("quantize_fp4")) != CSA2_OK) return st;
+  return launch_quantize_fp4(*args, reinterpret_cast<cudaStream_t>(stream));
+}
+
+csa2_status csa2_quantize_index_q(const void* q, const float* w, int64_t nq, int32_t hi,
+                                  int32_t di, uint8_t* q8, float* c, csa2_stream_t stream) {
+  csa2_status st = check_index_q(q, w, nq, hi, di, q8, c);
+  if (st != CSA2_OK) return st;
+  if ((st = injected("quantize_index_q")) != CSA2_OK) return st;
+  return launch_quantize_index_q(q, w, nq, hi, di, q8, c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t csa2_index_score_workspace_bytes(const csa2_index_args* args) {
+  return args ? index_ws(args) : 0;
+}
+
+csa2_status csa2_index_score(const csa2_index_args* args, csa2_stream_t stream) {
+  csa2_status st = check_index(args);
+  if (st != CSA2_OK) return st;
+  if ((st = injected("index_score")) != CSA2_OK) return st;
+  return run_index(*args, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t csa2_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k) {
+  if (rows < 0 || k < 1) return 0;
+  return topk_workspace_bytes(rows, n, k);
+}
+
+csa2_status csa2_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
+                      const int32_t* n_valid, int32_t k, int32_t* idx_out, int64_t idx_ld,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                      csa2_stream_t stream) {
+  csa2_status st = check_topk(scores, rows, n, ld, k, idx_out, idx_ld, workspace, workspace_bytes);
+  if (st != CSA2_OK) return st;
+  if ((st = injected("topk")) != CSA2_OK) return st;
+  return launch_topk(scores, rows, n, ld, n_valid, k, idx_out, idx_ld, workspace, dev_status,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t csa2_sparse_attn_workspace_bytes(const csa2_attn_args* args) {
+  return args ? attn_workspace_bytes(*args) : 0;
+}
+
+csa2_status csa2_sparse_attn(const csa2_attn_args* args, csa2_stream_t stream) {
+  csa2_status st = check_attn(args);
+  if (st != CSA2_OK) return st;
+  if ((st = injected("sparse_attn")) != CSA2_OK) return st;
+  return launch_sparse_attn(*args, reinterpret_cast<cudaStream_t>(stream));
+}
+
+csa2_status csa2_validate_plan(const csa2_layer_desc* L, int32_t n_layers, int32_t* bad_layer) {
+  if (bad_layer) *bad_layer = -1;
+  if (!L || n_layers < 1) return CSA2_ERR_INVALID_ARG;
+  int32_t last_full = -1;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const csa2_layer_desc& d = L[l];
+    bool ok = true;
+    switch (d.mode) {
+      case CSA2_MODE_FULL:
+        ok = d.kv_src == l && d.idx_src == l;
+        if (ok) last_full = l;
+        break;
+      case CSA2_MODE_REINDEX:
+        // the last Full layer's main KV and indexer K, a fresh selection
+        ok = last_full >= 0 && d.kv_src == last_full && d.idx_src == l;
+        break;
+      case CSA2_MODE_REUSE:
+        ok = d.kv_src >= 0 && d.kv_src < l && L[d.kv_src].mode == CSA2_MODE_FULL &&
+             d.idx_src >= 0 && d.idx_src < l &&
+             (L[d.idx_src].mode == CSA2_MODE_FULL || L[d.idx_src].mode == CSA2_MODE_REINDEX) &&
+             L[d.idx_src].kv_src == d.kv_src;
+        break;
+      default:
+        ok = false;
+    }
+    if (!ok) {
+      if (bad_layer) *bad_layer = l;
+      return CSA2_ERR_INVALID_ARG;
+    }
+  }
+  return CSA2_OK;
+}
+
+size_t csa2_layer_stack_workspace_bytes(const csa2_stack_args* s) {
+  if (!s) return 0;
+  StackPieces p = stack_pieces(*s);
+  return p.scores + std::max(p.ix, std::max(p.tk, p.at));
+}
+
+csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
+                             const csa2_stack_args* s, csa2_stream_t stream) {
+  csa2_status st = csa2_validate_plan(L, n_layers, nullptr);
+  if (st != CSA2_OK) return st;
+  if (!s || s->B < 1 || s->q_per_seq < 1 || s->n < 1 || s->k < 1) return CSA2_ERR_INVALID_ARG;
+  const StackPieces p = stack_pieces(*s);
+  const size_t need = p.scores + std::max(p.ix, std::max(p.tk, p.at));
+  if (!s->workspace || s->workspace_bytes < need) return CSA2_ERR_WORKSPACE;
+  if (!aligned(s->workspace, 256)) return CSA2_ERR_ALIGNMENT;
+  float* scores = static_cast<float*>(s->workspace);
+  void* scratch = static_cast<uint8_t*>(s->workspace) + p.scores;
+  const size_t scratch_bytes = s->workspace_bytes - p.scores;
+  const int64_t nq = s->B * s->q_per_seq;
+  // check every call's arguments before anything is enqueued
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const csa2_layer_desc& d = L[l];
+    const csa2_layer_desc& kv = L[d.kv_src];
+    if (d.mode == CSA2_MODE_FULL) {
+      if (!d.codes || !d.scales || !d.idxk) return CSA2_ERR_INVALID_ARG;
+      if ((d.new_kv == nullptr) != (d.new_idxk == nullptr)) return CSA2_ERR_INVALID_ARG;
+      const int64_t nr = d.new_rows > 0 ? d.new_rows : 1;
+      if (d.new_kv && (d.new_row < 0 || d.new_rows < 0 || d.new_row + nr > s->n))
+        return CSA2_ERR_INVALID_ARG;
+    }
+    if (d.mode != CSA2_MODE_REUSE) {
+      if (!d.topk_idx) return CSA2_ERR_INVALID_ARG;
+      csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
+      if ((st = check_index(&ia)) != CSA2_OK) return st;
+      if ((st = check_topk(scores, nq, s->n, s->n, s->k, d.topk_idx, s->k, scratch,
+                           scratch_bytes)) != CSA2_OK)
+        return st;
+    }
+    const int32_t* idx = L[d.mode == CSA2_MODE_REUSE ? d.idx_src : l].topk_idx;
+    csa2_attn_args aa = stack_attn_args(*s, d, kv, idx, scratch, scratch_bytes);
+    if ((st = check_attn(&aa)) != CSA2_OK) return st;
+  }
+  if ((st = injected("layer_stack")) != CSA2_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const csa2_layer_desc& d = L[l];
+    const csa2_layer_desc& kv = L[d.kv_src];
+    if (d.mode == CSA2_MODE_FULL && d.new_kv) {
+      if ((st = quantize_new_rows(*s, d, cs)) != CSA2_OK) return st;
+    }
+    if (d.mode != CSA2_MODE_REUSE) {
+      csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
+      if ((st = run_index(ia, cs)) != CSA2_OK) return st;
+      if ((st = launch_topk(scores, nq, s->n, s->n, s->n_valid, s->k, d.topk_idx, s->k, scratch,
+                            s->dev_status, cs)) != CSA2_OK)
+        return st;
+    }
+    const int32_t* idx = L[d.mode == CSA2_MODE_REUSE ? d.idx_src : l].topk_idx;
+    csa2_attn_args aa = stack_attn_args(*s, d, kv, idx, scratch, scratch_bytes);
+    if ((st = launch_sparse_attn(aa, cs)) != CSA2_OK) return st;
+  }
+  return CSA2_OK;
+}
+
+}  // extern "C"

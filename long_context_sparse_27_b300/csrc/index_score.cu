@@ -1,0 +1,436 @@
+// index_score.cu -- a3, the indexer score
+//   s[q, j] = sum_h w'[q, h] * max(0, <q_h, k_j>)   (j < n_valid[q], else -inf)
+// over every compressed entry of the query's sequence.  The pages name an
+// indexer Q scored against indexer K per layer ("Unlocking Extreme Context
+// Scaling with DeepSeek-V4.1-Flash", "Compressed Sparse Attention 2
+// (CSA2)"); the weighted-ReLU head sum is this library's definition.
+//
+// Two kernels:
+//  * idx_score_f32_kernel  fp32 q / k on CUDA cores (small indexers).
+//  * idx_score_tc_kernel   E4M3 q8 / k on tcgen05 tensor cores.  Per tile of
+//    128 entries: D[128 x 64*QG] = K_tile[128 x 128] . Q8[64*QG x 128]^T in
+//    tensor memory, then an epilogue applies ReLU, the head weights c and the
+//    head sum.  Warp 0 streams K tiles with TMA into an 8-deep ring of 16 KB
+//    stages, warp 1 issues the MMAs, warps 2-5 drain the double-buffered
+//    accumulator.  In decode (QG = 1) the kernel is a stream over the
+//    indexer keys (128 B per entry) and is bound by HBM; in a prefill chunk
+//    (QG = 4, 4 queries x 64 heads per MMA) it is a dense contraction.
+#include <cstdio>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+
+// ===========================================================================
+// fp32 path
+// ===========================================================================
+
+namespace {
+
+constexpr int kF32Warps = 8;
+
+// block = (entry chunk, query); warp w handles entries j = chunk*8*R + w, +8, ...
+__global__ void __launch_bounds__(kF32Warps * 32)
+    idx_score_f32_kernel(const float* __restrict__ q, const float* __restrict__ w,
+                         const float* __restrict__ k, int64_t q_per_seq, int32_t hi, int32_t di,
+                         int64_t n, int64_t k_ld, int64_t k_seq_stride,
+                         const int32_t* __restrict__ n_valid, float* __restrict__ scores,
+                         int64_t scores_ld, int64_t per_block) {
+  extern __shared__ float sq[];  // [hi * di] query, then [hi] weights
+  const int64_t qi = blockIdx.y;
+  const float* qsrc = q + qi * (int64_t)hi * di;
+  for (int i = threadIdx.x; i < hi * di; i += blockDim.x) sq[i] = qsrc[i];
+  for (int i = threadIdx.x; i < hi; i += blockDim.x) sq[hi * di + i] = w[qi * hi + i];
+  __syncthreads();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int64_t nv = n_valid ? (int64_t)n_valid[qi] : n;
+  const float* kseq = k + (qi / q_per_seq) * k_seq_stride;
+  const int64_t j0 = (int64_t)blockIdx.x * per_block;
+  const int64_t j1 = min(n, j0 + per_block);
+  for (int64_t j = j0 + warp; j < j1; j += kF32Warps) {
+    if (j >= nv) {
+      if (lane == 0) scores[qi * scores_ld + j] = -INFINITY;
+      continue;
+    }
+    const float* kj = kseq + j * k_ld;
+    float kv[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) kv[t] = (lane + 32 * t < di) ? kj[lane + 32 * t] : 0.f;
+    float s = 0.f;
+    for (int h = 0; h < hi; ++h) {
+      float dot = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        if (lane + 32 * t < di) dot = fmaf(sq[h * di + lane + 32 * t], kv[t], dot);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      s = fmaf(sq[hi * di + h], fmaxf(dot, 0.f), s);
+    }
+    if (lane == 0) scores[qi * scores_ld + j] = s;
+  }
+}
+
+}  // namespace
+
+csa2_status launch_index_score_f32(const csa2_index_args& a, cudaStream_t s) {
+  const int64_t nq = a.B * a.q_per_seq;
+  if (nq == 0 || a.n == 0) return CSA2_OK;
+  const int64_t per_block = 256;
+  dim3 grid((unsigned)((a.n + per_block - 1) / per_block), (unsigned)nq);
+  const size_t smem = sizeof(float) * ((size_t)a.hi * a.di + a.hi);
+  idx_score_f32_kernel<<<grid, kF32Warps * 32, smem, s>>>(
+      static_cast<const float*>(a.q), a.w, static_cast<const float*>(a.k), a.q_per_seq, a.hi,
+      a.di, a.n, a.k_ld, a.k_seq_stride, a.n_valid, a.scores, a.scores_ld, per_block);
+  return check_launch();
+}
+
+// ===========================================================================
+// FP8 tcgen05 path
+// ===========================================================================
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
+
+template <int QG>
+struct TcCfg {
+  static constexpr int BM = 128;        // entries per tile (MMA M)
+  static constexpr int BN = 64 * QG;    // 64 heads x QG queries (MMA N)
+  static constexpr int BK = 128;        // indexer dim: 128 E4M3 bytes per row
+  static constexpr int STAGES = QG == 1 ? 8 : 6;
+  static constexpr int KTILE = BM * BK;  // 16 KB
+  static constexpr int QTILE = BN * BK;  // 8 KB or 32 KB
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  // shared memory carve-up (offsets from a 1024-byte aligned base)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_Q = OFF_K + STAGES * KTILE;
+  static constexpr int OFF_C = OFF_Q + 2 * QTILE;             // float [EPI_WARPS][2][BN]
+  static constexpr int OFF_BAR = OFF_C + EPI_WARPS * 2 * BN * 4;
+  // barriers: full[S], empty[S], qfull[2], qempty[2], tfull[2], tempty[2], fin
+  static constexpr int NBAR = 2 * STAGES + 9;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem slot, abort flag
+  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr int SMEM_ALLOC = SMEM + 1024;
+};
+
+struct TcParams {
+  const float* c;          // [nq, 64] head weights (w * sigma)
+  const int32_t* n_valid;  // [nq] or null
+  float* scores;
+  int64_t scores_ld;
+  int64_t n;               // entries per sequence
+  int64_t q_per_seq;
+  int64_t groups;          // nq / QG
+  int64_t ktiles;          // ceil(n / 128)
+  int32_t* dev_status;
+};
+
+template <int QG>
+__global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
+    idx_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap qmap, const TcParams p) {
+  using C = TcCfg<QG>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* kbuf = smem + C::OFF_K;
+  uint8_t* qbuf = smem + C::OFF_Q;
+  float* cbuf = reinterpret_cast<float*>(smem + C::OFF_C);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* qfull = bars + 2 * C::STAGES;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* tfull = qempty + 2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* fin = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int64_t total = p.groups * p.ktiles;
+  const int64_t t_begin = (int64_t)blockIdx.x * total / gridDim.x;
+  const int64_t t_end = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], C::EPI_WARPS);
+    }
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&qmap);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol_k = l2_policy_evict_first();
+      const uint64_t pol_q = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t ph = 0;
+      int64_t g_prev = -1, qcount = 0, issued = 0;
+      bool ok = true;
+      for (int64_t t = t_begin; t < t_end && ok; ++t) {
+        const int64_t g = t / p.ktiles, kt = t % p.ktiles;
+        if (g != g_prev) {
+          const int qs = (int)(qcount & 1);
+          const uint32_t qph = (uint32_t)((qcount >> 1) & 1);
+          if (!mbar_wait(&qempty[qs], qph ^ 1, abort_flag, p.dev_status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&qfull[qs], C::QTILE);
+          tma_load_2d(&qmap, &qfull[qs], qbuf + qs * C::QTILE, 0, (int32_t)(g * C::BN), pol_q);
+          ++qcount;
+          g_prev = g;
+        }
+        if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, p.dev_status, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const int64_t b = (g * QG) / p.q_per_seq;
+        mbar_arrive_expect_tx(&full[stage], C::KTILE);
+        tma_load_3d(&kmap, &full[stage], kbuf + stage * C::KTILE, 0, (int32_t)(kt * C::BM),
+                    (int32_t)b, pol_k);
+        ++issued;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          ph ^= 1;
+        }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA's shared
+        // memory goes away: wait (bounded, ignoring the abort flag) for the
+        // full barrier of every stage filled but possibly not consumed
+        int dummy = 0;
+        const int64_t first = issued > C::STAGES ? issued - C::STAGES : 0;
+        for (int64_t u = first; u < issued; ++u)
+          mbar_wait(&full[u % C::STAGES], (uint32_t)((u / C::STAGES) & 1), &dummy, nullptr,
+                    kWaitLimitNs / 20);
+        if (qcount > 0)
+          mbar_wait(&qfull[(qcount - 1) & 1], (uint32_t)(((qcount - 1) >> 1) & 1), &dummy,
+                    nullptr, kWaitLimitNs / 20);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(C::BM, C::BN);
+      int stage = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      int64_t g_prev = -1, qcount = 0;
+      int qs = 0;
+      bool any = false;
+      for (int64_t t = t_begin; t < t_end; ++t) {
+        const int64_t g = t / p.ktiles;
+        if (g != g_prev) {
+          if (g_prev >= 0) tc_commit(&qempty[qs]);  // old Q free once its MMAs finish
+          qs = (int)(qcount & 1);
+          if (!mbar_wait(&qfull[qs], (uint32_t)((qcount >> 1) & 1), abort_flag, p.dev_status,
+                         kWaitLimitNs))
+            break;
+          ++qcount;
+          g_prev = g;
+        }
+        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.dev_status, kWaitLimitNs)) break;
+        tc_fence_after();
+        if (!mbar_wait(&full[stage], ph, abort_flag, p.dev_status, kWaitLimitNs)) break;
+        tc_fence_after();
+        const uint64_t adesc = sdesc_k_sw128(smem_u32(kbuf + stage * C::KTILE));
+        const uint64_t bdesc = sdesc_k_sw128(smem_u32(qbuf + qs * C::QTILE));
+        const uint32_t dtm = tmem_base + (uint32_t)(acc * C::BN);
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 32; ++kk)  // K = 32 E4M3 per MMA: +32 B = +2 in the address field
+          tc_mma_f8(dtm, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+        tc_commit(&empty[stage]);
+        tc_commit(&tfull[acc]);
+        any = true;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          ph ^= 1;
+        }
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1;
+        }
+      }
+      if (any) {
+        // every MMA issued has completed before tensor memory is released
+        int dummy = 0;
+        tc_commit(fin);
+        mbar_wait(fin, 0, &dummy, p.dev_status, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 2;         // 0..3
+    const int lq = warp & 3;        // TMEM lane quarter this warp may access
+    const int row = lq * 32 + lane;  // entry within the tile
+    int acc = 0;
+    uint32_t aph = 0;
+    int64_t g_prev = -1;
+    // each epilogue warp keeps its own copy of the group's head weights
+    // (double-buffered), so the warps never wait on one another
+    float* my_c = cbuf + ew * 2 * C::BN;
+    int cb = 1;
+    int64_t nv[QG];
+    for (int64_t t = t_begin; t < t_end; ++t) {
+      const int64_t g = t / p.ktiles, kt = t % p.ktiles;
+      if (g != g_prev) {
+        cb ^= 1;
+        __syncwarp();
+        for (int i = lane; i < C::BN; i += 32) my_c[cb * C::BN + i] = p.c[g * C::BN + i];
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < QG; ++i) nv[i] = p.n_valid ? (int64_t)p.n_valid[g * QG + i] : p.n;
+        g_prev = g;
+      }
+      // every lane waits; the warp goes on only if all of them saw the phase
+      // complete, so the warp-collective loads below never run diverged
+      const bool got = mbar_wait(&tfull[acc], aph, abort_flag, p.dev_status, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(lq * 32) << 16) + (uint32_t)(acc * C::BN);
+      const float* cw = my_c + cb * C::BN;
+      float sc[QG];
+#pragma unroll
+      for (int qq = 0; qq < QG; ++qq) {
+        float v[64];
+        tmem_ld32(taddr + qq * 64, v);
+        tmem_ld32(taddr + qq * 64 + 32, v + 32);
+        tmem_ld_wait();
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 64; h += 2) {
+          s0 = fmaf(cw[qq * 64 + h], fmaxf(v[h], 0.f), s0);
+          s1 = fmaf(cw[qq * 64 + h + 1], fmaxf(v[h + 1], 0.f), s1);
+        }
+        sc[qq] = s0 + s1;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      const int64_t j = kt * C::BM + row;
+      if (j < p.n) {
+#pragma unroll
+        for (int qq = 0; qq < QG; ++qq) {
+          const int64_t qi = g * QG + qq;
+          p.scores[qi * p.scores_ld + j] = (j < nv[qq]) ? sc[qq] : -INFINITY;
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        aph ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---- host side: tensor maps ----
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+template <int QG>
+csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* c,
+                      cudaStream_t s) {
+  using C = TcCfg<QG>;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cuda_fail(cudaErrorNotSupported);
+  const int64_t nq = a.B * a.q_per_seq;
+  CUtensorMap kmap, qmap;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)a.di, (cuuint64_t)a.n, (cuuint64_t)a.B};
+    cuuint64_t strides[2] = {(cuuint64_t)a.k_ld, (cuuint64_t)a.k_seq_stride};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(a.k), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return CSA2_ERR_INVALID_ARG;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)a.di, (cuuint64_t)(nq * a.hi)};
+    cuuint64_t strides[1] = {(cuuint64_t)a.di};
+    cuuint32_t box[2] = {128, (cuuint32_t)C::BN};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q8), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return CSA2_ERR_INVALID_ARG;
+  }
+  TcParams p;
+  p.c = c;
+  p.n_valid = a.n_valid;
+  p.scores = a.scores;
+  p.scores_ld = a.scores_ld;
+  p.n = a.n;
+  p.q_per_seq = a.q_per_seq;
+  p.groups = nq / QG;
+  p.ktiles = (a.n + C::BM - 1) / C::BM;
+  p.dev_status = a.dev_status;
+  const int64_t total = p.groups * p.ktiles;
+  if (total == 0) return CSA2_OK;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(idx_score_tc_kernel<QG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_ALLOC);
+    if (e != cudaSuccess) return cuda_fail(e);
+    attr_set = true;
+  }
+  const int grid = (int)std::min<int64_t>(total, sm_count());
+  idx_score_tc_kernel<QG><<<grid, C::THREADS, C::SMEM_ALLOC, s>>>(kmap, qmap, p);
+  return check_launch();
+}
+
+}  // namespace
+
+csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, const float* c,
+                                   cudaStream_t s) {
+  if (a.hi != 64 || a.di != 128) return CSA2_ERR_UNSUPPORTED;
+  if (a.B * a.q_per_seq == 0 || a.n == 0) return CSA2_OK;
+  if (a.q_per_seq % 4 == 0) return launch_tc<4>(a, q8, c, s);
+  return launch_tc<1>(a, q8, c, s);
+}
+
+}  // namespace csa2

@@ -1,0 +1,42 @@
+// internal.h -- launchers shared between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+
+namespace csa2 {
+
+// Round up to a multiple of 256 bytes (every workspace region starts aligned).
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Records a failed CUDA call for csa2_last_cuda_error() and maps it to a status.
+csa2_status cuda_fail(cudaError_t e);
+// cudaGetLastError() after a launch, mapped to a status.
+csa2_status check_launch();
+
+// a1
+csa2_status launch_quantize_fp4(const csa2_quant_args& a, cudaStream_t s);
+// a2
+csa2_status launch_quantize_index_q(const void* q, const float* w, int64_t nq, int32_t hi,
+                                    int32_t di, uint8_t* q8, float* c, cudaStream_t s);
+// a3, fp32 CUDA-core path
+csa2_status launch_index_score_f32(const csa2_index_args& a, cudaStream_t s);
+// a3, FP8 tensor-core path: q8 / c already quantised
+csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, const float* c,
+                                   cudaStream_t s);
+// a4
+size_t topk_workspace_bytes(int64_t rows, int64_t n, int32_t k);
+csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
+                        const int32_t* n_valid, int32_t k, int32_t* idx_out, int64_t idx_ld,
+                        void* ws, int32_t* dev_status, cudaStream_t s);
+// a5
+size_t attn_workspace_bytes(const csa2_attn_args& a);
+csa2_status launch_sparse_attn(const csa2_attn_args& a, cudaStream_t s);
+
+// number of SMs of the current device (cached per device)
+int sm_count();
+
+}  // namespace csa2

@@ -1,0 +1,152 @@
+// quant.cu -- a1 (FP4 E2M1 main-KV quantiser + E4M3 indexer-K cast) and
+// a2 (indexer-Q E4M3 quantiser).
+//
+// a1 follows the FP4 main-KV cache of "Unlocking Extreme Context Scaling
+// with DeepSeek-V4.1-Flash" ("Deployment and Infrastructure") in the E2M1
+// format named on the aiany.app DeepSeek-V4.1-Flash page ("What Sets It
+// Apart"), with the OCP MX v1.0 per-32 power-of-two scale:
+// X = 2^(floor(log2 amax) - 2).  Memory-bound and tiny (one new row per
+// sequence per decode step): each thread converts 8 elements (one 16-byte
+// load), four threads share a 32-element block and reduce its amax with
+// two shuffles.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+// Threads [0, kv_threads) quantise main-KV rows; threads from the next
+// multiple of 32 on cast indexer-K rows.  Every thread of a warp takes part
+// in the shuffles; threads past the end work on zeros and store nothing.
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_fp4_kernel(const uint16_t* __restrict__ x, int64_t rows, int32_t d, int64_t x_ld,
+                     uint8_t* __restrict__ codes, int64_t codes_ld, uint8_t* __restrict__ scales,
+                     int64_t scales_ld, const uint16_t* __restrict__ kx, int32_t di,
+                     int64_t k_ld, uint8_t* __restrict__ k8, int64_t k8_ld, int64_t kv_threads,
+                     int64_t k_begin) {
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid < k_begin) {
+    const int64_t per_row = d / 8;
+    const bool live = gid < kv_threads;
+    const int64_t row = live ? gid / per_row : 0;
+    const int64_t part = live ? gid % per_row : 0;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (live) raw = *reinterpret_cast<const uint4*>(x + row * x_ld + part * 8);
+    float v[8];
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+      v[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if (!live) return;
+    uint32_t packed = 0, sbyte = 0;
+    if (amax > 0.f) {
+      int e = floor_log2_pos(amax) - 2;
+      e = max(-127, min(127, e));
+      sbyte = (uint32_t)(e + 127);
+      const float inv = exp2_int(-e);  // -e in [-127, 127]: exact power of two
+#pragma unroll
+      for (int i = 0; i < 8; ++i) packed |= e2m1_encode(v[i] * inv) << (4 * i);
+    }
+    *reinterpret_cast<uint32_t*>(codes + row * codes_ld + part * 4) = packed;
+    if ((part & 3) == 0) scales[row * scales_ld + part / 4] = (uint8_t)sbyte;
+  } else {
+    const int64_t t = gid - k_begin;
+    const int64_t per_row = di / 8;
+    if (t >= rows * per_row) return;
+    const int64_t row = t / per_row, part = t % per_row;
+    const uint4 raw = *reinterpret_cast<const uint4*>(kx + row * k_ld + part * 8);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      lo |= e4m3_encode(bf16_bits_to_float(w[i] & 0xFFFFu)) << (16 * i);
+      lo |= e4m3_encode(bf16_bits_to_float(w[i] >> 16)) << (16 * i + 8);
+      hi |= e4m3_encode(bf16_bits_to_float(w[i + 2] & 0xFFFFu)) << (16 * i);
+      hi |= e4m3_encode(bf16_bits_to_float(w[i + 2] >> 16)) << (16 * i + 8);
+    }
+    *reinterpret_cast<uint2*>(k8 + row * k8_ld + part * 8) = make_uint2(lo, hi);
+  }
+}
+
+// a2: one warp per (row, head); each lane holds di/32 consecutive values.
+template <int DI>
+__global__ void __launch_bounds__(256)
+    quant_index_q_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
+                         int64_t n_heads_total, uint8_t* __restrict__ q8, float* __restrict__ c) {
+  constexpr int PER = DI / 32;
+  const int64_t head = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (head >= n_heads_total) return;  // whole warp leaves together
+  const uint16_t* src = q + head * DI + lane * PER;
+  float v[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) v[i] = bf16_bits_to_float(src[i]);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int e = 0;
+  if (amax > 0.f) {
+    // smallest e with amax / 2^e <= 448 = 1.75 * 2^8: with amax = m 2^E
+    // (m in [1, 2)), e = E - 8 when m <= 1.75, else E - 7.
+    const int E = floor_log2_pos(amax);
+    // fraction bits of m, normalising a subnormal amax first
+    const uint32_t u = __float_as_uint(amax);
+    uint32_t frac = u & 0x7FFFFFu;
+    if (((u >> 23) & 0xFFu) == 0) frac = (frac << (__clz(frac) - 8)) & 0x7FFFFFu;
+    e = (frac <= 0x600000u) ? E - 8 : E - 7;  // 0x600000: fraction of 1.75
+    e = max(e, -126);
+  }
+  const float inv = exp2_int(-e);
+  uint8_t out[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) out[i] = amax > 0.f ? (uint8_t)e4m3_encode(v[i] * inv) : 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) q8[head * DI + lane * PER + i] = out[i];
+  if (lane == 0) c[head] = w[head] * exp2_int(e);
+}
+
+}  // namespace
+
+csa2_status launch_quantize_fp4(const csa2_quant_args& a, cudaStream_t s) {
+  if (a.rows == 0) return CSA2_OK;
+  const int64_t kv_threads = a.rows * (a.d / 8);
+  const int64_t k_begin = (kv_threads + 31) / 32 * 32;
+  const int64_t k_threads = a.idxk ? a.rows * (a.di / 8) : 0;
+  const int64_t total = k_begin + k_threads;
+  const int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
+  quant_fp4_kernel<<<(unsigned)blocks, kQuantThreads, 0, s>>>(
+      static_cast<const uint16_t*>(a.x), a.rows, a.d, a.x_ld, a.codes, a.codes_ld, a.scales,
+      a.scales_ld, static_cast<const uint16_t*>(a.idxk), a.di, a.idxk_ld, a.idxk_e4m3,
+      a.idxk_e4m3_ld, kv_threads, k_begin);
+  return check_launch();
+}
+
+csa2_status launch_quantize_index_q(const void* q, const float* w, int64_t nq, int32_t hi,
+                                    int32_t di, uint8_t* q8, float* c, cudaStream_t s) {
+  const int64_t heads = nq * hi;
+  if (heads == 0) return CSA2_OK;
+  const unsigned blocks = (unsigned)((heads + 7) / 8);
+  const uint16_t* qp = static_cast<const uint16_t*>(q);
+  switch (di) {
+    case 32: quant_index_q_kernel<32><<<blocks, 256, 0, s>>>(qp, w, heads, q8, c); break;
+    case 64: quant_index_q_kernel<64><<<blocks, 256, 0, s>>>(qp, w, heads, q8, c); break;
+    case 128: quant_index_q_kernel<128><<<blocks, 256, 0, s>>>(qp, w, heads, q8, c); break;
+    case 256: quant_index_q_kernel<256><<<blocks, 256, 0, s>>>(qp, w, heads, q8, c); break;
+    default: return CSA2_ERR_UNSUPPORTED;
+  }
+  return check_launch();
+}
+
+}  // namespace csa2

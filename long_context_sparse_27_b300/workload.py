@@ -1,0 +1,145 @@
+"""Device-resident inputs for one step of a CSA2 layer schedule.
+
+Draws every tensor with the seeded generators of `synth`, fills each Full
+layer's FP4 main-KV cache and E4M3 indexer-K cache for entries 0 .. N-2 with
+the library's own quantiser, and keeps entry N-1 (the compressed entry that
+completes in this decode step) as the step's new rows, which the layer
+schedule quantises itself.  Also builds the descriptor array and stack
+arguments for csa2_layer_stack.
+
+Schedule sources: a Reindex layer reads the most recent Full layer's caches;
+a Reuse layer reads the most recent Full layer's caches and top-k indices.
+"""
+import math
+
+import torch
+
+from . import csa2, synth
+
+FULL, REINDEX, REUSE = synth.FULL, synth.REINDEX, synth.REUSE
+
+
+def default_sources(modes):
+    out, last_full = [], -1
+    for l, m in enumerate(modes):
+        if m == FULL:
+            last_full = l
+            out.append((l, l))
+        elif m == REINDEX:
+            out.append((last_full, l))
+        else:
+            out.append((last_full, last_full))
+    return out
+
+
+class StackWorkload:
+    """All tensors of one decode (or prefill) step, on `device`.
+
+    gen_device: where the random draws happen ("cpu" keeps them reproducible
+    for the oracle; "cuda" is fast for the large workloads).
+    keep_bf16: keep the unquantised KV / indexer-K rows (on the host) so an
+    oracle can quantise them itself.
+    """
+
+    def __init__(self, wl: synth.Workload, seed=0, device="cuda", gen_device=None,
+                 keep_bf16=False, sources=None):
+        self.wl = wl
+        self.device = device
+        gen = gen_device or device
+        self.plan = sources or default_sources(wl.modes)
+        self.layers = []
+        self.bf16 = []
+        B, N = wl.B, wl.N
+        nq = wl.nq
+        for l, m in enumerate(wl.modes):
+            s = seed * 1000 + 20 * l
+            kv_src, idx_src = self.plan[l]
+            L = {"mode": m, "kv_src": kv_src, "idx_src": idx_src,
+                 "attn_q": synth.attn_q(wl, s + 1, gen).to(device),
+                 "window": synth.window_rows(wl, s + 2, gen).to(device),
+                 "out": torch.empty(nq, wl.Hq, wl.D, dtype=torch.float32, device=device)}
+            host = {}
+            if m in (FULL, REINDEX):
+                L["idx_q"] = synth.index_q(wl, s + 3, gen).to(device)
+                L["idx_w"] = synth.index_w(wl, s + 4, gen).to(device)
+                L["topk_idx"] = torch.full((nq, wl.k), -1, dtype=torch.int32, device=device)
+            if m == FULL:
+                kv = synth.kv_rows(wl, s + 5, gen)
+                kk = synth.index_k_rows(wl, s + 6, gen)
+                if keep_bf16:
+                    host["kv"] = kv.cpu()
+                    host["kk"] = kk.cpu()
+                self._fill_cache(L, kv.to(device), kk.to(device))
+                del kv, kk
+            self.layers.append(L)
+            self.bf16.append(host)
+        self.n_valid = None
+        self.win_start = self.win_len = None
+        if wl.q_per_seq > 1:
+            self.n_valid = synth.prefill_n_valid(wl, device)
+            self.win_start = torch.arange(wl.q_per_seq, dtype=torch.int32,
+                                          device=device).repeat(wl.B)
+            self.win_len = torch.full((nq,), wl.W, dtype=torch.int32, device=device)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.descs = csa2.layer_descs(self.layers)
+        self.sargs = self.stack_args()
+        need = csa2.layer_stack_workspace_bytes(self.sargs)
+        self.workspace = torch.empty(need + 256, dtype=torch.uint8, device=device)
+
+    def _fill_cache(self, L, kv, kk):
+        wl = self.wl
+        B, N = wl.B, wl.N
+        L["codes"] = torch.zeros(B, N, wl.D // 2, dtype=torch.uint8, device=self.device)
+        L["scales"] = torch.zeros(B, N, wl.D // 32, dtype=torch.uint8, device=self.device)
+        if wl.fp32_indexer:
+            L["idxk"] = torch.zeros(B, N, wl.Di, dtype=torch.float32, device=self.device)
+            L["idxk"][:, : N - (1 if wl.q_per_seq == 1 else wl.q_per_seq // 4)] = \
+                kk[:, : N - (1 if wl.q_per_seq == 1 else wl.q_per_seq // 4)].float()
+        else:
+            L["idxk"] = torch.zeros(B, N, wl.Di, dtype=torch.uint8, device=self.device)
+        # decode completes one compressed entry per sequence; a prefill chunk
+        # of T tokens completes T / 4 entries (4 tokens per entry)
+        rows_new = 1 if wl.q_per_seq == 1 else wl.q_per_seq // 4
+        old = N - rows_new
+        for b in range(B):
+            if wl.fp32_indexer:
+                csa2.quantize_fp4(kv[b, :old], L["codes"][b, :old], L["scales"][b, :old])
+            else:
+                csa2.quantize_fp4(kv[b, :old], L["codes"][b, :old], L["scales"][b, :old],
+                                  kk[b, :old], L["idxk"][b, :old])
+        L["new_kv"] = kv[:, old:].contiguous()
+        L["new_idxk"] = (kk[:, old:].float() if wl.fp32_indexer else kk[:, old:]).contiguous()
+        L["new_row"] = old
+        L["new_rows"] = rows_new
+
+    def stack_args(self):
+        wl = self.wl
+        return csa2.stack_args(
+            B=wl.B, q_per_seq=wl.q_per_seq, n=wl.N, hi=wl.Hi, di=wl.Di, hq=wl.Hq, d=wl.D,
+            k=wl.k, w_rows=self.layers[0]["window"].shape[1],
+            idx_q_dtype=csa2.F32 if wl.fp32_indexer else csa2.BF16,
+            idx_k_dtype=csa2.F32 if wl.fp32_indexer else csa2.E4M3,
+            attn_q_dtype=csa2.F32 if wl.attn_q_fp32 else csa2.BF16,
+            softmax_scale=1.0 / math.sqrt(wl.D), n_valid=self.n_valid,
+            win_start=self.win_start, win_len=self.win_len, dev_status=self.dev_status)
+
+    def run(self):
+        """Enqueue one step on the current stream."""
+        csa2.layer_stack(self.descs, self.sargs, self.workspace)
+
+    # bytes the method must move per step (the roofline numerator); the
+    # scores scratch is excluded.
+    def algorithmic_bytes(self):
+        wl = self.wl
+        nq = wl.nq
+        index_layers = sum(1 for m in wl.modes if m in (FULL, REINDEX))
+        per_index = (wl.B * wl.N * wl.Di * (4 if wl.fp32_indexer else 1)
+                     + nq * wl.Hi * wl.Di * (4 if wl.fp32_indexer else 2)
+                     + nq * wl.Hi * 4 + nq * wl.k * 4)
+        per_layer = (nq * wl.k * (wl.D // 2 + wl.D // 32) + nq * wl.W * wl.D * 2
+                     + nq * wl.Hq * wl.D * (4 if wl.attn_q_fp32 else 2) + nq * wl.Hq * wl.D * 4)
+        return index_layers * per_index + len(wl.modes) * per_layer
+
+    def indexer_bytes_per_layer(self):
+        wl = self.wl
+        return wl.B * wl.N * wl.Di * (4 if wl.fp32_indexer else 1)

@@ -1,0 +1,196 @@
+"""Host-only checks of the C ABI (no GPU work is ever enqueued here).
+
+The library loads without a GPU (the CUDA runtime is linked statically).
+Calls below either fail argument validation or are stopped by the host
+fault injection before any launch, so they never touch a device.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "csa2.h")
+
+# These tests pass fake device pointers; on a machine with a GPU a wrong
+# branch could launch with them, so they run only where no GPU is visible.
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(), reason="host-only test")
+
+
+@pytest.fixture(scope="module")
+def csa2():
+    from long_context_sparse_27_b300 import build
+    build.build()
+    from long_context_sparse_27_b300 import csa2 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(csa2_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(csa2):
+    names = declared_functions()
+    assert len(names) >= 15
+    out = subprocess.check_output(["nm", "-D", "--defined-only", csa2.LIB_PATH], text=True)
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    # and the binding describes every one of them
+    assert set(names) <= set(csa2.EXPORTS)
+
+
+def test_struct_layouts_match_c(csa2, tmp_path):
+    structs = {"csa2_quant_args": csa2.QuantArgs, "csa2_index_args": csa2.IndexArgs,
+               "csa2_attn_args": csa2.AttnArgs, "csa2_layer_desc": csa2.LayerDesc,
+               "csa2_stack_args": csa2.StackArgs}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "csa2.h"', "int main(void){"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0;}")
+    src = tmp_path / "probe.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "probe"
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                           str(exe)])
+    got = dict(l.split() for l in subprocess.check_output([str(exe)], text=True).splitlines())
+    for cname, py in structs.items():
+        assert int(got[cname]) == ctypes.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert int(got[f"{cname}.{f}"]) == getattr(py, f).offset, (cname, f)
+
+
+def test_status_strings(csa2):
+    assert csa2.lib.csa2_status_string(0) == b"CSA2_OK"
+    assert csa2.lib.csa2_status_string(5) == b"CSA2_ERR_WORKSPACE"
+    assert csa2.lib.csa2_status_string(99) == b"CSA2_ERR_UNKNOWN"
+    assert csa2.lib.csa2_status_from_device(0) == 0
+    assert csa2.lib.csa2_status_from_device(csa2.DEVFLAG_BOUNDS) == 7
+    assert csa2.lib.csa2_status_from_device(csa2.DEVFLAG_TIMEOUT | csa2.DEVFLAG_BOUNDS) == 6
+    assert csa2.version().count(".") == 2
+
+
+def test_workspace_sizes(csa2):
+    assert csa2.topk_workspace_bytes(8, 262144, 512) > 8 * 2 * 4096 * 4
+    assert csa2.topk_workspace_bytes(8, 262144, 512) % 256 == 0
+    a = csa2.IndexArgs(q_dtype=csa2.BF16, k_dtype=csa2.E4M3, B=8, q_per_seq=1, hi=64, di=128,
+                       n=262144)
+    assert csa2.lib.csa2_index_score_workspace_bytes(ctypes.byref(a)) == 8 * 64 * 128 + 8 * 64 * 4
+    a.q_dtype = a.k_dtype = csa2.F32
+    assert csa2.lib.csa2_index_score_workspace_bytes(ctypes.byref(a)) == 0
+
+
+# ---- plan validation (pure host logic) ----
+
+def plan(*triples):
+    return [{"mode": m, "kv_src": kv, "idx_src": ix} for m, kv, ix in triples]
+
+
+F, RI, RU = 0, 1, 2
+
+
+@pytest.mark.parametrize("layers,ok,bad", [
+    (plan((F, 0, 0), (RI, 0, 1), (RU, 0, 0)), True, -1),
+    (plan((F, 0, 0), (RI, 0, 1), (RU, 0, 1)), True, -1),      # Reuse of the Reindex indices
+    (plan((F, 0, 0), (RI, 0, 1), (RU, 0, 0), (RU, 0, 0), (F, 4, 4), (RI, 4, 5), (RU, 4, 4)),
+     True, -1),
+    (plan((RI, 0, 0)), False, 0),                              # no Full first
+    (plan((F, 0, 0), (F, 0, 1)), False, 1),                    # Full must name itself
+    (plan((F, 0, 0), (F, 1, 1), (RI, 0, 2)), False, 2),        # Reindex: the LAST Full layer
+    (plan((F, 0, 0), (RU, 1, 0)), False, 1),                   # KV from a later layer
+    (plan((F, 0, 0), (F, 1, 1), (RU, 1, 0)), False, 2),        # indices of another cache
+    (plan((F, 0, 0), (RU, 0, 0), (RU, 0, 1)), False, 2),       # indices of a Reuse layer
+    (plan((F, 0, 0), (3, 0, 0)), False, 1),                    # unknown mode
+])
+def test_validate_plan(csa2, layers, ok, bad):
+    st, where = csa2.validate_plan(layers)
+    assert (st == 0) == ok
+    assert where == bad
+
+
+# ---- argument validation and host fault injection (never launches) ----
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced
+
+
+@no_gpu
+def test_topk_validation(csa2):
+    L = csa2.lib
+    ws = csa2.topk_workspace_bytes(4, 1000, 64)
+    assert L.csa2_topk(FAKE, 4, 1000, 1000, None, 0, FAKE, 64, FAKE, ws, None, None) == 1
+    assert L.csa2_topk(FAKE, 4, 1000, 1000, None, 4096, FAKE, 4096, FAKE, ws, None, None) == 2
+    assert L.csa2_topk(FAKE, 4, 1000, 1000, None, 64, FAKE, 64, FAKE, ws - 1, None, None) == 5
+    assert L.csa2_topk(FAKE, 4, 1000, 1000, None, 64, FAKE, 64, FAKE + 8, ws, None, None) == 3
+    assert L.csa2_topk(FAKE, 4, 1000, 999, None, 64, FAKE, 64, FAKE, ws, None, None) == 1
+
+
+@no_gpu
+def test_fault_injection_stops_before_launch(csa2, monkeypatch):
+    L = csa2.lib
+    ws = csa2.topk_workspace_bytes(4, 1000, 64)
+    monkeypatch.setenv("CSA2_FAULT_INJECT", "topk:4")
+    assert L.csa2_topk(FAKE, 4, 1000, 1000, None, 64, FAKE, 64, FAKE, ws, None, None) == 4
+    monkeypatch.setenv("CSA2_FAULT_INJECT", "topk:6")
+    assert L.csa2_topk(FAKE, 4, 1000, 1000, None, 64, FAKE, 64, FAKE, ws, None, None) == 6
+    # a bad argument is reported before the injected failure
+    assert L.csa2_topk(FAKE, 4, 1000, 1000, None, 0, FAKE, 64, FAKE, ws, None, None) == 1
+
+
+@no_gpu
+def test_index_validation(csa2, monkeypatch):
+    L = csa2.lib
+    a = csa2.IndexArgs(q=FAKE, q_dtype=csa2.BF16, w=FAKE, k=FAKE, k_dtype=csa2.E4M3, B=2,
+                       q_per_seq=1, hi=64, di=128, n=1000, k_ld=128, k_seq_stride=128 * 1000,
+                       scores=FAKE, scores_ld=1000)
+    assert L.csa2_index_score(ctypes.byref(a), None) == 5          # no workspace
+    a.workspace, a.workspace_bytes = FAKE, L.csa2_index_score_workspace_bytes(ctypes.byref(a))
+    a.hi = 32
+    assert L.csa2_index_score(ctypes.byref(a), None) == 2          # only 64 x 128 is built
+    a.hi = 64
+    a.k = FAKE + 8
+    assert L.csa2_index_score(ctypes.byref(a), None) == 3          # TMA needs 16-byte rows
+    a.k = FAKE
+    a.k_seq_stride = 100
+    assert L.csa2_index_score(ctypes.byref(a), None) == 1          # overlapping sequences
+    a.k_seq_stride = 128 * 1000
+    monkeypatch.setenv("CSA2_FAULT_INJECT", "index_score:4")
+    assert L.csa2_index_score(ctypes.byref(a), None) == 4
+
+
+@no_gpu
+def test_attn_and_quant_validation(csa2, monkeypatch):
+    L = csa2.lib
+    a = csa2.AttnArgs(q=FAKE, q_dtype=csa2.BF16, nq=2, q_per_seq=1, hq=64, d=512, codes=FAKE,
+                      scales=FAKE, n=100, codes_ld=256, codes_seq_stride=25600, scales_ld=16,
+                      scales_seq_stride=1600, idx=FAKE, k=64, idx_ld=64, window=FAKE, w_rows=8,
+                      win_ld=512, win_seq_stride=4096, softmax_scale=0.04, out=FAKE)
+    assert L.csa2_sparse_attn(ctypes.byref(a), None) == 5
+    need = L.csa2_sparse_attn_workspace_bytes(ctypes.byref(a))
+    assert need == 2 * 4 * 2 * (16 * 512 + 32) * 4  # 2 queries x 4 head groups x 2 chunks
+    a.workspace, a.workspace_bytes = FAKE, need
+    a.hq = 24
+    assert L.csa2_sparse_attn(ctypes.byref(a), None) == 2
+    a.hq = 64
+    a.codes_ld = 264
+    assert L.csa2_sparse_attn(ctypes.byref(a), None) == 3
+    a.codes_ld = 256
+    monkeypatch.setenv("CSA2_FAULT_INJECT", "sparse_attn:4")
+    assert L.csa2_sparse_attn(ctypes.byref(a), None) == 4
+    q = csa2.QuantArgs(x=FAKE, rows=4, d=48, x_ld=48, codes=FAKE, codes_ld=24, scales=FAKE,
+                       scales_ld=2)
+    assert L.csa2_quantize_fp4(ctypes.byref(q), None) == 1      # d % 32 != 0
+    q.d, q.x_ld, q.codes_ld, q.scales_ld = 64, 64, 32, 2
+    q.x = FAKE + 2
+    assert L.csa2_quantize_fp4(ctypes.byref(q), None) == 3
+    q.x = FAKE
+    monkeypatch.setenv("CSA2_FAULT_INJECT", "quantize_fp4:4")
+    assert L.csa2_quantize_fp4(ctypes.byref(q), None) == 4

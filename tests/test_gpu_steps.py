@@ -1,0 +1,274 @@
+"""GPU parity of each CSA2 step against the fp64 oracle (through the C ABI).
+
+Inputs come from the seeded generators in long_context_sparse_27_b300.synth
+(drawn on the CPU, copied to the GPU); the oracle consumes the same bytes and
+never any output of the CUDA path.  Bars: quantisers bit-exact, top-k
+bit-exact on the same float32 scores, indexer scores within 1e-3 relative,
+attention within 2e-3 relative L2 per (query, head).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import f64, need_gpu, rel_l2, score_close
+from long_context_sparse_27_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csa2():
+    return need_gpu()
+
+
+def dev(t):
+    return t.to("cuda")
+
+
+# ---------------------------------------------------------------- a1 quantiser
+
+def fp4_inputs(rows, d, seed):
+    x = synth.normal((rows, d), seed, dtype=torch.float32)
+    # blocks across magnitudes, zero blocks, tiny and huge blocks, ties
+    scale = torch.exp2(torch.randint(-130, 120, (rows, d // 32),
+                                     generator=torch.Generator().manual_seed(seed + 1)).float())
+    x = (x.view(rows, d // 32, 32) * scale[:, :, None]).view(rows, d)
+    x[0, :32] = 0.0
+    x[1, :32] = -0.0
+    x[2, :8] = torch.tensor([6.0, 7.0, -5.0, 2.5, 0.25, 0.75, 1.25, 3.5])
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,d", [(1000, 512), (37, 128), (5, 32)])
+def test_quantize_fp4_bit_exact(csa2, orc, rows, d):
+    x = fp4_inputs(rows, d, 100 + d)
+    codes, scales = csa2.quantize_fp4(dev(x))
+    rc, rs = orc.quantize_fp4(f64(x))
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+
+
+def test_quantize_fp4_every_bf16_pattern(csa2, orc):
+    # all 65536 bf16 bit patterns (finite ones) as elements of 32-blocks
+    bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    v = bits[torch.isfinite(bits.float())]
+    v = v[: (v.numel() // 512) * 512].reshape(-1, 512)
+    codes, scales = csa2.quantize_fp4(dev(v))
+    rc, rs = orc.quantize_fp4(f64(v))
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_quantize_fp4_strided_rows_and_idxk(csa2, orc):
+    # one new row per sequence written at row N-1 of a [B, N, ...] cache
+    B, N, d, di = 4, 10, 512, 128
+    cache_c = torch.zeros(B, N, d // 2, dtype=torch.uint8, device="cuda")
+    cache_s = torch.zeros(B, N, d // 32, dtype=torch.uint8, device="cuda")
+    cache_k = torch.zeros(B, N, di, dtype=torch.uint8, device="cuda")
+    x = synth.normal((B, d), 7)
+    kx = synth.normal((B, di), 8) * 100  # reach the E4M3 saturation
+    csa2.quantize_fp4(dev(x), cache_c[:, N - 1], cache_s[:, N - 1], dev(kx), cache_k[:, N - 1])
+    rc, rs = orc.quantize_fp4(f64(x))
+    assert np.array_equal(cache_c[:, N - 1].cpu().numpy(), rc)
+    assert np.array_equal(cache_s[:, N - 1].cpu().numpy(), rs)
+    assert np.array_equal(cache_k[:, N - 1].cpu().numpy(), orc.cast_e4m3(f64(kx)))
+    assert int(cache_c[:, : N - 1].sum()) == 0 and int(cache_k[:, : N - 1].sum()) == 0
+
+
+def test_cast_e4m3_every_bf16_pattern(csa2, orc):
+    bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    v = bits[torch.isfinite(bits.float())]
+    v = v[: (v.numel() // 128) * 128].reshape(-1, 128)
+    x = torch.zeros(v.shape[0], 32, dtype=torch.bfloat16)
+    _, _, k8 = csa2.quantize_fp4(dev(x), idxk=dev(v))
+    assert np.array_equal(k8.cpu().numpy(), orc.cast_e4m3(f64(v)))
+
+
+# ---------------------------------------------------------- a2 indexer-Q quant
+
+def test_quantize_index_q_bit_exact(csa2, orc):
+    nq, hi, di = 12, 64, 128
+    q = synth.normal((nq, hi, di), 11, dtype=torch.float32)
+    mag = torch.exp2(torch.randint(-140, 100, (nq, hi, 1),
+                                   generator=torch.Generator().manual_seed(12)).float())
+    q = (q * mag).to(torch.bfloat16)
+    q[0, 0] = 0.0
+    q[0, 1, 3] = 448.0
+    q[0, 2, 3] = 450.0
+    w = synth.uniform((nq, hi), 13, scale=1 / 64)
+    q8, c = csa2.quantize_index_q(dev(q), dev(w))
+    rq8, rc = orc.quantize_index_q(f64(q), f64(w))
+    assert np.array_equal(q8.cpu().numpy(), rq8)
+    assert np.array_equal(c.cpu().double().numpy(), rc)
+
+
+# ------------------------------------------------------------- a3 index score
+
+def test_index_score_f32_tiny(csa2, orc):
+    w_ = synth.TINY
+    q = synth.index_q(w_, 20)
+    w = synth.index_w(w_, 21)
+    k = synth.index_k_rows(w_, 22)
+    s = csa2.index_score(dev(q), dev(w), dev(k))
+    ref = orc.index_score(f64(q), f64(w), f64(k))
+    assert score_close(s.cpu().numpy(), ref) <= 1.0
+
+
+@pytest.mark.parametrize("B,n", [(2, 1000), (3, 4096), (1, 128), (1, 77)])
+def test_index_score_fp8_decode(csa2, orc, B, n):
+    wl = synth.scaled(synth.C128K, B=B, N=n)
+    q = synth.index_q(wl, 30 + n)
+    w = synth.index_w(wl, 31 + n)
+    kb = synth.index_k_rows(wl, 32 + n)
+    x = torch.zeros(B * n, 32, dtype=torch.bfloat16, device="cuda")
+    _, _, k8 = csa2.quantize_fp4(x, idxk=dev(kb.reshape(B * n, 128)))
+    k8 = k8.reshape(B, n, 128)
+    s = csa2.index_score(dev(q), dev(w), k8)
+    ref = orc.index_score_fp8(f64(q), f64(w), orc.cast_e4m3(f64(kb)))
+    assert score_close(s.cpu().numpy(), ref) <= 1.0
+
+
+def test_index_score_fp8_prefill_causal(csa2, orc):
+    # 8 queries of one sequence at the end of a 4x-compressed context
+    wl = synth.scaled(synth.PREFILL, q_per_seq=8, N=700, pos0=4 * 700 - 8)
+    q = synth.index_q(wl, 40)
+    w = synth.index_w(wl, 41)
+    kb = synth.index_k_rows(wl, 42)
+    nv = synth.prefill_n_valid(wl)
+    assert int(nv.min()) < 700 and int(nv.max()) == 700
+    x = torch.zeros(700, 32, dtype=torch.bfloat16, device="cuda")
+    _, _, k8 = csa2.quantize_fp4(x, idxk=dev(kb.reshape(700, 128)))
+    s = csa2.index_score(dev(q), dev(w), k8.reshape(1, 700, 128), q_per_seq=8, n_valid=dev(nv))
+    ref = orc.index_score_fp8(f64(q), f64(w), orc.cast_e4m3(f64(kb)), q_per_seq=8,
+                              n_valid=nv.numpy())
+    assert score_close(s.cpu().numpy(), ref) <= 1.0
+
+
+def test_index_score_fp8_exact_small_integers(csa2, orc):
+    # q and k with small-integer E4M3 values (q8 in {0, +-64, 448}, k in
+    # {0, +-1}): every product and partial sum is an integer below 2^14, so
+    # the tensor-core path must reproduce the oracle exactly
+    B, n = 1, 256
+    g = torch.Generator().manual_seed(50)
+    q = torch.randint(-1, 2, (1, 64, 128), generator=g).to(torch.bfloat16)
+    q[0, :, 0] = 7  # fixes every head's scale at 2^-6 (amax 7)
+    w = torch.full((1, 64), 1.0 / 64)
+    kb = torch.randint(-1, 2, (n, 128), generator=g).to(torch.bfloat16)
+    x = torch.zeros(n, 32, dtype=torch.bfloat16, device="cuda")
+    _, _, k8 = csa2.quantize_fp4(x, idxk=dev(kb))
+    s = csa2.index_score(dev(q), dev(w), k8.reshape(1, n, 128))
+    ref = orc.index_score_fp8(f64(q), f64(w), orc.cast_e4m3(f64(kb)).reshape(1, n, 128))
+    assert np.array_equal(s.cpu().double().numpy(), ref)
+
+
+# -------------------------------------------------------------------- a4 top-k
+
+@pytest.mark.parametrize("rows,n,k,levels", [
+    (3, 5000, 64, 0), (4, 4096, 512, 0), (5, 3000, 512, 40), (2, 262144, 512, 0),
+    (2, 70000, 512, 3), (6, 1000, 2048, 0), (1, 100, 512, 0), (9, 1, 1, 0)])
+def test_topk_bit_exact(csa2, orc, rows, n, k, levels):
+    s = synth.scores_with_ties(rows, n, seed=60 + rows + k, levels=levels)
+    g = torch.Generator().manual_seed(61)
+    nv = torch.randint(0, n + 1, (rows,), generator=g).int()
+    nv[0] = n
+    got = csa2.topk(dev(s), k, n_valid=dev(nv))
+    ref = orc.topk(f64(s), k, nv.numpy())
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_topk_degenerate_rows(csa2, orc):
+    n, k = 20000, 512
+    s = torch.zeros(6, n)
+    s[1] = 1.0                                   # all equal: lowest indices win
+    s[2, ::2] = -0.0                             # signed zeros compare equal
+    s[3, 5000:] = 2.0                            # a run of 15000 equal maxima
+    s[4] = torch.arange(n).float().flip(0)       # strictly decreasing
+    s[5] = -torch.inf
+    s[5, 17] = 3.0
+    got = csa2.topk(dev(s), k)
+    ref = orc.topk(f64(s), k)
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_topk_strided_rows(csa2, orc):
+    s = synth.scores_with_ties(4, 3000, seed=70)
+    big = torch.full((4, 3100), 99.0)
+    big[:, :3000] = s
+    out = torch.full((4, 600), -7, dtype=torch.int32, device="cuda")
+    csa2.topk(dev(big)[:, :3000], 512, out=out[:, :512])
+    assert np.array_equal(out[:, :512].cpu().numpy(), orc.topk(f64(s), 512))
+    assert int((out[:, 512:] != -7).sum()) == 0
+
+
+# -------------------------------------------------------- a5 sparse attention
+
+def make_cache(csa2, B, n, d, seed):
+    x = synth.normal((B * n, d), seed)
+    codes, scales = csa2.quantize_fp4(dev(x))
+    return (codes.reshape(B, n, d // 2), scales.reshape(B, n, d // 32))
+
+
+def oracle_cache(orc, B, n, d, seed):
+    x = synth.normal((B * n, d), seed)
+    c, s = orc.quantize_fp4(f64(x))
+    return c.reshape(B, n, d // 2), s.reshape(B, n, d // 32)
+
+
+def test_attn_f32_tiny(csa2, orc):
+    wl = synth.TINY
+    codes, scales = make_cache(csa2, 1, wl.N, wl.D, 80)
+    rc, rs = oracle_cache(orc, 1, wl.N, wl.D, 80)
+    q = synth.attn_q(wl, 81)
+    idx = synth.random_indices(1, wl.k, wl.N, 82, pad=5)
+    win = synth.window_rows(wl, 83)
+    scale = 1 / math.sqrt(wl.D)
+    out = csa2.sparse_attn(dev(q), codes, scales, dev(idx), dev(win), scale)
+    ref = orc.sparse_attn(f64(q), rc, rs, idx.numpy(), f64(win), scale)
+    assert rel_l2(out.cpu().numpy(), ref) <= 2e-3
+
+
+@pytest.mark.parametrize("nq,hq,n,k,W", [(3, 64, 2000, 512, 128), (2, 16, 300, 64, 7),
+                                          (1, 32, 50, 8, 0), (2, 16, 600, 512, 128)])
+def test_attn_bf16(csa2, orc, nq, hq, n, k, W):
+    d = 512
+    codes, scales = make_cache(csa2, nq, n, d, 90 + n)
+    rc, rs = oracle_cache(orc, nq, n, d, 90 + n)
+    q = synth.normal((nq, hq, d), 91)
+    idx = synth.random_indices(nq, k, n, 92, pad=min(k, 13))
+    win = synth.normal((nq, max(W, 1), d), 93)[:, :W]
+    scale = 1 / math.sqrt(d)
+    out = csa2.sparse_attn(dev(q), codes, scales, dev(idx), dev(win).contiguous(), scale)
+    ref = orc.sparse_attn(f64(q), rc, rs, idx.numpy(), f64(win), scale)
+    assert rel_l2(out.cpu().numpy(), ref) <= 2e-3
+
+
+def test_attn_bf16_prefill_windows(csa2, orc):
+    # 6 queries of one sequence; query t attends window rows t .. t + W - 1
+    T, W, n, k, d, hq = 6, 5, 400, 64, 512, 16
+    codes, scales = make_cache(csa2, 1, n, d, 95)
+    rc, rs = oracle_cache(orc, 1, n, d, 95)
+    q = synth.normal((T, hq, d), 96)
+    idx = synth.random_indices(T, k, n, 97, pad=3)
+    win = synth.normal((1, T + W - 1, d), 98)
+    ws = torch.arange(T, dtype=torch.int32)
+    wl = torch.tensor([W, W, 2, 0, W, 1], dtype=torch.int32)
+    out = csa2.sparse_attn(dev(q), codes, scales, dev(idx), dev(win), 0.05, q_per_seq=T,
+                           win_start=dev(ws), win_len=dev(wl), win_max=W)
+    ref = orc.sparse_attn(f64(q), rc, rs, idx.numpy(), f64(win), 0.05, q_per_seq=T,
+                          win_start=ws.numpy(), win_len=wl.numpy())
+    assert rel_l2(out.cpu().numpy(), ref) <= 2e-3
+
+
+def test_attn_bounds_flag(csa2):
+    d, n = 512, 100
+    codes, scales = make_cache(csa2, 1, n, d, 99)
+    q = dev(synth.normal((1, 16, d), 100))
+    idx = torch.tensor([[3, 5, n, -2, 7, -1]], dtype=torch.int32, device="cuda")
+    win = dev(synth.normal((1, 4, d), 101))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = csa2.sparse_attn(q, codes, scales, idx, win, 0.04, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & csa2.DEVFLAG_BOUNDS
+    assert torch.isfinite(out).all()
