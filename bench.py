@@ -350,7 +350,7 @@ def cpu_baseline(wl, budget_s):
             L = layers[l]
             if m in (0, 1):
                 q8, c = q8c[l]
-                sc = orc.index_score(table[q8], c, kd[None])
+                sc = orc.index_score(table[q8], c, kd)
                 idx = orc.topk(sc, wl.k)
             sel = idx[0][idx[0] >= 0]
             c_rows, s_rows = orc.quantize_fp4(

@@ -101,7 +101,9 @@ def test_quantize_index_q_bit_exact(csa2, orc):
     q8, c = csa2.quantize_index_q(dev(q), dev(w))
     rq8, rc = orc.quantize_index_q(f64(q), f64(w))
     assert np.array_equal(q8.cpu().numpy(), rq8)
-    assert np.array_equal(c.cpu().double().numpy(), rc)
+    # c is an fp32 output: the oracle's exact w * sigma rounded to fp32 (they
+    # differ from the exact value only where w * sigma is an fp32 subnormal)
+    assert np.array_equal(c.cpu().numpy(), rc.astype(np.float32))
 
 
 # ------------------------------------------------------------- a3 index score
