@@ -221,6 +221,32 @@ csa2_status csa2_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
                       csa2_stream_t stream);
 
+/*
+ * csa2_topk_noalloc: the same selection as csa2_topk, for callers that
+ * cannot allocate device memory -- for example code running inside an
+ * allocator callback, a plugin whose host framework owns every device
+ * allocation, or a process that must not grow its memory footprint after
+ * start-up.  The pages have no counterpart to this entry point; it exists
+ * only for those callers.
+ *
+ * The caller still passes the scores and idx_out buffers; the selector's
+ * scratch comes from one fixed 4 MiB array compiled into the library, which
+ * every GPU that loads the library keeps until the process exits.  Limit:
+ * rows * csa2_topk_workspace_bytes(1, n, k) must not exceed 4 MiB (at
+ * k = 512 that is 61 rows); larger calls return CSA2_ERR_WORKSPACE and
+ * enqueue nothing.  The call allocates nothing (no cudaMalloc / cudaFree).
+ * The first call on a device looks up the array's device address for that
+ * device (with that device current), so make that first call before any
+ * stream capture.  Every call shares the one array: calls that may overlap
+ * on the GPU (different streams, or different host threads) race and give
+ * wrong results; serialise them.  The parts of the array that must start at
+ * zero are cleared by each call, so a call never sees a previous call's data.
+ * Other arguments and errors as for csa2_topk.
+ */
+csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int64_t n, int64_t ld,
+                              const int32_t* n_valid, int32_t k, int32_t* idx_out,
+                              int64_t idx_ld, int32_t* dev_status, csa2_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* a5: sparse attention over gathered FP4 rows + the bf16 sliding window     */
 /* ------------------------------------------------------------------------ */

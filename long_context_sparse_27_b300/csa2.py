@@ -78,6 +78,8 @@ EXPORTS = {
     "csa2_topk_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i32]),
     "csa2_topk": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_p, _c_sz,
                            _c_p, _c_p]),
+    "csa2_topk_noalloc": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_i32, _c_p, _c_i64,
+                                   _c_p, _c_p]),
     "csa2_sparse_attn_workspace_bytes": (_c_sz, [ctypes.POINTER(AttnArgs)]),
     "csa2_sparse_attn": (_c_i32, [ctypes.POINTER(AttnArgs), _c_p]),
     "csa2_validate_plan": (_c_i32, [ctypes.POINTER(LayerDesc), _c_i32, ctypes.POINTER(_c_i32)]),
@@ -227,6 +229,19 @@ def topk(scores, k, n_valid=None, out=None, workspace=None, dev_status=None):
     _check(lib.csa2_topk(_ptr(scores), rows, n, scores.stride(0), _ptr(n_valid), k, _ptr(out),
                          out.stride(0), _aligned_ptr(ws), need, _ptr(dev_status), _stream()),
            "csa2_topk")
+    return out
+
+
+def topk_noalloc(scores, k, n_valid=None, out=None, dev_status=None):
+    """As topk(), for callers that cannot allocate device memory: the scratch
+    is a fixed array inside the library (see csa2_topk_noalloc); only `out`
+    is allocated here when not given."""
+    rows, n = scores.shape
+    if out is None:
+        out = torch.empty(rows, k, dtype=torch.int32, device=scores.device)
+    _check(lib.csa2_topk_noalloc(_ptr(scores), rows, n, scores.stride(0), _ptr(n_valid), k,
+                                 _ptr(out), out.stride(0), _ptr(dev_status), _stream()),
+           "csa2_topk_noalloc")
     return out
 
 

@@ -19,6 +19,8 @@
 // A row whose threshold bins overflow the candidate buffers (huge runs of
 // equal scores) is finished by an exact 8-pass radix select over its
 // 64-bit (key, ~index) values inside topk_final_kernel.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -354,3 +356,51 @@ csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld
 }
 
 }  // namespace csa2
+
+// ===========================================================================
+// Variant without allocation: the scratch lives in the library itself, for
+// callers that cannot allocate device memory.  All calls share this array.
+// ===========================================================================
+
+namespace csa2 {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;  // 4 MiB per device
+static __device__ __align__(256) uint8_t g_topk_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array, looked up once per device (host code cannot
+// use the array's name as a device pointer).
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+}  // namespace
+}  // namespace csa2
+
+extern "C" csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int64_t n,
+                                         int64_t ld, const int32_t* n_valid, int32_t k,
+                                         int32_t* idx_out, int64_t idx_ld, int32_t* dev_status,
+                                         csa2_stream_t stream) {
+  using namespace csa2;
+  if (rows < 0 || n < 0 || k < 1 || idx_ld < k || ld < n) return CSA2_ERR_INVALID_ARG;
+  if (k > kMaxK || n >= ((int64_t)1 << 31)) return CSA2_ERR_UNSUPPORTED;
+  if (rows == 0) return CSA2_OK;
+  if (!idx_out || (n > 0 && !scores)) return CSA2_ERR_INVALID_ARG;
+  if (topk_workspace_bytes(rows, n, k) > kNoAllocScratchBytes) return CSA2_ERR_WORKSPACE;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return CSA2_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      e = cudaGetSymbolAddress(&scratch, g_topk_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_fail(e);
+      g_noalloc_ptr[dev] = scratch;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // launch_topk clears the histograms and counters of every row it uses
+  return launch_topk(scores, rows, n, ld, n_valid, k, idx_out, idx_ld, scratch, dev_status,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
