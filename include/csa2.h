@@ -165,8 +165,8 @@ csa2_status csa2_quantize_index_q(const void* q, const float* w, int64_t nq, int
  *     (w' = c, into the workspace), then scored by an FP8 tcgen05
  *     tensor-core kernel (hi == 64, di == 128).
  *   q E4M3 + k E4M3: q is already quantised (the q8 of
- *     csa2_quantize_index_q) and w holds the folded weights c; only the
- *     tensor-core kernel runs (no workspace).
+ *     csa2_quantize_index_q) and w holds the folded weights c (16-byte
+ *     aligned); only the tensor-core kernel runs (no workspace).
  *
  * k       device, row j of sequence b at k + b * k_seq_stride + j * k_ld
  *         (elements); E4M3 needs k, k_ld, k_seq_stride 16-byte aligned.
@@ -212,7 +212,10 @@ csa2_status csa2_index_score(const csa2_index_args* args, csa2_stream_t stream);
  *
  * scores  device f32, row r at scores + r * ld;  n_valid optional [rows]
  * idx_out device int32, row r at idx_out + r * idx_ld
- * 1 <= k <= 2048.  Workspace: csa2_topk_workspace_bytes(rows, n, k).
+ * 1 <= k <= 2048.  Workspace: csa2_topk_workspace_bytes(rows, n, k) =
+ * rows * 16 KiB (one 4096-bin histogram per row, cleared by the call).
+ * Kernels: a histogram pass over the scores, then one selection kernel with
+ * a cluster of 8 CTAs per row (each owning 1/8 of the row).
  * Errors: INVALID_ARG, UNSUPPORTED (k > 2048), WORKSPACE, CUDA.
  */
 size_t csa2_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k);
@@ -232,9 +235,8 @@ csa2_status csa2_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
  * The caller still passes the scores and idx_out buffers; the selector's
  * scratch comes from one fixed 4 MiB array compiled into the library, which
  * every GPU that loads the library keeps until the process exits.  Limit:
- * rows * csa2_topk_workspace_bytes(1, n, k) must not exceed 4 MiB (at
- * k = 512 that is 61 rows); larger calls return CSA2_ERR_WORKSPACE and
- * enqueue nothing.  The call allocates nothing (no cudaMalloc / cudaFree).
+ * rows * csa2_topk_workspace_bytes(1, n, k) must not exceed 4 MiB (that is
+ * 256 rows); larger calls return CSA2_ERR_WORKSPACE and enqueue nothing.  The call allocates nothing (no cudaMalloc / cudaFree).
  * The first call on a device looks up the array's device address for that
  * device (with that device current), so make that first call before any
  * stream capture.  Every call shares the one array: calls that may overlap
@@ -262,7 +264,10 @@ csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int64_t n, int6
  *
  * Paths: q F32 (hq <= 64, d <= 256; CUDA cores) or q BF16 (hq % 16 == 0,
  * d == 512; bf16 tensor-core MMA, fp32 accumulation, probabilities split
- * into two bf16 terms).
+ * into two bf16 terms).  The BF16 path cuts the k + win_max keys of a query
+ * into chunks of 80; with at most 8 chunks (k + win_max <= 640) the chunks
+ * of a query are merged on chip and the call needs no workspace, otherwise
+ * it needs csa2_sparse_attn_workspace_bytes of it.
  * q        device [nq, hq, d] contiguous
  * codes    device u8: row j of sequence b at codes + b*codes_seq_stride + j*codes_ld
  * scales   device u8: likewise with scales_seq_stride / scales_ld
@@ -273,8 +278,8 @@ csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int64_t n, int6
  * out      device f32 [nq, hq, d]
  * An index outside [-1, n) is skipped and raises CSA2_DEVFLAG_BOUNDS; a
  * window range outside [0, w_rows) is clipped the same way.
- * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT (codes rows 16-byte aligned,
- *         window rows 16-byte aligned), WORKSPACE, CUDA.
+ * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT (BF16 path: codes, scales
+ *         and window rows 16-byte aligned), WORKSPACE, CUDA.
  */
 typedef struct csa2_attn_args {
   const void* q;

@@ -117,7 +117,7 @@ csa2_status check_index(const csa2_index_args* a) {
       return CSA2_ERR_ALIGNMENT;
     if (!aligned(a->q, 16)) return CSA2_ERR_ALIGNMENT;
     if (a->n > (int64_t)1 << 31 || nq * a->hi > (int64_t)1 << 31) return CSA2_ERR_UNSUPPORTED;
-    if (a->q_dtype == CSA2_E4M3) return CSA2_OK;
+    if (a->q_dtype == CSA2_E4M3) return aligned(a->w, 16) ? CSA2_OK : CSA2_ERR_ALIGNMENT;
     if (!a->workspace || a->workspace_bytes < index_ws(a)) return CSA2_ERR_WORKSPACE;
     if (!aligned(a->workspace, 256)) return CSA2_ERR_ALIGNMENT;
     return CSA2_OK;
@@ -129,17 +129,19 @@ csa2_status check_index(const csa2_index_args* a) {
   return CSA2_ERR_UNSUPPORTED;
 }
 
-csa2_status run_index(const csa2_index_args& a, cudaStream_t s) {
+// hist1 (nullable): first-level top-k histograms the decode FP8 kernel adds
+// the scores' keys to (index_fuses_topk_hist).
+csa2_status run_index(const csa2_index_args& a, uint32_t* hist1, cudaStream_t s) {
   if (a.B * a.q_per_seq == 0 || a.n == 0) return CSA2_OK;
   if (!fp8_path(&a)) return launch_index_score_f32(a, s);
   if (a.q_dtype == CSA2_E4M3)
-    return launch_index_score_fp8(a, static_cast<const uint8_t*>(a.q), a.w, s);
+    return launch_index_score_fp8(a, static_cast<const uint8_t*>(a.q), a.w, hist1, s);
   const int64_t nq = a.B * a.q_per_seq;
   uint8_t* q8 = static_cast<uint8_t*>(a.workspace);
   float* c = reinterpret_cast<float*>(q8 + align256((size_t)nq * a.hi * a.di));
   csa2_status st = launch_quantize_index_q(a.q, a.w, nq, a.hi, a.di, q8, c, s);
   if (st != CSA2_OK) return st;
-  return launch_index_score_fp8(a, q8, c, s);
+  return launch_index_score_fp8(a, q8, c, hist1, s);
 }
 
 csa2_status check_topk(const float* scores, int64_t rows, int64_t n, int64_t ld, int32_t k,
@@ -176,7 +178,8 @@ csa2_status check_attn(const csa2_attn_args* a) {
   if (a->nq > 65535) return CSA2_ERR_UNSUPPORTED;
   if (!aligned(a->q, 16)) return CSA2_ERR_ALIGNMENT;
   if (a->k > 0 && (!aligned(a->codes, 16) || a->codes_ld % 16 != 0 ||
-                   a->codes_seq_stride % 16 != 0))
+                   a->codes_seq_stride % 16 != 0 || !aligned(a->scales, 16) ||
+                   a->scales_ld % 16 != 0 || a->scales_seq_stride % 16 != 0))
     return CSA2_ERR_ALIGNMENT;
   if (a->window && (!aligned(a->window, 16) || a->win_ld % 8 != 0 || a->win_seq_stride % 8 != 0))
     return CSA2_ERR_ALIGNMENT;
@@ -366,7 +369,7 @@ csa2_status csa2_index_score(const csa2_index_args* args, csa2_stream_t stream) 
   csa2_status st = check_index(args);
   if (st != CSA2_OK) return st;
   if ((st = injected("index_score")) != CSA2_OK) return st;
-  return run_index(*args, reinterpret_cast<cudaStream_t>(stream));
+  return run_index(*args, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t csa2_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k) {
@@ -432,7 +435,7 @@ csa2_status csa2_validate_plan(const csa2_layer_desc* L, int32_t n_layers, int32
 size_t csa2_layer_stack_workspace_bytes(const csa2_stack_args* s) {
   if (!s) return 0;
   StackPieces p = stack_pieces(*s);
-  return p.scores + std::max(p.ix, std::max(p.tk, p.at));
+  return p.scores + p.tk + std::max(p.ix, p.at);
 }
 
 csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
@@ -440,13 +443,16 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
   csa2_status st = csa2_validate_plan(L, n_layers, nullptr);
   if (st != CSA2_OK) return st;
   if (!s || s->B < 1 || s->q_per_seq < 1 || s->n < 1 || s->k < 1) return CSA2_ERR_INVALID_ARG;
+  // workspace: scores | per-row top-k histograms | scratch of the index
+  // (quantised Q) or attention (chunk partials) step
   const StackPieces p = stack_pieces(*s);
-  const size_t need = p.scores + std::max(p.ix, std::max(p.tk, p.at));
+  const size_t need = p.scores + p.tk + std::max(p.ix, p.at);
   if (!s->workspace || s->workspace_bytes < need) return CSA2_ERR_WORKSPACE;
   if (!aligned(s->workspace, 256)) return CSA2_ERR_ALIGNMENT;
   float* scores = static_cast<float*>(s->workspace);
-  void* scratch = static_cast<uint8_t*>(s->workspace) + p.scores;
-  const size_t scratch_bytes = s->workspace_bytes - p.scores;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(s->workspace) + p.scores);
+  void* scratch = static_cast<uint8_t*>(s->workspace) + p.scores + p.tk;
+  const size_t scratch_bytes = s->workspace_bytes - p.scores - p.tk;
   const int64_t nq = s->B * s->q_per_seq;
   // check every call's arguments before anything is enqueued
   for (int32_t l = 0; l < n_layers; ++l) {
@@ -463,8 +469,8 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
       if (!d.topk_idx) return CSA2_ERR_INVALID_ARG;
       csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
       if ((st = check_index(&ia)) != CSA2_OK) return st;
-      if ((st = check_topk(scores, nq, s->n, s->n, s->k, d.topk_idx, s->k, scratch,
-                           scratch_bytes)) != CSA2_OK)
+      if ((st = check_topk(scores, nq, s->n, s->n, s->k, d.topk_idx, s->k, hist, p.tk)) !=
+          CSA2_OK)
         return st;
     }
     const int32_t* idx = L[d.mode == CSA2_MODE_REUSE ? d.idx_src : l].topk_idx;
@@ -481,9 +487,16 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
     }
     if (d.mode != CSA2_MODE_REUSE) {
       csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
-      if ((st = run_index(ia, cs)) != CSA2_OK) return st;
-      if ((st = launch_topk(scores, nq, s->n, s->n, s->n_valid, s->k, d.topk_idx, s->k, scratch,
-                            s->dev_status, cs)) != CSA2_OK)
+      // decode: the indexer kernel also builds the top-k's first-level
+      // histograms; otherwise a histogram pass over the scores does
+      const bool fused = index_fuses_topk_hist(ia);
+      if ((st = clear_topk_hist(hist, nq, cs)) != CSA2_OK) return st;
+      if ((st = run_index(ia, fused ? hist : nullptr, cs)) != CSA2_OK) return st;
+      if (!fused &&
+          (st = launch_topk_hist(scores, nq, s->n, s->n, s->n_valid, hist, cs)) != CSA2_OK)
+        return st;
+      if ((st = launch_topk_select(scores, nq, s->n, s->n, s->n_valid, s->k, hist, d.topk_idx,
+                                   s->k, cs)) != CSA2_OK)
         return st;
     }
     const int32_t* idx = L[d.mode == CSA2_MODE_REUSE ? d.idx_src : l].topk_idx;

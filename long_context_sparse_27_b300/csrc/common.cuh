@@ -66,6 +66,20 @@ __device__ __forceinline__ uint32_t e4m3_encode(float x) {
 }
 
 // ---------------------------------------------------------------------------
+// top-k keys and histograms
+// ---------------------------------------------------------------------------
+
+// Order-preserving 32-bit key of a score: a larger float gives a larger key;
+// -0 maps like +0 (the two compare equal).
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+constexpr int kTopkBins = 4096;  // first-level digit: the key's top 12 bits
+
+// ---------------------------------------------------------------------------
 // device status
 // ---------------------------------------------------------------------------
 
@@ -277,6 +291,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// cp.async (16-byte global -> shared copies, completion per thread)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------

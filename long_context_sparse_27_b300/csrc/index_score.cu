@@ -10,11 +10,13 @@
 //  * idx_score_tc_kernel   E4M3 q8 / k on tcgen05 tensor cores.  Per tile of
 //    128 entries: D[128 x 64*QG] = K_tile[128 x 128] . Q8[64*QG x 128]^T in
 //    tensor memory, then an epilogue applies ReLU, the head weights c and the
-//    head sum.  Warp 0 streams K tiles with TMA into an 8-deep ring of 16 KB
-//    stages, warp 1 issues the MMAs, warps 2-5 drain the double-buffered
-//    accumulator.  In decode (QG = 1) the kernel is a stream over the
-//    indexer keys (128 B per entry) and is bound by HBM; in a prefill chunk
-//    (QG = 4, 4 queries x 64 heads per MMA) it is a dense contraction.
+//    head sum.  Warp 0 streams K tiles with TMA into a ring of 16 KB stages,
+//    warp 1 issues the MMAs into a ring of NACC tensor-memory accumulators,
+//    and two epilogue warpgroups (warps 2-5 and 6-9) drain alternate tiles,
+//    so two warps per SM sub-partition hide each other's tcgen05.ld and FMA
+//    latency.  In decode (QG = 1) the kernel is a stream over the indexer
+//    keys (128 B per entry) and is bound by HBM; in a prefill chunk (QG = 4,
+//    4 queries x 64 heads per MMA) it is a dense contraction.
 #include <cstdio>
 
 #include "common.cuh"
@@ -94,26 +96,41 @@ namespace {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
 
 template <int QG>
+struct TcCfgDefault {
+  static constexpr int EPI_WGS = QG == 1 ? 4 : 2;  // epilogue warpgroups
+};
+
+template <int QG, int EPI_WGS_ = TcCfgDefault<QG>::EPI_WGS>
 struct TcCfg {
   static constexpr int BM = 128;        // entries per tile (MMA M)
   static constexpr int BN = 64 * QG;    // 64 heads x QG queries (MMA N)
   static constexpr int BK = 128;        // indexer dim: 128 E4M3 bytes per row
   static constexpr int STAGES = QG == 1 ? 8 : 6;
+  static constexpr int EPI_WGS = EPI_WGS_;
+  static constexpr int NACC = QG == 1 ? EPI_WGS : 2;  // accumulators in tensor memory
   static constexpr int KTILE = BM * BK;  // 16 KB
   static constexpr int QTILE = BN * BK;  // 8 KB or 32 KB
-  static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int EPI_WARPS = 4;
+  static constexpr int TMEM_USED = NACC * BN;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
+                                 : TMEM_USED <= 256 ? 256 : 512;  // power of two
+  static constexpr int EPI_WARPS = 4 * EPI_WGS;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   // shared memory carve-up (offsets from a 1024-byte aligned base)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_Q = OFF_K + STAGES * KTILE;
   static constexpr int OFF_C = OFF_Q + 2 * QTILE;             // float [EPI_WARPS][2][BN]
-  static constexpr int OFF_BAR = OFF_C + EPI_WARPS * 2 * BN * 4;
-  // barriers: full[S], empty[S], qfull[2], qempty[2], tfull[2], tempty[2], fin
-  static constexpr int NBAR = 2 * STAGES + 9;
+  // fused first-level top-k histogram (decode): two group slots of 4096 bins
+  static constexpr int OFF_H = OFF_C + EPI_WARPS * 2 * BN * 4;
+  static constexpr int HIST_BYTES = QG == 1 ? 2 * kTopkBins * 4 : 0;
+  static constexpr int OFF_BAR = OFF_H + HIST_BYTES;
+  // barriers: full[S], empty[S], qfull[2], qempty[2], tfull[NACC], tempty[NACC], fin
+  static constexpr int NBAR = 2 * STAGES + 4 + 2 * NACC + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem slot, abort flag
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
+  static_assert(NACC % EPI_WGS == 0, "accumulator a is drained by warpgroup a % EPI_WGS");
+  static_assert(TMEM_USED <= 512, "tensor memory holds 512 columns");
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory per CTA");
 };
 
 struct TcParams {
@@ -126,13 +143,28 @@ struct TcParams {
   int64_t groups;          // nq / QG
   int64_t ktiles;          // ceil(n / 128)
   int32_t* dev_status;
+  uint32_t* hist1;         // QG = 1: [nq][4096] first-level top-k histograms to add to, or null
 };
 
-template <int QG>
-__global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
+// (group, tile within the group) of the CTA's tiles, advanced without
+// 64-bit divisions: tile t is group t / ktiles, tile t % ktiles.
+struct TileCursor {
+  int64_t g, kt, ktiles;
+  __device__ TileCursor(int64_t t, int64_t ktiles_) : g(t / ktiles_), kt(t % ktiles_), ktiles(ktiles_) {}
+  __device__ void advance(int64_t by) {
+    kt += by;
+    while (kt >= ktiles) {
+      kt -= ktiles;
+      ++g;
+    }
+  }
+};
+
+template <int QG, int EPI_WGS>
+__global__ void __launch_bounds__(TcCfg<QG, EPI_WGS>::THREADS, 1)
     idx_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap qmap, const TcParams p) {
-  using C = TcCfg<QG>;
+  using C = TcCfg<QG, EPI_WGS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -145,8 +177,9 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
   uint64_t* qfull = bars + 2 * C::STAGES;
   uint64_t* qempty = qfull + 2;
   uint64_t* tfull = qempty + 2;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* fin = tempty + 2;
+  uint64_t* tempty = tfull + C::NACC;
+  uint64_t* fin = tempty + C::NACC;
+  uint32_t* hslot = reinterpret_cast<uint32_t*>(smem + C::OFF_H);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -163,8 +196,10 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
+    }
+    for (int i = 0; i < C::NACC; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], C::EPI_WARPS);
+      mbar_init(&tempty[i], 4);  // the 4 warps of one warpgroup
     }
     mbar_init(fin, 1);
     *abort_flag = 0;
@@ -173,6 +208,10 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
     tma_prefetch_desc(&qmap);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if constexpr (QG == 1) {
+    for (int i = threadIdx.x; i < 2 * kTopkBins; i += C::THREADS) hslot[i] = 0;
+  }
+  const int64_t g_first = total > 0 ? t_begin / p.ktiles : 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -180,15 +219,16 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
+    if (lane == 0 && t_begin < t_end) {
       const uint64_t pol_k = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
       int stage = 0;
       uint32_t ph = 0;
       int64_t g_prev = -1, qcount = 0, issued = 0;
       bool ok = true;
-      for (int64_t t = t_begin; t < t_end && ok; ++t) {
-        const int64_t g = t / p.ktiles, kt = t % p.ktiles;
+      TileCursor cur(t_begin, p.ktiles);
+      for (int64_t t = t_begin; t < t_end; ++t, cur.advance(1)) {
+        const int64_t g = cur.g, kt = cur.kt;
         if (g != g_prev) {
           const int qs = (int)(qcount & 1);
           const uint32_t qph = (uint32_t)((qcount >> 1) & 1);
@@ -231,15 +271,16 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    if (lane == 0 && t_begin < t_end) {
       constexpr uint32_t idesc = idesc_e4m3_f32(C::BM, C::BN);
       int stage = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       int64_t g_prev = -1, qcount = 0;
       int qs = 0;
       bool any = false;
-      for (int64_t t = t_begin; t < t_end; ++t) {
-        const int64_t g = t / p.ktiles;
+      TileCursor cur(t_begin, p.ktiles);
+      for (int64_t t = t_begin; t < t_end; ++t, cur.advance(1)) {
+        const int64_t g = cur.g;
         if (g != g_prev) {
           if (g_prev >= 0) tc_commit(&qempty[qs]);  // old Q free once its MMAs finish
           qs = (int)(qcount & 1);
@@ -266,7 +307,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
           stage = 0;
           ph ^= 1;
         }
-        if (++acc == 2) {
+        if (++acc == C::NACC) {
           acc = 0;
           aph ^= 1;
         }
@@ -280,19 +321,22 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
     }
   } else {
     // ---------------- epilogue ----------------
-    const int ew = warp - 2;         // 0..3
-    const int lq = warp & 3;        // TMEM lane quarter this warp may access
-    const int row = lq * 32 + lane;  // entry within the tile
-    int acc = 0;
-    uint32_t aph = 0;
+    // warpgroup wg drains the tiles with local number li = wg, wg + EPI_WGS,
+    // ...; tile li sits in accumulator li % NACC.
+    const int ew = warp - 2;          // 0 .. EPI_WARPS-1
+    const int wg = ew >> 2;
+    const int lq = warp & 3;          // TMEM lane quarter this warp may access
+    const int row = lq * 32 + lane;   // entry within the tile
     int64_t g_prev = -1;
-    // each epilogue warp keeps its own copy of the group's head weights
-    // (double-buffered), so the warps never wait on one another
+    // each warp keeps its own double-buffered copy of the group's head weights
     float* my_c = cbuf + ew * 2 * C::BN;
     int cb = 1;
     int64_t nv[QG];
-    for (int64_t t = t_begin; t < t_end; ++t) {
-      const int64_t g = t / p.ktiles, kt = t % p.ktiles;
+    TileCursor cur(t_begin + wg, p.ktiles);
+    for (int64_t li = wg; t_begin + li < t_end; li += C::EPI_WGS, cur.advance(C::EPI_WGS)) {
+      const int64_t g = cur.g, kt = cur.kt;
+      const int acc = (int)(li % C::NACC);
+      const uint32_t aph = (uint32_t)((li / C::NACC) & 1);
       if (g != g_prev) {
         cb ^= 1;
         __syncwarp();
@@ -308,25 +352,37 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(lq * 32) << 16) + (uint32_t)(acc * C::BN);
-      const float* cw = my_c + cb * C::BN;
       float sc[QG];
 #pragma unroll
       for (int qq = 0; qq < QG; ++qq) {
-        float v[64];
-        tmem_ld32(taddr + qq * 64, v);
-        tmem_ld32(taddr + qq * 64 + 32, v + 32);
-        tmem_ld_wait();
-        float s0 = 0.f, s1 = 0.f;
+        float s8[8];
 #pragma unroll
-        for (int h = 0; h < 64; h += 2) {
-          s0 = fmaf(cw[qq * 64 + h], fmaxf(v[h], 0.f), s0);
-          s1 = fmaf(cw[qq * 64 + h + 1], fmaxf(v[h + 1], 0.f), s1);
+        for (int i = 0; i < 8; ++i) s8[i] = 0.f;
+        // two halves of 32 heads: 32 accumulator values live at a time
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          tmem_ld32(taddr + qq * 64 + half * 32, v);
+          tmem_ld_wait();
+          if (qq == QG - 1 && half == 1) {
+            // the accumulator is in registers: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          const float4* cw =
+              reinterpret_cast<const float4*>(my_c + cb * C::BN + qq * 64 + half * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 f = cw[i];
+            s8[(4 * i) & 7] = fmaf(f.x, fmaxf(v[4 * i], 0.f), s8[(4 * i) & 7]);
+            s8[(4 * i + 1) & 7] = fmaf(f.y, fmaxf(v[4 * i + 1], 0.f), s8[(4 * i + 1) & 7]);
+            s8[(4 * i + 2) & 7] = fmaf(f.z, fmaxf(v[4 * i + 2], 0.f), s8[(4 * i + 2) & 7]);
+            s8[(4 * i + 3) & 7] = fmaf(f.w, fmaxf(v[4 * i + 3], 0.f), s8[(4 * i + 3) & 7]);
+          }
         }
-        sc[qq] = s0 + s1;
+        sc[qq] = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
       const int64_t j = kt * C::BM + row;
       if (j < p.n) {
 #pragma unroll
@@ -335,9 +391,18 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
           p.scores[qi * p.scores_ld + j] = (j < nv[qq]) ? sc[qq] : -INFINITY;
         }
       }
-      if (++acc == 2) {
-        acc = 0;
-        aph ^= 1;
+      if constexpr (QG == 1) {
+        // first-level histogram of the visible keys (the top-k's level 1):
+        // the CTA's first two groups in shared memory, any later one (short
+        // rows) straight to global memory
+        if (p.hist1 && j < p.n && j < nv[0]) {
+          const uint32_t bin = score_key(sc[0]) >> 20;
+          const int64_t slot = g - g_first;
+          if (slot < 2)
+            atomicAdd(hslot + slot * kTopkBins + bin, 1u);
+          else
+            atomicAdd(p.hist1 + g * kTopkBins + bin, 1u);
+        }
       }
     }
   }
@@ -345,8 +410,19 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+  if constexpr (QG == 1) {
+    if (p.hist1 && t_end > t_begin) {
+      const int64_t g_last = (t_end - 1) / p.ktiles;
+      for (int sl = 0; sl < 2 && g_first + sl <= g_last; ++sl)
+        for (int i = threadIdx.x; i < kTopkBins; i += C::THREADS) {
+          const uint32_t v = hslot[sl * kTopkBins + i];
+          if (v) atomicAdd(&p.hist1[(g_first + sl) * kTopkBins + i], v);
+        }
+    }
   }
 }
 
@@ -372,8 +448,9 @@ EncodeTiledFn encode_fn() {
 
 template <int QG>
 csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* c,
-                      cudaStream_t s) {
+                      uint32_t* hist1, cudaStream_t s) {
   using C = TcCfg<QG>;
+  constexpr int W = C::EPI_WGS;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cuda_fail(cudaErrorNotSupported);
   const int64_t nq = a.B * a.q_per_seq;
@@ -408,29 +485,35 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   p.groups = nq / QG;
   p.ktiles = (a.n + C::BM - 1) / C::BM;
   p.dev_status = a.dev_status;
+  p.hist1 = QG == 1 ? hist1 : nullptr;
   const int64_t total = p.groups * p.ktiles;
   if (total == 0) return CSA2_OK;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(idx_score_tc_kernel<QG>,
+    cudaError_t e = cudaFuncSetAttribute(idx_score_tc_kernel<QG, W>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_ALLOC);
     if (e != cudaSuccess) return cuda_fail(e);
     attr_set = true;
   }
   const int grid = (int)std::min<int64_t>(total, sm_count());
-  idx_score_tc_kernel<QG><<<grid, C::THREADS, C::SMEM_ALLOC, s>>>(kmap, qmap, p);
+  idx_score_tc_kernel<QG, W><<<grid, C::THREADS, C::SMEM_ALLOC, s>>>(kmap, qmap, p);
   return check_launch();
 }
 
 }  // namespace
 
 csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, const float* c,
-                                   cudaStream_t s) {
+                                   uint32_t* hist1, cudaStream_t s) {
   if (a.hi != 64 || a.di != 128) return CSA2_ERR_UNSUPPORTED;
   if (a.B * a.q_per_seq == 0 || a.n == 0) return CSA2_OK;
-  if (a.q_per_seq % 4 == 0) return launch_tc<4>(a, q8, c, s);
-  return launch_tc<1>(a, q8, c, s);
+  if (a.q_per_seq % 4 == 0) return launch_tc<4>(a, q8, c, nullptr, s);
+  return launch_tc<1>(a, q8, c, hist1, s);
+}
+
+bool index_fuses_topk_hist(const csa2_index_args& a) {
+  return (a.q_dtype == CSA2_BF16 || a.q_dtype == CSA2_E4M3) && a.k_dtype == CSA2_E4M3 &&
+         a.q_per_seq % 4 != 0;
 }
 
 }  // namespace csa2

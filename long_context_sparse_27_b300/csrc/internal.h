@@ -24,14 +24,26 @@ csa2_status launch_quantize_index_q(const void* q, const float* w, int64_t nq, i
                                     int32_t di, uint8_t* q8, float* c, cudaStream_t s);
 // a3, fp32 CUDA-core path
 csa2_status launch_index_score_f32(const csa2_index_args& a, cudaStream_t s);
-// a3, FP8 tensor-core path: q8 / c already quantised
+// a3, FP8 tensor-core path: q8 / c already quantised.  hist1 (nullable):
+// [nq][4096] first-level top-k histograms the decode kernel adds its scores'
+// keys to (see index_fuses_topk_hist).
 csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, const float* c,
-                                   cudaStream_t s);
-// a4
+                                   uint32_t* hist1, cudaStream_t s);
+// whether launch_index_score_fp8 builds the top-k histograms for `a`
+bool index_fuses_topk_hist(const csa2_index_args& a);
+// a4: the workspace holds one 4096-bin first-level histogram per row
 size_t topk_workspace_bytes(int64_t rows, int64_t n, int32_t k);
 csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
                         const int32_t* n_valid, int32_t k, int32_t* idx_out, int64_t idx_ld,
                         void* ws, int32_t* dev_status, cudaStream_t s);
+// the pieces of launch_topk: zero the histograms; select from scores whose
+// histograms are complete
+csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s);
+csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
+                             const int32_t* n_valid, uint32_t* hist1, cudaStream_t s);
+csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int64_t ld,
+                               const int32_t* n_valid, int32_t k, const uint32_t* hist1,
+                               int32_t* idx_out, int64_t idx_ld, cudaStream_t s);
 // a5
 size_t attn_workspace_bytes(const csa2_attn_args& a);
 csa2_status launch_sparse_attn(const csa2_attn_args& a, cudaStream_t s);

@@ -9,15 +9,20 @@
 // both key and value.
 //
 // attn_f32_kernel    fp32 queries, one CTA per (query, head), CUDA cores.
-// attn_bf16_kernel   bf16 queries, d = 512: one CTA per (64-key chunk, 16
+// attn_bf16_kernel   bf16 queries, d = 512: one CTA per (80-key chunk, 16
 //                    heads, query).  The chunk's rows are gathered and
 //                    dequantised into shared memory as bf16 (exact: every
 //                    E2M1 value times a UE8M0 scale is a bf16 value), then
 //                    S = Q K^T and O = P V run as m16n8k16 bf16 MMAs with
 //                    fp32 accumulation; P is split into two bf16 terms
 //                    (p = hi + lo) so the probabilities keep ~16 bits.
-//                    Each CTA writes (max, sum, unnormalised O) for its
-//                    chunk; attn_combine_kernel merges the chunks.
+//                    The chunks of one (query, head group) form a thread-
+//                    block cluster and merge their (max, sum, unnormalised
+//                    O) through distributed shared memory; with more than
+//                    8 chunks they go through the workspace and
+//                    attn_combine_kernel instead.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -150,25 +155,54 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const csa2_attn_args a) {
 }
 
 // ---------------------------------------------------------------------------
-// bf16 tensor-core path (d = 512, 16 heads per CTA, 64 keys per chunk)
+// bf16 tensor-core path (d = 512, 16 heads per CTA, 80 keys per chunk)
 // ---------------------------------------------------------------------------
 
 constexpr int kD = 512;
 constexpr int kHG = 16;                  // heads per CTA (MMA M)
-constexpr int kKC = 64;                  // keys per chunk
-constexpr int kRowBytes = kD * 2 + 16;   // padded bf16 row (breaks ldmatrix bank conflicts)
+constexpr int kKC = 80;                  // keys per chunk
+constexpr int kPairs = kKC / 16;         // S = Q K^T: warp w < kPairs owns keys 16w .. 16w+15
+constexpr int kAttnWarps = 8;            // O = P V: warp w owns dims 64w .. 64w+63
+constexpr int kAttnThreads = 32 * kAttnWarps;
+constexpr int kMaxClusterChunks = 8;     // portable cluster size
+constexpr int kRowBytes = kD * 2 + 16;   // padded bf16 row (conflict-free ldmatrix)
 constexpr int kPRow = kKC * 2 + 16;      // padded P row
-constexpr int kAttnThreads = 128;
 constexpr int kSmemQ = kHG * kRowBytes;
-constexpr int kSmemK = kKC * kRowBytes;
-constexpr int kSmemP = 2 * kHG * kPRow;
+constexpr int kSmemK = kKC * kRowBytes;  // later reused for the chunk's fp32 O [16][512]
+constexpr int kSmemP = 2 * kHG * kPRow;  // P split into bf16 hi and lo
 constexpr int kAttnSmem = kSmemQ + kSmemK + kSmemP;
+constexpr int kPieces = kD / 8;         // 16-byte pieces of a bf16 row
+constexpr int kKItems = kKC * kPieces / kAttnThreads;  // pieces of the K tile per thread
+constexpr int kORow = kD + 8;            // padded fp32 row of the chunk output
+static_assert(kKC * kPieces % kAttnThreads == 0, "K-tile pieces split evenly");
+static_assert(kHG * kORow * 4 <= kSmemK, "the fp32 chunk output fits in the K tile");
+static_assert(kPairs <= kAttnWarps && kKC % 16 == 0, "S tiling");
 
 struct PartialLayout {
   // per (query, head group, chunk): O [16][512] f32, then m [16], l [16]
   static constexpr int64_t kFloats = (int64_t)kHG * kD + 2 * kHG;
 };
 
+// Rows of one chunk: a FP4 row (codes + scales), a bf16 window row, or none.
+struct ChunkRows {
+  const uint8_t* codes[kKC];
+  const uint8_t* scales[kKC];
+  const uint16_t* win[kKC];
+};
+
+// One CTA = (key chunk, 16 heads, query).  Phases:
+//  1. key sources of the chunk (idx reads); Q rows start copying (cp.async);
+//  2. window rows copy straight into the K tile (cp.async); FP4 rows load
+//     into registers (all loads in flight together), dequantise exactly to
+//     bf16 and store; empty rows are zeroed;
+//  3. S = Q K^T (warps 0..4, m16n8k16 bf16 MMA, fp32 accumulate), chunk-local
+//     softmax statistics, P = exp(S - m) split into bf16 hi + lo;
+//  4. O = P V (all 8 warps, 64 dims each);
+//  5. CLUSTER: the chunks of one (query, head group) form a thread-block
+//     cluster and merge (m, l, O) through distributed shared memory, each
+//     CTA writing 1/nchunks of the output; otherwise (m, l, O) go to the
+//     workspace and attn_combine_kernel merges them.
+template <bool CLUSTER>
 __global__ void __launch_bounds__(kAttnThreads, 2)
     attn_bf16_kernel(const csa2_attn_args a, int nchunks, float* __restrict__ partial) {
   extern __shared__ __align__(16) uint8_t sm_raw[];
@@ -176,10 +210,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   uint8_t* sK = sm_raw + kSmemQ;
   uint8_t* sPh = sK + kSmemK;
   uint8_t* sPl = sPh + kHG * kPRow;
-  __shared__ const uint8_t* row_codes[kKC];
-  __shared__ const uint8_t* row_scales[kKC];
-  __shared__ const uint16_t* row_win[kKC];
-  __shared__ float red_m[4][kHG], red_l[4][kHG];
+  __shared__ ChunkRows rows;
+  __shared__ float red_m[kPairs][kHG], red_l[kPairs][kHG];
+  __shared__ float s_m[kHG], s_l[kHG];                 // this chunk's (max, sum) per head
+  __shared__ float s_f[kMaxClusterChunks][kHG];        // merge weights per (chunk, head)
+  __shared__ uint32_t lut[256];  // code byte -> the two E2M1 values as bf16x2 (low nibble first)
 
   const int chunk = blockIdx.x, hg = blockIdx.y;
   const int64_t qi = blockIdx.z;
@@ -190,63 +225,86 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   if (wl > a.win_max) wl = a.win_max;
   const int64_t nkeys = a.k + wl;
 
-  // 1. key sources of this chunk
+  // ---- 1. key sources; Q copy; E2M1 table
+  lut[tid] = pack_bf16x2(e2m1_value(tid & 15u), e2m1_value((uint32_t)tid >> 4));
+  static_assert(kAttnThreads == 256, "one table entry per thread");
   if (tid < kKC) {
     const int64_t t = (int64_t)chunk * kKC + tid;
     KeySrc src{nullptr, nullptr, nullptr};
     if (t < nkeys) src = key_source(a, qi, t, ws, wl);
-    row_codes[tid] = src.codes;
-    row_scales[tid] = src.scales;
-    row_win[tid] = src.win;
+    rows.codes[tid] = src.codes;
+    rows.scales[tid] = src.scales;
+    rows.win[tid] = src.win;
   }
-  // 2. the 16 query heads (bf16 rows of 1024 bytes)
   {
     const uint8_t* qsrc = static_cast<const uint8_t*>(a.q) +
                           ((qi * a.hq + (int64_t)hg * kHG) * kD) * 2;
     for (int i = tid; i < kHG * (kD * 2 / 16); i += kAttnThreads) {
       const int r = i / (kD * 2 / 16), c = i % (kD * 2 / 16);
-      *reinterpret_cast<uint4*>(sQ + r * kRowBytes + c * 16) =
-          *reinterpret_cast<const uint4*>(qsrc + r * kD * 2 + c * 16);
+      cp_async16(sQ + r * kRowBytes + c * 16, qsrc + r * kD * 2 + c * 16);
     }
-  }
-  __syncthreads();
-  // 3. gather + dequantise: item = (row, 32-element block)
-  for (int i = tid; i < kKC * (kD / 32); i += kAttnThreads) {
-    const int r = i / (kD / 32), blk = i % (kD / 32);
-    uint8_t* dst = sK + r * kRowBytes + blk * 64;
-    uint4 o[4];
-    if (row_codes[r]) {
-      const uint4 cw = *reinterpret_cast<const uint4*>(row_codes[r] + blk * 16);
-      const float sc = ue8m0_value(row_scales[r][blk]);
-      const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
-      uint32_t packed[16];
-#pragma unroll
-      for (int wi = 0; wi < 4; ++wi)
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const uint32_t byte = (w4[wi] >> (8 * p)) & 0xFFu;
-          packed[wi * 4 + p] =
-              pack_bf16x2(e2m1_value(byte & 15u) * sc, e2m1_value(byte >> 4) * sc);
-        }
-#pragma unroll
-      for (int v = 0; v < 4; ++v)
-        o[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-    } else if (row_win[r]) {
-      const uint4* src = reinterpret_cast<const uint4*>(row_win[r] + blk * 32);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) o[v] = src[v];
-    } else {
-#pragma unroll
-      for (int v = 0; v < 4; ++v) o[v] = make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(dst + v * 16) = o[v];
   }
   __syncthreads();
 
-  // 4. S = Q K^T for this warp's 16 keys (two n-tiles of 8)
-  float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  // ---- 2. K tile: item = (row, 16-byte piece of the bf16 row) = 8 elements;
+  // consecutive threads take consecutive pieces (coalesced loads, stores
+  // spread over every bank).  FP4 pieces load 4 code bytes + their scale
+  // byte into registers first (all loads in flight), then dequantise.
   {
+    uint32_t cw[kKItems];
+    uint32_t sb[kKItems];
+#pragma unroll
+    for (int u = 0; u < kKItems; ++u) {
+      const int i = tid + u * kAttnThreads;
+      const int r = i / kPieces, c = i % kPieces;
+      cw[u] = 0;
+      sb[u] = 0;
+      if (rows.codes[r]) {
+        cw[u] = __ldg(reinterpret_cast<const uint32_t*>(rows.codes[r]) + c);
+        sb[u] = __ldg(rows.scales[r] + c / 4);
+      } else if (rows.win[r]) {
+        cp_async16(sK + r * kRowBytes + c * 16, rows.win[r] + c * 8);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kKItems; ++u) {
+      const int i = tid + u * kAttnThreads;
+      const int r = i / kPieces, c = i % kPieces;
+      if (rows.win[r]) continue;  // copied by cp.async
+      uint32_t packed[4] = {0u, 0u, 0u, 0u};  // no key: zero piece (P is 0 there)
+      if (rows.codes[r]) {
+        if (sb[u] >= 8 && sb[u] <= 250) {
+          // scale 2^(sb - 127) keeps every product a normal bf16: one exact
+          // bf16x2 multiply per two elements
+          const __nv_bfloat16 sc1 = __float2bfloat16_rn(ue8m0_value(sb[u]));
+          const __nv_bfloat162 sc2 = __halves2bfloat162(sc1, sc1);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t pair = lut[(cw[u] >> (8 * p)) & 0xFFu];
+            const __nv_bfloat162 v2 =
+                __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&pair), sc2);
+            packed[p] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+        } else {
+          const float sc = ue8m0_value(sb[u]);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t byte = (cw[u] >> (8 * p)) & 0xFFu;
+            packed[p] = pack_bf16x2(e2m1_value(byte & 15u) * sc, e2m1_value(byte >> 4) * sc);
+          }
+        }
+      }
+      *reinterpret_cast<uint4*>(sK + r * kRowBytes + c * 16) =
+          make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- 3. S = Q K^T and the chunk softmax (warps 0 .. kPairs-1)
+  const int r0 = lane >> 2;
+  if (warp < kPairs) {
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     const uint32_t qbase = smem_u32(sQ) + (lane & 15) * kRowBytes + (lane >> 4) * 16;
     const int krow = warp * 16 + (lane & 7) + ((lane >> 4) << 3);
     const uint32_t kbase = smem_u32(sK) + krow * kRowBytes + ((lane >> 3) & 1) * 16;
@@ -258,86 +316,97 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       mma_bf16_16816(s[0], a0, a1, a2, a3, b0, b1);
       mma_bf16_16816(s[1], a0, a1, a2, a3, b2, b3);
     }
-  }
-  // 5. chunk softmax: rows r0 = lane/4 and r0 + 8; keys 16*warp + 8*nt + 2*(lane%4) + {0,1}
-  const int r0 = lane >> 2;
-  float x[2][4];
-  float m0 = -INFINITY, m1 = -INFINITY;
+    // rows r0 (e = 0, 1) and r0 + 8 (e = 2, 3); keys 16w + 8nt + 2(lane%4) + (e&1)
+    float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int key = warp * 16 + nt * 8 + 2 * (lane & 3) + (e & 1);
-      const bool valid = row_codes[key] || row_win[key];
-      x[nt][e] = valid ? s[nt][e] * a.softmax_scale : -INFINITY;
-      if (e < 2)
-        m0 = fmaxf(m0, x[nt][e]);
-      else
-        m1 = fmaxf(m1, x[nt][e]);
+      for (int e = 0; e < 4; ++e) {
+        const int key = warp * 16 + nt * 8 + 2 * (lane & 3) + (e & 1);
+        const bool valid = rows.codes[key] || rows.win[key];
+        s[nt][e] = valid ? s[nt][e] * a.softmax_scale : -INFINITY;
+        if (e < 2)
+          m0 = fmaxf(m0, s[nt][e]);
+        else
+          m1 = fmaxf(m1, s[nt][e]);
+      }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+    if ((lane & 3) == 0) {
+      red_m[warp][r0] = m0;
+      red_m[warp][r0 + 8] = m1;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kPairs * 32) : "memory");  // S warps only
+    m0 = m1 = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kPairs; ++w) {
+      m0 = fmaxf(m0, red_m[w][r0]);
+      m1 = fmaxf(m1, red_m[w][r0 + 8]);
+    }
+    float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float m = e < 2 ? m0 : m1;
+        p[e] = (s[nt][e] == -INFINITY) ? 0.f : expf(s[nt][e] - m);
+      }
+      l0 += p[0] + p[1];
+      l1 += p[2] + p[3];
+      const int col = warp * 16 + nt * 8 + 2 * (lane & 3);
+      // p = hi + lo with hi = bf16(p), lo = bf16(p - hi): ~16 significant bits
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
+      const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
+      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+      *reinterpret_cast<__nv_bfloat162*>(sPh + r0 * kPRow + col * 2) = h01;
+      *reinterpret_cast<__nv_bfloat162*>(sPh + (r0 + 8) * kPRow + col * 2) = h23;
+      *reinterpret_cast<uint32_t*>(sPl + r0 * kPRow + col * 2) =
+          pack_bf16x2(p[0] - f01.x, p[1] - f01.y);
+      *reinterpret_cast<uint32_t*>(sPl + (r0 + 8) * kPRow + col * 2) =
+          pack_bf16x2(p[2] - f23.x, p[3] - f23.y);
     }
 #pragma unroll
-  for (int o = 1; o < 4; o <<= 1) {
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-  }
-  if ((lane & 3) == 0) {
-    red_m[warp][r0] = m0;
-    red_m[warp][r0 + 8] = m1;
-  }
-  __syncthreads();
-  m0 = fmaxf(fmaxf(red_m[0][r0], red_m[1][r0]), fmaxf(red_m[2][r0], red_m[3][r0]));
-  m1 = fmaxf(fmaxf(red_m[0][r0 + 8], red_m[1][r0 + 8]),
-             fmaxf(red_m[2][r0 + 8], red_m[3][r0 + 8]));
-  float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    float p[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float m = e < 2 ? m0 : m1;
-      p[e] = (x[nt][e] == -INFINITY) ? 0.f : expf(x[nt][e] - m);
+    for (int o = 1; o < 4; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-    l0 += p[0] + p[1];
-    l1 += p[2] + p[3];
-    const int col = warp * 16 + nt * 8 + 2 * (lane & 3);
-    // hi / lo bf16 split of p
-    const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
-    const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
-    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-    const uint32_t lo01 = pack_bf16x2(p[0] - f01.x, p[1] - f01.y);
-    const uint32_t lo23 = pack_bf16x2(p[2] - f23.x, p[3] - f23.y);
-    *reinterpret_cast<__nv_bfloat162*>(sPh + r0 * kPRow + col * 2) = h01;
-    *reinterpret_cast<__nv_bfloat162*>(sPh + (r0 + 8) * kPRow + col * 2) = h23;
-    *reinterpret_cast<uint32_t*>(sPl + r0 * kPRow + col * 2) = lo01;
-    *reinterpret_cast<uint32_t*>(sPl + (r0 + 8) * kPRow + col * 2) = lo23;
-  }
-#pragma unroll
-  for (int o = 1; o < 4; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-  }
-  if ((lane & 3) == 0) {
-    red_l[warp][r0] = l0;
-    red_l[warp][r0 + 8] = l1;
+    if ((lane & 3) == 0) {
+      red_l[warp][r0] = l0;
+      red_l[warp][r0 + 8] = l1;
+    }
   }
   __syncthreads();
+  if (tid < kHG) {
+    float m = -INFINITY, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPairs; ++w) {
+      m = fmaxf(m, red_m[w][tid]);
+      l += red_l[w][tid];
+    }
+    s_m[tid] = m;
+    s_l[tid] = l;
+  }
 
-  // 6. O = P V for this warp's 128 dims (16 n-tiles), keys as the K dimension
-  float o[16][4];
+  // ---- 4. O = P V for dims 64w .. 64w+63 (8 n-tiles), keys as the K dimension
+  float o[8][4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   {
     const uint32_t pbase_h = smem_u32(sPh) + (lane & 15) * kPRow + (lane >> 4) * 16;
     const uint32_t pbase_l = smem_u32(sPl) + (lane & 15) * kPRow + (lane >> 4) * 16;
     const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const uint32_t vbase = smem_u32(sK) + vrow * kRowBytes + (warp * 128 + (lane >> 4) * 8) * 2;
+    const uint32_t vbase = smem_u32(sK) + vrow * kRowBytes + (warp * 64 + (lane >> 4) * 8) * 2;
 #pragma unroll
     for (int ks = 0; ks < kKC / 16; ++ks) {
       uint32_t h0, h1, h2, h3, l0r, l1r, l2r, l3r;
       ldmatrix_x4(pbase_h + ks * 32, h0, h1, h2, h3);
       ldmatrix_x4(pbase_l + ks * 32, l0r, l1r, l2r, l3r);
 #pragma unroll
-      for (int np = 0; np < 8; ++np) {
+      for (int np = 0; np < 4; ++np) {
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(vbase + ks * 16 * kRowBytes + np * 32, b0, b1, b2, b3);
         mma_bf16_16816(o[2 * np], h0, h1, h2, h3, b0, b1);
@@ -347,19 +416,68 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       }
     }
   }
-  // 7. partial results
-  float* part = partial + ((qi * (a.hq / kHG) + hg) * (int64_t)nchunks + chunk) *
-                              PartialLayout::kFloats;
+
+  // ---- 5. merge the chunks
+  if constexpr (CLUSTER) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    __syncthreads();  // every warp is done reading the K tile
+    float* sO = reinterpret_cast<float*>(sK);  // [16][kORow] fp32, this chunk's unnormalised O
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const int col = warp * 128 + nt * 8 + 2 * (lane & 3);
-    *reinterpret_cast<float2*>(part + r0 * kD + col) = make_float2(o[nt][0], o[nt][1]);
-    *reinterpret_cast<float2*>(part + (r0 + 8) * kD + col) = make_float2(o[nt][2], o[nt][3]);
-  }
-  if (tid < kHG) {
-    part[kHG * kD + tid] = fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]),
-                                 fmaxf(red_m[2][tid], red_m[3][tid]));
-    part[kHG * kD + kHG + tid] = red_l[0][tid] + red_l[1][tid] + red_l[2][tid] + red_l[3][tid];
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = warp * 64 + nt * 8 + 2 * (lane & 3);
+      *reinterpret_cast<float2*>(sO + r0 * kORow + col) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(sO + (r0 + 8) * kORow + col) = make_float2(o[nt][2], o[nt][3]);
+    }
+    cluster.sync();  // every chunk's (m, l, O) is visible cluster-wide
+    if (tid < kHG) {
+      float mc[kMaxClusterChunks];
+      float M = -INFINITY;
+      for (int c = 0; c < nchunks; ++c) {
+        mc[c] = *cluster.map_shared_rank(&s_m[tid], c);
+        M = fmaxf(M, mc[c]);
+      }
+      float L = 0.f;
+      for (int c = 0; c < nchunks; ++c)
+        if (mc[c] != -INFINITY) L += expf(mc[c] - M) * *cluster.map_shared_rank(&s_l[tid], c);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int c = 0; c < nchunks; ++c)
+        s_f[c][tid] = (mc[c] == -INFINITY) ? 0.f : expf(mc[c] - M) * inv;
+    }
+    __syncthreads();
+    const int rank = (int)cluster.block_rank();
+    constexpr int kVec = kHG * kD / 4;  // float4s of the [16][512] output
+    const int v0 = rank * kVec / nchunks, v1 = (rank + 1) * kVec / nchunks;
+    for (int v = v0 + tid; v < v1; v += kAttnThreads) {
+      const int h = (v * 4) / kD;
+      const float4* src = reinterpret_cast<const float4*>(sO + h * kORow + (v * 4) % kD);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < nchunks; ++c) {
+        const float f = s_f[c][h];
+        const float4 x = *cluster.map_shared_rank(src, c);
+        acc.x += f * x.x;
+        acc.y += f * x.y;
+        acc.z += f * x.z;
+        acc.w += f * x.w;
+      }
+      *reinterpret_cast<float4*>(a.out + (qi * a.hq + (int64_t)hg * kHG + h) * kD +
+                                 (v * 4) % kD) = acc;
+    }
+    cluster.sync();  // no CTA leaves while another still reads its shared memory
+  } else {
+    float* part = partial + ((qi * (a.hq / kHG) + hg) * (int64_t)nchunks + chunk) *
+                                PartialLayout::kFloats;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = warp * 64 + nt * 8 + 2 * (lane & 3);
+      *reinterpret_cast<float2*>(part + r0 * kD + col) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(part + (r0 + 8) * kD + col) = make_float2(o[nt][2], o[nt][3]);
+    }
+    __syncthreads();
+    if (tid < kHG) {
+      part[kHG * kD + tid] = s_m[tid];
+      part[kHG * kD + kHG + tid] = s_l[tid];
+    }
   }
 }
 
@@ -398,11 +516,16 @@ __global__ void __launch_bounds__(128)
 
 int win_bound(const csa2_attn_args& a) { return a.win_max > 0 ? a.win_max : a.w_rows; }
 
+int attn_chunks(const csa2_attn_args& a) {
+  return (int)((a.k + win_bound(a) + kKC - 1) / kKC);
+}
+
 }  // namespace
 
 size_t attn_workspace_bytes(const csa2_attn_args& a) {
   if (a.q_dtype != CSA2_BF16) return 0;
-  const int64_t nchunks = (a.k + win_bound(a) + kKC - 1) / kKC;
+  const int64_t nchunks = attn_chunks(a);
+  if (nchunks <= kMaxClusterChunks) return 0;  // merged on chip
   return (size_t)a.nq * (a.hq / kHG) * nchunks * PartialLayout::kFloats * sizeof(float);
 }
 
@@ -416,21 +539,41 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s) {
     attn_f32_kernel<<<dim3((unsigned)a.hq, (unsigned)a.nq), 128, smem, s>>>(a);
     return check_launch();
   }
-  const int nchunks = (int)((a.k + a.win_max + kKC - 1) / kKC);
+  const int nchunks = attn_chunks(a);
   if (nchunks == 0) {
     cudaError_t e = cudaMemsetAsync(a.out, 0, (size_t)a.nq * a.hq * kD * sizeof(float), s);
     return e == cudaSuccess ? CSA2_OK : cuda_fail(e);
   }
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel,
+    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_bf16_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     if (e != cudaSuccess) return cuda_fail(e);
     attr_set = true;
   }
+  const dim3 grid((unsigned)nchunks, (unsigned)(a.hq / kHG), (unsigned)a.nq);
+  if (nchunks <= kMaxClusterChunks) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = kAttnSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nchunks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_bf16_kernel<true>, a, nchunks,
+                                       static_cast<float*>(nullptr));
+    return e == cudaSuccess ? check_launch() : cuda_fail(e);
+  }
   float* partial = static_cast<float*>(a.workspace);
-  attn_bf16_kernel<<<dim3((unsigned)nchunks, (unsigned)(a.hq / kHG), (unsigned)a.nq),
-                     kAttnThreads, kAttnSmem, s>>>(a, nchunks, partial);
+  attn_bf16_kernel<false><<<grid, kAttnThreads, kAttnSmem, s>>>(a, nchunks, partial);
   csa2_status st = check_launch();
   if (st != CSA2_OK) return st;
   attn_combine_kernel<<<dim3((unsigned)a.hq, (unsigned)a.nq), 128, 0, s>>>(partial, nchunks,

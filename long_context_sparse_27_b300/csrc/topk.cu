@@ -5,20 +5,24 @@
 // (CSA2)").  Order is (score descending, index ascending); the output row
 // holds the chosen indices ascending, padded with -1.
 //
-// Radix select on an order-preserving 32-bit key (+0 and -0 share a key):
-//   1. topk_hist_kernel     (chunks x rows CTAs) 4096-bin histogram of the
-//                           key's top 12 bits into the workspace.
-//   2. topk_compact_kernel  (chunks x rows) every CTA finds the threshold bin
-//                           T1 from the histogram; entries above it are
-//                           written out as selected, entries in it are
-//                           appended as 64-bit (key, ~index) candidates and
-//                           histogrammed on the next 12 key bits.
-//   3. topk_final_kernel    (one CTA per row) finds the second-level bin T2,
-//                           takes the candidates above it, sorts the few in
-//                           it exactly, and writes the k indices ascending.
-// A row whose threshold bins overflow the candidate buffers (huge runs of
-// equal scores) is finished by an exact 8-pass radix select over its
-// 64-bit (key, ~index) values inside topk_final_kernel.
+// Radix select on an order-preserving 32-bit key (+0 and -0 share a key),
+// one row per thread-block cluster of kTkCluster CTAs, each CTA owning a
+// contiguous chunk of the row:
+//   level 1   the row's 4096-bin histogram of the key's top 12 bits comes
+//             from global memory (topk_hist_kernel, or the indexer epilogue
+//             that produced the scores); every CTA finds the threshold bin
+//             T1 itself and keeps its entries in bins >= T1, in index order;
+//   level 2/3 if bin T1 holds more entries than are still needed, the CTAs
+//             histogram the next 12 (then 8) key bits of those entries and
+//             combine the histograms through distributed shared memory;
+//   ties      entries whose whole key equals the threshold key are taken in
+//             index order, CTA by CTA;
+//   output    each CTA learns how many entries the CTAs before it keep and
+//             writes its own ascending, so the row needs no final sort.
+// Every CTA of a cluster takes the same branches (they derive the same
+// thresholds from the same histograms), so the cluster barriers match.
+#include <cooperative_groups.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -28,301 +32,437 @@ namespace csa2 {
 
 namespace {
 
-constexpr int kBins = 4096;       // 12-bit digits
-constexpr int kCandCap = 4096;    // first-level candidates kept per row
-constexpr int kTinyCap = 2048;    // second-level ties sorted in shared memory
+namespace cg = cooperative_groups;
+
+constexpr int kBins = kTopkBins;    // 12-bit digits (levels 1 and 2)
+constexpr int kBins3 = 256;         // 8-bit digit (level 3)
 constexpr int kMaxK = 2048;
-constexpr int kThreads = 512;
-
-struct RowWS {
-  uint32_t hist1[kBins];
-  uint32_t hist2[kBins];
-  uint32_t n_sel;   // entries above T1 written to sel
-  uint32_t n_cand;  // entries in T1 (may exceed kCandCap: then only counted)
-  int32_t t1;       // threshold bin (-1: every visible entry is selected)
-  uint32_t above1;  // visible entries in bins above t1
-  uint32_t pad[60];
-};
-
-size_t row_stride_bytes(int32_t k) {
-  return align256(sizeof(RowWS)) + align256((size_t)k * 4) + align256((size_t)kCandCap * 8);
-}
-
-struct RowPtrs {
-  RowWS* ws;
-  int32_t* sel;
-  uint64_t* cand;
-};
-
-__device__ __forceinline__ RowPtrs row_ptrs(void* base, int64_t row, int32_t k) {
-  const size_t h = (sizeof(RowWS) + 255) & ~(size_t)255;
-  const size_t s = ((size_t)k * 4 + 255) & ~(size_t)255;
-  const size_t c = ((size_t)kCandCap * 8 + 255) & ~(size_t)255;
-  uint8_t* p = static_cast<uint8_t*>(base) + (size_t)row * (h + s + c);
-  return {reinterpret_cast<RowWS*>(p), reinterpret_cast<int32_t*>(p + h),
-          reinterpret_cast<uint64_t*>(p + h + s)};
-}
-
-// order-preserving key: larger float -> larger key; -0 maps like +0
-__device__ __forceinline__ uint32_t score_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ uint64_t composite(uint32_t key, int64_t j) {
-  return ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)j);
-}
+constexpr int kTkThreads = 512;
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kTkCluster = 8;       // CTAs per row (portable cluster size)
+constexpr int kLCap = 512;          // per-warp ordered list of entries in bins >= T1
+constexpr int kTkDynSmem = 2 * kTkWarps * kLCap * 4;  // keys + indices
+constexpr int kHistThreads = 512;
 
 __device__ __forceinline__ int64_t row_nvalid(const int32_t* n_valid, int64_t row, int64_t n) {
   int64_t nv = n_valid ? (int64_t)n_valid[row] : n;
   return nv < 0 ? 0 : (nv > n ? n : nv);
 }
 
-// Block-wide: the largest bin t with (sum of hist[b], b >= t) >= target, and
-// the count strictly above it.  t = -1 if the whole histogram holds fewer
-// than `target`.  nbins = kBins, blockDim = kThreads (8 bins per thread,
-// thread 0 owning the top bins).  Results in *t_out / *above_out (shared).
-__device__ void find_threshold(const uint32_t* hist, uint32_t target, int* t_out,
-                               uint32_t* above_out, uint32_t* scratch /* [kThreads/32] */) {
-  constexpr int PER = kBins / kThreads;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid / 32;
-  const int hi_bin = kBins - 1 - tid * PER;  // bins hi_bin .. hi_bin-PER+1
-  uint32_t local = 0;
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// ---------------------------------------------------------------------------
+// level-1 histogram of a row's visible keys (when the scores come from
+// elsewhere than the fused indexer epilogue)
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kHistThreads)
+    topk_hist_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
+                     const int32_t* __restrict__ n_valid, uint32_t* __restrict__ hist1,
+                     int64_t chunk) {
+  __shared__ uint32_t h[kBins];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kBins; i += kHistThreads) h[i] = 0;
+  __syncthreads();
+  const int64_t row = blockIdx.y;
+  const int64_t nv = row_nvalid(n_valid, row, n);
+  const int64_t j0 = (int64_t)blockIdx.x * chunk;
+  const int64_t j1 = min(nv, j0 + chunk);
+  const float* s = scores + row * ld;
+  constexpr int U = 4;
+  for (int64_t base = j0 + warp * 32; base < j1; base += (int64_t)kHistThreads * U) {
+    float x[U];
 #pragma unroll
-  for (int i = 0; i < PER; ++i) local += hist[hi_bin - i];
-  // exclusive prefix over threads in order tid = 0, 1, ... (top bins first)
+    for (int u = 0; u < U; ++u) {
+      const int64_t j = base + u * kHistThreads + lane;
+      x[u] = j < j1 ? s[j] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t j = base + u * kHistThreads + lane;
+      if (j < j1) atomicAdd(&h[score_key(x[u]) >> 20], 1u);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < kBins; i += kHistThreads)
+    if (h[i]) atomicAdd(&hist1[row * kBins + i], h[i]);
+}
+
+// ---------------------------------------------------------------------------
+// selection
+// ---------------------------------------------------------------------------
+
+struct TkTmp {
+  uint32_t wsum[kTkWarps];
+  uint32_t tot[kTkCluster];
+  int t;            // find_top: bin
+  uint32_t above;   // find_top: entries in higher bins
+  int R;            // cluster_top: slice holding the threshold
+  uint32_t cum;     // cluster_top: entries in higher slices
+  uint32_t T, A, cnt;  // cluster_top results: bin, entries above it, entries in it
+};
+
+// Largest bin t with sum(h[t .. nb)) >= target, and above = sum(h[t+1 ..
+// nb)).  Needs 1 <= target <= sum(h).  Block-wide; results in tmp->t /
+// tmp->above.  Thread i owns bins nb-1-i*per down to nb-(i+1)*per.
+__device__ void find_top(const uint32_t* h, int nb, uint32_t target, TkTmp* tmp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (nb + kTkThreads - 1) / kTkThreads;
+  const int hi = nb - 1 - tid * per;
+  uint32_t local = 0;
+  for (int i = 0; i < per; ++i)
+    if (hi - i >= 0) local += h[hi - i];
   uint32_t incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
-  if (lane == 31) scratch[warp] = incl;
-  if (tid == 0) *t_out = -1;
+  if (lane == 31) tmp->wsum[warp] = incl;
   __syncthreads();
-  uint32_t warp_off = 0;
-  for (int w = 0; w < warp; ++w) warp_off += scratch[w];
-  const uint32_t before = warp_off + incl - local;
-  if (before < target && before + local >= target) {
+  uint32_t woff = 0;
+  for (int w = 0; w < warp; ++w) woff += tmp->wsum[w];
+  const uint32_t before = woff + incl - local;
+  if (local > 0 && before < target && before + local >= target) {
     uint32_t cum = before;
-    for (int i = 0; i < PER; ++i) {
-      const uint32_t h = hist[hi_bin - i];
-      if (cum + h >= target) {
-        *t_out = hi_bin - i;
-        *above_out = cum;
+    for (int i = 0; i < per; ++i) {
+      const uint32_t x = h[hi - i];
+      if (cum + x >= target) {
+        tmp->t = hi - i;
+        tmp->above = cum;
         break;
       }
-      cum += h;
+      cum += x;
     }
   }
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads)
-    topk_hist_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
-                     const int32_t* __restrict__ n_valid, int32_t k, void* ws, int64_t chunk) {
-  __shared__ uint32_t h[kBins];
-  const int64_t row = blockIdx.y;
-  for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0;
+// The cluster-wide histogram is the sum of every CTA's `hist` (nb bins).
+// CTA r reduces bins [r*sl, (r+1)*sl) (sl = nb / C) into `slice`; then every
+// CTA finds the slice that holds the target-th largest entry and the bin in
+// it.  All CTAs end with the same tmp->T / A / cnt.  `hist` is overwritten.
+template <int C>
+__device__ void cluster_top(cg::cluster_group& cluster, uint32_t* hist, uint32_t* slice,
+                            uint32_t* s_tot, int nb, uint32_t target, TkTmp* tmp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = (int)cluster.block_rank();
+  const int sl = nb / C;
+  cluster.sync();  // every CTA's histogram is complete
+  uint32_t part = 0;
+  for (int i = tid; i < sl; i += kTkThreads) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int c = 0; c < C; ++c) v += *cluster.map_shared_rank(hist + r * sl + i, c);
+    slice[i] = v;
+    part += v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if (lane == 0) tmp->wsum[warp] = part;
   __syncthreads();
+  if (tid == 0) {
+    uint32_t t = 0;
+    for (int w = 0; w < kTkWarps; ++w) t += tmp->wsum[w];
+    *s_tot = t;
+  }
+  cluster.sync();  // every slice and slice total is complete
+  if (tid < C) tmp->tot[tid] = *cluster.map_shared_rank(s_tot, tid);
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t cum = 0;
+    int R = C - 1;
+    for (; R > 0; --R) {
+      if (cum + tmp->tot[R] >= target) break;
+      cum += tmp->tot[R];
+    }
+    tmp->R = R;
+    tmp->cum = cum;
+  }
+  __syncthreads();
+  const int R = tmp->R;
+  // the other CTAs no longer read this CTA's `hist`: reuse it for slice R
+  for (int i = tid; i < sl; i += kTkThreads) hist[i] = *cluster.map_shared_rank(slice + i, R);
+  __syncthreads();
+  find_top(hist, sl, target - tmp->cum, tmp);
+  if (tid == 0) {
+    tmp->T = (uint32_t)(R * sl + tmp->t);
+    tmp->A = tmp->cum + tmp->above;
+    tmp->cnt = hist[tmp->t];
+  }
+  __syncthreads();
+}
+
+template <int C>
+__global__ void __launch_bounds__(kTkThreads, 1)
+    topk_select_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
+                       const int32_t* __restrict__ n_valid, int32_t k,
+                       const uint32_t* __restrict__ hist1, int32_t* __restrict__ idx_out,
+                       int64_t idx_ld, int vec) {
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ __align__(16) uint8_t dyn[];
+  uint32_t* lkey = reinterpret_cast<uint32_t*>(dyn);
+  int32_t* lj = reinterpret_cast<int32_t*>(dyn + kTkWarps * kLCap * 4);
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t slice[kBins / C];
+  __shared__ TkTmp tmp;
+  __shared__ uint32_t s_tot, s_gt, s_tie, s_off, s_quota;
+  __shared__ uint32_t wgt[kTkWarps], wtie[kTkWarps];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = (int)cluster.block_rank();
+  const int64_t row = blockIdx.x / C;
   const int64_t nv = row_nvalid(n_valid, row, n);
-  const int64_t j0 = (int64_t)blockIdx.x * chunk;
-  const int64_t j1 = min(nv, j0 + chunk);
-  const float* s = scores + row * ld;
-  for (int64_t j = j0 + threadIdx.x; j < j1; j += kThreads)
-    atomicAdd(&h[score_key(s[j]) >> 20], 1u);
-  __syncthreads();
-  RowPtrs rp = row_ptrs(ws, row, k);
-  for (int i = threadIdx.x; i < kBins; i += kThreads)
-    if (h[i]) atomicAdd(&rp.ws->hist1[i], h[i]);
-}
-
-__global__ void __launch_bounds__(kThreads)
-    topk_compact_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
-                        const int32_t* __restrict__ n_valid, int32_t k, void* ws,
-                        int64_t chunk) {
-  __shared__ uint32_t h[kBins];
-  __shared__ uint32_t scratch[kThreads / 32];
-  __shared__ int t1;
-  __shared__ uint32_t above1;
-  const int64_t row = blockIdx.y;
-  RowPtrs rp = row_ptrs(ws, row, k);
-  const int64_t nv = row_nvalid(n_valid, row, n);
-  if (nv <= k) return;  // every visible entry is selected; the final kernel writes them
-  for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = rp.ws->hist1[i];
-  __syncthreads();
-  find_threshold(h, (uint32_t)k, &t1, &above1, scratch);
-  const int T1 = t1;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    rp.ws->t1 = T1;
-    rp.ws->above1 = above1;
-  }
-  const int64_t j0 = (int64_t)blockIdx.x * chunk;
-  const int64_t j1 = min(nv, j0 + chunk);
-  const float* s = scores + row * ld;
-  for (int64_t j = j0 + threadIdx.x; j < j1; j += kThreads) {
-    const uint32_t key = score_key(s[j]);
-    const int b1 = (int)(key >> 20);
-    if (b1 > T1) {
-      const uint32_t pos = atomicAdd(&rp.ws->n_sel, 1u);
-      if (pos < (uint32_t)k) rp.sel[pos] = (int32_t)j;
-    } else if (b1 == T1) {
-      const uint32_t pos = atomicAdd(&rp.ws->n_cand, 1u);
-      if (pos < (uint32_t)kCandCap) {
-        rp.cand[pos] = composite(key, j);
-        atomicAdd(&rp.ws->hist2[(key >> 8) & (kBins - 1)], 1u);
-      }
-    }
-  }
-}
-
-// Rank sort of `cnt` distinct indices held in shared memory, written
-// ascending to out[0 .. cnt).
-__device__ void write_ascending(const int32_t* list, int cnt, int32_t* out) {
-  for (int i = threadIdx.x; i < cnt; i += kThreads) {
-    const int32_t x = list[i];
-    int rank = 0;
-    for (int t = 0; t < cnt; ++t) rank += (list[t] < x);
-    out[rank] = x;
-  }
-}
-
-// Bitonic sort (descending) of m <= kTinyCap 64-bit values in shared memory,
-// padded with zeros to a power of two.
-__device__ void bitonic_desc(uint64_t* v, int m) {
-  int p = 1;
-  while (p < m) p <<= 1;
-  for (int i = m + threadIdx.x; i < p; i += kThreads) v[i] = 0;
-  __syncthreads();
-  for (int size = 2; size <= p; size <<= 1) {
-    for (int stride = size / 2; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < p / 2; i += kThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = ((lo & size) == 0);
-        const uint64_t a = v[lo], b = v[hi];
-        if ((a < b) == desc) {
-          v[lo] = b;
-          v[hi] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kThreads)
-    topk_final_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
-                      const int32_t* __restrict__ n_valid, int32_t k, void* ws,
-                      int32_t* __restrict__ idx_out, int64_t idx_ld) {
-  __shared__ int32_t outl[kMaxK];
-  __shared__ uint64_t tiny[kTinyCap];
-  __shared__ uint32_t h2[kBins];
-  __shared__ uint32_t scratch[kThreads / 32];
-  __shared__ uint32_t n_out, n_tiny;
-  __shared__ int t2;
-  __shared__ uint32_t above2;
-  __shared__ int slow;
-  const int64_t row = blockIdx.x;
-  RowPtrs rp = row_ptrs(ws, row, k);
   int32_t* out = idx_out + row * idx_ld;
-  const int64_t nv = row_nvalid(n_valid, row, n);
-  if (nv <= k) {
-    for (int64_t i = threadIdx.x; i < k; i += kThreads) out[i] = i < nv ? (int32_t)i : -1;
+  if (nv <= k) {  // every visible entry is selected (the whole cluster returns here)
+    for (int64_t i = (int64_t)r * kTkThreads + tid; i < k; i += (int64_t)C * kTkThreads)
+      out[i] = i < nv ? (int32_t)i : -1;
     return;
   }
-  const uint32_t above1 = rp.ws->above1;
-  const uint32_t m1 = rp.ws->n_cand;
-  const uint32_t r1 = (uint32_t)k - above1;  // needed from bin T1 (>= 1)
-  if (threadIdx.x == 0) {
-    n_out = 0;
-    n_tiny = 0;
-    slow = m1 > (uint32_t)kCandCap;
-  }
-  for (int i = threadIdx.x; i < (int)above1; i += kThreads) outl[i] = rp.sel[i];
+  const float* s = scores + row * ld;
+
+  // ---- level 1: threshold bin from the row's histogram
+  for (int i = tid; i < kBins; i += kTkThreads) hist[i] = hist1[row * kBins + i];
   __syncthreads();
-  if (!slow) {
-    for (int i = threadIdx.x; i < kBins; i += kThreads) h2[i] = rp.ws->hist2[i];
-    __syncthreads();
-    find_threshold(h2, r1, &t2, &above2, scratch);
-    const int T2 = t2;
-    const uint32_t m2 = h2[T2];
-    if (threadIdx.x == 0) {
-      n_out = above1;
-      if (m2 > (uint32_t)kTinyCap) slow = 1;
-    }
-    __syncthreads();
-    if (!slow) {
-      for (uint32_t i = threadIdx.x; i < m1; i += kThreads) {
-        const uint64_t c = rp.cand[i];
-        const int b2 = (int)((c >> 40) & (kBins - 1));
-        const int32_t j = (int32_t)(0xFFFFFFFFu - (uint32_t)c);
-        if (b2 > T2)
-          outl[atomicAdd(&n_out, 1u)] = j;
-        else if (b2 == T2)
-          tiny[atomicAdd(&n_tiny, 1u)] = c;
-      }
-      __syncthreads();
-      const int mt = (int)n_tiny;
-      bitonic_desc(tiny, mt);
-      const uint32_t r2 = r1 - above2;
-      const uint32_t base = n_out;
-      for (uint32_t i = threadIdx.x; i < r2; i += kThreads)
-        outl[base + i] = (int32_t)(0xFFFFFFFFu - (uint32_t)tiny[i]);
-      __syncthreads();
-    }
-  }
-  if (slow) {
-    // exact radix select over every visible entry's (key, ~index), 8 bits
-    // at a time from the top; the values are distinct, so the k-th largest
-    // V leaves exactly k entries >= V
-    uint32_t* hh = h2;  // first 256 bins reused
-    __shared__ uint64_t prefix;
-    __shared__ uint32_t need;
-    if (threadIdx.x == 0) {
-      prefix = 0;
-      need = (uint32_t)k;
-    }
-    __syncthreads();
-    const float* s = scores + row * ld;
-    for (int shift = 56; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < 256; i += kThreads) hh[i] = 0;
-      __syncthreads();
-      const uint64_t pre = prefix;
-      const uint64_t mask_hi = (shift == 56) ? 0 : (~0ull << (shift + 8));
-      for (int64_t j = threadIdx.x; j < nv; j += kThreads) {
-        const uint64_t c = composite(score_key(s[j]), j);
-        if ((c & mask_hi) == pre) atomicAdd(&hh[(c >> shift) & 255], 1u);
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        uint32_t cum = 0;
-        int d = 255;
-        for (; d > 0; --d) {
-          if (cum + hh[d] >= need) break;
-          cum += hh[d];
+  find_top(hist, kBins, (uint32_t)k, &tmp);
+  const uint32_t T1 = (uint32_t)tmp.t;
+  uint32_t need = (uint32_t)k - tmp.above;
+  const uint32_t cnt1 = hist[T1];
+
+  // ---- this CTA's chunk; warp w scans its contiguous segment in order and
+  // keeps (key, index) of every entry in a bin >= T1
+  const int64_t chunk = (((nv + C - 1) / C) + 31) & ~(int64_t)31;
+  const int64_t j0 = min(nv, (int64_t)r * chunk), j1 = min(nv, j0 + chunk);
+  const int64_t seg = (((chunk + kTkWarps - 1) / kTkWarps) + 31) & ~(int64_t)31;
+  const int64_t wj0 = min(j1, j0 + warp * seg), wj1 = min(j1, wj0 + seg);
+  uint32_t* mykey = lkey + warp * kLCap;
+  int32_t* myj = lj + warp * kLCap;
+  uint32_t cnt = 0;
+  {
+    constexpr int U = 8;  // 8 x 4 scores per lane in flight
+    for (int64_t base = wj0; base < wj1; base += 128 * U) {
+      float4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = base + u * 128 + lane * 4;
+        if (vec && j + 3 < wj1) {
+          x[u] = __ldcs(reinterpret_cast<const float4*>(s + j));
+        } else {
+          x[u].x = j < wj1 ? s[j] : 0.f;
+          x[u].y = j + 1 < wj1 ? s[j + 1] : 0.f;
+          x[u].z = j + 2 < wj1 ? s[j + 2] : 0.f;
+          x[u].w = j + 3 < wj1 ? s[j + 3] : 0.f;
         }
-        need -= cum;
-        prefix = pre | ((uint64_t)d << shift);
       }
-      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = base + u * 128 + lane * 4;
+        const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+        uint32_t key[4];
+        bool p[4];
+        uint32_t c = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          key[e] = score_key(xv[e]);
+          p[e] = (j + e < wj1) && (key[e] >> 20) >= T1;
+          c += p[e];
+        }
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        uint32_t pos = cnt + incl - c;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (p[e]) {
+            if (pos < (uint32_t)kLCap) {
+              mykey[pos] = key[e];
+              myj[pos] = (int32_t)(j + e);
+            }
+            ++pos;
+          }
+        cnt += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
-    const uint64_t V = prefix;
-    if (threadIdx.x == 0) n_out = 0;
-    __syncthreads();
-    for (int64_t j = threadIdx.x; j < nv; j += kThreads)
-      if (composite(score_key(s[j]), j) >= V) outl[atomicAdd(&n_out, 1u)] = (int32_t)j;
-    __syncthreads();
   }
-  write_ascending(outl, k, out);
+  // A warp whose list overflowed re-reads its segment instead (rare: it needs
+  // more than kLCap entries in the top bins of one segment).
+  const bool ovf = cnt > (uint32_t)kLCap;
+  // f(key, index, valid) over the warp's kept entries in index order; all
+  // lanes take the same number of steps.
+  auto walk = [&](auto&& f) {
+    if (!ovf) {
+      for (uint32_t base = 0; base < cnt; base += 32) {
+        const uint32_t i = base + lane;
+        const bool v = i < cnt;
+        f(v ? mykey[i] : 0u, v ? myj[i] : 0, v);
+      }
+    } else {
+      for (int64_t base = wj0; base < wj1; base += 32) {
+        const int64_t j = base + lane;
+        bool v = j < wj1;
+        const uint32_t key = v ? score_key(s[j]) : 0u;
+        v = v && (key >> 20) >= T1;
+        f(key, (int32_t)j, v);
+      }
+    }
+  };
+  __syncwarp();
+
+  // ---- levels 2 and 3 (only while the threshold bin holds surplus entries)
+  int depth = 1;        // key digits resolved: 1 -> 12 bits, 2 -> 24, 3/4 -> 32
+  uint32_t thr = T1;    // threshold key prefix
+  if (cnt1 != need) {
+    __syncthreads();
+    for (int i = tid; i < kBins; i += kTkThreads) hist[i] = 0;
+    __syncthreads();
+    walk([&](uint32_t key, int32_t, bool v) {
+      if (v && (key >> 20) == T1) atomicAdd(&hist[(key >> 8) & (kBins - 1)], 1u);
+    });
+    __syncthreads();
+    cluster_top<C>(cluster, hist, slice, &s_tot, kBins, need, &tmp);
+    need -= tmp.A;
+    depth = 2;
+    thr = (T1 << 12) | tmp.T;
+    if (tmp.cnt != need) {
+      for (int i = tid; i < kBins3; i += kTkThreads) hist[i] = 0;
+      __syncthreads();
+      const uint32_t t12 = thr;
+      walk([&](uint32_t key, int32_t, bool v) {
+        if (v && (key >> 8) == t12) atomicAdd(&hist[key & (kBins3 - 1)], 1u);
+      });
+      __syncthreads();
+      cluster_top<C>(cluster, hist, slice, &s_tot, kBins3, need, &tmp);
+      need -= tmp.A;
+      thr = (thr << 8) | tmp.T;
+      depth = tmp.cnt != need ? 4 : 3;
+    }
+  }
+  const int shift = depth == 1 ? 20 : (depth == 2 ? 8 : 0);
+  // g: kept for sure; t: a tie on the full key, kept in index order up to `need`
+  auto is_g = [&](uint32_t key) {
+    return (key >> shift) > thr || (depth <= 3 && (key >> shift) == thr);
+  };
+  auto is_t = [&](uint32_t key) { return depth == 4 && key == thr; };
+
+  // ---- counts, offsets, output
+  uint32_t ng = 0, nt = 0;
+  walk([&](uint32_t key, int32_t, bool v) {
+    ng += __popc(__ballot_sync(0xffffffffu, v && is_g(key)));
+    nt += __popc(__ballot_sync(0xffffffffu, v && is_t(key)));
+  });
+  if (lane == 0) {
+    wgt[warp] = ng;
+    wtie[warp] = nt;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t g = 0, t = 0;
+    for (int w = 0; w < kTkWarps; ++w) {
+      g += wgt[w];
+      t += wtie[w];
+    }
+    s_gt = g;
+    s_tie = t;
+  }
+  cluster.sync();  // every CTA's counts are visible
+  if (tid == 0) {
+    uint32_t pre_sel = 0, pre_tie = 0;
+    for (int c = 0; c < r; ++c) {
+      const uint32_t gc = *cluster.map_shared_rank(&s_gt, c);
+      const uint32_t tc = *cluster.map_shared_rank(&s_tie, c);
+      const uint32_t qc = min(tc, need > pre_tie ? need - pre_tie : 0u);
+      pre_tie += tc;
+      pre_sel += gc + qc;
+    }
+    s_quota = min(s_tie, need > pre_tie ? need - pre_tie : 0u);
+    s_off = pre_sel;
+  }
+  cluster.sync();  // no CTA reads another's shared memory after this point
+  uint32_t woff = s_off, tq = s_quota;
+  for (int w = 0; w < warp; ++w) {
+    const uint32_t qw = min(wtie[w], tq);
+    tq -= qw;
+    woff += wgt[w] + qw;
+  }
+  const uint32_t myq = min(wtie[warp], tq);
+  uint32_t run_sel = 0, run_tie = 0;
+  const uint32_t lt = lanemask_lt();
+  walk([&](uint32_t key, int32_t j, bool v) {
+    const bool g = v && is_g(key);
+    const bool t = v && is_t(key);
+    const uint32_t tm = __ballot_sync(0xffffffffu, t);
+    const bool sel = g || (t && run_tie + __popc(tm & lt) < myq);
+    const uint32_t sm = __ballot_sync(0xffffffffu, sel);
+    const uint32_t pos = woff + run_sel + __popc(sm & lt);
+    if (sel && pos < (uint32_t)k) out[pos] = j;
+    run_sel += __popc(sm);
+    run_tie += __popc(tm);
+  });
 }
+
+bool g_select_attr = false;
 
 }  // namespace
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n, int32_t k) {
   (void)n;
-  return (size_t)rows * row_stride_bytes(k);
+  (void)k;
+  return (size_t)rows * kBins * sizeof(uint32_t);
+}
+
+csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s) {
+  if (rows == 0) return CSA2_OK;
+  cudaError_t e = cudaMemsetAsync(hist1, 0, (size_t)rows * kBins * sizeof(uint32_t), s);
+  return e == cudaSuccess ? CSA2_OK : cuda_fail(e);
+}
+
+csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int64_t ld,
+                               const int32_t* n_valid, int32_t k, const uint32_t* hist1,
+                               int32_t* idx_out, int64_t idx_ld, cudaStream_t s) {
+  if (rows == 0) return CSA2_OK;
+  if (!g_select_attr) {
+    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel<kTkCluster>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTkDynSmem);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_select_attr = true;
+  }
+  const int vec = (ld % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) % 16) == 0) ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(rows * kTkCluster));
+  cfg.blockDim = dim3(kTkThreads);
+  cfg.dynamicSmemBytes = kTkDynSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kTkCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_select_kernel<kTkCluster>, scores, n, ld, n_valid,
+                                     k, hist1, idx_out, idx_ld, vec);
+  return e == cudaSuccess ? check_launch() : cuda_fail(e);
+}
+
+csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
+                             const int32_t* n_valid, uint32_t* hist1, cudaStream_t s) {
+  if (rows == 0 || n == 0) return CSA2_OK;
+  // enough CTAs to cover the GPU about twice
+  const int64_t want = (2 * (int64_t)sm_count() + rows - 1) / rows;
+  const int64_t max_chunks = (n + 4095) / 4096;
+  const int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(want, max_chunks));
+  const int64_t chunk = (n + chunks - 1) / chunks;
+  topk_hist_kernel<<<dim3((unsigned)chunks, (unsigned)rows), kHistThreads, 0, s>>>(
+      scores, n, ld, n_valid, hist1, chunk);
+  return check_launch();
 }
 
 csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
@@ -330,29 +470,11 @@ csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld
                         void* ws, int32_t* dev_status, cudaStream_t s) {
   (void)dev_status;
   if (rows == 0) return CSA2_OK;
-  const size_t stride = row_stride_bytes(k);
-  // zero the histograms and counters of every row (the selected / candidate
-  // lists need no clearing: only their counted prefix is read)
-  const size_t head = align256(sizeof(RowWS));
-  cudaError_t e = cudaMemset2DAsync(ws, stride, 0, head, (size_t)rows, s);
-  if (e != cudaSuccess) return cuda_fail(e);
-  // chunks per row: enough CTAs to cover the GPU about twice
-  const int64_t want = (2 * (int64_t)sm_count() + rows - 1) / rows;
-  const int64_t max_chunks = (n + 4095) / 4096;
-  const int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(want, max_chunks));
-  const int64_t chunk = (n + chunks - 1) / chunks;
-  if (n > 0) {
-    dim3 grid((unsigned)chunks, (unsigned)rows);
-    topk_hist_kernel<<<grid, kThreads, 0, s>>>(scores, n, ld, n_valid, k, ws, chunk);
-    csa2_status st = check_launch();
-    if (st != CSA2_OK) return st;
-    topk_compact_kernel<<<grid, kThreads, 0, s>>>(scores, n, ld, n_valid, k, ws, chunk);
-    st = check_launch();
-    if (st != CSA2_OK) return st;
-  }
-  topk_final_kernel<<<(unsigned)rows, kThreads, 0, s>>>(scores, n, ld, n_valid, k, ws, idx_out,
-                                                        idx_ld);
-  return check_launch();
+  uint32_t* hist1 = static_cast<uint32_t*>(ws);
+  csa2_status st = clear_topk_hist(hist1, rows, s);
+  if (st != CSA2_OK) return st;
+  if ((st = launch_topk_hist(scores, rows, n, ld, n_valid, hist1, s)) != CSA2_OK) return st;
+  return launch_topk_select(scores, rows, n, ld, n_valid, k, hist1, idx_out, idx_ld, s);
 }
 
 }  // namespace csa2
@@ -400,7 +522,7 @@ extern "C" csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int6
     }
     scratch = g_noalloc_ptr[dev];
   }
-  // launch_topk clears the histograms and counters of every row it uses
+  // launch_topk clears the histograms of every row it uses
   return launch_topk(scores, rows, n, ld, n_valid, k, idx_out, idx_ld, scratch, dev_status,
                      reinterpret_cast<cudaStream_t>(stream));
 }

@@ -80,8 +80,9 @@ def test_status_strings(csa2):
 
 
 def test_workspace_sizes(csa2):
-    assert csa2.topk_workspace_bytes(8, 262144, 512) > 8 * 2 * 4096 * 4
-    assert csa2.topk_workspace_bytes(8, 262144, 512) % 256 == 0
+    # one 4096-bin u32 histogram per row, whatever n and k
+    assert csa2.topk_workspace_bytes(8, 262144, 512) == 8 * 4096 * 4
+    assert csa2.topk_workspace_bytes(3, 100, 2048) == 3 * 4096 * 4
     a = csa2.IndexArgs(q_dtype=csa2.BF16, k_dtype=csa2.E4M3, B=8, q_per_seq=1, hi=64, di=128,
                        n=262144)
     assert csa2.lib.csa2_index_score_workspace_bytes(ctypes.byref(a)) == 8 * 64 * 128 + 8 * 64 * 4
@@ -173,9 +174,12 @@ def test_attn_and_quant_validation(csa2, monkeypatch):
                       scales=FAKE, n=100, codes_ld=256, codes_seq_stride=25600, scales_ld=16,
                       scales_seq_stride=1600, idx=FAKE, k=64, idx_ld=64, window=FAKE, w_rows=8,
                       win_ld=512, win_seq_stride=4096, softmax_scale=0.04, out=FAKE)
+    # 64 + 8 keys: one 80-key chunk, merged on chip: no workspace
+    assert L.csa2_sparse_attn_workspace_bytes(ctypes.byref(a)) == 0
+    a.k = a.idx_ld = 1024  # 1032 keys = 13 chunks > 8: merged through the workspace
     assert L.csa2_sparse_attn(ctypes.byref(a), None) == 5
     need = L.csa2_sparse_attn_workspace_bytes(ctypes.byref(a))
-    assert need == 2 * 4 * 2 * (16 * 512 + 32) * 4  # 2 queries x 4 head groups x 2 chunks
+    assert need == 2 * 4 * 13 * (16 * 512 + 32) * 4  # 2 queries x 4 head groups x 13 chunks
     a.workspace, a.workspace_bytes = FAKE, need
     a.hq = 24
     assert L.csa2_sparse_attn(ctypes.byref(a), None) == 2

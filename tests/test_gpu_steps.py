@@ -194,6 +194,21 @@ def test_topk_degenerate_rows(csa2, orc):
     assert np.array_equal(got.cpu().numpy(), ref)
 
 
+def test_topk_long_equal_runs(csa2, orc):
+    # rows long enough that one warp's share of a row holds more entries in
+    # the top bins than its ordered list keeps, so the selector re-reads them
+    n, k = 200000, 512
+    s = torch.zeros(4, n)
+    s[0] = 0.5                                    # all equal
+    s[1, 100000:] = 1.0                           # a long run of equal maxima
+    s[2] = synth.scores_with_ties(1, n, seed=71, levels=3)[0]  # three values
+    s[3, ::3] = 7.0
+    s[3, 150000:150010] = 8.0                     # a few above a long tie run
+    got = csa2.topk(dev(s), k)
+    ref = orc.topk(f64(s), k)
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
 def test_topk_strided_rows(csa2, orc):
     s = synth.scores_with_ties(4, 3000, seed=70)
     big = torch.full((4, 3100), 99.0)
@@ -231,8 +246,12 @@ def test_attn_f32_tiny(csa2, orc):
     assert rel_l2(out.cpu().numpy(), ref) <= 2e-3
 
 
+# (3, 64, 2000, 512, 128): 640 keys = 8 chunks of 80, merged on chip (the
+# 128K / 1M decode shape); (2, 16, 3000, 1024, 128): 15 chunks, merged
+# through the workspace; the others are ragged single / few-chunk cases.
 @pytest.mark.parametrize("nq,hq,n,k,W", [(3, 64, 2000, 512, 128), (2, 16, 300, 64, 7),
-                                          (1, 32, 50, 8, 0), (2, 16, 600, 512, 128)])
+                                          (1, 32, 50, 8, 0), (2, 16, 600, 512, 128),
+                                          (2, 16, 3000, 1024, 128), (1, 16, 700, 560, 80)])
 def test_attn_bf16(csa2, orc, nq, hq, n, k, W):
     d = 512
     codes, scales = make_cache(csa2, nq, n, d, 90 + n)
@@ -243,6 +262,20 @@ def test_attn_bf16(csa2, orc, nq, hq, n, k, W):
     scale = 1 / math.sqrt(d)
     out = csa2.sparse_attn(dev(q), codes, scales, dev(idx), dev(win).contiguous(), scale)
     ref = orc.sparse_attn(f64(q), rc, rs, idx.numpy(), f64(win), scale)
+    assert rel_l2(out.cpu().numpy(), ref) <= 2e-3
+
+
+def test_attn_bf16_empty_chunks(csa2, orc):
+    # 200 selected entries then 312 x -1: chunks 3..5 hold no key at all and
+    # must drop out of the merge (their max is -inf)
+    d, n, k, W, hq = 512, 400, 512, 128, 32
+    codes, scales = make_cache(csa2, 2, n, d, 120)
+    rc, rs = oracle_cache(orc, 2, n, d, 120)
+    q = synth.normal((2, hq, d), 121)
+    idx = synth.random_indices(2, k, n, 122, pad=312)
+    win = synth.normal((2, W, d), 123)
+    out = csa2.sparse_attn(dev(q), codes, scales, dev(idx), dev(win), 1 / math.sqrt(d))
+    ref = orc.sparse_attn(f64(q), rc, rs, idx.numpy(), f64(win), 1 / math.sqrt(d))
     assert rel_l2(out.cpu().numpy(), ref) <= 2e-3
 
 
