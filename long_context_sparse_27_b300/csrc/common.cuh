@@ -334,6 +334,40 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Eight E2M1 codes (4 bytes; element 2i in the low nibble of byte i), each
+// times the power of two held in both halves of sc2, as eight bf16 in four
+// 32-bit words (element 2i in the low half).  Byte-permute table lookups:
+// the unscaled magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} have bf16 high bytes
+// {00,3F,3F,3F,40,40,40,40} and low bytes {00,00,80,C0,00,40,80,C0}; the
+// code's sign bit becomes bit 15.  The scale multiply is exact when every
+// product is a normal bf16 (the caller checks the scale's range).
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t code4, __nv_bfloat162 sc2,
+                                               uint32_t out[4]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t c16 = (code4 >> (16 * h)) & 0xFFFFu;  // four codes
+    const uint32_t mag = c16 & 0x7777u;
+    const uint32_t lo = prmt(0xC0800000u, 0xC0804000u, mag);
+    uint32_t hi = prmt(0x3F3F3F00u, 0x40404040u, mag);
+    // selector bit 3 (the code's sign) makes prmt replicate the selected
+    // byte's top bit: 0x7F -> 0x00 for negative codes, 0x7F for positive
+    const uint32_t t = prmt(0x7F7F7F7Fu, 0x7F7F7F7Fu, c16);
+    hi |= ((t + 0x01010101u) & 0x80808080u) ^ 0x80808080u;
+    const uint32_t w0 = prmt(lo, hi, 0x5140u);  // elements 4h, 4h+1
+    const uint32_t w1 = prmt(lo, hi, 0x7362u);  // elements 4h+2, 4h+3
+    const __nv_bfloat162 p0 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&w0), sc2);
+    const __nv_bfloat162 p1 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&w1), sc2);
+    out[2 * h] = *reinterpret_cast<const uint32_t*>(&p0);
+    out[2 * h + 1] = *reinterpret_cast<const uint32_t*>(&p1);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
   return *reinterpret_cast<uint32_t*>(&v);

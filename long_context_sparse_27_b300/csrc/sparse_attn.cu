@@ -155,31 +155,39 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const csa2_attn_args a) {
 }
 
 // ---------------------------------------------------------------------------
-// bf16 tensor-core path (d = 512, 16 heads per CTA, 80 keys per chunk)
+// bf16 tensor-core path (d = 512, 32 heads per CTA, 80 keys per chunk)
 // ---------------------------------------------------------------------------
 
 constexpr int kD = 512;
-constexpr int kHG = 16;                  // heads per CTA (MMA M)
+// 16 heads per CTA keep two CTAs on an SM (about 104 KB of shared memory
+// each), so the 8-CTA clusters of a 1M-context decode step all run at once.
+constexpr int kHG = 16;                  // heads per CTA
+constexpr int kMT = kHG / 16;            // m16 tiles of heads
 constexpr int kKC = 80;                  // keys per chunk
-constexpr int kPairs = kKC / 16;         // S = Q K^T: warp w < kPairs owns keys 16w .. 16w+15
-constexpr int kAttnWarps = 8;            // O = P V: warp w owns dims 64w .. 64w+63
+constexpr int kPairs = kKC / 16;         // key pairs of 16 (two n8 tiles)
+constexpr int kAttnWarps = 8;
 constexpr int kAttnThreads = 32 * kAttnWarps;
+constexpr int kSWarps = kMT * kPairs;    // S = Q K^T: warp w < kSWarps owns (m-tile w / 5, keys 16 (w % 5) ..)
+constexpr int kPVSlice = kD * kMT / kAttnWarps;  // O = P V: warp w owns (m-tile, 64 dims)
 constexpr int kMaxClusterChunks = 8;     // portable cluster size
 constexpr int kRowBytes = kD * 2 + 16;   // padded bf16 row (conflict-free ldmatrix)
 constexpr int kPRow = kKC * 2 + 16;      // padded P row
 constexpr int kSmemQ = kHG * kRowBytes;
-constexpr int kSmemK = kKC * kRowBytes;  // later reused for the chunk's fp32 O [16][512]
+constexpr int kSmemK = kKC * kRowBytes;  // later reused for the chunk's fp32 O [kHG][kORow]
 constexpr int kSmemP = 2 * kHG * kPRow;  // P split into bf16 hi and lo
 constexpr int kAttnSmem = kSmemQ + kSmemK + kSmemP;
-constexpr int kPieces = kD / 8;         // 16-byte pieces of a bf16 row
-constexpr int kKItems = kKC * kPieces / kAttnThreads;  // pieces of the K tile per thread
+constexpr int kPieces = kD / 8;          // 16-byte pieces of a bf16 row (8 elements)
+constexpr int kKItems = kKC * kPieces / kAttnThreads;  // K-tile pieces per thread
+constexpr int kQItems = kHG * kPieces / kAttnThreads;  // Q-tile pieces per thread
 constexpr int kORow = kD + 8;            // padded fp32 row of the chunk output
-static_assert(kKC * kPieces % kAttnThreads == 0, "K-tile pieces split evenly");
+static_assert(kKC * kPieces % kAttnThreads == 0 && kHG * kPieces % kAttnThreads == 0,
+              "tiles split evenly over the threads");
 static_assert(kHG * kORow * 4 <= kSmemK, "the fp32 chunk output fits in the K tile");
-static_assert(kPairs <= kAttnWarps && kKC % 16 == 0, "S tiling");
+static_assert(kSWarps <= kAttnWarps && kKC % 16 == 0, "S tiling");
+static_assert(kPVSlice == 64 && kAttnWarps % kMT == 0, "PV tiling");
 
 struct PartialLayout {
-  // per (query, head group, chunk): O [16][512] f32, then m [16], l [16]
+  // per (query, head group, chunk): O [kHG][512] f32, then m [kHG], l [kHG]
   static constexpr int64_t kFloats = (int64_t)kHG * kD + 2 * kHG;
 };
 
@@ -192,12 +200,13 @@ struct ChunkRows {
 
 // One CTA = (key chunk, 16 heads, query).  Phases:
 //  1. key sources of the chunk (idx reads); Q rows start copying (cp.async);
-//  2. window rows copy straight into the K tile (cp.async); FP4 rows load
-//     into registers (all loads in flight together), dequantise exactly to
-//     bf16 and store; empty rows are zeroed;
+//  2. K tile in 16-byte pieces (8 elements), consecutive threads on
+//     consecutive pieces: window pieces copy with cp.async; FP4 pieces load
+//     their 4 code bytes and scale byte into registers (all loads in flight),
+//     then dequantise exactly to bf16; empty rows are zeroed;
 //  3. S = Q K^T (warps 0..4, m16n8k16 bf16 MMA, fp32 accumulate), chunk-local
 //     softmax statistics, P = exp(S - m) split into bf16 hi + lo;
-//  4. O = P V (all 8 warps, 64 dims each);
+//  4. O = P V (8 warps, 64 dims each);
 //  5. CLUSTER: the chunks of one (query, head group) form a thread-block
 //     cluster and merge (m, l, O) through distributed shared memory, each
 //     CTA writing 1/nchunks of the output; otherwise (m, l, O) go to the
@@ -214,7 +223,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   __shared__ float red_m[kPairs][kHG], red_l[kPairs][kHG];
   __shared__ float s_m[kHG], s_l[kHG];                 // this chunk's (max, sum) per head
   __shared__ float s_f[kMaxClusterChunks][kHG];        // merge weights per (chunk, head)
-  __shared__ uint32_t lut[256];  // code byte -> the two E2M1 values as bf16x2 (low nibble first)
 
   const int chunk = blockIdx.x, hg = blockIdx.y;
   const int64_t qi = blockIdx.z;
@@ -225,9 +233,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   if (wl > a.win_max) wl = a.win_max;
   const int64_t nkeys = a.k + wl;
 
-  // ---- 1. key sources; Q copy; E2M1 table
-  lut[tid] = pack_bf16x2(e2m1_value(tid & 15u), e2m1_value((uint32_t)tid >> 4));
-  static_assert(kAttnThreads == 256, "one table entry per thread");
+  // ---- 1. key sources; Q copy
   if (tid < kKC) {
     const int64_t t = (int64_t)chunk * kKC + tid;
     KeySrc src{nullptr, nullptr, nullptr};
@@ -236,20 +242,24 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     rows.scales[tid] = src.scales;
     rows.win[tid] = src.win;
   }
+  // heads of this group that exist (hq may be an odd multiple of 16)
+  const int hvalid = min(kHG, a.hq - hg * kHG);
   {
     const uint8_t* qsrc = static_cast<const uint8_t*>(a.q) +
                           ((qi * a.hq + (int64_t)hg * kHG) * kD) * 2;
-    for (int i = tid; i < kHG * (kD * 2 / 16); i += kAttnThreads) {
-      const int r = i / (kD * 2 / 16), c = i % (kD * 2 / 16);
-      cp_async16(sQ + r * kRowBytes + c * 16, qsrc + r * kD * 2 + c * 16);
+#pragma unroll
+    for (int u = 0; u < kQItems; ++u) {
+      const int i = tid + u * kAttnThreads;
+      const int r = i / kPieces, c = i % kPieces;
+      if (r < hvalid)
+        cp_async16(sQ + r * kRowBytes + c * 16, qsrc + r * kD * 2 + c * 16);
+      else
+        *reinterpret_cast<uint4*>(sQ + r * kRowBytes + c * 16) = make_uint4(0, 0, 0, 0);
     }
   }
   __syncthreads();
 
-  // ---- 2. K tile: item = (row, 16-byte piece of the bf16 row) = 8 elements;
-  // consecutive threads take consecutive pieces (coalesced loads, stores
-  // spread over every bank).  FP4 pieces load 4 code bytes + their scale
-  // byte into registers first (all loads in flight), then dequantise.
+  // ---- 2. K tile
   {
     uint32_t cw[kKItems];
     uint32_t sb[kKItems];
@@ -257,14 +267,15 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     for (int u = 0; u < kKItems; ++u) {
       const int i = tid + u * kAttnThreads;
       const int r = i / kPieces, c = i % kPieces;
-      cw[u] = 0;
-      sb[u] = 0;
-      if (rows.codes[r]) {
-        cw[u] = __ldg(reinterpret_cast<const uint32_t*>(rows.codes[r]) + c);
-        sb[u] = __ldg(rows.scales[r] + c / 4);
-      } else if (rows.win[r]) {
-        cp_async16(sK + r * kRowBytes + c * 16, rows.win[r] + c * 8);
-      }
+      const uint8_t* cp = rows.codes[r];
+      cw[u] = cp ? __ldg(reinterpret_cast<const uint32_t*>(cp) + c) : 0u;
+      sb[u] = cp ? (uint32_t)__ldg(rows.scales[r] + c / 4) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kKItems; ++u) {
+      const int i = tid + u * kAttnThreads;
+      const int r = i / kPieces, c = i % kPieces;
+      if (rows.win[r]) cp_async16(sK + r * kRowBytes + c * 16, rows.win[r] + c * 8);
     }
 #pragma unroll
     for (int u = 0; u < kKItems; ++u) {
@@ -274,17 +285,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       uint32_t packed[4] = {0u, 0u, 0u, 0u};  // no key: zero piece (P is 0 there)
       if (rows.codes[r]) {
         if (sb[u] >= 8 && sb[u] <= 250) {
-          // scale 2^(sb - 127) keeps every product a normal bf16: one exact
-          // bf16x2 multiply per two elements
+          // scale 2^(sb - 127) in [2^-119, 2^123]: every product is a normal
+          // bf16, so the bf16x2 multiply is exact
           const __nv_bfloat16 sc1 = __float2bfloat16_rn(ue8m0_value(sb[u]));
-          const __nv_bfloat162 sc2 = __halves2bfloat162(sc1, sc1);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const uint32_t pair = lut[(cw[u] >> (8 * p)) & 0xFFu];
-            const __nv_bfloat162 v2 =
-                __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&pair), sc2);
-            packed[p] = *reinterpret_cast<const uint32_t*>(&v2);
-          }
+          e2m1x8_to_bf16(cw[u], __halves2bfloat162(sc1, sc1), packed);
         } else {
           const float sc = ue8m0_value(sb[u]);
 #pragma unroll
@@ -301,30 +305,39 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   cp_async_wait_all();
   __syncthreads();
 
-  // ---- 3. S = Q K^T and the chunk softmax (warps 0 .. kPairs-1)
+  // ---- 3. S = Q K^T and the chunk softmax (warps 0 .. kSWarps-1)
   const int r0 = lane >> 2;
-  if (warp < kPairs) {
+  if (warp < kSWarps) {
+    const int mt = warp / kPairs, pr = warp % kPairs;
+    // two independent accumulator chains per n-tile: dims 0..255 and 256..511
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    const uint32_t qbase = smem_u32(sQ) + (lane & 15) * kRowBytes + (lane >> 4) * 16;
-    const int krow = warp * 16 + (lane & 7) + ((lane >> 4) << 3);
+    float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const uint32_t qbase =
+        smem_u32(sQ) + (mt * 16 + (lane & 15)) * kRowBytes + (lane >> 4) * 16;
+    const int krow = pr * 16 + (lane & 7) + ((lane >> 4) << 3);
     const uint32_t kbase = smem_u32(sK) + krow * kRowBytes + ((lane >> 3) & 1) * 16;
-#pragma unroll 8
-    for (int ks = 0; ks < kD / 16; ++ks) {
+#pragma unroll 4
+    for (int ks = 0; ks < kD / 32; ++ks) {
       uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+      uint32_t c0, c1, c2, c3, d0, d1, d2, d3;
       ldmatrix_x4(qbase + ks * 32, a0, a1, a2, a3);
       ldmatrix_x4(kbase + ks * 32, b0, b1, b2, b3);
+      ldmatrix_x4(qbase + (ks + kD / 32) * 32, c0, c1, c2, c3);
+      ldmatrix_x4(kbase + (ks + kD / 32) * 32, d0, d1, d2, d3);
       mma_bf16_16816(s[0], a0, a1, a2, a3, b0, b1);
       mma_bf16_16816(s[1], a0, a1, a2, a3, b2, b3);
+      mma_bf16_16816(s2[0], c0, c1, c2, c3, d0, d1);
+      mma_bf16_16816(s2[1], c0, c1, c2, c3, d2, d3);
     }
-    // rows r0 (e = 0, 1) and r0 + 8 (e = 2, 3); keys 16w + 8nt + 2(lane%4) + (e&1)
+    // rows mt*16 + r0 (e = 0, 1) and + 8 (e = 2, 3); keys 16pr + 8nt + 2(lane%4) + (e&1)
     float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int key = warp * 16 + nt * 8 + 2 * (lane & 3) + (e & 1);
+        const int key = pr * 16 + nt * 8 + 2 * (lane & 3) + (e & 1);
         const bool valid = rows.codes[key] || rows.win[key];
-        s[nt][e] = valid ? s[nt][e] * a.softmax_scale : -INFINITY;
+        s[nt][e] = valid ? (s[nt][e] + s2[nt][e]) * a.softmax_scale : -INFINITY;
         if (e < 2)
           m0 = fmaxf(m0, s[nt][e]);
         else
@@ -335,16 +348,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
       m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
     }
+    const int h0 = mt * 16 + r0;
     if ((lane & 3) == 0) {
-      red_m[warp][r0] = m0;
-      red_m[warp][r0 + 8] = m1;
+      red_m[pr][h0] = m0;
+      red_m[pr][h0 + 8] = m1;
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kPairs * 32) : "memory");  // S warps only
+    asm volatile("bar.sync 1, %0;" ::"n"(kSWarps * 32) : "memory");  // S warps only
     m0 = m1 = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kPairs; ++w) {
-      m0 = fmaxf(m0, red_m[w][r0]);
-      m1 = fmaxf(m1, red_m[w][r0 + 8]);
+      m0 = fmaxf(m0, red_m[w][h0]);
+      m1 = fmaxf(m1, red_m[w][h0 + 8]);
     }
     float l0 = 0.f, l1 = 0.f;
 #pragma unroll
@@ -357,16 +371,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       }
       l0 += p[0] + p[1];
       l1 += p[2] + p[3];
-      const int col = warp * 16 + nt * 8 + 2 * (lane & 3);
+      const int col = pr * 16 + nt * 8 + 2 * (lane & 3);
       // p = hi + lo with hi = bf16(p), lo = bf16(p - hi): ~16 significant bits
       const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
       const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
       const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-      *reinterpret_cast<__nv_bfloat162*>(sPh + r0 * kPRow + col * 2) = h01;
-      *reinterpret_cast<__nv_bfloat162*>(sPh + (r0 + 8) * kPRow + col * 2) = h23;
-      *reinterpret_cast<uint32_t*>(sPl + r0 * kPRow + col * 2) =
+      *reinterpret_cast<__nv_bfloat162*>(sPh + h0 * kPRow + col * 2) = h01;
+      *reinterpret_cast<__nv_bfloat162*>(sPh + (h0 + 8) * kPRow + col * 2) = h23;
+      *reinterpret_cast<uint32_t*>(sPl + h0 * kPRow + col * 2) =
           pack_bf16x2(p[0] - f01.x, p[1] - f01.y);
-      *reinterpret_cast<uint32_t*>(sPl + (r0 + 8) * kPRow + col * 2) =
+      *reinterpret_cast<uint32_t*>(sPl + (h0 + 8) * kPRow + col * 2) =
           pack_bf16x2(p[2] - f23.x, p[3] - f23.y);
     }
 #pragma unroll
@@ -375,8 +389,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
     if ((lane & 3) == 0) {
-      red_l[warp][r0] = l0;
-      red_l[warp][r0 + 8] = l1;
+      red_l[pr][h0] = l0;
+      red_l[pr][h0 + 8] = l1;
     }
   }
   __syncthreads();
@@ -391,87 +405,105 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     s_l[tid] = l;
   }
 
-  // ---- 4. O = P V for dims 64w .. 64w+63 (8 n-tiles), keys as the K dimension
+  // ---- 4. O = P V: m-tile pm, dims d0 .. d0+63 (8 n-tiles), keys as the K dimension
+  const int pm = warp / (kAttnWarps / kMT);
+  const int d0 = (warp % (kAttnWarps / kMT)) * kPVSlice;
   float o[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   {
-    const uint32_t pbase_h = smem_u32(sPh) + (lane & 15) * kPRow + (lane >> 4) * 16;
-    const uint32_t pbase_l = smem_u32(sPl) + (lane & 15) * kPRow + (lane >> 4) * 16;
+    const uint32_t pbase_h =
+        smem_u32(sPh) + (pm * 16 + (lane & 15)) * kPRow + (lane >> 4) * 16;
+    const uint32_t pbase_l =
+        smem_u32(sPl) + (pm * 16 + (lane & 15)) * kPRow + (lane >> 4) * 16;
     const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const uint32_t vbase = smem_u32(sK) + vrow * kRowBytes + (warp * 64 + (lane >> 4) * 8) * 2;
+    const uint32_t vbase = smem_u32(sK) + vrow * kRowBytes + (d0 + (lane >> 4) * 8) * 2;
 #pragma unroll
     for (int ks = 0; ks < kKC / 16; ++ks) {
-      uint32_t h0, h1, h2, h3, l0r, l1r, l2r, l3r;
-      ldmatrix_x4(pbase_h + ks * 32, h0, h1, h2, h3);
+      uint32_t h0r, h1r, h2r, h3r, l0r, l1r, l2r, l3r;
+      ldmatrix_x4(pbase_h + ks * 32, h0r, h1r, h2r, h3r);
       ldmatrix_x4(pbase_l + ks * 32, l0r, l1r, l2r, l3r);
 #pragma unroll
       for (int np = 0; np < 4; ++np) {
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(vbase + ks * 16 * kRowBytes + np * 32, b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * np], h0, h1, h2, h3, b0, b1);
+        mma_bf16_16816(o[2 * np], h0r, h1r, h2r, h3r, b0, b1);
         mma_bf16_16816(o[2 * np], l0r, l1r, l2r, l3r, b0, b1);
-        mma_bf16_16816(o[2 * np + 1], h0, h1, h2, h3, b2, b3);
+        mma_bf16_16816(o[2 * np + 1], h0r, h1r, h2r, h3r, b2, b3);
         mma_bf16_16816(o[2 * np + 1], l0r, l1r, l2r, l3r, b2, b3);
       }
     }
   }
 
   // ---- 5. merge the chunks
+  const int hr0 = pm * 16 + r0;  // output rows (heads within the CTA) of this thread
   if constexpr (CLUSTER) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     __syncthreads();  // every warp is done reading the K tile
-    float* sO = reinterpret_cast<float*>(sK);  // [16][kORow] fp32, this chunk's unnormalised O
+    float* sO = reinterpret_cast<float*>(sK);  // [kHG][kORow] fp32, this chunk's unnormalised O
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      const int col = warp * 64 + nt * 8 + 2 * (lane & 3);
-      *reinterpret_cast<float2*>(sO + r0 * kORow + col) = make_float2(o[nt][0], o[nt][1]);
-      *reinterpret_cast<float2*>(sO + (r0 + 8) * kORow + col) = make_float2(o[nt][2], o[nt][3]);
+      const int col = d0 + nt * 8 + 2 * (lane & 3);
+      *reinterpret_cast<float2*>(sO + hr0 * kORow + col) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(sO + (hr0 + 8) * kORow + col) = make_float2(o[nt][2], o[nt][3]);
     }
     cluster.sync();  // every chunk's (m, l, O) is visible cluster-wide
+    // loads from the other CTAs are all issued before any is used
     if (tid < kHG) {
-      float mc[kMaxClusterChunks];
-      float M = -INFINITY;
-      for (int c = 0; c < nchunks; ++c) {
-        mc[c] = *cluster.map_shared_rank(&s_m[tid], c);
-        M = fmaxf(M, mc[c]);
+      float mc[kMaxClusterChunks], lc[kMaxClusterChunks];
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c) {
+        mc[c] = c < nchunks ? *cluster.map_shared_rank(&s_m[tid], c) : -INFINITY;
+        lc[c] = c < nchunks ? *cluster.map_shared_rank(&s_l[tid], c) : 0.f;
       }
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c) M = fmaxf(M, mc[c]);
       float L = 0.f;
-      for (int c = 0; c < nchunks; ++c)
-        if (mc[c] != -INFINITY) L += expf(mc[c] - M) * *cluster.map_shared_rank(&s_l[tid], c);
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c) {
+        mc[c] = (mc[c] == -INFINITY) ? 0.f : expf(mc[c] - M);
+        L += mc[c] * lc[c];
+      }
       const float inv = L > 0.f ? 1.f / L : 0.f;
-      for (int c = 0; c < nchunks; ++c)
-        s_f[c][tid] = (mc[c] == -INFINITY) ? 0.f : expf(mc[c] - M) * inv;
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c) s_f[c][tid] = mc[c] * inv;
     }
     __syncthreads();
     const int rank = (int)cluster.block_rank();
-    constexpr int kVec = kHG * kD / 4;  // float4s of the [16][512] output
+    constexpr int kVec = kHG * kD / 4;  // float4s of the [kHG][512] output
     const int v0 = rank * kVec / nchunks, v1 = (rank + 1) * kVec / nchunks;
     for (int v = v0 + tid; v < v1; v += kAttnThreads) {
       const int h = (v * 4) / kD;
+      if (h >= hvalid) break;  // v grows with h
       const float4* src = reinterpret_cast<const float4*>(sO + h * kORow + (v * 4) % kD);
+      float4 x[kMaxClusterChunks];
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c)
+        x[c] = c < nchunks ? *cluster.map_shared_rank(src, c) : make_float4(0.f, 0.f, 0.f, 0.f);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < nchunks; ++c) {
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c) {
         const float f = s_f[c][h];
-        const float4 x = *cluster.map_shared_rank(src, c);
-        acc.x += f * x.x;
-        acc.y += f * x.y;
-        acc.z += f * x.z;
-        acc.w += f * x.w;
+        acc.x += f * x[c].x;
+        acc.y += f * x[c].y;
+        acc.z += f * x[c].z;
+        acc.w += f * x[c].w;
       }
       *reinterpret_cast<float4*>(a.out + (qi * a.hq + (int64_t)hg * kHG + h) * kD +
                                  (v * 4) % kD) = acc;
     }
     cluster.sync();  // no CTA leaves while another still reads its shared memory
   } else {
-    float* part = partial + ((qi * (a.hq / kHG) + hg) * (int64_t)nchunks + chunk) *
+    const int ngroups = (a.hq + kHG - 1) / kHG;
+    float* part = partial + ((qi * ngroups + hg) * (int64_t)nchunks + chunk) *
                                 PartialLayout::kFloats;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      const int col = warp * 64 + nt * 8 + 2 * (lane & 3);
-      *reinterpret_cast<float2*>(part + r0 * kD + col) = make_float2(o[nt][0], o[nt][1]);
-      *reinterpret_cast<float2*>(part + (r0 + 8) * kD + col) = make_float2(o[nt][2], o[nt][3]);
+      const int col = d0 + nt * 8 + 2 * (lane & 3);
+      *reinterpret_cast<float2*>(part + hr0 * kD + col) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(part + (hr0 + 8) * kD + col) = make_float2(o[nt][2], o[nt][3]);
     }
     __syncthreads();
     if (tid < kHG) {
@@ -488,8 +520,9 @@ __global__ void __launch_bounds__(128)
   const int h = blockIdx.x;
   const int64_t qi = blockIdx.y;
   const int hg = h / kHG, hr = h % kHG;
+  const int ngroups = (hq + kHG - 1) / kHG;
   const float* base =
-      partial + ((qi * (hq / kHG) + hg) * (int64_t)nchunks) * PartialLayout::kFloats;
+      partial + ((qi * ngroups + hg) * (int64_t)nchunks) * PartialLayout::kFloats;
   float M = -INFINITY;
   for (int c = 0; c < nchunks; ++c)
     M = fmaxf(M, base[c * PartialLayout::kFloats + kHG * kD + hr]);
@@ -526,7 +559,8 @@ size_t attn_workspace_bytes(const csa2_attn_args& a) {
   if (a.q_dtype != CSA2_BF16) return 0;
   const int64_t nchunks = attn_chunks(a);
   if (nchunks <= kMaxClusterChunks) return 0;  // merged on chip
-  return (size_t)a.nq * (a.hq / kHG) * nchunks * PartialLayout::kFloats * sizeof(float);
+  return (size_t)a.nq * ((a.hq + kHG - 1) / kHG) * nchunks * PartialLayout::kFloats *
+         sizeof(float);
 }
 
 csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s) {
@@ -554,7 +588,7 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e);
     attr_set = true;
   }
-  const dim3 grid((unsigned)nchunks, (unsigned)(a.hq / kHG), (unsigned)a.nq);
+  const dim3 grid((unsigned)nchunks, (unsigned)((a.hq + kHG - 1) / kHG), (unsigned)a.nq);
   if (nchunks <= kMaxClusterChunks) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;

@@ -225,8 +225,14 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   }
   const float* s = scores + row * ld;
 
-  // ---- level 1: threshold bin from the row's histogram
-  for (int i = tid; i < kBins; i += kTkThreads) hist[i] = hist1[row * kBins + i];
+  // ---- level 1: threshold bin from the row's histogram (all loads in flight)
+  {
+    uint32_t hv[kBins / kTkThreads];
+#pragma unroll
+    for (int u = 0; u < kBins / kTkThreads; ++u) hv[u] = hist1[row * kBins + tid + u * kTkThreads];
+#pragma unroll
+    for (int u = 0; u < kBins / kTkThreads; ++u) hist[tid + u * kTkThreads] = hv[u];
+  }
   __syncthreads();
   find_top(hist, kBins, (uint32_t)k, &tmp);
   const uint32_t T1 = (uint32_t)tmp.t;
@@ -271,6 +277,8 @@ __global__ void __launch_bounds__(kTkThreads, 1)
           p[e] = (j + e < wj1) && (key[e] >> 20) >= T1;
           c += p[e];
         }
+        // most steps hold no entry in the top bins: skip the lane scan
+        if (__ballot_sync(0xffffffffu, c != 0) == 0) continue;
         uint32_t incl = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -372,19 +380,22 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     s_tie = t;
   }
   cluster.sync();  // every CTA's counts are visible
+  if (tid < C) {  // every CTA's counts, one remote load per thread
+    tmp.tot[tid] = *cluster.map_shared_rank(&s_gt, tid);
+    tmp.wsum[tid] = *cluster.map_shared_rank(&s_tie, tid);
+  }
+  cluster.sync();  // no CTA reads another's shared memory after this point
   if (tid == 0) {
     uint32_t pre_sel = 0, pre_tie = 0;
     for (int c = 0; c < r; ++c) {
-      const uint32_t gc = *cluster.map_shared_rank(&s_gt, c);
-      const uint32_t tc = *cluster.map_shared_rank(&s_tie, c);
-      const uint32_t qc = min(tc, need > pre_tie ? need - pre_tie : 0u);
-      pre_tie += tc;
-      pre_sel += gc + qc;
+      const uint32_t qc = min(tmp.wsum[c], need > pre_tie ? need - pre_tie : 0u);
+      pre_tie += tmp.wsum[c];
+      pre_sel += tmp.tot[c] + qc;
     }
     s_quota = min(s_tie, need > pre_tie ? need - pre_tie : 0u);
     s_off = pre_sel;
   }
-  cluster.sync();  // no CTA reads another's shared memory after this point
+  __syncthreads();
   uint32_t woff = s_off, tq = s_quota;
   for (int w = 0; w < warp; ++w) {
     const uint32_t qw = min(wtie[w], tq);

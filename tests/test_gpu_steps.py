@@ -265,6 +265,29 @@ def test_attn_bf16(csa2, orc, nq, hq, n, k, W):
     assert rel_l2(out.cpu().numpy(), ref) <= 2e-3
 
 
+def test_attn_bf16_single_key_is_the_dequantised_row(csa2, orc):
+    # one selected entry, no window and q = 0: its softmax weight is exactly
+    # 1, so the output is the dequantised FP4 row itself, bit for bit.  The
+    # rows hold every code byte, with scale bytes 0..252 -- every byte the
+    # quantiser writes for bf16 input (the fast bf16 path for 8..250, the
+    # fp32 path outside it; 253 and 254 would overflow bf16).
+    d, n, hq = 512, 253, 48
+    codes = torch.arange(n * d // 2, dtype=torch.int64).remainder(256).to(torch.uint8)
+    codes = codes.reshape(n, d // 2)
+    codes = codes[:, torch.randperm(d // 2, generator=torch.Generator().manual_seed(124))]
+    scales = torch.arange(n * d // 32, dtype=torch.int64).remainder(253).to(torch.uint8)
+    scales = scales.reshape(n, d // 32)
+    ref_rows = orc.dequantize_fp4(codes.numpy(), scales.numpy(), d)      # [n, d]
+    # n queries of one sequence; query j selects entry j
+    q = torch.zeros((n, hq, d), dtype=torch.bfloat16)
+    idx = torch.arange(n, dtype=torch.int32).reshape(n, 1)
+    win = torch.zeros((1, 0, d), dtype=torch.bfloat16)
+    out = csa2.sparse_attn(dev(q), dev(codes)[None], dev(scales)[None], dev(idx), dev(win), 0.01,
+                           q_per_seq=n)
+    got = out.cpu().double().numpy()
+    assert np.array_equal(got, np.broadcast_to(ref_rows[:, None, :], got.shape))
+
+
 def test_attn_bf16_empty_chunks(csa2, orc):
     # 200 selected entries then 312 x -1: chunks 3..5 hold no key at all and
     # must drop out of the merge (their max is -inf)
