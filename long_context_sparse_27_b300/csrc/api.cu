@@ -131,17 +131,18 @@ csa2_status check_index(const csa2_index_args* a) {
 
 // hist1 (nullable): first-level top-k histograms the decode FP8 kernel adds
 // the scores' keys to (index_fuses_topk_hist).
-csa2_status run_index(const csa2_index_args& a, uint32_t* hist1, cudaStream_t s) {
+csa2_status run_index(const csa2_index_args& a, uint32_t* hist1, IndexTuning tune,
+                      cudaStream_t s) {
   if (a.B * a.q_per_seq == 0 || a.n == 0) return CSA2_OK;
   if (!fp8_path(&a)) return launch_index_score_f32(a, s);
   if (a.q_dtype == CSA2_E4M3)
-    return launch_index_score_fp8(a, static_cast<const uint8_t*>(a.q), a.w, hist1, s);
+    return launch_index_score_fp8(a, static_cast<const uint8_t*>(a.q), a.w, hist1, tune, s);
   const int64_t nq = a.B * a.q_per_seq;
   uint8_t* q8 = static_cast<uint8_t*>(a.workspace);
   float* c = reinterpret_cast<float*>(q8 + align256((size_t)nq * a.hi * a.di));
   csa2_status st = launch_quantize_index_q(a.q, a.w, nq, a.hi, a.di, q8, c, s);
   if (st != CSA2_OK) return st;
-  return launch_index_score_fp8(a, q8, c, hist1, s);
+  return launch_index_score_fp8(a, q8, c, hist1, tune, s);
 }
 
 csa2_status check_topk(const float* scores, int64_t rows, int64_t n, int64_t ld, int32_t k,
@@ -369,7 +370,7 @@ csa2_status csa2_index_score(const csa2_index_args* args, csa2_stream_t stream) 
   csa2_status st = check_index(args);
   if (st != CSA2_OK) return st;
   if ((st = injected("index_score")) != CSA2_OK) return st;
-  return run_index(*args, nullptr, reinterpret_cast<cudaStream_t>(stream));
+  return run_index(*args, nullptr, IndexTuning{}, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t csa2_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k) {
@@ -479,6 +480,17 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
   }
   if ((st = injected("layer_stack")) != CSA2_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // indexer-key traffic: a Full layer's keys are read again by the Reindex
+  // layers that take that Full layer as their source.  A read that has a
+  // later re-read keeps its keys in L2 (normal policy); each re-read walks
+  // the tiles in the opposite direction to the previous read, so it starts
+  // on the tiles that read touched last -- the ones still in L2.
+  bool reverse_next[64] = {false};  // per Full layer (by index, plans of <= 64 layers)
+  auto read_again = [&](int32_t from, int32_t src) {
+    for (int32_t m = from + 1; m < n_layers; ++m)
+      if (L[m].mode == CSA2_MODE_REINDEX && L[m].kv_src == src) return true;
+    return false;
+  };
   for (int32_t l = 0; l < n_layers; ++l) {
     const csa2_layer_desc& d = L[l];
     const csa2_layer_desc& kv = L[d.kv_src];
@@ -490,8 +502,14 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
       // decode: the indexer kernel also builds the top-k's first-level
       // histograms; otherwise a histogram pass over the scores does
       const bool fused = index_fuses_topk_hist(ia);
+      IndexTuning tune;
+      if (d.kv_src < 64) {
+        tune.reverse = reverse_next[d.kv_src];
+        tune.keep_in_l2 = read_again(l, d.kv_src);
+        reverse_next[d.kv_src] = !tune.reverse;
+      }
       if ((st = clear_topk_hist(hist, nq, cs)) != CSA2_OK) return st;
-      if ((st = run_index(ia, fused ? hist : nullptr, cs)) != CSA2_OK) return st;
+      if ((st = run_index(ia, fused ? hist : nullptr, tune, cs)) != CSA2_OK) return st;
       if (!fused &&
           (st = launch_topk_hist(scores, nq, s->n, s->n, s->n_valid, hist, cs)) != CSA2_OK)
         return st;

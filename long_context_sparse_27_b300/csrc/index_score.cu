@@ -144,10 +144,12 @@ struct TcParams {
   int64_t ktiles;          // ceil(n / 128)
   int32_t* dev_status;
   uint32_t* hist1;         // QG = 1: [nq][4096] first-level top-k histograms to add to, or null
+  int reverse;             // walk each CTA's tile range from its end
+  int keep_in_l2;          // load keys with the normal L2 policy instead of evict-first
 };
 
-// (group, tile within the group) of the CTA's tiles, advanced without
-// 64-bit divisions: tile t is group t / ktiles, tile t % ktiles.
+// (group, tile within the group) of the CTA's tiles, moved without 64-bit
+// divisions: tile t is group t / ktiles, tile t % ktiles.
 struct TileCursor {
   int64_t g, kt, ktiles;
   __device__ TileCursor(int64_t t, int64_t ktiles_) : g(t / ktiles_), kt(t % ktiles_), ktiles(ktiles_) {}
@@ -156,6 +158,10 @@ struct TileCursor {
     while (kt >= ktiles) {
       kt -= ktiles;
       ++g;
+    }
+    while (kt < 0) {
+      kt += ktiles;
+      --g;
     }
   }
 };
@@ -220,14 +226,15 @@ __global__ void __launch_bounds__(TcCfg<QG, EPI_WGS>::THREADS, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && t_begin < t_end) {
-      const uint64_t pol_k = l2_policy_evict_first();
+      const uint64_t pol_k = p.keep_in_l2 ? l2_policy_evict_normal() : l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
       int stage = 0;
       uint32_t ph = 0;
       int64_t g_prev = -1, qcount = 0, issued = 0;
       bool ok = true;
-      TileCursor cur(t_begin, p.ktiles);
-      for (int64_t t = t_begin; t < t_end; ++t, cur.advance(1)) {
+      const int64_t dir = p.reverse ? -1 : 1;
+      TileCursor cur(p.reverse ? t_end - 1 : t_begin, p.ktiles);
+      for (int64_t i = 0; i < t_end - t_begin; ++i, cur.advance(dir)) {
         const int64_t g = cur.g, kt = cur.kt;
         if (g != g_prev) {
           const int qs = (int)(qcount & 1);
@@ -278,8 +285,9 @@ __global__ void __launch_bounds__(TcCfg<QG, EPI_WGS>::THREADS, 1)
       int64_t g_prev = -1, qcount = 0;
       int qs = 0;
       bool any = false;
-      TileCursor cur(t_begin, p.ktiles);
-      for (int64_t t = t_begin; t < t_end; ++t, cur.advance(1)) {
+      const int64_t dir = p.reverse ? -1 : 1;
+      TileCursor cur(p.reverse ? t_end - 1 : t_begin, p.ktiles);
+      for (int64_t i = 0; i < t_end - t_begin; ++i, cur.advance(dir)) {
         const int64_t g = cur.g;
         if (g != g_prev) {
           if (g_prev >= 0) tc_commit(&qempty[qs]);  // old Q free once its MMAs finish
@@ -332,8 +340,10 @@ __global__ void __launch_bounds__(TcCfg<QG, EPI_WGS>::THREADS, 1)
     float* my_c = cbuf + ew * 2 * C::BN;
     int cb = 1;
     int64_t nv[QG];
-    TileCursor cur(t_begin + wg, p.ktiles);
-    for (int64_t li = wg; t_begin + li < t_end; li += C::EPI_WGS, cur.advance(C::EPI_WGS)) {
+    // li counts tiles in processing order (from the range's end when reversed)
+    const int64_t dir = p.reverse ? -1 : 1;
+    TileCursor cur(p.reverse ? t_end - 1 - wg : t_begin + wg, p.ktiles);
+    for (int64_t li = wg; li < t_end - t_begin; li += C::EPI_WGS, cur.advance(dir * C::EPI_WGS)) {
       const int64_t g = cur.g, kt = cur.kt;
       const int acc = (int)(li % C::NACC);
       const uint32_t aph = (uint32_t)((li / C::NACC) & 1);
@@ -448,7 +458,7 @@ EncodeTiledFn encode_fn() {
 
 template <int QG>
 csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* c,
-                      uint32_t* hist1, cudaStream_t s) {
+                      uint32_t* hist1, IndexTuning tune, cudaStream_t s) {
   using C = TcCfg<QG>;
   constexpr int W = C::EPI_WGS;
   EncodeTiledFn enc = encode_fn();
@@ -486,6 +496,8 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   p.ktiles = (a.n + C::BM - 1) / C::BM;
   p.dev_status = a.dev_status;
   p.hist1 = QG == 1 ? hist1 : nullptr;
+  p.reverse = tune.reverse ? 1 : 0;
+  p.keep_in_l2 = tune.keep_in_l2 ? 1 : 0;
   const int64_t total = p.groups * p.ktiles;
   if (total == 0) return CSA2_OK;
   static bool attr_set = false;
@@ -504,11 +516,11 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
 }  // namespace
 
 csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, const float* c,
-                                   uint32_t* hist1, cudaStream_t s) {
+                                   uint32_t* hist1, IndexTuning tune, cudaStream_t s) {
   if (a.hi != 64 || a.di != 128) return CSA2_ERR_UNSUPPORTED;
   if (a.B * a.q_per_seq == 0 || a.n == 0) return CSA2_OK;
-  if (a.q_per_seq % 4 == 0) return launch_tc<4>(a, q8, c, nullptr, s);
-  return launch_tc<1>(a, q8, c, hist1, s);
+  if (a.q_per_seq % 4 == 0) return launch_tc<4>(a, q8, c, nullptr, tune, s);
+  return launch_tc<1>(a, q8, c, hist1, tune, s);
 }
 
 bool index_fuses_topk_hist(const csa2_index_args& a) {

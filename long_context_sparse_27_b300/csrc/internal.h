@@ -24,11 +24,21 @@ csa2_status launch_quantize_index_q(const void* q, const float* w, int64_t nq, i
                                     int32_t di, uint8_t* q8, float* c, cudaStream_t s);
 // a3, fp32 CUDA-core path
 csa2_status launch_index_score_f32(const csa2_index_args& a, cudaStream_t s);
+// How one FP8 indexer launch walks the keys.  Each CTA owns a contiguous
+// range of 128-entry tiles; `reverse` walks it from its end (so a launch
+// that follows another reader of the same keys starts on the tiles that
+// reader left in L2), `keep_in_l2` loads with the normal L2 policy instead of
+// evict-first (when a later layer reads the same keys again).
+struct IndexTuning {
+  bool reverse = false;
+  bool keep_in_l2 = false;
+};
+
 // a3, FP8 tensor-core path: q8 / c already quantised.  hist1 (nullable):
 // [nq][4096] first-level top-k histograms the decode kernel adds its scores'
 // keys to (see index_fuses_topk_hist).
 csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, const float* c,
-                                   uint32_t* hist1, cudaStream_t s);
+                                   uint32_t* hist1, IndexTuning tune, cudaStream_t s);
 // whether launch_index_score_fp8 builds the top-k histograms for `a`
 bool index_fuses_topk_hist(const csa2_index_args& a);
 // a4: the workspace holds one 4096-bin first-level histogram per row

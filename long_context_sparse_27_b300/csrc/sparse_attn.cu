@@ -177,11 +177,13 @@ constexpr int kSmemK = kKC * kRowBytes;  // later reused for the chunk's fp32 O 
 constexpr int kSmemP = 2 * kHG * kPRow;  // P split into bf16 hi and lo
 constexpr int kAttnSmem = kSmemQ + kSmemK + kSmemP;
 constexpr int kPieces = kD / 8;          // 16-byte pieces of a bf16 row (8 elements)
-constexpr int kKItems = kKC * kPieces / kAttnThreads;  // K-tile pieces per thread
+constexpr int kBlocks = kD / 32;         // 32-element blocks of a row (16 code bytes each)
+constexpr int kBItems = kKC * kBlocks / kAttnThreads;  // K-tile blocks per thread
 constexpr int kQItems = kHG * kPieces / kAttnThreads;  // Q-tile pieces per thread
 constexpr int kORow = kD + 8;            // padded fp32 row of the chunk output
-static_assert(kKC * kPieces % kAttnThreads == 0 && kHG * kPieces % kAttnThreads == 0,
-              "tiles split evenly over the threads");
+static_assert(kKC * kBlocks % kAttnThreads == 0 && kAttnThreads % kBlocks == 0 &&
+                  kHG * kPieces % kAttnThreads == 0,
+              "tiles split evenly over the threads, one block column per thread");
 static_assert(kHG * kORow * 4 <= kSmemK, "the fp32 chunk output fits in the K tile");
 static_assert(kSWarps <= kAttnWarps && kKC % 16 == 0, "S tiling");
 static_assert(kPVSlice == 64 && kAttnWarps % kMT == 0, "PV tiling");
@@ -259,47 +261,66 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   }
   __syncthreads();
 
-  // ---- 2. K tile
+  // ---- 2. K tile: item = (row r, 32-element block c) = 16 code bytes -> 64
+  // bf16 bytes; thread t always takes block c = t % 16 of rows t / 16 + 16u.
+  // FP4 items load their 16 code bytes and scale byte into registers first
+  // (every load in flight at once); window items copy 64 bytes with
+  // cp.async.  An item's four 16-byte output pieces go out in the order
+  // (v + t / 2) % 4, so each group of 8 lanes covers all 8 bank quads of its
+  // 128-byte wavefront.
   {
-    uint32_t cw[kKItems];
-    uint32_t sb[kKItems];
+    const int c = tid % kBlocks;
+    const int rot = (tid >> 1) & 3;
+    uint4 cw[kBItems];
+    uint32_t sb[kBItems];
 #pragma unroll
-    for (int u = 0; u < kKItems; ++u) {
-      const int i = tid + u * kAttnThreads;
-      const int r = i / kPieces, c = i % kPieces;
+    for (int u = 0; u < kBItems; ++u) {
+      const int r = tid / kBlocks + u * (kAttnThreads / kBlocks);
       const uint8_t* cp = rows.codes[r];
-      cw[u] = cp ? __ldg(reinterpret_cast<const uint32_t*>(cp) + c) : 0u;
-      sb[u] = cp ? (uint32_t)__ldg(rows.scales[r] + c / 4) : 0u;
+      cw[u] = cp ? __ldg(reinterpret_cast<const uint4*>(cp) + c) : make_uint4(0, 0, 0, 0);
+      sb[u] = cp ? (uint32_t)__ldg(rows.scales[r] + c) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < kKItems; ++u) {
-      const int i = tid + u * kAttnThreads;
-      const int r = i / kPieces, c = i % kPieces;
-      if (rows.win[r]) cp_async16(sK + r * kRowBytes + c * 16, rows.win[r] + c * 8);
-    }
+    for (int u = 0; u < kBItems; ++u) {
+      const int r = tid / kBlocks + u * (kAttnThreads / kBlocks);
+      const uint16_t* wrow = rows.win[r];
+      if (wrow) {
 #pragma unroll
-    for (int u = 0; u < kKItems; ++u) {
-      const int i = tid + u * kAttnThreads;
-      const int r = i / kPieces, c = i % kPieces;
-      if (rows.win[r]) continue;  // copied by cp.async
-      uint32_t packed[4] = {0u, 0u, 0u, 0u};  // no key: zero piece (P is 0 there)
-      if (rows.codes[r]) {
-        if (sb[u] >= 8 && sb[u] <= 250) {
-          // scale 2^(sb - 127) in [2^-119, 2^123]: every product is a normal
-          // bf16, so the bf16x2 multiply is exact
-          const __nv_bfloat16 sc1 = __float2bfloat16_rn(ue8m0_value(sb[u]));
-          e2m1x8_to_bf16(cw[u], __halves2bfloat162(sc1, sc1), packed);
-        } else {
-          const float sc = ue8m0_value(sb[u]);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const uint32_t byte = (cw[u] >> (8 * p)) & 0xFFu;
-            packed[p] = pack_bf16x2(e2m1_value(byte & 15u) * sc, e2m1_value(byte >> 4) * sc);
-          }
+        for (int v = 0; v < 4; ++v) {
+          const int vv = (v + rot) & 3;
+          cp_async16(sK + r * kRowBytes + c * 64 + vv * 16, wrow + c * 32 + vv * 8);
         }
       }
-      *reinterpret_cast<uint4*>(sK + r * kRowBytes + c * 16) =
-          make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+#pragma unroll
+    for (int u = 0; u < kBItems; ++u) {
+      const int r = tid / kBlocks + u * (kAttnThreads / kBlocks);
+      if (rows.win[r]) continue;  // copied by cp.async
+      const bool fp4 = rows.codes[r] != nullptr;  // else: no key, zero row (P is 0 there)
+      // scale 2^(sb - 127) in [2^-119, 2^123]: every product is a normal
+      // bf16, so the bf16x2 multiply is exact; other scales take fp32
+      const bool fast = sb[u] >= 8 && sb[u] <= 250;
+      const float scf = ue8m0_value(sb[u]);
+      const __nv_bfloat16 sc1 = __float2bfloat16_rn(fast ? scf : 1.f);
+      const __nv_bfloat162 sc2 = __halves2bfloat162(sc1, sc1);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int vv = (v + rot) & 3;
+        const uint32_t word =
+            vv == 0 ? cw[u].x : (vv == 1 ? cw[u].y : (vv == 2 ? cw[u].z : cw[u].w));
+        uint32_t packed[4] = {0u, 0u, 0u, 0u};
+        if (fast) {
+          e2m1x8_to_bf16(word, sc2, packed);
+        } else if (fp4) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t byte = (word >> (8 * p)) & 0xFFu;
+            packed[p] = pack_bf16x2(e2m1_value(byte & 15u) * scf, e2m1_value(byte >> 4) * scf);
+          }
+        }
+        *reinterpret_cast<uint4*>(sK + r * kRowBytes + c * 64 + vv * 16) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      }
     }
   }
   cp_async_wait_all();

@@ -140,6 +140,13 @@ class StackWorkload:
                      + nq * wl.Hq * wl.D * (4 if wl.attn_q_fp32 else 2) + nq * wl.Hq * wl.D * 4)
         return index_layers * per_index + len(wl.modes) * per_layer
 
+    def visible_pairs(self):
+        """(query, entry) pairs the indexer scores: nq * N in decode, the
+        causal count in a prefill chunk."""
+        if self.n_valid is None:
+            return self.wl.nq * self.wl.N
+        return int(self.n_valid.to(torch.int64).sum().item())
+
     def indexer_bytes_per_layer(self):
         wl = self.wl
         return wl.B * wl.N * wl.Di * (4 if wl.fp32_indexer else 1)

@@ -160,52 +160,86 @@ def test_stack_rejects_bad_plans(csa2):
 
 # ------------------------------------------------------------------ full size
 
-def test_full_size_1m_sampled(csa2, orc):
-    """The 1M-context, 20-layer decode step as the benchmark runs it, checked
-    on samples: layer 0's scores at sampled entries, layer 0's selection as a
-    valid top-k of the GPU's own scores, recall against the oracle's fp64
-    selection for two sequences, and the attention of layers 0-3 for those
-    sequences."""
+def sampled_full_check(csa2, orc, wl, seed, queries, index_layers=(0,)):
+    """A full-size step as the benchmark runs it (device-drawn inputs, the
+    same launch configuration), checked on sampled queries: for each index
+    layer in `index_layers` and each sampled query, the GPU's scores at
+    sampled entries against the oracle, the GPU selection as a valid top-k
+    of the GPU's own scores, recall >= 0.999 against the oracle's fp64
+    selection, and the attention output of that layer (and of the Reuse
+    layers that take its indices) wherever the two selections agree."""
     from long_context_sparse_27_b300.workload import StackWorkload
-    wl = synth.C1M
-    W = StackWorkload(wl, seed=11, gen_device="cuda", keep_bf16=False)
-    # keep the first Full layer's bf16 rows for the oracle (regenerated: the
-    # draws are seeded)
-    s0 = 11 * 1000
-    kk = synth.index_k_rows(wl, s0 + 6, "cuda")
-    kv = synth.kv_rows(wl, s0 + 5, "cuda")
+    W = StackWorkload(wl, seed=seed, gen_device="cuda", keep_bf16=False)
     run_stack(W)
-    L0 = W.layers[0]
-    scores = csa2.index_score(L0["idx_q"], L0["idx_w"], L0["idxk"])
-    torch.cuda.synchronize()
-    g_scores = scores.cpu().numpy()
-    g_idx = L0["topk_idx"].cpu().numpy()
-    for b in range(wl.B):
-        assert topk_valid(g_scores[b], g_idx[b], wl.k, wl.N), b
-    rng = np.random.default_rng(0)
-    for b in (0, wl.B - 1):
-        k8 = orc.cast_e4m3(f64(kk[b]))[None]
-        ref_s = orc.index_score_fp8(f64(L0["idx_q"][b:b + 1]), f64(L0["idx_w"][b:b + 1]), k8)
-        cols = rng.choice(wl.N, 4096, replace=False)
-        cols[:wl.k] = np.sort(g_idx[b])  # include the selected entries
-        assert score_close(g_scores[b:b + 1, cols], ref_s[:, cols]) <= 1.0
-        ref_idx = orc.topk(ref_s, wl.k)
-        assert recall(g_idx[b:b + 1], ref_idx) >= 0.999
-        # attention of the Full layer and of the layers that reuse its cache
-        sel = np.unique(np.concatenate([ref_idx[0], g_idx[b]]))
-        sel = sel[sel >= 0]
-        c, sc = orc.quantize_fp4(f64(kv[b, sel]))
-        codes = np.zeros((1, wl.N, wl.D // 2), np.uint8)
-        scl = np.zeros((1, wl.N, wl.D // 32), np.uint8)
-        codes[0, sel], scl[0, sel] = c, sc
-        for l in range(4):
-            m, (kvs, ixs) = wl.modes[l], W.plan[l]
-            L = W.layers[l]
-            if m == synth.REINDEX:
-                continue  # its own selection: covered by the scaled tests
-            idx = g_idx[b:b + 1] if np.array_equal(g_idx[b], ref_idx[0]) else None
-            if idx is None:
+    nv_all = None if W.n_valid is None else W.n_valid.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    checked_attn = 0
+    for l in index_layers:
+        m, (kvs, _) = wl.modes[l], W.plan[l]
+        assert m in (synth.FULL, synth.REINDEX)
+        L, src = W.layers[l], W.layers[kvs]
+        # the source Full layer's rows, drawn again (the draws are seeded)
+        s0 = seed * 1000 + 20 * kvs
+        kk = synth.index_k_rows(wl, s0 + 6, "cuda")
+        kv = synth.kv_rows(wl, s0 + 5, "cuda")
+        scores = csa2.index_score(L["idx_q"], L["idx_w"], src["idxk"], q_per_seq=wl.q_per_seq,
+                                  n_valid=W.n_valid)
+        torch.cuda.synchronize()
+        g_idx_all = L["topk_idx"].cpu().numpy()
+        for q in queries:
+            b = q // wl.q_per_seq
+            nvq = wl.N if nv_all is None else int(nv_all[q])
+            g_s = scores[q:q + 1].cpu().numpy()
+            g_idx = g_idx_all[q:q + 1]
+            assert topk_valid(g_s[0], g_idx[0], wl.k, nvq), (l, q)
+            k8 = orc.cast_e4m3(f64(kk[b]))[None]
+            ref_s = orc.index_score_fp8(f64(L["idx_q"][q:q + 1]), f64(L["idx_w"][q:q + 1]), k8,
+                                        1, None if nv_all is None else nv_all[q:q + 1])
+            cols = rng.choice(wl.N, min(4096, wl.N), replace=False)
+            sel = g_idx[0][g_idx[0] >= 0]
+            cols[: len(sel)] = sel  # include the selected entries
+            assert score_close(g_s[:, cols], ref_s[:, cols]) <= 1.0, (l, q)
+            ref_idx = orc.topk(ref_s, wl.k, None if nv_all is None else nv_all[q:q + 1])
+            assert recall(g_idx, ref_idx) >= 0.999, (l, q)
+            if not np.array_equal(g_idx, ref_idx):
                 continue
-            ref = orc.sparse_attn(f64(L["attn_q"][b:b + 1]), codes, scl, ref_idx,
-                                  f64(L["window"][b:b + 1]), 1 / math.sqrt(wl.D))
-            assert rel_l2(L["out"][b:b + 1].cpu().numpy(), ref) <= 2e-3, l
+            rows = ref_idx[0][ref_idx[0] >= 0]
+            c, sc = orc.quantize_fp4(f64(kv[b, rows]))
+            codes = np.zeros((1, wl.N, wl.D // 2), np.uint8)
+            scl = np.zeros((1, wl.N, wl.D // 32), np.uint8)
+            codes[0, rows], scl[0, rows] = c, sc
+            # this layer and every Reuse layer that takes its indices
+            for l2 in [l] + [j for j, (mm, (kv2, ix2)) in enumerate(zip(wl.modes, W.plan))
+                             if mm == synth.REUSE and ix2 == l]:
+                L2 = W.layers[l2]
+                kw = {}
+                if W.win_start is not None:  # prefill: query t attends window rows t .. t+W-1
+                    kw = dict(win_start=W.win_start.cpu().numpy()[q:q + 1],
+                              win_len=W.win_len.cpu().numpy()[q:q + 1])
+                win = f64(L2["window"][b:b + 1])
+                ref = orc.sparse_attn(f64(L2["attn_q"][q:q + 1]), codes, scl, ref_idx, win,
+                                      1 / math.sqrt(wl.D), **kw)
+                assert rel_l2(L2["out"][q:q + 1].cpu().numpy(), ref) <= 2e-3, (l2, q)
+                checked_attn += 1
+    assert checked_attn > 0
+
+
+def test_full_size_1m_sampled(csa2, orc):
+    """The 1M-context, 20-layer decode step as the benchmark runs it: the
+    first group's Full and Reindex layers (and the Reuse layers after them)
+    for the first and last sequence."""
+    sampled_full_check(csa2, orc, synth.C1M, 11, queries=(0, 7), index_layers=(0, 1))
+
+
+def test_full_size_128k_sampled(csa2, orc):
+    sampled_full_check(csa2, orc, synth.C128K, 12, queries=(0, 9, 15))
+
+
+def test_full_size_group3_sampled(csa2, orc):
+    sampled_full_check(csa2, orc, synth.GROUP3, 13, queries=(0, 31), index_layers=(0, 1))
+
+
+def test_full_size_prefill_sampled(csa2, orc):
+    """The 4096-query prefill chunk at N = 262144: the first, a middle and the
+    last query (their causal visibility differs)."""
+    sampled_full_check(csa2, orc, synth.PREFILL, 14, queries=(0, 2047, 4095))
