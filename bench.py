@@ -322,12 +322,18 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches_per_step(wl) * args.steps,
         "clocks": clk.summary(),
     }
-    traffic = os.path.join(ROOT, "profiles", "idx_score_tc_traffic.json")
+    # DRAM bytes of one indexer launch from the committed ncu summary, when it
+    # was taken on this workload's indexer launch shape
+    traffic = os.path.join(ROOT, "profiles", "idx_score_tc_traffic.txt")
     if os.path.exists(traffic):
+        kv = {}
         with open(traffic) as f:
-            t = json.load(f)
-        if t.get("workload") == wl.name:
-            line["roofline"]["traffic"] = t.get("bytes_per_launch")
+            for ln in f:
+                if ":" in ln and not ln.startswith("#"):
+                    key, val = ln.split(":", 1)
+                    kv[key.strip()] = val.strip()
+        if kv.get("workload") == wl.name and "bytes_per_launch" in kv:
+            line["roofline"]["traffic"] = int(kv["bytes_per_launch"])
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
     return line
