@@ -31,6 +31,14 @@ csa2_status check_launch() {
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e);
 }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("CSA2_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -491,6 +499,9 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
       if (L[m].mode == CSA2_MODE_REINDEX && L[m].kv_src == src) return true;
     return false;
   };
+  // the top-k histograms start at zero; every selection leaves them zeroed,
+  // so one clear serves the whole stack (and keeps the launches back to back)
+  if ((st = clear_topk_hist(hist, nq, cs)) != CSA2_OK) return st;
   for (int32_t l = 0; l < n_layers; ++l) {
     const csa2_layer_desc& d = L[l];
     const csa2_layer_desc& kv = L[d.kv_src];
@@ -508,7 +519,6 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
         tune.keep_in_l2 = read_again(l, d.kv_src);
         reverse_next[d.kv_src] = !tune.reverse;
       }
-      if ((st = clear_topk_hist(hist, nq, cs)) != CSA2_OK) return st;
       if ((st = run_index(ia, fused ? hist : nullptr, tune, cs)) != CSA2_OK) return st;
       if (!fused &&
           (st = launch_topk_hist(scores, nq, s->n, s->n, s->n_valid, hist, cs)) != CSA2_OK)

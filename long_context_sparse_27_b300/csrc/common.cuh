@@ -80,6 +80,25 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 constexpr int kTopkBins = 4096;  // first-level digit: the key's top 12 bits
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Every kernel of this library is launched with programmatic stream
+// serialisation.  Each kernel waits for the previous kernel on the stream to
+// finish and its writes to be visible (pdl_wait) before its first global-
+// memory access, and lets the next kernel launch once its own CTAs are
+// finishing (pdl_trigger near its end; a CTA that exits counts as having
+// triggered).  The next kernel's launch and prologue (shared-memory setup,
+// barrier init, tensor-memory allocation) thereby overlap this kernel's
+// drain; the data order is the stream order.  Triggering at kernel entry
+// was measured slower: the early CTAs of the next kernel took SM resources
+// from the running one.  Both are no-ops for a launch without the attribute.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // device status
 // ---------------------------------------------------------------------------
 

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kF32Warps * 32)
                          const int32_t* __restrict__ n_valid, float* __restrict__ scores,
                          int64_t scores_ld, int64_t per_block) {
   extern __shared__ float sq[];  // [hi * di] query, then [hi] weights
+  pdl_wait();
   const int64_t qi = blockIdx.y;
   const float* qsrc = q + qi * (int64_t)hi * di;
   for (int i = threadIdx.x; i < hi * di; i += blockDim.x) sq[i] = qsrc[i];
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kF32Warps * 32)
     }
     if (lane == 0) scores[qi * scores_ld + j] = s;
   }
+  pdl_trigger();
 }
 
 }  // namespace
@@ -81,10 +83,10 @@ csa2_status launch_index_score_f32(const csa2_index_args& a, cudaStream_t s) {
   const int64_t per_block = 256;
   dim3 grid((unsigned)((a.n + per_block - 1) / per_block), (unsigned)nq);
   const size_t smem = sizeof(float) * ((size_t)a.hi * a.di + a.hi);
-  idx_score_f32_kernel<<<grid, kF32Warps * 32, smem, s>>>(
-      static_cast<const float*>(a.q), a.w, static_cast<const float*>(a.k), a.q_per_seq, a.hi,
-      a.di, a.n, a.k_ld, a.k_seq_stride, a.n_valid, a.scores, a.scores_ld, per_block);
-  return check_launch();
+  return launch_kernel(idx_score_f32_kernel, grid, dim3(kF32Warps * 32), smem, s, 1,
+                       static_cast<const float*>(a.q), a.w, static_cast<const float*>(a.k),
+                       a.q_per_seq, a.hi, a.di, a.n, a.k_ld, a.k_seq_stride, a.n_valid, a.scores,
+                       a.scores_ld, per_block);
 }
 
 // ===========================================================================
@@ -222,6 +224,7 @@ __global__ void __launch_bounds__(TcCfg<QG, EPI_WGS>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the setup above overlapped the previous kernel; global data from here on
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -419,6 +422,7 @@ __global__ void __launch_bounds__(TcCfg<QG, EPI_WGS>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();  // the next kernel may start launching while this one drains
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -509,8 +513,8 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
     attr_set = true;
   }
   const int grid = (int)std::min<int64_t>(total, sm_count());
-  idx_score_tc_kernel<QG, W><<<grid, C::THREADS, C::SMEM_ALLOC, s>>>(kmap, qmap, p);
-  return check_launch();
+  return launch_kernel(idx_score_tc_kernel<QG, W>, dim3(grid), dim3(C::THREADS),
+                       (size_t)C::SMEM_ALLOC, s, 1, kmap, qmap, p);
 }
 
 }  // namespace

@@ -47,12 +47,12 @@ csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld
                         const int32_t* n_valid, int32_t k, int32_t* idx_out, int64_t idx_ld,
                         void* ws, int32_t* dev_status, cudaStream_t s);
 // the pieces of launch_topk: zero the histograms; select from scores whose
-// histograms are complete
+// histograms are complete (the selection leaves the histograms zeroed)
 csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s);
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
                              const int32_t* n_valid, uint32_t* hist1, cudaStream_t s);
 csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int64_t ld,
-                               const int32_t* n_valid, int32_t k, const uint32_t* hist1,
+                               const int32_t* n_valid, int32_t k, uint32_t* hist1,
                                int32_t* idx_out, int64_t idx_ld, cudaStream_t s);
 // a5
 size_t attn_workspace_bytes(const csa2_attn_args& a);
@@ -60,5 +60,40 @@ csa2_status launch_sparse_attn(const csa2_attn_args& a, cudaStream_t s);
 
 // number of SMs of the current device (cached per device)
 int sm_count();
+
+// Whether launches use programmatic dependent launch: CSA2_PDL=0 turns it
+// off (read once per process; default on).
+bool pdl_enabled();
+
+// Launch with programmatic dependent launch (see pdl_trigger / pdl_wait in
+// common.cuh) and, if cluster_x > 1, thread-block clusters of cluster_x CTAs
+// along x.
+template <typename... KArgs, typename... Args>
+csa2_status launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  return e == cudaSuccess ? check_launch() : cuda_fail(e);
+}
 
 }  // namespace csa2

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kQuantThreads)
                      int64_t scales_ld, const uint16_t* __restrict__ kx, int32_t di,
                      int64_t k_ld, uint8_t* __restrict__ k8, int64_t k8_ld, int64_t kv_threads,
                      int64_t k_begin) {
+  pdl_wait();
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid < k_begin) {
     const int64_t per_row = d / 8;
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(256)
     quant_index_q_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
                          int64_t n_heads_total, uint8_t* __restrict__ q8, float* __restrict__ c) {
   constexpr int PER = DI / 32;
+  pdl_wait();
   const int64_t head = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (head >= n_heads_total) return;  // whole warp leaves together
@@ -126,11 +128,10 @@ csa2_status launch_quantize_fp4(const csa2_quant_args& a, cudaStream_t s) {
   const int64_t k_threads = a.idxk ? a.rows * (a.di / 8) : 0;
   const int64_t total = k_begin + k_threads;
   const int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
-  quant_fp4_kernel<<<(unsigned)blocks, kQuantThreads, 0, s>>>(
-      static_cast<const uint16_t*>(a.x), a.rows, a.d, a.x_ld, a.codes, a.codes_ld, a.scales,
-      a.scales_ld, static_cast<const uint16_t*>(a.idxk), a.di, a.idxk_ld, a.idxk_e4m3,
-      a.idxk_e4m3_ld, kv_threads, k_begin);
-  return check_launch();
+  return launch_kernel(quant_fp4_kernel, dim3((unsigned)blocks), dim3(kQuantThreads), 0, s, 1,
+                       static_cast<const uint16_t*>(a.x), a.rows, a.d, a.x_ld, a.codes,
+                       a.codes_ld, a.scales, a.scales_ld, static_cast<const uint16_t*>(a.idxk),
+                       a.di, a.idxk_ld, a.idxk_e4m3, a.idxk_e4m3_ld, kv_threads, k_begin);
 }
 
 csa2_status launch_quantize_index_q(const void* q, const float* w, int64_t nq, int32_t hi,
@@ -140,13 +141,12 @@ csa2_status launch_quantize_index_q(const void* q, const float* w, int64_t nq, i
   const unsigned blocks = (unsigned)((heads + 7) / 8);
   const uint16_t* qp = static_cast<const uint16_t*>(q);
   switch (di) {
-    case 32: quant_index_q_kernel<32><<<blocks, 256, 0, s>>>(qp, w, heads, q8, c); break;
-    case 64: quant_index_q_kernel<64><<<blocks, 256, 0, s>>>(qp, w, heads, q8, c); break;
-    case 128: quant_index_q_kernel<128><<<blocks, 256, 0, s>>>(qp, w, heads, q8, c); break;
-    case 256: quant_index_q_kernel<256><<<blocks, 256, 0, s>>>(qp, w, heads, q8, c); break;
+    case 32: return launch_kernel(quant_index_q_kernel<32>, dim3(blocks), dim3(256), 0, s, 1, qp, w, heads, q8, c);
+    case 64: return launch_kernel(quant_index_q_kernel<64>, dim3(blocks), dim3(256), 0, s, 1, qp, w, heads, q8, c);
+    case 128: return launch_kernel(quant_index_q_kernel<128>, dim3(blocks), dim3(256), 0, s, 1, qp, w, heads, q8, c);
+    case 256: return launch_kernel(quant_index_q_kernel<256>, dim3(blocks), dim3(256), 0, s, 1, qp, w, heads, q8, c);
     default: return CSA2_ERR_UNSUPPORTED;
   }
-  return check_launch();
 }
 
 }  // namespace csa2

@@ -77,6 +77,7 @@ __device__ __forceinline__ void window_of(const csa2_attn_args& a, int64_t qi, i
 
 __global__ void __launch_bounds__(128) attn_f32_kernel(const csa2_attn_args a) {
   extern __shared__ float sm[];  // q [d], logits [k + win_max]
+  pdl_wait();
   const int64_t qi = blockIdx.y;
   const int h = blockIdx.x;
   const int d = a.d;
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const int chunk = blockIdx.x, hg = blockIdx.y;
   const int64_t qi = blockIdx.z;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
+  pdl_wait();
 
   int32_t ws, wl;
   window_of(a, qi, ws, wl);
@@ -457,6 +459,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   }
 
   // ---- 5. merge the chunks
+  pdl_trigger();
   const int hr0 = pm * 16 + r0;  // output rows (heads within the CTA) of this thread
   if constexpr (CLUSTER) {
     namespace cg = cooperative_groups;
@@ -541,6 +544,7 @@ __global__ void __launch_bounds__(128)
   const int h = blockIdx.x;
   const int64_t qi = blockIdx.y;
   const int hg = h / kHG, hr = h % kHG;
+  pdl_wait();
   const int ngroups = (hq + kHG - 1) / kHG;
   const float* base =
       partial + ((qi * ngroups + hg) * (int64_t)nchunks) * PartialLayout::kFloats;
@@ -591,8 +595,8 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s) {
   if (a.q_dtype == CSA2_F32) {
     const size_t smem = sizeof(float) * ((size_t)a.d + a.k + a.win_max);
     if (smem > 48 * 1024) return CSA2_ERR_UNSUPPORTED;
-    attn_f32_kernel<<<dim3((unsigned)a.hq, (unsigned)a.nq), 128, smem, s>>>(a);
-    return check_launch();
+    return launch_kernel(attn_f32_kernel, dim3((unsigned)a.hq, (unsigned)a.nq), dim3(128), smem, s,
+                         1, a);
   }
   const int nchunks = attn_chunks(a);
   if (nchunks == 0) {
@@ -610,30 +614,15 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s) {
     attr_set = true;
   }
   const dim3 grid((unsigned)nchunks, (unsigned)((a.hq + kHG - 1) / kHG), (unsigned)a.nq);
-  if (nchunks <= kMaxClusterChunks) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = kAttnSmem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)nchunks;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, attn_bf16_kernel<true>, a, nchunks,
-                                       static_cast<float*>(nullptr));
-    return e == cudaSuccess ? check_launch() : cuda_fail(e);
-  }
+  if (nchunks <= kMaxClusterChunks)
+    return launch_kernel(attn_bf16_kernel<true>, grid, dim3(kAttnThreads), (size_t)kAttnSmem, s,
+                         (unsigned)nchunks, a, nchunks, static_cast<float*>(nullptr));
   float* partial = static_cast<float*>(a.workspace);
-  attn_bf16_kernel<false><<<grid, kAttnThreads, kAttnSmem, s>>>(a, nchunks, partial);
-  csa2_status st = check_launch();
+  csa2_status st = launch_kernel(attn_bf16_kernel<false>, grid, dim3(kAttnThreads),
+                                 (size_t)kAttnSmem, s, 1, a, nchunks, partial);
   if (st != CSA2_OK) return st;
-  attn_combine_kernel<<<dim3((unsigned)a.hq, (unsigned)a.nq), 128, 0, s>>>(partial, nchunks,
-                                                                         a.hq, a.out);
-  return check_launch();
+  return launch_kernel(attn_combine_kernel, dim3((unsigned)a.hq, (unsigned)a.nq), dim3(128), 0, s,
+                       1, static_cast<const float*>(partial), nchunks, (int)a.hq, a.out);
 }
 
 }  // namespace csa2

@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kHistThreads)
   __shared__ uint32_t h[kBins];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < kBins; i += kHistThreads) h[i] = 0;
+  pdl_wait();
   __syncthreads();
   const int64_t row = blockIdx.y;
   const int64_t nv = row_nvalid(n_valid, row, n);
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(kHistThreads)
     }
   }
   __syncthreads();
+  pdl_trigger();
   for (int i = tid; i < kBins; i += kHistThreads)
     if (h[i]) atomicAdd(&hist1[row * kBins + i], h[i]);
 }
@@ -201,7 +203,7 @@ template <int C>
 __global__ void __launch_bounds__(kTkThreads, 1)
     topk_select_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
                        const int32_t* __restrict__ n_valid, int32_t k,
-                       const uint32_t* __restrict__ hist1, int32_t* __restrict__ idx_out,
+                       uint32_t* __restrict__ hist1, int32_t* __restrict__ idx_out,
                        int64_t idx_ld, int vec) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) uint8_t dyn[];
@@ -214,13 +216,19 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   __shared__ uint32_t wgt[kTkWarps], wtie[kTkWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
   const int r = (int)cluster.block_rank();
   const int64_t row = blockIdx.x / C;
   const int64_t nv = row_nvalid(n_valid, row, n);
   int32_t* out = idx_out + row * idx_ld;
+  // The row's histogram goes back to zero once read, ready for the next
+  // selection that uses the same workspace: CTA r clears bins r*512 ..
+  // (after every CTA has read them).
+  uint32_t* hrow = hist1 + row * kBins;
   if (nv <= k) {  // every visible entry is selected (the whole cluster returns here)
     for (int64_t i = (int64_t)r * kTkThreads + tid; i < k; i += (int64_t)C * kTkThreads)
       out[i] = i < nv ? (int32_t)i : -1;
+    for (int i = tid; i < kBins / C; i += kTkThreads) hrow[r * (kBins / C) + i] = 0;  // nobody else reads it
     return;
   }
   const float* s = scores + row * ld;
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   {
     uint32_t hv[kBins / kTkThreads];
 #pragma unroll
-    for (int u = 0; u < kBins / kTkThreads; ++u) hv[u] = hist1[row * kBins + tid + u * kTkThreads];
+    for (int u = 0; u < kBins / kTkThreads; ++u) hv[u] = hrow[tid + u * kTkThreads];
 #pragma unroll
     for (int u = 0; u < kBins / kTkThreads; ++u) hist[tid + u * kTkThreads] = hv[u];
   }
@@ -385,6 +393,8 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     tmp.wsum[tid] = *cluster.map_shared_rank(&s_tie, tid);
   }
   cluster.sync();  // no CTA reads another's shared memory after this point
+  // every CTA read the row's histogram at its start: clear this CTA's share
+  for (int i = tid; i < kBins / C; i += kTkThreads) hrow[r * (kBins / C) + i] = 0;
   if (tid == 0) {
     uint32_t pre_sel = 0, pre_tie = 0;
     for (int c = 0; c < r; ++c) {
@@ -403,6 +413,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     woff += wgt[w] + qw;
   }
   const uint32_t myq = min(wtie[warp], tq);
+  pdl_trigger();
   uint32_t run_sel = 0, run_tie = 0;
   const uint32_t lt = lanemask_lt();
   walk([&](uint32_t key, int32_t j, bool v) {
@@ -435,7 +446,7 @@ csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s) {
 }
 
 csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int64_t ld,
-                               const int32_t* n_valid, int32_t k, const uint32_t* hist1,
+                               const int32_t* n_valid, int32_t k, uint32_t* hist1,
                                int32_t* idx_out, int64_t idx_ld, cudaStream_t s) {
   if (rows == 0) return CSA2_OK;
   if (!g_select_attr) {
@@ -446,21 +457,9 @@ csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int
     g_select_attr = true;
   }
   const int vec = (ld % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) % 16) == 0) ? 1 : 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(rows * kTkCluster));
-  cfg.blockDim = dim3(kTkThreads);
-  cfg.dynamicSmemBytes = kTkDynSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kTkCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_select_kernel<kTkCluster>, scores, n, ld, n_valid,
-                                     k, hist1, idx_out, idx_ld, vec);
-  return e == cudaSuccess ? check_launch() : cuda_fail(e);
+  return launch_kernel(topk_select_kernel<kTkCluster>, dim3((unsigned)(rows * kTkCluster)),
+                       dim3(kTkThreads), (size_t)kTkDynSmem, s, kTkCluster, scores, n, ld, n_valid,
+                       k, hist1, idx_out, idx_ld, vec);
 }
 
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
@@ -471,9 +470,8 @@ csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64
   const int64_t max_chunks = (n + 4095) / 4096;
   const int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(want, max_chunks));
   const int64_t chunk = (n + chunks - 1) / chunks;
-  topk_hist_kernel<<<dim3((unsigned)chunks, (unsigned)rows), kHistThreads, 0, s>>>(
-      scores, n, ld, n_valid, hist1, chunk);
-  return check_launch();
+  return launch_kernel(topk_hist_kernel, dim3((unsigned)chunks, (unsigned)rows),
+                       dim3(kHistThreads), 0, s, 1, scores, n, ld, n_valid, hist1, chunk);
 }
 
 csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
