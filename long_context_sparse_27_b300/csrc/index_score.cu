@@ -11,12 +11,15 @@
 //    128 entries: D[128 x 64*QG] = K_tile[128 x 128] . Q8[64*QG x 128]^T in
 //    tensor memory, then an epilogue applies ReLU, the head weights c and the
 //    head sum.  Warp 0 streams K tiles with TMA into a ring of 16 KB stages,
-//    warp 1 issues the MMAs into a ring of NACC tensor-memory accumulators,
+//    warp 1 issues the MMAs into a ring of two tensor-memory accumulators,
 //    and two epilogue warpgroups (warps 2-5 and 6-9) drain alternate tiles,
 //    so two warps per SM sub-partition hide each other's tcgen05.ld and FMA
 //    latency.  In decode (QG = 1) the kernel is a stream over the indexer
-//    keys (128 B per entry) and is bound by HBM; in a prefill chunk (QG = 4,
-//    4 queries x 64 heads per MMA) it is a dense contraction.
+//    keys (128 B per entry): one CTA's load -> MMA -> epilogue -> accumulator
+//    hand-back chain is latency-bound well short of HBM speed, so two CTAs
+//    with 3-stage rings share each SM and overlap their chains.  In a prefill
+//    chunk (QG = 4, 4 queries x 64 heads per MMA) it is a dense contraction,
+//    one CTA per SM with a 6-stage ring.
 #include <cstdio>
 
 #include "common.cuh"
@@ -98,18 +101,14 @@ namespace {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
 
 template <int QG>
-struct TcCfgDefault {
-  static constexpr int EPI_WGS = QG == 1 ? 4 : 2;  // epilogue warpgroups
-};
-
-template <int QG, int EPI_WGS_ = TcCfgDefault<QG>::EPI_WGS>
 struct TcCfg {
   static constexpr int BM = 128;        // entries per tile (MMA M)
   static constexpr int BN = 64 * QG;    // 64 heads x QG queries (MMA N)
   static constexpr int BK = 128;        // indexer dim: 128 E4M3 bytes per row
-  static constexpr int STAGES = QG == 1 ? 8 : 6;
-  static constexpr int EPI_WGS = EPI_WGS_;
-  static constexpr int NACC = QG == 1 ? EPI_WGS : 2;  // accumulators in tensor memory
+  static constexpr int CTAS_PER_SM = QG == 1 ? 2 : 1;
+  static constexpr int STAGES = QG == 1 ? 3 : 6;
+  static constexpr int EPI_WGS = 2;     // epilogue warpgroups
+  static constexpr int NACC = 2;        // accumulators in tensor memory
   static constexpr int KTILE = BM * BK;  // 16 KB
   static constexpr int QTILE = BN * BK;  // 8 KB or 32 KB
   static constexpr int TMEM_USED = NACC * BN;
@@ -133,6 +132,8 @@ struct TcCfg {
   static_assert(NACC % EPI_WGS == 0, "accumulator a is drained by warpgroup a % EPI_WGS");
   static_assert(TMEM_USED <= 512, "tensor memory holds 512 columns");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory per CTA");
+  static_assert(CTAS_PER_SM * (SMEM_ALLOC + 1024) <= 228 * 1024, "CTAs resident per SM");
+  static_assert(CTAS_PER_SM * TMEM_COLS <= 512, "tensor memory shared by the SM's CTAs");
 };
 
 struct TcParams {
@@ -168,11 +169,11 @@ struct TileCursor {
   }
 };
 
-template <int QG, int EPI_WGS>
-__global__ void __launch_bounds__(TcCfg<QG, EPI_WGS>::THREADS, 1)
+template <int QG>
+__global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     idx_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap qmap, const TcParams p) {
-  using C = TcCfg<QG, EPI_WGS>;
+  using C = TcCfg<QG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -464,7 +465,6 @@ template <int QG>
 csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* c,
                       uint32_t* hist1, IndexTuning tune, cudaStream_t s) {
   using C = TcCfg<QG>;
-  constexpr int W = C::EPI_WGS;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cuda_fail(cudaErrorNotSupported);
   const int64_t nq = a.B * a.q_per_seq;
@@ -506,14 +506,14 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   if (total == 0) return CSA2_OK;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(idx_score_tc_kernel<QG, W>,
+    cudaError_t e = cudaFuncSetAttribute(idx_score_tc_kernel<QG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_ALLOC);
     if (e != cudaSuccess) return cuda_fail(e);
     attr_set = true;
   }
-  const int grid = (int)std::min<int64_t>(total, sm_count());
-  return launch_kernel(idx_score_tc_kernel<QG, W>, dim3(grid), dim3(C::THREADS),
+  const int grid = (int)std::min<int64_t>(total, (int64_t)C::CTAS_PER_SM * sm_count());
+  return launch_kernel(idx_score_tc_kernel<QG>, dim3(grid), dim3(C::THREADS),
                        (size_t)C::SMEM_ALLOC, s, 1, kmap, qmap, p);
 }
 
