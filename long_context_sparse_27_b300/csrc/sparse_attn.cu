@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   __shared__ ChunkRows rows;
   __shared__ float red_m[kPairs][kHG], red_l[kPairs][kHG];
   __shared__ float s_m[kHG], s_l[kHG];                 // this chunk's (max, sum) per head
-  __shared__ float s_f[kMaxClusterChunks][kHG];        // merge weights per (chunk, head)
+  __shared__ float2 s_ml[kHG];                         // the same pair, read by the cluster
 
   const int chunk = blockIdx.x, hg = blockIdx.y;
   const int64_t qi = blockIdx.z;
@@ -426,6 +426,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     }
     s_m[tid] = m;
     s_l[tid] = l;
+    s_ml[tid] = make_float2(m, l);
   }
 
   // ---- 4. O = P V: m-tile pm, dims d0 .. d0+63 (8 n-tiles), keys as the K dimension
@@ -473,28 +474,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       *reinterpret_cast<float2*>(sO + (hr0 + 8) * kORow + col) = make_float2(o[nt][2], o[nt][3]);
     }
     cluster.sync();  // every chunk's (m, l, O) is visible cluster-wide
-    // loads from the other CTAs are all issued before any is used
-    if (tid < kHG) {
-      float mc[kMaxClusterChunks], lc[kMaxClusterChunks];
-#pragma unroll
-      for (int c = 0; c < kMaxClusterChunks; ++c) {
-        mc[c] = c < nchunks ? *cluster.map_shared_rank(&s_m[tid], c) : -INFINITY;
-        lc[c] = c < nchunks ? *cluster.map_shared_rank(&s_l[tid], c) : 0.f;
-      }
-      float M = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kMaxClusterChunks; ++c) M = fmaxf(M, mc[c]);
-      float L = 0.f;
-#pragma unroll
-      for (int c = 0; c < kMaxClusterChunks; ++c) {
-        mc[c] = (mc[c] == -INFINITY) ? 0.f : expf(mc[c] - M);
-        L += mc[c] * lc[c];
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-      for (int c = 0; c < kMaxClusterChunks; ++c) s_f[c][tid] = mc[c] * inv;
-    }
-    __syncthreads();
     const int rank = (int)cluster.block_rank();
     constexpr int kVec = kHG * kD / 4;  // float4s of the [kHG][512] output
     const int v0 = rank * kVec / nchunks, v1 = (rank + 1) * kVec / nchunks;
@@ -502,18 +481,33 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const int h = (v * 4) / kD;
       if (h >= hvalid) break;  // v grows with h
       const float4* src = reinterpret_cast<const float4*>(sO + h * kORow + (v * 4) % kD);
+      // every remote load, (m, l) and O alike, is issued before any is used
+      float2 ml[kMaxClusterChunks];
       float4 x[kMaxClusterChunks];
 #pragma unroll
-      for (int c = 0; c < kMaxClusterChunks; ++c)
+      for (int c = 0; c < kMaxClusterChunks; ++c) {
+        ml[c] = c < nchunks ? *cluster.map_shared_rank(&s_ml[h], c)
+                            : make_float2(-INFINITY, 0.f);
         x[c] = c < nchunks ? *cluster.map_shared_rank(src, c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c) M = fmaxf(M, ml[c].x);
+      float L = 0.f, f[kMaxClusterChunks];
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c) {
+        f[c] = (ml[c].x == -INFINITY) ? 0.f : expf(ml[c].x - M);
+        L += f[c] * ml[c].y;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < kMaxClusterChunks; ++c) {
-        const float f = s_f[c][h];
-        acc.x += f * x[c].x;
-        acc.y += f * x[c].y;
-        acc.z += f * x[c].z;
-        acc.w += f * x[c].w;
+        const float w = f[c] * inv;
+        acc.x += w * x[c].x;
+        acc.y += w * x[c].y;
+        acc.z += w * x[c].z;
+        acc.w += w * x[c].w;
       }
       *reinterpret_cast<float4*>(a.out + (qi * a.hq + (int64_t)hg * kHG + h) * kD +
                                  (v * 4) % kD) = acc;
