@@ -11,6 +11,7 @@ Schedule sources: a Reindex layer reads the most recent Full layer's caches;
 a Reuse layer reads the most recent Full layer's caches and top-k indices.
 """
 import math
+from dataclasses import dataclass
 
 import torch
 
@@ -30,6 +31,16 @@ def default_sources(modes):
         else:
             out.append((last_full, last_full))
     return out
+
+
+@dataclass
+class StepIO:
+    dev_in: torch.Tensor    # uint8: every per-step input of the step, packed
+    dev_out: torch.Tensor   # uint8: every output of the step, packed
+    layers: list            # the workload's layer dicts with inputs / outputs in the blocks
+    descs: object           # csa2 layer descriptors of `layers`
+    in_bytes: int           # payload bytes of dev_in (without alignment padding)
+    out_bytes: int
 
 
 class StackWorkload:
@@ -126,6 +137,43 @@ class StackWorkload:
     def run(self):
         """Enqueue one step on the current stream."""
         csa2.layer_stack(self.descs, self.sargs, self.workspace)
+
+    IO_IN = ("new_kv", "new_idxk", "idx_q", "idx_w", "attn_q")
+
+    def make_io(self):
+        """A copy of the step's per-step inputs (new KV and indexer-K rows,
+        indexer Q and weights, attention Q) packed into one device block and
+        of its outputs (the attention results) in another, with layer
+        descriptors that read and write those blocks; every other tensor
+        (caches, windows, selected indices) is shared with this workload.
+        A host copy of `dev_in`, then one run of `descs`, then a copy of
+        `dev_out` to the host is one end-to-end step: one transfer each way."""
+        align = 256
+
+        def pack(keys):
+            slots, off = [], 0
+            for l, L in enumerate(self.layers):
+                for key in keys:
+                    if key in L:
+                        t = L[key]
+                        slots.append((l, key, off, t))
+                        off += (t.numel() * t.element_size() + align - 1) // align * align
+            return slots, off
+
+        in_slots, in_bytes = pack(self.IO_IN)
+        out_slots, out_bytes = pack(("out",))
+        dev_in = torch.empty(max(in_bytes, align), dtype=torch.uint8, device=self.device)
+        dev_out = torch.empty(max(out_bytes, align), dtype=torch.uint8, device=self.device)
+        layers = [dict(L) for L in self.layers]
+        for buf, slots in ((dev_in, in_slots), (dev_out, out_slots)):
+            for l, key, off, t in slots:
+                nb = t.numel() * t.element_size()
+                view = buf[off:off + nb].view(t.dtype).view(t.shape)
+                view.copy_(t)
+                layers[l][key] = view
+        payload_in = sum(t.numel() * t.element_size() for _, _, _, t in in_slots)
+        payload_out = sum(t.numel() * t.element_size() for _, _, _, t in out_slots)
+        return StepIO(dev_in, dev_out, layers, csa2.layer_descs(layers), payload_in, payload_out)
 
     # bytes the method must move per step (the roofline numerator); the
     # scores scratch is excluded.
