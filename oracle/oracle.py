@@ -244,7 +244,26 @@ def default_plan(modes):
     return [(m, kv, ix) for m, (kv, ix) in zip(modes, default_sources(modes))]
 
 
-def layer_stack(plan, layers, k, scale, q_per_seq=1, n_valid=None):
+def pool_restrict(scores, pool):
+    """Scores of the entries outside each row's candidate pool set to -inf.
+
+    [P5 Method; P3 "CSA2"] Hierarchical Sparse Indexer: an indexer restricted
+    to a shared candidate pool chosen by an earlier indexer scores only the
+    pool's entries.  Reading: an entry outside the pool is no candidate at all
+    (its score is -inf, below every scored entry); pool rows hold entry
+    indices, -1 for an empty slot.
+    """
+    scores = np.array(scores, dtype=np.float64)
+    rows, n = scores.shape
+    keep = np.zeros((rows, n), dtype=bool)
+    for r in range(rows):
+        p = pool[r][pool[r] >= 0]
+        keep[r, p] = True
+    scores[~keep] = -np.inf
+    return scores
+
+
+def layer_stack(plan, layers, k, scale, q_per_seq=1, n_valid=None, pool=0):
     """Run a static CSA2 schedule.
 
     plan: list of (mode, kv_src, idx_src).
@@ -253,9 +272,15 @@ def layer_stack(plan, layers, k, scale, q_per_seq=1, n_valid=None):
     layers hold 'idx_q' and 'idx_w'; every layer holds 'attn_q' and
     'window'.  An optional 'k_f32' in place of 'k8' (and fp32 'idx_q')
     selects the fp32 indexer.
+    pool > 0 runs the Hierarchical Sparse Indexer [P5 Method]: a Full layer's
+    indexer, which scores every entry, also chooses the candidate pool, its
+    top-`pool` entries (the same order as top-k); a Reindex layer scores only
+    the pool of the Full layer whose KV it reads.  Readings: the pool is the
+    earlier indexer's top-P under the top-k order; a Full layer's own top-k
+    is unchanged (it lies inside its pool).
     Returns (idx per layer, out per layer).
     """
-    idx_of, out_of = [], []
+    idx_of, out_of, pool_of = [], [], {}
     for l, (mode, kv_src, idx_src) in enumerate(plan):
         L = layers[l]
         src = layers[kv_src]
@@ -264,6 +289,10 @@ def layer_stack(plan, layers, k, scale, q_per_seq=1, n_valid=None):
                 s = index_score_fp8(L["idx_q"], L["idx_w"], src["k8"], q_per_seq, n_valid)
             else:
                 s = index_score(L["idx_q"], L["idx_w"], src["k_f32"], q_per_seq, n_valid)
+            if pool > 0 and mode == FULL:
+                pool_of[l] = topk(s, pool, n_valid)
+            if pool > 0 and mode == REINDEX:
+                s = pool_restrict(s, pool_of[kv_src])
             idx = topk(s, k, n_valid)
         else:
             idx = idx_of[idx_src].copy()

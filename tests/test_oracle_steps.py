@@ -279,3 +279,62 @@ def test_modes_reindex_uses_full_layer_kv(orc):
     layers[1].update({"codes": other["codes"], "scales": other["scales"], "k8": other["k8"]})
     idx_b, out_b = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125)
     assert np.array_equal(idx_a[1], idx_b[1]) and np.array_equal(out_a[1], out_b[1])
+
+
+# ---- Hierarchical Sparse Indexer (candidate pool shared by a Full layer) ----
+
+def test_pool_covering_every_entry_is_the_plain_schedule(orc):
+    # a pool as large as the sequence restricts nothing: the hierarchical
+    # schedule reduces to the plain one
+    modes = [F, RI, RU, RI]
+    layers = small_stack_layers(orc, modes, 90, n=300)
+    plain = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125)
+    pooled = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125, pool=300)
+    for a, b in zip(plain[0], pooled[0]):
+        assert np.array_equal(a, b)
+    for a, b in zip(plain[1], pooled[1]):
+        assert np.array_equal(a, b)
+
+
+def test_pool_same_q_reproduces_full(orc):
+    # the Full layer's top-k lies inside its own pool, so a Reindex layer with
+    # the Full layer's queries still selects exactly the Full layer's entries
+    modes = [F, RI]
+    layers = small_stack_layers(orc, modes, 91, same_q=True)
+    idx, _ = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125, pool=64)
+    assert np.array_equal(idx[1], idx[0])
+
+
+def test_pool_selection_by_sorting(orc):
+    # brute force: score every entry with the Reindex queries, keep the pool
+    # members of the Full layer's 64 best (by sorting), sort those by (score
+    # descending, index ascending) and take 32
+    modes = [F, RI]
+    layers = small_stack_layers(orc, modes, 92, B=3, n=200)
+    idx, _ = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125, pool=64)
+    full = orc.index_score_fp8(layers[0]["idx_q"], layers[0]["idx_w"], layers[0]["k8"])
+    re = orc.index_score_fp8(layers[1]["idx_q"], layers[1]["idx_w"], layers[0]["k8"])
+    plain, _ = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125)
+    left_pool = 0
+    for q in range(3):
+        pool = sorted(range(200), key=lambda j: (-full[q, j], j))[:64]
+        best = sorted(pool, key=lambda j: (-re[q, j], j))[:32]
+        assert list(idx[1][q]) == sorted(best)
+        left_pool += not set(plain[1][q]) <= set(pool)
+    # the case is not trivial: the plain Reindex selection leaves the pool
+    assert left_pool > 0
+
+
+def test_pool_with_short_rows(orc):
+    # fewer visible entries than the pool: the pool is every visible entry and
+    # the Reindex layer selects as in the plain schedule; -1 pads a row with
+    # fewer visible entries than k
+    modes = [F, RI]
+    layers = small_stack_layers(orc, modes, 93, B=3, n=120)
+    nv = np.array([120, 50, 20], dtype=np.int32)
+    plain, _ = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125, n_valid=nv)
+    pooled, _ = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125, n_valid=nv,
+                                pool=64)
+    assert np.array_equal(plain[0], pooled[0])
+    assert np.array_equal(plain[1][1:], pooled[1][1:])   # rows with nv <= pool
+    assert list(pooled[1][2][20:]) == [-1] * 12
