@@ -200,6 +200,26 @@ typedef struct csa2_index_args {
 size_t csa2_index_score_workspace_bytes(const csa2_index_args* args);
 csa2_status csa2_index_score(const csa2_index_args* args, csa2_stream_t stream);
 
+/*
+ * The restricted step of the Hierarchical Sparse Indexer: score only a
+ * candidate pool chosen by an earlier indexer [P5 Method: indexers
+ * restricted to a shared candidate pool selected by an earlier indexer].
+ * For query q and slot i < pool_n:
+ *   scores[q, i] = sum_h w'[q,h] * max(0, <q_h, k_pool[q,i]>)
+ * (the FP8 path of csa2_index_score at entry pool[q, i] of q's sequence),
+ * -inf for a slot holding -1.  Only the FP8 path (q BF16 or E4M3, k E4M3,
+ * hi == 64, di == 128); n_valid is not read (pool entries are visible by
+ * construction); scores / scores_ld hold [nq, pool_n], scores_ld >= pool_n.
+ * pool    device int32, row q at pool + q * pool_ld, entries in [-1, n)
+ * pool_n  1 <= pool_n <= 2048
+ * Workspace: csa2_index_score_workspace_bytes(args) (the quantised Q).
+ * Errors: as csa2_index_score; UNSUPPORTED for another path or pool_n.
+ * Device: CSA2_DEVFLAG_BOUNDS for a pool entry outside [-1, n) (the slot is
+ *         scored as empty).
+ */
+csa2_status csa2_index_score_pool(const csa2_index_args* args, const int32_t* pool,
+                                  int64_t pool_ld, int32_t pool_n, csa2_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* a4: top-k                                                                 */
 /* ------------------------------------------------------------------------ */
@@ -345,6 +365,14 @@ csa2_status csa2_sparse_attn(const csa2_attn_args* args, csa2_stream_t stream);
  *   topk_idx int32 [nq, k]; out f32 [nq, hq, d].
  * Workspace: csa2_layer_stack_workspace_bytes (scores, selector and
  * attention scratch, reused layer after layer).
+ *
+ * Hierarchical Sparse Indexer (args->pool = P > 0) [P5 Method]: every Full
+ * layer's indexer, which scores all entries, also keeps its top-P entries
+ * (the top-k order) as the candidate pool, and every Reindex layer scores
+ * only the pool of its kv_src (the last Full layer, so one pool lives in
+ * the workspace) and takes its top-k inside it.  A Full layer's own top-k
+ * is unchanged.  Needs the FP8 indexer (idx_k_dtype E4M3) and
+ * k <= P <= 2048; P >= n restricts nothing.
  */
 typedef struct csa2_layer_desc {
   int32_t mode;
@@ -385,6 +413,7 @@ typedef struct csa2_stack_args {
   void* workspace;
   size_t workspace_bytes;
   int32_t* dev_status;
+  int32_t pool;  /* candidate pool size P of the Hierarchical Sparse Indexer; 0 = off */
 } csa2_stack_args;
 
 /* Checks a schedule (see above) without touching the GPU.  Returns CSA2_OK

@@ -63,7 +63,7 @@ class StackArgs(ctypes.Structure):
                 ("idx_q_dtype", _c_i32), ("idx_k_dtype", _c_i32), ("attn_q_dtype", _c_i32),
                 ("n_valid", _c_p), ("win_start", _c_p), ("win_len", _c_p),
                 ("softmax_scale", _c_f), ("workspace", _c_p), ("workspace_bytes", _c_sz),
-                ("dev_status", _c_p)]
+                ("dev_status", _c_p), ("pool", _c_i32)]
 
 
 EXPORTS = {
@@ -75,6 +75,7 @@ EXPORTS = {
     "csa2_quantize_index_q": (_c_i32, [_c_p, _c_p, _c_i64, _c_i32, _c_i32, _c_p, _c_p, _c_p]),
     "csa2_index_score_workspace_bytes": (_c_sz, [ctypes.POINTER(IndexArgs)]),
     "csa2_index_score": (_c_i32, [ctypes.POINTER(IndexArgs), _c_p]),
+    "csa2_index_score_pool": (_c_i32, [ctypes.POINTER(IndexArgs), _c_p, _c_i64, _c_i32, _c_p]),
     "csa2_topk_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i32]),
     "csa2_topk": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_p, _c_sz,
                            _c_p, _c_p]),
@@ -213,6 +214,24 @@ def index_score(q, w, k, q_per_seq=1, n_valid=None, scores=None, dev_status=None
     return scores
 
 
+def index_score_pool(q, w, k, pool, q_per_seq=1, scores=None, dev_status=None):
+    """The Hierarchical Sparse Indexer's restricted scoring: q bf16 [nq, 64,
+    128] (or its E4M3 quantisation with w = c), w f32 [nq, 64], k E4M3 [B, n,
+    128] as uint8, pool int32 [nq, P] (entry indices, -1 = empty slot) ->
+    scores f32 [nq, P] (-inf at empty slots)."""
+    nq, P = pool.shape
+    if scores is None:
+        scores = torch.empty(nq, P, dtype=torch.float32, device=q.device)
+    a = index_args(q, w, k, q_per_seq, None, scores, dev_status)
+    need = lib.csa2_index_score_workspace_bytes(ctypes.byref(a))
+    ws = _workspace(need, q.device) if need else None
+    if ws is not None:
+        a.workspace, a.workspace_bytes = _aligned_ptr(ws), need
+    _check(lib.csa2_index_score_pool(ctypes.byref(a), _ptr(pool), pool.stride(0), P, _stream()),
+           "csa2_index_score_pool")
+    return scores
+
+
 # ---- a4 ----------------------------------------------------------------------
 
 def topk_workspace_bytes(rows, n, k):
@@ -307,12 +326,12 @@ def validate_plan(layers):
 
 def stack_args(B, q_per_seq, n, hi, di, hq, d, k, w_rows, idx_q_dtype, idx_k_dtype,
                attn_q_dtype, softmax_scale, n_valid=None, win_start=None, win_len=None,
-               dev_status=None):
+               dev_status=None, pool=0):
     return StackArgs(B=B, q_per_seq=q_per_seq, n=n, hi=hi, di=di, hq=hq, d=d, k=k,
                      w_rows=w_rows, idx_q_dtype=idx_q_dtype, idx_k_dtype=idx_k_dtype,
                      attn_q_dtype=attn_q_dtype, n_valid=_ptr(n_valid),
                      win_start=_ptr(win_start), win_len=_ptr(win_len),
-                     softmax_scale=softmax_scale, dev_status=_ptr(dev_status))
+                     softmax_scale=softmax_scale, dev_status=_ptr(dev_status), pool=pool)
 
 
 def layer_stack_workspace_bytes(sargs):

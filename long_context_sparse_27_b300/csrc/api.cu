@@ -201,8 +201,14 @@ csa2_status check_attn(const csa2_attn_args* a) {
 // ---- layer stack ----
 
 struct StackPieces {
-  size_t scores, ix, tk, at;
+  size_t scores, ix, tk, pl, at;
+  size_t total() const { return scores + tk + pl + std::max(ix, at); }
 };
+
+// slots of the Hierarchical Sparse Indexer's candidate pool (0 = off)
+int64_t pool_slots(const csa2_stack_args& s) {
+  return s.pool > 0 ? std::min<int64_t>(s.pool, s.n) : 0;
+}
 
 csa2_index_args stack_index_args(const csa2_stack_args& s, const csa2_layer_desc& L,
                                  const csa2_layer_desc& src, float* scores, void* ws,
@@ -319,6 +325,7 @@ StackPieces stack_pieces(const csa2_stack_args& s) {
   csa2_index_args ia = stack_index_args(s, dummy, dummy, nullptr, nullptr, 0);
   p.ix = align256(index_ws(&ia));
   p.tk = align256(topk_workspace_bytes(nq, s.n, s.k));
+  p.pl = align256((size_t)nq * pool_slots(s) * sizeof(int32_t));
   csa2_attn_args aa = stack_attn_args(s, dummy, dummy, nullptr, nullptr, 0);
   p.at = align256(attn_workspace_bytes(aa));
   return p;
@@ -379,6 +386,37 @@ csa2_status csa2_index_score(const csa2_index_args* args, csa2_stream_t stream) 
   if (st != CSA2_OK) return st;
   if ((st = injected("index_score")) != CSA2_OK) return st;
   return run_index(*args, nullptr, IndexTuning{}, reinterpret_cast<cudaStream_t>(stream));
+}
+
+csa2_status csa2_index_score_pool(const csa2_index_args* args, const int32_t* pool,
+                                  int64_t pool_ld, int32_t pool_n, csa2_stream_t stream) {
+  if (!args) return CSA2_ERR_INVALID_ARG;
+  // the checks of csa2_index_score, with rows of pool_n scores
+  csa2_index_args chk = *args;
+  chk.scores_ld = std::max(chk.scores_ld, chk.n);
+  csa2_status st = check_index(&chk);
+  if (st != CSA2_OK) return st;
+  if (!fp8_path(args)) return CSA2_ERR_UNSUPPORTED;
+  if (pool_n < 1 || pool_ld < pool_n || args->scores_ld < pool_n) return CSA2_ERR_INVALID_ARG;
+  if (pool_n > 2048) return CSA2_ERR_UNSUPPORTED;
+  const int64_t nq = args->B * args->q_per_seq;
+  if (nq == 0 || args->n == 0) return CSA2_OK;
+  if (!pool) return CSA2_ERR_INVALID_ARG;
+  if ((st = injected("index_score_pool")) != CSA2_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const uint8_t* q8 = static_cast<const uint8_t*>(args->q);
+  const float* c = args->w;
+  if (args->q_dtype != CSA2_E4M3) {
+    uint8_t* wq = static_cast<uint8_t*>(args->workspace);
+    float* wc = reinterpret_cast<float*>(wq + align256((size_t)nq * args->hi * args->di));
+    if ((st = launch_quantize_index_q(args->q, args->w, nq, args->hi, args->di, wq, wc, cs)) !=
+        CSA2_OK)
+      return st;
+    q8 = wq;
+    c = wc;
+  }
+  return launch_index_score_pool(*args, q8, c, pool, pool_ld, pool_n, args->scores,
+                                 args->scores_ld, cs);
 }
 
 size_t csa2_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k) {
@@ -443,26 +481,32 @@ csa2_status csa2_validate_plan(const csa2_layer_desc* L, int32_t n_layers, int32
 
 size_t csa2_layer_stack_workspace_bytes(const csa2_stack_args* s) {
   if (!s) return 0;
-  StackPieces p = stack_pieces(*s);
-  return p.scores + p.tk + std::max(p.ix, p.at);
+  return stack_pieces(*s).total();
 }
 
 csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
                              const csa2_stack_args* s, csa2_stream_t stream) {
   csa2_status st = csa2_validate_plan(L, n_layers, nullptr);
   if (st != CSA2_OK) return st;
-  if (!s || s->B < 1 || s->q_per_seq < 1 || s->n < 1 || s->k < 1) return CSA2_ERR_INVALID_ARG;
-  // workspace: scores | per-row top-k histograms | scratch of the index
-  // (quantised Q) or attention (chunk partials) step
+  if (!s || s->B < 1 || s->q_per_seq < 1 || s->n < 1 || s->k < 1 || s->pool < 0)
+    return CSA2_ERR_INVALID_ARG;
+  if (s->pool > 0) {
+    if (s->pool < s->k) return CSA2_ERR_INVALID_ARG;
+    if (s->pool > 2048 || s->idx_k_dtype != CSA2_E4M3) return CSA2_ERR_UNSUPPORTED;
+  }
+  // workspace: scores | per-row top-k histograms | the candidate pool |
+  // scratch of the index (quantised Q) or attention (chunk partials) step
   const StackPieces p = stack_pieces(*s);
-  const size_t need = p.scores + p.tk + std::max(p.ix, p.at);
-  if (!s->workspace || s->workspace_bytes < need) return CSA2_ERR_WORKSPACE;
+  if (!s->workspace || s->workspace_bytes < p.total()) return CSA2_ERR_WORKSPACE;
   if (!aligned(s->workspace, 256)) return CSA2_ERR_ALIGNMENT;
   float* scores = static_cast<float*>(s->workspace);
   uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(s->workspace) + p.scores);
-  void* scratch = static_cast<uint8_t*>(s->workspace) + p.scores + p.tk;
-  const size_t scratch_bytes = s->workspace_bytes - p.scores - p.tk;
+  int32_t* pool = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(s->workspace) + p.scores +
+                                             p.tk);
+  void* scratch = static_cast<uint8_t*>(s->workspace) + p.scores + p.tk + p.pl;
+  const size_t scratch_bytes = s->workspace_bytes - p.scores - p.tk - p.pl;
   const int64_t nq = s->B * s->q_per_seq;
+  const int64_t P = pool_slots(*s);
   // check every call's arguments before anything is enqueued
   for (int32_t l = 0; l < n_layers; ++l) {
     const csa2_layer_desc& d = L[l];
@@ -481,6 +525,9 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
       if ((st = check_topk(scores, nq, s->n, s->n, s->k, d.topk_idx, s->k, hist, p.tk)) !=
           CSA2_OK)
         return st;
+      if (P > 0 && (st = check_topk(scores, nq, s->n, s->n, (int32_t)P, pool, P, hist, p.tk)) !=
+                       CSA2_OK)
+        return st;
     }
     const int32_t* idx = L[d.mode == CSA2_MODE_REUSE ? d.idx_src : l].topk_idx;
     csa2_attn_args aa = stack_attn_args(*s, d, kv, idx, scratch, scratch_bytes);
@@ -495,6 +542,7 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
   // on the tiles that read touched last -- the ones still in L2.
   bool reverse_next[64] = {false};  // per Full layer (by index, plans of <= 64 layers)
   auto read_again = [&](int32_t from, int32_t src) {
+    if (P > 0) return false;  // pooled Reindex layers read only the pool's rows
     for (int32_t m = from + 1; m < n_layers; ++m)
       if (L[m].mode == CSA2_MODE_REINDEX && L[m].kv_src == src) return true;
     return false;
@@ -508,7 +556,28 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
     if (d.mode == CSA2_MODE_FULL && d.new_kv) {
       if ((st = quantize_new_rows(*s, d, cs)) != CSA2_OK) return st;
     }
-    if (d.mode != CSA2_MODE_REUSE) {
+    if (d.mode == CSA2_MODE_REINDEX && P > 0) {
+      // Hierarchical Sparse Indexer: score the last Full layer's pool only,
+      // then its top-k (pool positions mapped back to entry indices)
+      csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
+      const uint8_t* q8 = static_cast<const uint8_t*>(ia.q);
+      const float* c = ia.w;
+      if (ia.q_dtype != CSA2_E4M3) {
+        uint8_t* wq = static_cast<uint8_t*>(scratch);
+        float* wc = reinterpret_cast<float*>(wq + align256((size_t)nq * s->hi * s->di));
+        if ((st = launch_quantize_index_q(ia.q, ia.w, nq, s->hi, s->di, wq, wc, cs)) != CSA2_OK)
+          return st;
+        q8 = wq;
+        c = wc;
+      }
+      if ((st = launch_index_score_pool(ia, q8, c, pool, P, (int32_t)P, scores, P, cs)) !=
+          CSA2_OK)
+        return st;
+      if ((st = launch_topk_hist(scores, nq, P, P, nullptr, hist, cs)) != CSA2_OK) return st;
+      if ((st = launch_topk_select(scores, nq, P, P, nullptr, s->k, hist, d.topk_idx, s->k, cs,
+                                   pool, P, true)) != CSA2_OK)
+        return st;
+    } else if (d.mode != CSA2_MODE_REUSE) {
       csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
       // decode: the indexer kernel also builds the top-k's first-level
       // histograms; otherwise a histogram pass over the scores does
@@ -522,6 +591,12 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
       if ((st = run_index(ia, fused ? hist : nullptr, tune, cs)) != CSA2_OK) return st;
       if (!fused &&
           (st = launch_topk_hist(scores, nq, s->n, s->n, s->n_valid, hist, cs)) != CSA2_OK)
+        return st;
+      // a Full layer of the Hierarchical Sparse Indexer first keeps its
+      // top-P as the pool (the histograms stay for the top-k that follows)
+      if (P > 0 && d.mode == CSA2_MODE_FULL &&
+          (st = launch_topk_select(scores, nq, s->n, s->n, s->n_valid, (int32_t)P, hist, pool, P,
+                                   cs, nullptr, 0, false)) != CSA2_OK)
         return st;
       if ((st = launch_topk_select(scores, nq, s->n, s->n, s->n_valid, s->k, hist, d.topk_idx,
                                    s->k, cs)) != CSA2_OK)

@@ -39,6 +39,14 @@ struct IndexTuning {
 // keys to (see index_fuses_topk_hist).
 csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, const float* c,
                                    uint32_t* hist1, IndexTuning tune, cudaStream_t s);
+// Scores of a candidate pool (the Hierarchical Sparse Indexer): for every
+// query q and slot i < pool_n, scores[q * scores_ld + i] = the FP8 indexer
+// score of entry pool[q * pool_ld + i] of q's sequence (-inf for a slot
+// holding -1).  a.k / k_ld / k_seq_stride / B / q_per_seq / dev_status as
+// for launch_index_score_fp8 (hi == 64, di == 128); q8 / c quantised Q.
+csa2_status launch_index_score_pool(const csa2_index_args& a, const uint8_t* q8, const float* c,
+                                    const int32_t* pool, int64_t pool_ld, int32_t pool_n,
+                                    float* scores, int64_t scores_ld, cudaStream_t s);
 // whether launch_index_score_fp8 builds the top-k histograms for `a`
 bool index_fuses_topk_hist(const csa2_index_args& a);
 // a4: the workspace holds one 4096-bin first-level histogram per row
@@ -51,9 +59,14 @@ csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld
 csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s);
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
                              const int32_t* n_valid, uint32_t* hist1, cudaStream_t s);
+// remap (optional): entry j of row r is written as remap[r * remap_ld + j]
+// (positions in a candidate pool -> entry indices); clear_hist = false
+// leaves the histograms for another selection from the same scores.
 csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int64_t ld,
                                const int32_t* n_valid, int32_t k, uint32_t* hist1,
-                               int32_t* idx_out, int64_t idx_ld, cudaStream_t s);
+                               int32_t* idx_out, int64_t idx_ld, cudaStream_t s,
+                               const int32_t* remap = nullptr, int64_t remap_ld = 0,
+                               bool clear_hist = true);
 // a5
 size_t attn_workspace_bytes(const csa2_attn_args& a);
 csa2_status launch_sparse_attn(const csa2_attn_args& a, cudaStream_t s);

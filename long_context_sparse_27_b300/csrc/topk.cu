@@ -204,7 +204,8 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     topk_select_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
                        const int32_t* __restrict__ n_valid, int32_t k,
                        uint32_t* __restrict__ hist1, int32_t* __restrict__ idx_out,
-                       int64_t idx_ld, int vec) {
+                       int64_t idx_ld, int vec, const int32_t* __restrict__ remap,
+                       int64_t remap_ld, int clear) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) uint8_t dyn[];
   uint32_t* lkey = reinterpret_cast<uint32_t*>(dyn);
@@ -221,14 +222,18 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   const int64_t row = blockIdx.x / C;
   const int64_t nv = row_nvalid(n_valid, row, n);
   int32_t* out = idx_out + row * idx_ld;
-  // The row's histogram goes back to zero once read, ready for the next
-  // selection that uses the same workspace: CTA r clears bins r*512 ..
-  // (after every CTA has read them).
+  // The row's histogram goes back to zero once read (unless the caller
+  // selects from it again), ready for the next selection that uses the same
+  // workspace: CTA r clears bins r*512 .. (after every CTA has read them).
+  // With `remap`, entry j of the row stands for remap[row * remap_ld + j]
+  // (its position in a candidate pool) and that is what is written.
   uint32_t* hrow = hist1 + row * kBins;
+  const int32_t* rmap = remap ? remap + row * remap_ld : nullptr;
   if (nv <= k) {  // every visible entry is selected (the whole cluster returns here)
     for (int64_t i = (int64_t)r * kTkThreads + tid; i < k; i += (int64_t)C * kTkThreads)
-      out[i] = i < nv ? (int32_t)i : -1;
-    for (int i = tid; i < kBins / C; i += kTkThreads) hrow[r * (kBins / C) + i] = 0;  // nobody else reads it
+      out[i] = i < nv ? (rmap ? rmap[i] : (int32_t)i) : -1;
+    if (clear)
+      for (int i = tid; i < kBins / C; i += kTkThreads) hrow[r * (kBins / C) + i] = 0;
     return;
   }
   const float* s = scores + row * ld;
@@ -394,7 +399,8 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   }
   cluster.sync();  // no CTA reads another's shared memory after this point
   // every CTA read the row's histogram at its start: clear this CTA's share
-  for (int i = tid; i < kBins / C; i += kTkThreads) hrow[r * (kBins / C) + i] = 0;
+  if (clear)
+    for (int i = tid; i < kBins / C; i += kTkThreads) hrow[r * (kBins / C) + i] = 0;
   if (tid == 0) {
     uint32_t pre_sel = 0, pre_tie = 0;
     for (int c = 0; c < r; ++c) {
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     const bool sel = g || (t && run_tie + __popc(tm & lt) < myq);
     const uint32_t sm = __ballot_sync(0xffffffffu, sel);
     const uint32_t pos = woff + run_sel + __popc(sm & lt);
-    if (sel && pos < (uint32_t)k) out[pos] = j;
+    if (sel && pos < (uint32_t)k) out[pos] = rmap ? rmap[j] : j;
     run_sel += __popc(sm);
     run_tie += __popc(tm);
   });
@@ -447,7 +453,8 @@ csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s) {
 
 csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int64_t ld,
                                const int32_t* n_valid, int32_t k, uint32_t* hist1,
-                               int32_t* idx_out, int64_t idx_ld, cudaStream_t s) {
+                               int32_t* idx_out, int64_t idx_ld, cudaStream_t s,
+                               const int32_t* remap, int64_t remap_ld, bool clear_hist) {
   if (rows == 0) return CSA2_OK;
   if (!g_select_attr) {
     cudaError_t e = cudaFuncSetAttribute(topk_select_kernel<kTkCluster>,
@@ -459,7 +466,7 @@ csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int
   const int vec = (ld % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) % 16) == 0) ? 1 : 0;
   return launch_kernel(topk_select_kernel<kTkCluster>, dim3((unsigned)(rows * kTkCluster)),
                        dim3(kTkThreads), (size_t)kTkDynSmem, s, kTkCluster, scores, n, ld, n_valid,
-                       k, hist1, idx_out, idx_ld, vec);
+                       k, hist1, idx_out, idx_ld, vec, remap, remap_ld, clear_hist ? 1 : 0);
 }
 
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,

@@ -49,6 +49,7 @@ class Workload:
     plant_frac: float
     modes: tuple      # static layer schedule
     pos0: int = -1    # prefill: absolute token position of the first query
+    pool: int = 0     # Hierarchical Sparse Indexer candidate pool (0 = off)
 
     @property
     def nq(self):
@@ -75,7 +76,11 @@ PREFILL = Workload("prefill", B=1, q_per_seq=4096, N=262144, Hi=64, Di=128, Hq=6
 # and launch shapes with a fifth of the device memory (profiling captures)
 C1M_GROUP = replace(C1M, name="1m4", modes=C1M.modes[:4])
 
-WORKLOADS = {w.name: w for w in (TINY, C128K, GROUP3, C1M, C1M_GROUP, PREFILL)}
+# the 1m stack with the Hierarchical Sparse Indexer: every Reindex layer
+# scores only the top-2048 pool of its Full layer
+C1M_POOL = replace(C1M, name="1m-pool", pool=2048)
+
+WORKLOADS = {w.name: w for w in (TINY, C128K, GROUP3, C1M, C1M_GROUP, PREFILL, C1M_POOL)}
 
 
 def scaled(w: Workload, **kw) -> Workload:

@@ -132,7 +132,8 @@ class StackWorkload:
             idx_k_dtype=csa2.F32 if wl.fp32_indexer else csa2.E4M3,
             attn_q_dtype=csa2.F32 if wl.attn_q_fp32 else csa2.BF16,
             softmax_scale=1.0 / math.sqrt(wl.D), n_valid=self.n_valid,
-            win_start=self.win_start, win_len=self.win_len, dev_status=self.dev_status)
+            win_start=self.win_start, win_len=self.win_len, dev_status=self.dev_status,
+            pool=wl.pool)
 
     def run(self):
         """Enqueue one step on the current stream."""
@@ -180,13 +181,17 @@ class StackWorkload:
     def algorithmic_bytes(self):
         wl = self.wl
         nq = wl.nq
-        index_layers = sum(1 for m in wl.modes if m in (FULL, REINDEX))
-        per_index = (wl.B * wl.N * wl.Di * (4 if wl.fp32_indexer else 1)
-                     + nq * wl.Hi * wl.Di * (4 if wl.fp32_indexer else 2)
-                     + nq * wl.Hi * 4 + nq * wl.k * 4)
+        queries = (nq * wl.Hi * wl.Di * (4 if wl.fp32_indexer else 2)
+                   + nq * wl.Hi * 4 + nq * wl.k * 4)
+        full_index = wl.B * wl.N * wl.Di * (4 if wl.fp32_indexer else 1) + queries
+        # a pooled Reindex layer reads its pool and the pool's indexer-K rows
+        P = min(wl.pool, wl.N)
+        reindex = full_index if P == 0 else nq * P * (wl.Di + 4) + queries
+        n_full = sum(1 for m in wl.modes if m == FULL)
+        n_re = sum(1 for m in wl.modes if m == REINDEX)
         per_layer = (nq * wl.k * (wl.D // 2 + wl.D // 32) + nq * wl.W * wl.D * 2
                      + nq * wl.Hq * wl.D * (4 if wl.attn_q_fp32 else 2) + nq * wl.Hq * wl.D * 4)
-        return index_layers * per_index + len(wl.modes) * per_layer
+        return n_full * full_index + n_re * reindex + len(wl.modes) * per_layer
 
     def visible_pairs(self):
         """(query, entry) pairs the indexer scores: nq * N in decode, the

@@ -198,3 +198,52 @@ def test_attn_and_quant_validation(csa2, monkeypatch):
     q.x = FAKE
     monkeypatch.setenv("CSA2_FAULT_INJECT", "quantize_fp4:4")
     assert L.csa2_quantize_fp4(ctypes.byref(q), None) == 4
+
+
+@no_gpu
+def test_pooled_index_validation(csa2, monkeypatch):
+    L = csa2.lib
+    a = csa2.IndexArgs(q=FAKE, q_dtype=csa2.BF16, w=FAKE, k=FAKE, k_dtype=csa2.E4M3, B=2,
+                       q_per_seq=1, hi=64, di=128, n=100000, k_ld=128,
+                       k_seq_stride=128 * 100000, scores=FAKE, scores_ld=2048)
+    ws = L.csa2_index_score_workspace_bytes(ctypes.byref(a))
+    a.workspace, a.workspace_bytes = FAKE, ws
+    # the pooled scores need rows of pool_n entries only (scores_ld < n)
+    monkeypatch.setenv("CSA2_FAULT_INJECT", "index_score_pool:4")
+    assert L.csa2_index_score_pool(ctypes.byref(a), FAKE, 2048, 2048, None) == 4
+    monkeypatch.delenv("CSA2_FAULT_INJECT")
+    assert L.csa2_index_score_pool(ctypes.byref(a), FAKE, 2048, 0, None) == 1     # empty pool
+    assert L.csa2_index_score_pool(ctypes.byref(a), FAKE, 1000, 2048, None) == 1  # pool_ld
+    assert L.csa2_index_score_pool(ctypes.byref(a), FAKE, 4096, 4096, None) == 1  # > scores_ld
+    a.scores_ld = 4096
+    assert L.csa2_index_score_pool(ctypes.byref(a), FAKE, 4096, 4096, None) == 2  # > 2048
+    assert L.csa2_index_score_pool(ctypes.byref(a), None, 2048, 2048, None) == 1  # no pool
+    a.q_dtype = a.k_dtype = csa2.F32
+    assert L.csa2_index_score_pool(ctypes.byref(a), FAKE, 2048, 2048, None) == 2  # FP8 only
+
+
+@no_gpu
+def test_stack_pool_validation(csa2, monkeypatch):
+    L = csa2.lib
+    descs = csa2.layer_descs([{"mode": 0, "kv_src": 0, "idx_src": 0},
+                              {"mode": 1, "kv_src": 0, "idx_src": 1}])
+    s = csa2.stack_args(B=2, q_per_seq=1, n=10000, hi=64, di=128, hq=64, d=512, k=512, w_rows=128,
+                        idx_q_dtype=csa2.BF16, idx_k_dtype=csa2.E4M3, attn_q_dtype=csa2.BF16,
+                        softmax_scale=0.04)
+    plain = L.csa2_layer_stack_workspace_bytes(ctypes.byref(s))
+    s.pool = 2048
+    pooled = L.csa2_layer_stack_workspace_bytes(ctypes.byref(s))
+    assert pooled == plain + 2 * 2048 * 4      # the pool: nq x P int32 (256-byte multiple)
+    s.pool = 20000                              # P >= n: the pool is every entry
+    assert L.csa2_layer_stack_workspace_bytes(ctypes.byref(s)) == plain + 2 * 10000 * 4 + 256 - \
+        (2 * 10000 * 4) % 256
+    s.workspace, s.workspace_bytes = FAKE, 1 << 40
+    s.pool = 256                                # smaller than k
+    assert L.csa2_layer_stack(descs, 2, ctypes.byref(s), None) == 1
+    s.pool = 4096
+    assert L.csa2_layer_stack(descs, 2, ctypes.byref(s), None) == 2
+    s.pool = -1
+    assert L.csa2_layer_stack(descs, 2, ctypes.byref(s), None) == 1
+    s.pool = 2048
+    s.idx_q_dtype = s.idx_k_dtype = csa2.F32   # the pooled scoring is FP8 only
+    assert L.csa2_layer_stack(descs, 2, ctypes.byref(s), None) == 2

@@ -76,7 +76,8 @@ def oracle_stack(orc, W, plan, nv):
     wl = W.wl
     layers = oracle_layers(orc, W)
     if wl.q_per_seq == 1:
-        return orc.layer_stack(plan, layers, wl.k, 1 / math.sqrt(wl.D), q_per_seq=1, n_valid=nv)
+        return orc.layer_stack(plan, layers, wl.k, 1 / math.sqrt(wl.D), q_per_seq=1, n_valid=nv,
+                               pool=wl.pool)
     # prefill: per-query windows (rows t .. t + W - 1)
     idx_of, out_of = [], []
     for l, (m, kv, ix) in enumerate(plan):
@@ -129,6 +130,29 @@ def test_stack_prefill_scaled(csa2, orc):
     W = build(wl, 5)
     run_stack(W)
     compare(orc, W)
+
+
+def test_stack_1m_pool_scaled(csa2, orc):
+    # the Hierarchical Sparse Indexer: Reindex layers score only the top-1024
+    # pool of their Full layer (pool < N, so the restriction matters)
+    W = build(synth.scaled(synth.C1M_POOL, B=2, N=2500, modes=synth.C1M.modes[:8], pool=1024), 8)
+    run_stack(W)
+    compare(orc, W)
+
+
+def test_stack_pool_covering_every_entry(csa2):
+    # a pool as large as the sequence restricts nothing: same selections and
+    # outputs as the plain schedule, bit for bit
+    from long_context_sparse_27_b300.workload import StackWorkload
+    wl = synth.scaled(synth.C1M, B=2, N=1500, modes=(synth.FULL, synth.REINDEX, synth.REUSE))
+    A = StackWorkload(wl, seed=9, gen_device="cuda")
+    B = StackWorkload(synth.scaled(wl, pool=2048), seed=9, gen_device="cuda")
+    run_stack(A)
+    run_stack(B)
+    for La, Lb in zip(A.layers, B.layers):
+        if "topk_idx" in La:
+            assert torch.equal(La["topk_idx"], Lb["topk_idx"])
+        assert torch.equal(La["out"], Lb["out"])
 
 
 def test_stack_mode_identities(csa2):
@@ -243,3 +267,51 @@ def test_full_size_prefill_sampled(csa2, orc):
     """The 4096-query prefill chunk at N = 262144: the first, a middle and the
     last query (their causal visibility differs)."""
     sampled_full_check(csa2, orc, synth.PREFILL, 14, queries=(0, 2047, 4095))
+
+
+def test_full_size_1m_pool_sampled(csa2, orc):
+    """The pooled 1M-context step (Reindex layers score only the top-2048 pool
+    of their Full layer) at full size, checked for the first Reindex layer on
+    the first and last sequence: the GPU pool is the top-2048 of the GPU's
+    Full-layer scores; the pooled scores against the oracle at every pool
+    entry; the GPU selection a valid top-k of its pooled scores; recall
+    against the oracle's selection inside the oracle's own pool; the
+    attention output where the two selections agree."""
+    from long_context_sparse_27_b300.workload import StackWorkload
+    wl, seed = synth.C1M_POOL, 15
+    W = StackWorkload(wl, seed=seed, gen_device="cuda", keep_bf16=False)
+    run_stack(W)
+    F0, R1 = W.layers[0], W.layers[1]
+    P = wl.pool
+    kk = synth.index_k_rows(wl, seed * 1000 + 6, "cuda")
+    kv = synth.kv_rows(wl, seed * 1000 + 5, "cuda")
+    g_full = csa2.index_score(F0["idx_q"], F0["idx_w"], F0["idxk"])
+    g_pool = orc.topk(g_full.cpu().numpy(), P)                 # the GPU's pool, decided on its scores
+    g_ps = csa2.index_score_pool(R1["idx_q"], R1["idx_w"], F0["idxk"],
+                                 torch.from_numpy(g_pool).cuda()).cpu().numpy()
+    g_idx_all = R1["topk_idx"].cpu().numpy()
+    checked = 0
+    for q in (0, 7):
+        k8 = orc.cast_e4m3(f64(kk[q]))[None]
+        ref_full = orc.index_score_fp8(f64(F0["idx_q"][q:q + 1]), f64(F0["idx_w"][q:q + 1]), k8)
+        ref_re = orc.index_score_fp8(f64(R1["idx_q"][q:q + 1]), f64(R1["idx_w"][q:q + 1]), k8)
+        assert score_close(g_ps[q:q + 1], ref_re[:, g_pool[q]]) <= 1.0, q
+        restricted = np.full((1, wl.N), -np.inf)
+        restricted[0, g_pool[q]] = g_ps[q]
+        g_idx = g_idx_all[q:q + 1]
+        assert topk_valid(restricted[0], g_idx[0], wl.k, wl.N), q
+        ref_pool = orc.topk(ref_full, P)
+        ref_idx = orc.topk(orc.pool_restrict(ref_re, ref_pool), wl.k)
+        assert recall(g_idx, ref_idx) >= 0.999, q
+        if not np.array_equal(g_idx, ref_idx):
+            continue
+        rows = ref_idx[0]
+        c, sc = orc.quantize_fp4(f64(kv[q, rows]))
+        codes = np.zeros((1, wl.N, wl.D // 2), np.uint8)
+        scl = np.zeros((1, wl.N, wl.D // 32), np.uint8)
+        codes[0, rows], scl[0, rows] = c, sc
+        ref = orc.sparse_attn(f64(R1["attn_q"][q:q + 1]), codes, scl, ref_idx,
+                              f64(R1["window"][q:q + 1]), 1 / math.sqrt(wl.D))
+        assert rel_l2(R1["out"][q:q + 1].cpu().numpy(), ref) <= 2e-3, q
+        checked += 1
+    assert checked > 0

@@ -165,6 +165,46 @@ def test_index_score_fp8_exact_small_integers(csa2, orc):
     assert np.array_equal(s.cpu().double().numpy(), ref)
 
 
+@pytest.mark.parametrize("B,n,P", [(2, 3000, 2048), (3, 1000, 300), (1, 200, 77)])
+def test_index_score_pool(csa2, orc, B, n, P):
+    # the Hierarchical Sparse Indexer's restricted scoring: each query's pool
+    # is a random set of its sequence's entries (some slots empty, -1); ragged
+    # pool sizes leave a partial 128-slot tile
+    wl = synth.scaled(synth.C128K, B=B, N=n)
+    q = synth.index_q(wl, 35 + n)
+    w = synth.index_w(wl, 36 + n)
+    kb = synth.index_k_rows(wl, 37 + n)
+    x = torch.zeros(B * n, 32, dtype=torch.bfloat16, device="cuda")
+    _, _, k8 = csa2.quantize_fp4(x, idxk=dev(kb.reshape(B * n, 128)))
+    k8 = k8.reshape(B, n, 128)
+    g = torch.Generator().manual_seed(38 + n)
+    pool = torch.stack([torch.randperm(n, generator=g)[:P] for _ in range(B)]).to(torch.int32)
+    pool[:, -5:] = -1
+    s = csa2.index_score_pool(dev(q), dev(w), k8, dev(pool)).cpu().numpy()
+    ref = orc.index_score_fp8(f64(q), f64(w), orc.cast_e4m3(f64(kb)))
+    for b in range(B):
+        keep = pool[b].numpy() >= 0
+        assert np.all(np.isneginf(s[b, ~keep]))
+        assert score_close(s[b:b + 1, keep], ref[b:b + 1, pool[b].numpy()[keep]]) <= 1.0
+
+
+def test_index_score_pool_exact_small_integers(csa2, orc):
+    # the exact case of the full indexer, through the pooled kernel: small
+    # integer E4M3 values make every product and sum exact
+    n, P = 256, 256
+    g = torch.Generator().manual_seed(51)
+    q = torch.randint(-1, 2, (1, 64, 128), generator=g).to(torch.bfloat16)
+    q[0, :, 0] = 7
+    w = torch.full((1, 64), 1.0 / 64)
+    kb = torch.randint(-1, 2, (n, 128), generator=g).to(torch.bfloat16)
+    x = torch.zeros(n, 32, dtype=torch.bfloat16, device="cuda")
+    _, _, k8 = csa2.quantize_fp4(x, idxk=dev(kb))
+    pool = torch.randperm(n, generator=g)[None, :P].to(torch.int32)
+    s = csa2.index_score_pool(dev(q), dev(w), k8.reshape(1, n, 128), dev(pool))
+    ref = orc.index_score_fp8(f64(q), f64(w), orc.cast_e4m3(f64(kb)).reshape(1, n, 128))
+    assert np.array_equal(s.cpu().double().numpy()[0], ref[0, pool[0].numpy()])
+
+
 # -------------------------------------------------------------------- a4 top-k
 
 @pytest.mark.parametrize("rows,n,k,levels", [
