@@ -149,18 +149,18 @@ def launches_per_step(wl):
     and attention; Reindex: the same without the new rows; Reuse: attention.
     A prefill chunk adds a top-k histogram pass per index layer (decode builds
     it inside the indexer kernel); attention over more than 8 key chunks of
-    80 adds a merge kernel.  With a candidate pool a Full layer adds the
-    pool's selection and a Reindex layer runs the Q quantiser, the pooled
-    scores, their histogram, the selection and attention."""
+    80 adds a merge kernel.  With a candidate pool a Full layer selects the
+    pool and then the top-k inside it (one kernel more) and a Reindex layer
+    runs the Q quantiser, the pooled scores, their selection and attention."""
     per = {0: 5, 1: 4, 2: 1}
     n = 0
     for m in wl.modes:
         if m == 1 and wl.pool:
-            n += 5  # Q quantiser, pooled scores, their histogram, selection, attention
+            n += 4  # Q quantiser, pooled scores, their selection, attention
         else:
             n += per[m]
             if m == 0 and wl.pool:
-                n += 1  # the pool's selection
+                n += 1  # the pool's selection, then the top-k inside it
             if m != 2 and wl.q_per_seq > 1:
                 n += 1
         if (wl.k + wl.W + 79) // 80 > 8:

@@ -234,8 +234,10 @@ csa2_status csa2_index_score_pool(const csa2_index_args* args, const int32_t* po
  * idx_out device int32, row r at idx_out + r * idx_ld
  * 1 <= k <= 2048.  Workspace: csa2_topk_workspace_bytes(rows, n, k) =
  * rows * 16 KiB (one 4096-bin histogram per row, cleared by the call).
- * Kernels: a histogram pass over the scores, then one selection kernel with
- * a cluster of 8 CTAs per row (each owning 1/8 of the row).
+ * Kernels: rows of at most 4096 entries run one CTA per row with every key
+ * in shared memory; longer rows a histogram pass over the scores, then one
+ * selection kernel with a cluster of 8 CTAs per row (each owning 1/8 of the
+ * row).
  * Errors: INVALID_ARG, UNSUPPORTED (k > 2048), WORKSPACE, CUDA.
  */
 size_t csa2_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k);

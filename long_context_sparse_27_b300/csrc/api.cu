@@ -573,9 +573,8 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
       if ((st = launch_index_score_pool(ia, q8, c, pool, P, (int32_t)P, scores, P, cs)) !=
           CSA2_OK)
         return st;
-      if ((st = launch_topk_hist(scores, nq, P, P, nullptr, hist, cs)) != CSA2_OK) return st;
-      if ((st = launch_topk_select(scores, nq, P, P, nullptr, s->k, hist, d.topk_idx, s->k, cs,
-                                   pool, P, true)) != CSA2_OK)
+      if ((st = launch_topk_small(scores, P, nullptr, 0, nq, (int32_t)P, nullptr, s->k, pool, P,
+                                  d.topk_idx, s->k, cs)) != CSA2_OK)
         return st;
     } else if (d.mode != CSA2_MODE_REUSE) {
       csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
@@ -592,15 +591,20 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
       if (!fused &&
           (st = launch_topk_hist(scores, nq, s->n, s->n, s->n_valid, hist, cs)) != CSA2_OK)
         return st;
-      // a Full layer of the Hierarchical Sparse Indexer first keeps its
-      // top-P as the pool (the histograms stay for the top-k that follows)
-      if (P > 0 && d.mode == CSA2_MODE_FULL &&
-          (st = launch_topk_select(scores, nq, s->n, s->n, s->n_valid, (int32_t)P, hist, pool, P,
-                                   cs, nullptr, 0, false)) != CSA2_OK)
+      if (P > 0 && d.mode == CSA2_MODE_FULL) {
+        // a Full layer of the Hierarchical Sparse Indexer keeps its top-P as
+        // the pool, then takes its top-k inside the pool (the same entries
+        // as the top-k of the whole row: the pool holds them)
+        if ((st = launch_topk_select(scores, nq, s->n, s->n, s->n_valid, (int32_t)P, hist, pool,
+                                     P, cs)) != CSA2_OK)
+          return st;
+        if ((st = launch_topk_small(scores, s->n, pool, P, nq, (int32_t)P, nullptr, s->k, pool,
+                                    P, d.topk_idx, s->k, cs)) != CSA2_OK)
+          return st;
+      } else if ((st = launch_topk_select(scores, nq, s->n, s->n, s->n_valid, s->k, hist,
+                                          d.topk_idx, s->k, cs)) != CSA2_OK) {
         return st;
-      if ((st = launch_topk_select(scores, nq, s->n, s->n, s->n_valid, s->k, hist, d.topk_idx,
-                                   s->k, cs)) != CSA2_OK)
-        return st;
+      }
     }
     const int32_t* idx = L[d.mode == CSA2_MODE_REUSE ? d.idx_src : l].topk_idx;
     csa2_attn_args aa = stack_attn_args(*s, d, kv, idx, scratch, scratch_bytes);

@@ -59,6 +59,14 @@ csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld
 csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s);
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
                              const int32_t* n_valid, uint32_t* hist1, cudaStream_t s);
+// Top-k of short rows (n <= 4096, one CTA per row; n_valid optional): value i of row r is
+// scores[r * ld + i], or with gather scores[r * ld + gather[r * gather_ld +
+// i]] (an index < 0 is an empty slot, below every value); positions are
+// written ascending as remap[r * remap_ld + i] (or i), padded with -1.
+csa2_status launch_topk_small(const float* scores, int64_t ld, const int32_t* gather,
+                              int64_t gather_ld, int64_t rows, int32_t n, const int32_t* n_valid,
+                              int32_t k, const int32_t* remap, int64_t remap_ld, int32_t* idx_out,
+                              int64_t idx_ld, cudaStream_t s);
 // remap (optional): entry j of row r is written as remap[r * remap_ld + j]
 // (positions in a candidate pool -> entry indices); clear_hist = false
 // leaves the histograms for another selection from the same scores.

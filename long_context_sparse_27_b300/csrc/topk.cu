@@ -435,6 +435,135 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   });
 }
 
+// ---------------------------------------------------------------------------
+// short rows (a candidate pool): one CTA per row, every key in shared memory
+
+constexpr int kSmallN = 4096;  // longest row
+
+// Row r of n <= kSmallN values (the first n_valid[r] of them when n_valid
+// is given): value i is scores[r * ld + i], or with `gather` scores[r * ld +
+// gather[r * gather_ld + i]] (an index < 0 is an empty slot, below every
+// value).  The k largest (value descending, position
+// ascending) are written ascending by position to out[r * out_ld ..] as
+// remap[r * remap_ld + i] (remap may be null: i), padded with -1.  The
+// same radix select as topk_select_kernel, on one CTA: 12 / 12 / 8-bit
+// digits, then ties on the whole key in position order.
+__global__ void __launch_bounds__(kTkThreads)
+    topk_small_kernel(const float* __restrict__ scores, int64_t ld,
+                      const int32_t* __restrict__ gather, int64_t gather_ld, int32_t n_row,
+                      const int32_t* __restrict__ n_valid, int32_t k,
+                      const int32_t* __restrict__ remap, int64_t remap_ld,
+                      int32_t* __restrict__ out, int64_t out_ld) {
+  __shared__ uint32_t key[kSmallN];
+  __shared__ uint32_t hist[kBins];
+  __shared__ TkTmp tmp;
+  __shared__ uint32_t wg[kTkWarps], wt[kTkWarps];
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const int n = (int)row_nvalid(n_valid, row, n_row);  // positions >= n_valid[row] do not exist
+  const float* s = scores + row * ld;
+  const int32_t* gi = gather ? gather + row * gather_ld : nullptr;
+  const int32_t* rm = remap ? remap + row * remap_ld : nullptr;
+  int32_t* o = out + row * out_ld;
+  for (int i = tid; i < kBins; i += kTkThreads) hist[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kTkThreads) {
+    uint32_t kk = 0;  // an empty slot
+    if (!gi) {
+      kk = score_key(s[i]);
+    } else {
+      const int32_t j = gi[i];
+      if (j >= 0) kk = score_key(s[j]);
+    }
+    key[i] = kk;
+    atomicAdd(&hist[kk >> 20], 1u);
+  }
+  __syncthreads();
+  const int m = min(k, n);
+  if (m == 0) {  // an empty row (the whole CTA returns here)
+    for (int i = tid; i < k; i += kTkThreads) o[i] = -1;
+    return;
+  }
+  // threshold: depth 1 (12 bits), 2 (24), 3 (32) or 4 (32 bits, ties)
+  find_top(hist, kBins, (uint32_t)m, &tmp);
+  uint32_t thr = (uint32_t)tmp.t;
+  uint32_t need = (uint32_t)m - tmp.above;
+  uint32_t cnt = hist[thr];
+  int depth = 1;
+  if (cnt != need) {
+    __syncthreads();
+    for (int i = tid; i < kBins; i += kTkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kTkThreads)
+      if ((key[i] >> 20) == thr) atomicAdd(&hist[(key[i] >> 8) & (kBins - 1)], 1u);
+    __syncthreads();
+    find_top(hist, kBins, need, &tmp);
+    need -= tmp.above;
+    thr = (thr << 12) | (uint32_t)tmp.t;
+    cnt = hist[tmp.t];
+    depth = 2;
+    if (cnt != need) {
+      __syncthreads();
+      for (int i = tid; i < kBins3; i += kTkThreads) hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < n; i += kTkThreads)
+        if ((key[i] >> 8) == thr) atomicAdd(&hist[key[i] & (kBins3 - 1)], 1u);
+      __syncthreads();
+      find_top(hist, kBins3, need, &tmp);
+      need -= tmp.above;
+      thr = (thr << 8) | (uint32_t)tmp.t;
+      cnt = hist[tmp.t];
+      depth = cnt != need ? 4 : 3;
+    }
+  }
+  const int shift = depth == 1 ? 20 : (depth == 2 ? 8 : 0);
+  // thread t owns positions [t * per, (t + 1) * per): counts, then offsets
+  const int per = (n + kTkThreads - 1) / kTkThreads;
+  const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+  uint32_t g = 0, t = 0;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t x = key[i] >> shift;
+    g += x > thr || (depth <= 3 && x == thr);
+    t += depth == 4 && key[i] == thr;
+  }
+  // block-wide exclusive scans of g and t
+  uint32_t ig = g, it = t;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t vg = __shfl_up_sync(0xffffffffu, ig, d);
+    const uint32_t vt = __shfl_up_sync(0xffffffffu, it, d);
+    if (lane >= d) {
+      ig += vg;
+      it += vt;
+    }
+  }
+  if (lane == 31) {
+    wg[warp] = ig;
+    wt[warp] = it;
+  }
+  __syncthreads();
+  uint32_t bg = 0, bt = 0;
+  for (int w = 0; w < warp; ++w) {
+    bg += wg[w];
+    bt += wt[w];
+  }
+  uint32_t gpre = bg + ig - g, tpre = bt + it - t;  // before this thread's range
+  // ties before this range taken (at most need), so positions before it
+  uint32_t pos = gpre + min(tpre, need);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t x = key[i] >> shift;
+    bool sel = x > thr || (depth <= 3 && x == thr);
+    if (!sel && depth == 4 && key[i] == thr) sel = tpre++ < need;
+    if (sel) {
+      if (pos < (uint32_t)m) o[pos] = rm ? rm[i] : i;
+      ++pos;
+    }
+  }
+  pdl_trigger();
+  for (int i = m + tid; i < k; i += kTkThreads) o[i] = -1;
+}
+
 bool g_select_attr = false;
 
 }  // namespace
@@ -469,6 +598,16 @@ csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int
                        k, hist1, idx_out, idx_ld, vec, remap, remap_ld, clear_hist ? 1 : 0);
 }
 
+csa2_status launch_topk_small(const float* scores, int64_t ld, const int32_t* gather,
+                              int64_t gather_ld, int64_t rows, int32_t n, const int32_t* n_valid,
+                              int32_t k, const int32_t* remap, int64_t remap_ld, int32_t* idx_out,
+                              int64_t idx_ld, cudaStream_t s) {
+  if (rows == 0) return CSA2_OK;
+  if (n < 0 || n > kSmallN || k < 1 || k > kMaxK) return CSA2_ERR_UNSUPPORTED;
+  return launch_kernel(topk_small_kernel, dim3((unsigned)rows), dim3(kTkThreads), 0, s, 1, scores,
+                       ld, gather, gather_ld, n, n_valid, k, remap, remap_ld, idx_out, idx_ld);
+}
+
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
                              const int32_t* n_valid, uint32_t* hist1, cudaStream_t s) {
   if (rows == 0 || n == 0) return CSA2_OK;
@@ -486,6 +625,10 @@ csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld
                         void* ws, int32_t* dev_status, cudaStream_t s) {
   (void)dev_status;
   if (rows == 0) return CSA2_OK;
+  // short rows: one CTA per row with every key in shared memory
+  if (n <= kSmallN)
+    return launch_topk_small(scores, ld, nullptr, 0, rows, (int32_t)n, n_valid, k, nullptr, 0,
+                             idx_out, idx_ld, s);
   uint32_t* hist1 = static_cast<uint32_t*>(ws);
   csa2_status st = clear_topk_hist(hist1, rows, s);
   if (st != CSA2_OK) return st;
