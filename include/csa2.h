@@ -416,6 +416,7 @@ typedef struct csa2_stack_args {
   size_t workspace_bytes;
   int32_t* dev_status;
   int32_t pool;  /* candidate pool size P of the Hierarchical Sparse Indexer; 0 = off */
+  int32_t win_max; /* host upper bound on win_len (0: w_rows); sizes the attention launch */
 } csa2_stack_args;
 
 /* Checks a schedule (see above) without touching the GPU.  Returns CSA2_OK

@@ -63,7 +63,7 @@ class StackArgs(ctypes.Structure):
                 ("idx_q_dtype", _c_i32), ("idx_k_dtype", _c_i32), ("attn_q_dtype", _c_i32),
                 ("n_valid", _c_p), ("win_start", _c_p), ("win_len", _c_p),
                 ("softmax_scale", _c_f), ("workspace", _c_p), ("workspace_bytes", _c_sz),
-                ("dev_status", _c_p), ("pool", _c_i32)]
+                ("dev_status", _c_p), ("pool", _c_i32), ("win_max", _c_i32)]
 
 
 EXPORTS = {
@@ -326,12 +326,13 @@ def validate_plan(layers):
 
 def stack_args(B, q_per_seq, n, hi, di, hq, d, k, w_rows, idx_q_dtype, idx_k_dtype,
                attn_q_dtype, softmax_scale, n_valid=None, win_start=None, win_len=None,
-               dev_status=None, pool=0):
+               dev_status=None, pool=0, win_max=0):
     return StackArgs(B=B, q_per_seq=q_per_seq, n=n, hi=hi, di=di, hq=hq, d=d, k=k,
                      w_rows=w_rows, idx_q_dtype=idx_q_dtype, idx_k_dtype=idx_k_dtype,
                      attn_q_dtype=attn_q_dtype, n_valid=_ptr(n_valid),
                      win_start=_ptr(win_start), win_len=_ptr(win_len),
-                     softmax_scale=softmax_scale, dev_status=_ptr(dev_status), pool=pool)
+                     softmax_scale=softmax_scale, dev_status=_ptr(dev_status), pool=pool,
+                     win_max=win_max)
 
 
 def layer_stack_workspace_bytes(sargs):

@@ -263,7 +263,7 @@ csa2_attn_args stack_attn_args(const csa2_stack_args& s, const csa2_layer_desc& 
   a.win_seq_stride = (int64_t)s.w_rows * s.d;
   a.win_start = s.win_start;
   a.win_len = s.win_len;
-  a.win_max = 0;
+  a.win_max = s.win_max;
   a.softmax_scale = s.softmax_scale;
   a.out = L.out;
   a.workspace = ws;
@@ -488,7 +488,8 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
                              const csa2_stack_args* s, csa2_stream_t stream) {
   csa2_status st = csa2_validate_plan(L, n_layers, nullptr);
   if (st != CSA2_OK) return st;
-  if (!s || s->B < 1 || s->q_per_seq < 1 || s->n < 1 || s->k < 1 || s->pool < 0)
+  if (!s || s->B < 1 || s->q_per_seq < 1 || s->n < 1 || s->k < 1 || s->pool < 0 ||
+      s->win_max < 0)
     return CSA2_ERR_INVALID_ARG;
   if (s->pool > 0) {
     if (s->pool < s->k) return CSA2_ERR_INVALID_ARG;

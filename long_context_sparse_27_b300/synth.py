@@ -80,7 +80,10 @@ C1M_GROUP = replace(C1M, name="1m4", modes=C1M.modes[:4])
 # scores only the top-2048 pool of its Full layer
 C1M_POOL = replace(C1M, name="1m-pool", pool=2048)
 
-WORKLOADS = {w.name: w for w in (TINY, C128K, GROUP3, C1M, C1M_GROUP, PREFILL, C1M_POOL)}
+C1M_POOL_GROUP = replace(C1M_POOL, name="1m4-pool", modes=C1M.modes[:4])
+
+WORKLOADS = {w.name: w for w in (TINY, C128K, GROUP3, C1M, C1M_GROUP, PREFILL, C1M_POOL,
+                                 C1M_POOL_GROUP)}
 
 
 def scaled(w: Workload, **kw) -> Workload:

@@ -133,7 +133,7 @@ class StackWorkload:
             attn_q_dtype=csa2.F32 if wl.attn_q_fp32 else csa2.BF16,
             softmax_scale=1.0 / math.sqrt(wl.D), n_valid=self.n_valid,
             win_start=self.win_start, win_len=self.win_len, dev_status=self.dev_status,
-            pool=wl.pool)
+            pool=wl.pool, win_max=wl.W if self.win_len is not None else 0)
 
     def run(self):
         """Enqueue one step on the current stream."""
