@@ -12,9 +12,10 @@
 //    tensor memory, then an epilogue applies ReLU, the head weights c and the
 //    head sum.  Warp 0 streams K tiles with TMA into a ring of 16 KB stages,
 //    warp 1 issues the MMAs into a ring of two tensor-memory accumulators,
-//    and two epilogue warpgroups (warps 2-5 and 6-9) drain alternate tiles,
-//    so two warps per SM sub-partition hide each other's tcgen05.ld and FMA
-//    latency.  In decode (QG = 1) the kernel is a stream over the indexer
+//    and the epilogue warpgroups drain alternate tiles (two in decode,
+//    warps 2-5 and 6-9; in a prefill chunk two per tile, each taking two of
+//    its four queries), so several warps per SM sub-partition hide each
+//    other's tcgen05.ld and FMA latency.  In decode (QG = 1) the kernel is a stream over the indexer
 //    keys (128 B per entry): one CTA's load -> MMA -> epilogue -> accumulator
 //    hand-back chain is latency-bound well short of HBM speed, so two CTAs
 //    with 3-stage rings share each SM and overlap their chains.  In a prefill
@@ -107,7 +108,12 @@ struct TcCfg {
   static constexpr int BK = 128;        // indexer dim: 128 E4M3 bytes per row
   static constexpr int CTAS_PER_SM = QG == 1 ? 2 : 1;
   static constexpr int STAGES = QG == 1 ? 3 : 6;
-  static constexpr int EPI_WGS = 2;     // epilogue warpgroups
+  // epilogue: STREAMS tiles drained at once, each by SPLIT warpgroups that
+  // share its queries (a prefill tile holds 4 queries x 64 heads)
+  static constexpr int SPLIT = QG == 1 ? 1 : 2;
+  static constexpr int STREAMS = 2;
+  static constexpr int EPI_WGS = STREAMS * SPLIT;  // epilogue warpgroups
+  static constexpr int QPW = QG / SPLIT;           // queries per epilogue warpgroup
   static constexpr int NACC = 2;        // accumulators in tensor memory
   static constexpr int KTILE = BM * BK;  // 16 KB
   static constexpr int QTILE = BN * BK;  // 8 KB or 32 KB
@@ -129,7 +135,8 @@ struct TcCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem slot, abort flag
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
-  static_assert(NACC % EPI_WGS == 0, "accumulator a is drained by warpgroup a % EPI_WGS");
+  static_assert(NACC % STREAMS == 0 && QG % SPLIT == 0,
+                "accumulator a is drained by the warpgroups of stream a % STREAMS");
   static_assert(TMEM_USED <= 512, "tensor memory holds 512 columns");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory per CTA");
   static_assert(CTAS_PER_SM * (SMEM_ALLOC + 1024) <= 228 * 1024, "CTAs resident per SM");
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     }
     for (int i = 0; i < C::NACC; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);  // the 4 warps of one warpgroup
+      mbar_init(&tempty[i], 4 * C::SPLIT);  // the warps of the warpgroups that share a tile
     }
     mbar_init(fin, 1);
     *abort_flag = 0;
@@ -333,21 +340,25 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     }
   } else {
     // ---------------- epilogue ----------------
-    // warpgroup wg drains the tiles with local number li = wg, wg + EPI_WGS,
-    // ...; tile li sits in accumulator li % NACC.
+    // warpgroup wg belongs to stream wg / SPLIT, which drains the tiles with
+    // local number li = stream, stream + STREAMS, ...; tile li sits in
+    // accumulator li % NACC; the warpgroup takes queries q0 .. q0 + QPW - 1.
     const int ew = warp - 2;          // 0 .. EPI_WARPS-1
     const int wg = ew >> 2;
+    const int stream = wg / C::SPLIT;
+    const int q0 = (wg % C::SPLIT) * C::QPW;
     const int lq = warp & 3;          // TMEM lane quarter this warp may access
     const int row = lq * 32 + lane;   // entry within the tile
     int64_t g_prev = -1;
     // each warp keeps its own double-buffered copy of the group's head weights
     float* my_c = cbuf + ew * 2 * C::BN;
     int cb = 1;
-    int64_t nv[QG];
+    int64_t nv[C::QPW];
     // li counts tiles in processing order (from the range's end when reversed)
     const int64_t dir = p.reverse ? -1 : 1;
-    TileCursor cur(p.reverse ? t_end - 1 - wg : t_begin + wg, p.ktiles);
-    for (int64_t li = wg; li < t_end - t_begin; li += C::EPI_WGS, cur.advance(dir * C::EPI_WGS)) {
+    TileCursor cur(p.reverse ? t_end - 1 - stream : t_begin + stream, p.ktiles);
+    for (int64_t li = stream; li < t_end - t_begin;
+         li += C::STREAMS, cur.advance(dir * C::STREAMS)) {
       const int64_t g = cur.g, kt = cur.kt;
       const int acc = (int)(li % C::NACC);
       const uint32_t aph = (uint32_t)((li / C::NACC) & 1);
@@ -357,7 +368,8 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         for (int i = lane; i < C::BN; i += 32) my_c[cb * C::BN + i] = p.c[g * C::BN + i];
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < QG; ++i) nv[i] = p.n_valid ? (int64_t)p.n_valid[g * QG + i] : p.n;
+        for (int i = 0; i < C::QPW; ++i)
+          nv[i] = p.n_valid ? (int64_t)p.n_valid[g * QG + q0 + i] : p.n;
         g_prev = g;
       }
       // every lane waits; the warp goes on only if all of them saw the phase
@@ -366,9 +378,9 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(lq * 32) << 16) + (uint32_t)(acc * C::BN);
-      float sc[QG];
+      float sc[C::QPW];
 #pragma unroll
-      for (int qq = 0; qq < QG; ++qq) {
+      for (int qq = 0; qq < C::QPW; ++qq) {
         float s8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) s8[i] = 0.f;
@@ -376,16 +388,16 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float v[32];
-          tmem_ld32(taddr + qq * 64 + half * 32, v);
+          tmem_ld32(taddr + (q0 + qq) * 64 + half * 32, v);
           tmem_ld_wait();
-          if (qq == QG - 1 && half == 1) {
+          if (qq == C::QPW - 1 && half == 1) {
             // the accumulator is in registers: hand it back to the MMA warp
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
           }
           const float4* cw =
-              reinterpret_cast<const float4*>(my_c + cb * C::BN + qq * 64 + half * 32);
+              reinterpret_cast<const float4*>(my_c + cb * C::BN + (q0 + qq) * 64 + half * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float4 f = cw[i];
@@ -400,8 +412,8 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       const int64_t j = kt * C::BM + row;
       if (j < p.n) {
 #pragma unroll
-        for (int qq = 0; qq < QG; ++qq) {
-          const int64_t qi = g * QG + qq;
+        for (int qq = 0; qq < C::QPW; ++qq) {
+          const int64_t qi = g * QG + q0 + qq;
           p.scores[qi * p.scores_ld + j] = (j < nv[qq]) ? sc[qq] : -INFINITY;
         }
       }

@@ -81,9 +81,12 @@ C1M_GROUP = replace(C1M, name="1m4", modes=C1M.modes[:4])
 C1M_POOL = replace(C1M, name="1m-pool", pool=2048)
 
 C1M_POOL_GROUP = replace(C1M_POOL, name="1m4-pool", modes=C1M.modes[:4])
+# a quarter of the prefill chunk (1024 queries): the same kernels with a
+# quarter of the score scratch (profiling captures)
+PREFILL_1K = replace(PREFILL, name="prefill1k", q_per_seq=1024, pos0=1048576 - 1024)
 
 WORKLOADS = {w.name: w for w in (TINY, C128K, GROUP3, C1M, C1M_GROUP, PREFILL, C1M_POOL,
-                                 C1M_POOL_GROUP)}
+                                 C1M_POOL_GROUP, PREFILL_1K)}
 
 
 def scaled(w: Workload, **kw) -> Workload:
