@@ -155,6 +155,22 @@ def test_stack_pool_covering_every_entry(csa2):
         assert torch.equal(La["out"], Lb["out"])
 
 
+@pytest.mark.parametrize("pool", [0, 512])
+def test_stack_sequences_shorter_than_k(csa2, orc, pool):
+    # N = 300 < k = 512: every selection is all 300 entries padded with -1,
+    # the pool (P = min(512, N)) holds every entry, attention sees 300 FP4
+    # keys and the window
+    wl = synth.scaled(synth.C1M, B=2, N=300, modes=(synth.FULL, synth.REINDEX, synth.REUSE),
+                      pool=pool)
+    W = build(wl, 16)
+    run_stack(W)
+    for L in W.layers[:2]:
+        idx = L["topk_idx"].cpu().numpy()
+        assert np.array_equal(idx[:, :300], np.tile(np.arange(300, dtype=np.int32), (2, 1)))
+        assert np.all(idx[:, 300:] == -1)
+    compare(orc, W, min_agree=1.0)
+
+
 def test_stack_mode_identities(csa2):
     from long_context_sparse_27_b300.workload import StackWorkload
     wl = synth.scaled(synth.C1M, B=2, N=3000, modes=(synth.FULL, synth.REINDEX, synth.REUSE))
