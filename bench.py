@@ -141,6 +141,16 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def workload_desc(wl):
+    """The workload as both arms name it in `config`."""
+    pool = f", candidate pool {wl.pool}" if wl.pool else ""
+    q = "" if wl.q_per_seq == 1 else f", {wl.q_per_seq} queries per sequence"
+    return (f"{wl.name}: B={wl.B}, N={wl.N}{q}, layers={len(wl.modes)} "
+            f"{''.join('FIU'[m] for m in wl.modes)}, indexer {wl.Hi}x{wl.Di} "
+            f"{'fp32' if wl.fp32_indexer else 'E4M3'}, top-{wl.k}{pool}, {wl.Hq} heads x {wl.D} "
+            f"FP4 KV, window {wl.W} bf16")
+
+
 # ---------------------------------------------------------------- our arm
 
 def launches_per_step(wl):
@@ -356,9 +366,7 @@ def run_ours(args, world, rank, local):
         "dtype": "e4m3",
         "data": "synthetic (seeded N(0,1); planted indexer keys)",
         "config": {
-            "workload": f"{wl.name}: B={wl.B}, N={wl.N}, layers={n_layers} "
-                        f"{''.join('FIU'[m] for m in wl.modes)}, indexer {wl.Hi}x{wl.Di} E4M3, "
-                        f"top-{wl.k}, {wl.Hq} heads x {wl.D} FP4 KV, window {wl.W} bf16",
+            "workload": workload_desc(wl),
             "l2": ("inputs larger than L2 (%.2f GB per step); L2 flushed before every "
                    "device-timed step, not in the pipelined end-to-end loop" % (alg / 1e9))
                   if alg >= 2 * L2_BYTES else
@@ -402,7 +410,8 @@ def cpu_baseline(wl, budget_s):
     whole sequences through the first group of layers (Full, Reindex,
     Reuse, Reuse), one sequence at a time until `budget_s` is spent.  Inputs
     are prepared outside the timed region (the oracle's own E4M3 / FP4
-    casts of the seeded bf16 rows); timed: scores, top-k and attention."""
+    casts of the seeded bf16 rows); timed: scores, top-k (with the candidate
+    pool when the workload has one) and attention."""
     import numpy as np
     from oracle import oracle as orc
     from long_context_sparse_27_b300 import synth
@@ -426,14 +435,22 @@ def cpu_baseline(wl, budget_s):
                            "w": synth.index_w(one, s + 20 + l).double().numpy(),
                            "aq": synth.attn_q(one, s + 30 + l).double().numpy(),
                            "win": synth.window_rows(one, s + 40 + l).double().numpy()})
-        q8c = [orc.quantize_index_q(L["q"], L["w"]) for L in layers]
+        q8c = [None if wl.fp32_indexer else orc.quantize_index_q(L["q"], L["w"]) for L in layers]
+        kf = kk.double().numpy()
         t0 = time.perf_counter()
-        idx = None
+        idx = pool = None
         for l, m in enumerate(group):
             L = layers[l]
             if m in (0, 1):
-                q8, c = q8c[l]
-                sc = orc.index_score(table[q8], c, kd)
+                if wl.fp32_indexer:
+                    sc = orc.index_score(L["q"], L["w"], kf)
+                else:
+                    q8, c = q8c[l]
+                    sc = orc.index_score(table[q8], c, kd)
+                if wl.pool and m == 0:
+                    pool = orc.topk(sc, wl.pool)   # the candidate pool
+                if wl.pool and m == 1:
+                    sc = orc.pool_restrict(sc, pool)
                 idx = orc.topk(sc, wl.k)
             sel = idx[0][idx[0] >= 0]
             c_rows, s_rows = orc.quantize_fp4(
@@ -478,8 +495,7 @@ def run_reference(args, world, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1); planted indexer keys)",
-        "config": {"workload": f"{wl.name}: B={wl.B}, N={wl.N}, layers={len(wl.modes)}",
-                   "sample": cb["sample"]},
+        "config": {"workload": workload_desc(wl), "sample": cb["sample"]},
         "cpu_baseline": cb,
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

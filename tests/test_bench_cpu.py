@@ -1,0 +1,29 @@
+"""Host-side pieces of bench.py: the kernel-count claim and the workload
+names both arms print (no GPU)."""
+import sys
+
+from conftest import ROOT
+
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from long_context_sparse_27_b300 import synth  # noqa: E402
+
+
+def test_launches_per_step():
+    W = synth.WORKLOADS
+    # Full: new-row quantiser, Q quantiser, indexer (histogram fused), select,
+    # attention; Reindex: the same without the new rows; Reuse: attention
+    assert bench.launches_per_step(W["1m"]) == 5 * (5 + 4 + 1 + 1)
+    assert bench.launches_per_step(W["group3"]) == 5 + 4 + 1
+    # the pool: Full adds the pool's selection (6), a pooled Reindex runs Q
+    # quantiser, pooled scores, short-row selection, attention (4)
+    assert bench.launches_per_step(W["1m-pool"]) == 5 * (6 + 4 + 1 + 1)
+    # a prefill chunk adds the histogram pass; 8 chunks of 80 keys need no merge kernel
+    assert bench.launches_per_step(W["prefill"]) == 6
+
+
+def test_workload_desc_names_the_variant():
+    d = bench.workload_desc(synth.WORKLOADS["1m-pool"])
+    assert d.startswith("1m-pool: B=8, N=262144") and "candidate pool 2048" in d
+    assert "fp32" in bench.workload_desc(synth.WORKLOADS["tiny"])
+    assert "4096 queries per sequence" in bench.workload_desc(synth.WORKLOADS["prefill"])
