@@ -247,3 +247,5 @@ def test_stack_pool_validation(csa2, monkeypatch):
     s.pool = 2048
     s.idx_q_dtype = s.idx_k_dtype = csa2.F32   # the pooled scoring is FP8 only
     assert L.csa2_layer_stack(descs, 2, ctypes.byref(s), None) == 2
+    s.pool, s.win_max = 0, -1                  # a negative window bound
+    assert L.csa2_layer_stack(descs, 2, ctypes.byref(s), None) == 1
