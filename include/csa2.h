@@ -367,6 +367,12 @@ csa2_status csa2_sparse_attn(const csa2_attn_args* args, csa2_stream_t stream);
  *   topk_idx int32 [nq, k]; out f32 [nq, hq, d].
  * Workspace: csa2_layer_stack_workspace_bytes (scores, selector and
  * attention scratch, reused layer after layer).
+ * Windows: win_start / win_len (optional, per query) select each query's
+ * rows of its layer's window buffer as in csa2_sparse_attn; win_max, a host
+ * upper bound on win_len (0: w_rows), sizes the attention launch (a prefill
+ * chunk's buffer holds T + W - 1 rows, each query sees W of them).
+ * Errors: INVALID_ARG (a plan or argument check, pool < k, win_max < 0),
+ *         UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA -- all before any launch.
  *
  * Hierarchical Sparse Indexer (args->pool = P > 0) [P5 Method]: every Full
  * layer's indexer, which scores all entries, also keeps its top-P entries
