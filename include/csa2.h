@@ -372,7 +372,8 @@ csa2_status csa2_sparse_attn(const csa2_attn_args* args, csa2_stream_t stream);
  * upper bound on win_len (0: w_rows), sizes the attention launch (a prefill
  * chunk's buffer holds T + W - 1 rows, each query sees W of them).
  * Errors: INVALID_ARG (a plan or argument check, pool < k, win_max < 0),
- *         UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA -- all before any launch.
+ *         UNSUPPORTED, ALIGNMENT, WORKSPACE -- found before any launch;
+ *         CUDA from a launch.
  *
  * Hierarchical Sparse Indexer (args->pool = P > 0) [P5 Method]: every Full
  * layer's indexer, which scores all entries, also keeps its top-P entries
