@@ -134,6 +134,21 @@ def quantize_fp4(x):
     return codes, scales
 
 
+def project_kv(h, w):
+    """The decoder's global KV of one layer: h [rows, hidden] (the final
+    encoder hidden state) times that layer's projection w [d, hidden]
+    (row c: the weights of output column c), in fp64: out [rows, d].
+    ["Unlocking...", Causal Encoder-Decoder (CED) Efficiency: the decoder
+    derives its global KV cache from the final encoder hidden state using
+    per-layer projections.]  Reading: a plain linear map, no bias."""
+    return _f64(h) @ _f64(w).T
+
+
+def project_quantize_fp4(h, w):
+    """project_kv, then the FP4 main-KV quantiser (a1) of its rows."""
+    return quantize_fp4(project_kv(h, w))
+
+
 def dequantize_fp4(codes, scales, d):
     codes = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1, d // 2)
     scales = np.ascontiguousarray(scales, dtype=np.uint8).reshape(-1, d // 32)

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 from conftest import read_golden
+from long_context_sparse_27_b300 import synth
 
 E2M1_GRID = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 
@@ -224,3 +225,40 @@ def test_fp4_storage_ratio(orc, rows, d):
     assert c.shape[1] + s.shape[1] == d // 2 + d // 32
     if d == 512:
         assert (c.shape[1] + s.shape[1]) / d == pytest.approx(0.53125)
+
+
+# ---- decoder global-KV projection + FP4 quantise (the CED path) ------------
+
+def test_projection_identity_is_the_quantiser(orc):
+    # w = [I 0] picks the first d hidden features: the projection reduces to
+    # the plain FP4 quantiser of those features
+    rows, hidden, d = 5, 96, 64
+    h = synth.normal((rows, hidden), 200).double().numpy()
+    w = np.zeros((d, hidden))
+    w[:, :d] = np.eye(d)
+    c1, s1 = orc.project_quantize_fp4(h, w)
+    c2, s2 = orc.quantize_fp4(h[:, :d])
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2)
+
+
+def test_projection_power_of_two_weights_shift_only_the_scales(orc):
+    rows, hidden, d = 4, 128, 96
+    h = synth.normal((rows, hidden), 201).double().numpy()
+    w = synth.normal((d, hidden), 202).double().numpy()
+    c1, s1 = orc.project_quantize_fp4(h, w)
+    c2, s2 = orc.project_quantize_fp4(h, w * 8.0)
+    assert np.array_equal(c1, c2)
+    assert np.array_equal(s2.astype(int), s1.astype(int) + 3)
+
+
+def test_projection_brute_force(orc):
+    rows, hidden, d = 3, 7, 5
+    h = synth.normal((rows, hidden), 203).double().numpy()
+    w = synth.normal((d, hidden), 204).double().numpy()
+    out = orc.project_kv(h, w)
+    for r in range(rows):
+        for c in range(d):
+            ref = 0.0
+            for k in range(hidden):
+                ref += h[r, k] * w[c, k]
+            assert abs(out[r, c] - ref) <= 1e-12 * max(1.0, abs(ref))
