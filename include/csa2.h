@@ -338,6 +338,45 @@ size_t csa2_sparse_attn_workspace_bytes(const csa2_attn_args* args);
 csa2_status csa2_sparse_attn(const csa2_attn_args* args, csa2_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* the decoder's global KV: projection of the encoder state + FP4 quantise   */
+/* ------------------------------------------------------------------------ */
+/*
+ * out[r, c] = sum_k h[r, k] * w[c, k] (fp32 accumulation of bf16 products),
+ * quantised per 32-element block of each row exactly as csa2_quantize_fp4
+ * into codes / scales.  [P3 "Causal Encoder-Decoder (CED) Efficiency": the
+ * decoder derives its global KV cache from the final encoder hidden state
+ * using per-layer projections; P3 "Deployment and Infrastructure": FP4 main
+ * KV.]  The codes are decided on the fp32 projection, which is also written
+ * to `out` when out is not NULL.
+ *
+ * h      device bf16 [rows, hidden], row r at h + r * h_ld (elements)
+ * w      device bf16 [d, hidden]: row c holds the weights of output column c
+ * codes  device u8 [rows, d/2] (even column in the low nibble), codes_ld
+ * scales device u8 [rows, d/32] (UE8M0), scales_ld
+ * out    optional device f32 [rows, d], out_ld
+ * hidden a multiple of 32; d a multiple of 64.
+ * Errors: INVALID_ARG, ALIGNMENT (h, w 16-byte aligned with h_ld, w_ld
+ *         multiples of 8; out 8-byte aligned with out_ld even), CUDA.
+ */
+typedef struct csa2_project_args {
+  const void* h;
+  const void* w;
+  int64_t rows;
+  int32_t hidden;
+  int32_t d;
+  int64_t h_ld;
+  int64_t w_ld;
+  uint8_t* codes;
+  int64_t codes_ld;
+  uint8_t* scales;
+  int64_t scales_ld;
+  float* out;
+  int64_t out_ld;
+} csa2_project_args;
+
+csa2_status csa2_project_fp4(const csa2_project_args* args, csa2_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* a6: the static Full / Reindex / Reuse layer schedule                      */
 /* ------------------------------------------------------------------------ */
 /*

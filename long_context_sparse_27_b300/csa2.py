@@ -57,6 +57,12 @@ class LayerDesc(ctypes.Structure):
                 ("idxk", _c_p), ("topk_idx", _c_p), ("out", _c_p)]
 
 
+class ProjectArgs(ctypes.Structure):
+    _fields_ = [("h", _c_p), ("w", _c_p), ("rows", _c_i64), ("hidden", _c_i32), ("d", _c_i32),
+                ("h_ld", _c_i64), ("w_ld", _c_i64), ("codes", _c_p), ("codes_ld", _c_i64),
+                ("scales", _c_p), ("scales_ld", _c_i64), ("out", _c_p), ("out_ld", _c_i64)]
+
+
 class StackArgs(ctypes.Structure):
     _fields_ = [("B", _c_i64), ("q_per_seq", _c_i64), ("n", _c_i64), ("hi", _c_i32),
                 ("di", _c_i32), ("hq", _c_i32), ("d", _c_i32), ("k", _c_i32), ("w_rows", _c_i32),
@@ -76,6 +82,7 @@ EXPORTS = {
     "csa2_index_score_workspace_bytes": (_c_sz, [ctypes.POINTER(IndexArgs)]),
     "csa2_index_score": (_c_i32, [ctypes.POINTER(IndexArgs), _c_p]),
     "csa2_index_score_pool": (_c_i32, [ctypes.POINTER(IndexArgs), _c_p, _c_i64, _c_i32, _c_p]),
+    "csa2_project_fp4": (_c_i32, [ctypes.POINTER(ProjectArgs), _c_p]),
     "csa2_topk_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i32]),
     "csa2_topk": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_p, _c_sz,
                            _c_p, _c_p]),
@@ -230,6 +237,24 @@ def index_score_pool(q, w, k, pool, q_per_seq=1, scores=None, dev_status=None):
     _check(lib.csa2_index_score_pool(ctypes.byref(a), _ptr(pool), pool.stride(0), P, _stream()),
            "csa2_index_score_pool")
     return scores
+
+
+def project_fp4(h, w, with_out=False):
+    """The decoder's global KV of one layer: h bf16 [rows, hidden] (final
+    encoder hidden state), w bf16 [d, hidden] (the layer's projection, one
+    row per output column) -> (codes u8 [rows, d/2], scales u8 [rows, d/32],
+    out f32 [rows, d] or None)."""
+    rows, hidden = h.shape
+    d = w.shape[0]
+    codes = torch.empty(rows, d // 2, dtype=torch.uint8, device=h.device)
+    scales = torch.empty(rows, d // 32, dtype=torch.uint8, device=h.device)
+    out = torch.empty(rows, d, dtype=torch.float32, device=h.device) if with_out else None
+    a = ProjectArgs(h=_ptr(h), w=_ptr(w), rows=rows, hidden=hidden, d=d, h_ld=h.stride(0),
+                    w_ld=w.stride(0), codes=_ptr(codes), codes_ld=codes.stride(0),
+                    scales=_ptr(scales), scales_ld=scales.stride(0), out=_ptr(out),
+                    out_ld=(out.stride(0) if out is not None else 0))
+    _check(lib.csa2_project_fp4(ctypes.byref(a), _stream()), "csa2_project_fp4")
+    return codes, scales, out
 
 
 # ---- a4 ----------------------------------------------------------------------

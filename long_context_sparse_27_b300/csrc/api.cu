@@ -419,6 +419,23 @@ csa2_status csa2_index_score_pool(const csa2_index_args* args, const int32_t* po
                                  args->scores_ld, cs);
 }
 
+csa2_status csa2_project_fp4(const csa2_project_args* a, csa2_stream_t stream) {
+  if (!a || a->rows < 0 || a->hidden < 32 || a->hidden % 32 != 0 || a->d < 64 || a->d % 64 != 0)
+    return CSA2_ERR_INVALID_ARG;
+  if (a->rows == 0) return CSA2_OK;
+  if (!a->h || !a->w || !a->codes || !a->scales) return CSA2_ERR_INVALID_ARG;
+  if (a->h_ld < a->hidden || a->w_ld < a->hidden || a->codes_ld < a->d / 2 ||
+      a->scales_ld < a->d / 32 || (a->out && a->out_ld < a->d))
+    return CSA2_ERR_INVALID_ARG;
+  if (!aligned(a->h, 16) || !aligned(a->w, 16) || a->h_ld % 8 != 0 || a->w_ld % 8 != 0)
+    return CSA2_ERR_ALIGNMENT;
+  if (a->out && (!aligned(a->out, 8) || a->out_ld % 2 != 0)) return CSA2_ERR_ALIGNMENT;
+  if (a->rows > (int64_t)65535 * 64 * 1024) return CSA2_ERR_UNSUPPORTED;
+  csa2_status st = injected("project_fp4");
+  if (st != CSA2_OK) return st;
+  return launch_project_fp4(*a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t csa2_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k) {
   if (rows < 0 || k < 1) return 0;
   return topk_workspace_bytes(rows, n, k);

@@ -59,6 +59,9 @@ csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld
 csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s);
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
                              const int32_t* n_valid, uint32_t* hist1, cudaStream_t s);
+// The decoder's global KV: h [rows, hidden] x w [d, hidden]^T quantised to
+// FP4 (codes / scales), the fp32 projection optionally to out.
+csa2_status launch_project_fp4(const csa2_project_args& a, cudaStream_t s);
 // Top-k of short rows (n <= 4096, one CTA per row; n_valid optional): value i of row r is
 // scores[r * ld + i], or with gather scores[r * ld + gather[r * gather_ld +
 // i]] (an index < 0 is an empty slot, below every value); positions are

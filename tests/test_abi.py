@@ -50,7 +50,7 @@ def test_every_declared_symbol_is_exported(csa2):
 def test_struct_layouts_match_c(csa2, tmp_path):
     structs = {"csa2_quant_args": csa2.QuantArgs, "csa2_index_args": csa2.IndexArgs,
                "csa2_attn_args": csa2.AttnArgs, "csa2_layer_desc": csa2.LayerDesc,
-               "csa2_stack_args": csa2.StackArgs}
+               "csa2_stack_args": csa2.StackArgs, "csa2_project_args": csa2.ProjectArgs}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "csa2.h"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
@@ -249,3 +249,25 @@ def test_stack_pool_validation(csa2, monkeypatch):
     assert L.csa2_layer_stack(descs, 2, ctypes.byref(s), None) == 2
     s.pool, s.win_max = 0, -1                  # a negative window bound
     assert L.csa2_layer_stack(descs, 2, ctypes.byref(s), None) == 1
+
+
+@no_gpu
+def test_project_validation(csa2, monkeypatch):
+    L = csa2.lib
+    a = csa2.ProjectArgs(h=FAKE, w=FAKE, rows=8, hidden=4096, d=512, h_ld=4096, w_ld=4096,
+                         codes=FAKE, codes_ld=256, scales=FAKE, scales_ld=16)
+    monkeypatch.setenv("CSA2_FAULT_INJECT", "project_fp4:4")
+    assert L.csa2_project_fp4(ctypes.byref(a), None) == 4         # valid: stopped by injection
+    a.hidden = 100
+    assert L.csa2_project_fp4(ctypes.byref(a), None) == 1         # hidden % 32
+    a.hidden, a.d = 4096, 96
+    assert L.csa2_project_fp4(ctypes.byref(a), None) == 1         # d % 64
+    a.d = 512
+    a.h = FAKE + 8
+    assert L.csa2_project_fp4(ctypes.byref(a), None) == 3         # 16-byte rows
+    a.h, a.w_ld = FAKE, 4100
+    assert L.csa2_project_fp4(ctypes.byref(a), None) == 3
+    a.w_ld, a.codes_ld = 4096, 100
+    assert L.csa2_project_fp4(ctypes.byref(a), None) == 1
+    a.codes_ld, a.out, a.out_ld = 256, FAKE, 511
+    assert L.csa2_project_fp4(ctypes.byref(a), None) == 1         # out_ld < d

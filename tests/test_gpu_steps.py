@@ -205,6 +205,40 @@ def test_index_score_pool_exact_small_integers(csa2, orc):
     assert np.array_equal(s.cpu().double().numpy()[0], ref[0, pool[0].numpy()])
 
 
+# ------------------------------------ the decoder's global KV (projection + a1)
+
+@pytest.mark.parametrize("rows,hidden,d", [(8, 4096, 512), (100, 256, 128), (1, 64, 64),
+                                           (1024, 512, 512)])
+def test_project_fp4(csa2, orc, rows, hidden, d):
+    h = synth.normal((rows, hidden), 210 + rows)
+    w = synth.normal((d, hidden), 211 + rows) * 0.05
+    w = w.to(torch.bfloat16)
+    h[0] = 0  # an all-zero row: scale byte 0, zero codes
+    codes, scales, out = csa2.project_fp4(dev(h), dev(w), with_out=True)
+    g = out.cpu().double().numpy()
+    ref = orc.project_kv(f64(h), f64(w))
+    # fp32 summation of exact bf16 products: |error| <= hidden * 2^-23 * sum |terms| (the
+    # recursive-summation bound with the unit of a truncating adder)
+    bound = hidden * 2.0 ** -23 * (np.abs(f64(h)) @ np.abs(f64(w)).T)
+    assert np.all(np.abs(g - ref) <= bound + 1e-30)
+    # the codes: the oracle's quantiser on the kernel's own fp32 projection
+    rc, rs = orc.quantize_fp4(g)
+    assert np.array_equal(codes.cpu().numpy(), rc) and np.array_equal(scales.cpu().numpy(), rs)
+    assert int(scales[0].abs().sum()) == 0 and int(codes[0].sum()) == 0
+
+
+def test_project_fp4_exact_small_integers(csa2, orc):
+    # integer inputs keep every product and partial sum exact in fp32: the
+    # projection and its codes match the oracle's fp64 path bit for bit
+    g = torch.Generator().manual_seed(212)
+    h = torch.randint(-3, 4, (70, 256), generator=g).to(torch.bfloat16)
+    w = torch.randint(-2, 3, (128, 256), generator=g).to(torch.bfloat16)
+    codes, scales, out = csa2.project_fp4(dev(h), dev(w), with_out=True)
+    assert np.array_equal(out.cpu().double().numpy(), orc.project_kv(f64(h), f64(w)))
+    rc, rs = orc.project_quantize_fp4(f64(h), f64(w))
+    assert np.array_equal(codes.cpu().numpy(), rc) and np.array_equal(scales.cpu().numpy(), rs)
+
+
 # -------------------------------------------------------------------- a4 top-k
 
 @pytest.mark.parametrize("rows,n,k,levels", [
