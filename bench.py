@@ -502,6 +502,42 @@ def run_reference(args, world, rank):
     }
 
 
+def run_project(args):
+    """The decoder's global-KV projection + FP4 quantiser on its own
+    (csa2_project_fp4): a decode step (one new row per sequence, B = 8) and
+    a prefill chunk's 1024 entries, hidden 4096, d 512, each timed with CUDA
+    events over `steps` launches after `warmup`, L2 flushed before each."""
+    from long_context_sparse_27_b300 import csa2, synth
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+    hidden, d = 4096, 512
+    w = (synth.normal((d, hidden), 300, "cuda") * 0.05).to(torch.bfloat16)
+    lines = []
+    for rows in (8, 1024):
+        h = synth.normal((rows, hidden), 301 + rows, "cuda")
+        for _ in range(max(args.warmup, 3)):
+            csa2.project_fp4(h, w)
+        stream = torch.cuda.current_stream()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            csa2.project_fp4(h, w)
+            b.record(stream)
+        torch.cuda.synchronize()
+        t = sum(a.elapsed_time(b) for a, b in ev) / args.steps * 1e-3
+        nbytes = (rows + d) * hidden * 2 + rows * (d // 2 + d // 32)
+        flops = 2.0 * rows * hidden * d
+        lines.append({"op": "csa2_project_fp4", "rows": rows, "hidden": hidden, "d": d,
+                      "us": round(t * 1e6, 3), "GB/s": round(nbytes / t / 1e9, 1),
+                      "hbm_frac": round(nbytes / t / 1e9 / hbm_peak, 4),
+                      "TFLOP/s": round(flops / t / 1e12, 2),
+                      "bf16_frac": round(flops / t / 1e12 / bf16_peak, 4), "peak_kind": peak_kind,
+                      "steps": args.steps, "warmup": args.warmup})
+    return lines
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -512,10 +548,16 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--op", default=None, choices=["project"],
+                    help="time one entry point on its own instead of the step")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world, rank, local = dist_env()
+    if args.op == "project":
+        for line in run_project(args):
+            print(json.dumps(line), flush=True)
+        return 0
     if args.impl == "reference":
         line = run_reference(args, world, rank)
         if line is not None:

@@ -8,9 +8,9 @@
 // power-of-two block scale of the library's quantiser.
 //
 // One CTA per (64 rows, 64 output columns), 4 warps of 16 rows: the hidden
-// dimension is walked in steps of 32 with a double-buffered cp.async ring of
-// h and w tiles, m16n8k16 bf16 MMAs accumulate in fp32, and the epilogue
-// quantises the accumulators in registers: each 32-column block of a row
+// dimension is walked in steps of 32 through a 4-stage cp.async ring of h
+// and w tiles (three steps in flight), m16n8k16 bf16 MMAs accumulate in
+// fp32, and the epilogue quantises the accumulators in registers: each 32-column block of a row
 // lives in the four threads of a quad (8 values each), whose amax is two
 // shuffles away.  The codes are decided on the fp32 projection, which can
 // also be written out.
@@ -27,6 +27,16 @@ constexpr int kPjK = 32;           // hidden features per step
 constexpr int kPjThreads = 128;    // 4 warps x 16 rows
 constexpr int kPjStride = kPjK + 8;  // padded smem row (bf16): conflict-free ldmatrix
 constexpr int kPjTile = kPjRows * kPjStride;  // elements of one h (or w) tile
+constexpr int kPjStages = 4;       // copies in flight: steps ks + 1 .. ks + 3 load during step ks
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// wait until at most N of this thread's committed copy groups are pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __global__ void __launch_bounds__(kPjThreads)
     project_fp4_kernel(const uint16_t* __restrict__ h, int64_t h_ld,
@@ -34,8 +44,8 @@ __global__ void __launch_bounds__(kPjThreads)
                        int32_t hidden, uint8_t* __restrict__ codes, int64_t codes_ld,
                        uint8_t* __restrict__ scales, int64_t scales_ld, float* __restrict__ out,
                        int64_t out_ld) {
-  __shared__ __align__(16) uint16_t sh[2][kPjTile];
-  __shared__ __align__(16) uint16_t sw[2][kPjTile];
+  __shared__ __align__(16) uint16_t sh[kPjStages][kPjTile];
+  __shared__ __align__(16) uint16_t sw[kPjStages][kPjTile];
   pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t r0 = (int64_t)blockIdx.x * kPjRows;
@@ -61,12 +71,19 @@ __global__ void __launch_bounds__(kPjThreads)
 #pragma unroll
   for (int nt = 0; nt < kPjCols / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
   const int steps = hidden / kPjK;
-  load(0, 0);
+  // a ring of kPjStages stages, one copy group per step (empty groups past
+  // the end keep the count uniform)
+#pragma unroll
+  for (int i = 0; i < kPjStages - 1; ++i) {
+    if (i < steps) load(i, i);
+    cp_async_commit();
+  }
   for (int ks = 0; ks < steps; ++ks) {
-    const int s = ks & 1;
-    cp_async_wait_all();
-    __syncthreads();  // stage s is in; every warp is done with stage s ^ 1
-    if (ks + 1 < steps) load(s ^ 1, ks + 1);
+    const int s = ks % kPjStages;
+    cp_async_wait_group<kPjStages - 2>();  // step ks's group has landed
+    __syncthreads();  // ... for every thread; every warp is done with step ks - 1's stage
+    if (ks + kPjStages - 1 < steps) load((ks + kPjStages - 1) % kPjStages, ks + kPjStages - 1);
+    cp_async_commit();
 #pragma unroll
     for (int kk = 0; kk < kPjK / 16; ++kk) {
       uint32_t a0, a1, a2, a3;
