@@ -107,7 +107,7 @@ struct TcCfg {
   static constexpr int BN = 64 * QG;    // 64 heads x QG queries (MMA N)
   static constexpr int BK = 128;        // indexer dim: 128 E4M3 bytes per row
   static constexpr int CTAS_PER_SM = QG == 1 ? 2 : 1;
-  static constexpr int STAGES = QG == 1 ? 3 : 6;
+  static constexpr int STAGES = QG == 1 ? 3 : 8;
   // epilogue: STREAMS tiles drained at once, each by SPLIT warpgroups that
   // share its queries (a prefill tile holds 4 queries x 64 heads)
   static constexpr int SPLIT = QG == 1 ? 1 : 2;
