@@ -516,14 +516,12 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   p.keep_in_l2 = tune.keep_in_l2 ? 1 : 0;
   const int64_t total = p.groups * p.ktiles;
   if (total == 0) return CSA2_OK;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(idx_score_tc_kernel<QG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_ALLOC);
-    if (e != cudaSuccess) return cuda_fail(e);
-    attr_set = true;
-  }
+  static uint64_t attr_done = 0;
+  cudaError_t e = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(idx_score_tc_kernel<QG>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
   const int grid = (int)std::min<int64_t>(total, (int64_t)C::CTAS_PER_SM * sm_count());
   return launch_kernel(idx_score_tc_kernel<QG>, dim3(grid), dim3(C::THREADS),
                        (size_t)C::SMEM_ALLOC, s, 1, kmap, qmap, p);

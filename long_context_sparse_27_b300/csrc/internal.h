@@ -85,6 +85,22 @@ csa2_status launch_sparse_attn(const csa2_attn_args& a, cudaStream_t s);
 // number of SMs of the current device (cached per device)
 int sm_count();
 
+// Kernel attributes (the dynamic shared-memory limit) are per device: runs
+// `set` once for each device the calling thread makes current (bit d of
+// `done` records device d; devices past 63 run it every time).  A repeat
+// from a race is harmless: the attributes are idempotent.
+template <class F>
+cudaError_t once_per_device(uint64_t& done, F&& set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t)1 << dev : 0;
+  if (bit && (done & bit)) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess) done |= bit;
+  return e;
+}
+
 // Whether launches use programmatic dependent launch: CSA2_PDL=0 turns it
 // off (read once per process; default on).
 bool pdl_enabled();

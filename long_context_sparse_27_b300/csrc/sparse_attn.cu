@@ -597,16 +597,16 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(a.out, 0, (size_t)a.nq * a.hq * kD * sizeof(float), s);
     return e == cudaSuccess ? CSA2_OK : cuda_fail(e);
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel<true>,
+  static uint64_t attr_done = 0;
+  cudaError_t e = once_per_device(attr_done, [] {
+    cudaError_t r = cudaFuncSetAttribute(attn_bf16_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_bf16_kernel<false>,
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(attn_bf16_kernel<false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-    if (e != cudaSuccess) return cuda_fail(e);
-    attr_set = true;
-  }
+    return r;
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
   const dim3 grid((unsigned)nchunks, (unsigned)((a.hq + kHG - 1) / kHG), (unsigned)a.nq);
   if (nchunks <= kMaxClusterChunks)
     return launch_kernel(attn_bf16_kernel<true>, grid, dim3(kAttnThreads), (size_t)kAttnSmem, s,

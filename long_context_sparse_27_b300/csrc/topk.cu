@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kTkThreads)
   for (int i = m + tid; i < k; i += kTkThreads) o[i] = -1;
 }
 
-bool g_select_attr = false;
+uint64_t g_select_attr = 0;  // devices on which the selector's attributes are set
 
 }  // namespace
 
@@ -585,13 +585,11 @@ csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int
                                int32_t* idx_out, int64_t idx_ld, cudaStream_t s,
                                const int32_t* remap, int64_t remap_ld, bool clear_hist) {
   if (rows == 0) return CSA2_OK;
-  if (!g_select_attr) {
-    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel<kTkCluster>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kTkDynSmem);
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_select_attr = true;
-  }
+  cudaError_t e = once_per_device(g_select_attr, [] {
+    return cudaFuncSetAttribute(topk_select_kernel<kTkCluster>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kTkDynSmem);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
   const int vec = (ld % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) % 16) == 0) ? 1 : 0;
   return launch_kernel(topk_select_kernel<kTkCluster>, dim3((unsigned)(rows * kTkCluster)),
                        dim3(kTkThreads), (size_t)kTkDynSmem, s, kTkCluster, scores, n, ld, n_valid,
