@@ -227,6 +227,8 @@ def index_score_pool(q, w, k, pool, q_per_seq=1, scores=None, dev_status=None):
     128] as uint8, pool int32 [nq, P] (entry indices, -1 = empty slot) ->
     scores f32 [nq, P] (-inf at empty slots)."""
     nq, P = pool.shape
+    if pool.stride(1) != 1:
+        raise ValueError("index_score_pool: rows of pool must be contiguous")
     if scores is None:
         scores = torch.empty(nq, P, dtype=torch.float32, device=q.device)
     a = index_args(q, w, k, q_per_seq, None, scores, dev_status)
@@ -246,6 +248,8 @@ def project_fp4(h, w, with_out=False):
     out f32 [rows, d] or None)."""
     rows, hidden = h.shape
     d = w.shape[0]
+    if h.stride(1) != 1 or w.stride(1) != 1:
+        raise ValueError("project_fp4: rows of h and w must be contiguous")
     codes = torch.empty(rows, d // 2, dtype=torch.uint8, device=h.device)
     scales = torch.empty(rows, d // 32, dtype=torch.uint8, device=h.device)
     out = torch.empty(rows, d, dtype=torch.float32, device=h.device) if with_out else None

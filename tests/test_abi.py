@@ -271,3 +271,15 @@ def test_project_validation(csa2, monkeypatch):
     assert L.csa2_project_fp4(ctypes.byref(a), None) == 1
     a.codes_ld, a.out, a.out_ld = 256, FAKE, 511
     assert L.csa2_project_fp4(ctypes.byref(a), None) == 1         # out_ld < d
+
+
+def test_bindings_reject_strided_rows(csa2):
+    # the bindings pass stride(0) as the row stride: a row must be contiguous
+    h = torch.zeros(64, 8, dtype=torch.bfloat16).t()      # [8, 64], column-major
+    w = torch.zeros(64, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        csa2.project_fp4(h, w)
+    pool = torch.zeros(4, 2, dtype=torch.int32).t()       # [2, 4], column-major
+    with pytest.raises(ValueError):
+        csa2.index_score_pool(torch.zeros(2, 64, 128, dtype=torch.bfloat16),
+                              torch.zeros(2, 64), torch.zeros(1, 10, 128, dtype=torch.uint8), pool)
