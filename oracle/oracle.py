@@ -134,6 +134,26 @@ def quantize_fp4(x):
     return codes, scales
 
 
+def gather_pages(pool, block_table, n):
+    """The logical per-sequence view of a paged cache: row j of sequence b
+    is row j % page_rows of physical page block_table[b, j // page_rows].
+
+    pool [num_pages, page_rows, ...] (codes, scales or indexer K rows);
+    block_table int [B, pages_per_seq]; n rows per sequence
+    (n <= pages_per_seq * page_rows).  Returns [B, n, ...].
+    Reading (the serving layout the pages' inference stacks use, "Unlocking
+    ...", Deployment and Infrastructure): fixed-size pages in one shared
+    pool and one block table per sequence; every other step reads the
+    logical view, so paging changes where rows live, not what is computed.
+    """
+    pool = np.asarray(pool)
+    bt = np.asarray(block_table, dtype=np.int64)
+    page_rows = pool.shape[1]
+    j = np.arange(n)
+    pages = bt[:, j // page_rows]                  # [B, n] physical page of each row
+    return pool[pages, (j % page_rows)[None, :]]
+
+
 def project_kv(h, w):
     """The decoder's global KV of one layer: h [rows, hidden] (the final
     encoder hidden state) times that layer's projection w [d, hidden]

@@ -338,3 +338,41 @@ def test_pool_with_short_rows(orc):
     assert np.array_equal(plain[0], pooled[0])
     assert np.array_equal(plain[1][1:], pooled[1][1:])   # rows with nv <= pool
     assert list(pooled[1][2][20:]) == [-1] * 12
+
+
+# ---- paged caches (the serving layout) --------------------------------------
+
+def test_pages_identity_table_is_the_contiguous_layout(orc):
+    B, n, page_rows = 3, 40, 16
+    cache = synth.normal((B, 48, 32), 300).double().numpy()  # 3 pages of 16 rows per sequence
+    pool = cache.reshape(B * 3, page_rows, 32)
+    table = np.arange(B * 3).reshape(B, 3)
+    assert np.array_equal(orc.gather_pages(pool, table, n), cache[:, :n])
+
+
+def test_pages_permuted_pool_gives_the_same_view(orc):
+    # moving physical pages (and updating the table) changes no logical row
+    B, page_rows = 2, 8
+    cache = synth.normal((B, 32, 4), 301).double().numpy()
+    pool = cache.reshape(B * 4, page_rows, 4)
+    table = np.arange(B * 4).reshape(B, 4)
+    perm = np.random.default_rng(302).permutation(B * 4)   # new position of each page
+    moved = np.empty_like(pool)
+    moved[perm] = pool
+    assert np.array_equal(orc.gather_pages(moved, perm[table], 30),
+                          orc.gather_pages(pool, table, 30))
+
+
+def test_pages_feed_the_selection_unchanged(orc):
+    # the stack on a paged indexer-K cache, read through its logical view,
+    # selects what the contiguous cache selects
+    B, n, page_rows = 2, 200, 64
+    kb = synth.normal((B, 256, 128), 303).double().numpy()
+    k8 = orc.cast_e4m3(kb)
+    q = synth.normal((B, 4, 128), 304).double().numpy()
+    w = np.full((B, 4), 0.25)
+    pool = k8.reshape(B * 4, page_rows, 128)[::-1].copy()   # pages stored in reverse order
+    table = (B * 4 - 1 - np.arange(B * 4)).reshape(B, 4)
+    ref = orc.topk(orc.index_score_fp8(q, w, k8[:, :n]), 16)
+    got = orc.topk(orc.index_score_fp8(q, w, orc.gather_pages(pool, table, n)), 16)
+    assert np.array_equal(got, ref)
