@@ -261,7 +261,11 @@ csa2_status csa2_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
  * 256 rows); larger calls return CSA2_ERR_WORKSPACE and enqueue nothing.  The call allocates nothing (no cudaMalloc / cudaFree).
  * The first call on a device looks up the array's device address for that
  * device (with that device current), so make that first call before any
- * stream capture.  Every call shares the one array: calls that may overlap
+ * stream capture.  The address is looked up again whenever a call runs in
+ * another CUDA context than the lookup did (after cudaDeviceReset, or from a
+ * non-primary context), since the array may then sit elsewhere; make such a
+ * first call in a new context before any capture too.  CSA2_FAULT_INJECT
+ * reaches it as "topk_noalloc".  Every call shares the one array: calls that may overlap
  * on the GPU (different streams, or different host threads) race and give
  * wrong results; serialise them.  The parts of the array that must start at
  * zero are cleared by each call, so a call never sees a previous call's data.
@@ -299,7 +303,8 @@ csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int64_t n, int6
  * win_max  host upper bound on win_len (0: w_rows); sizes the launch
  * out      device f32 [nq, hq, d]
  * An index outside [-1, n) is skipped and raises CSA2_DEVFLAG_BOUNDS; a
- * window range outside [0, w_rows) is clipped the same way.
+ * window range outside [0, w_rows), or a win_len above the bound win_max,
+ * is clipped the same way (and raises the same flag).
  * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT (BF16 path: codes, scales
  *         and window rows 16-byte aligned), WORKSPACE, CUDA.
  */

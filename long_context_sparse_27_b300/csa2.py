@@ -267,11 +267,22 @@ def topk_workspace_bytes(rows, n, k):
     return lib.csa2_topk_workspace_bytes(rows, n, k)
 
 
+def _check_topk_tensors(where, scores, out, n_valid):
+    # the C ABI takes one row stride per tensor: rows must be contiguous
+    if scores.dtype != torch.float32 or scores.stride(1) != 1:
+        raise ValueError(f"{where}: scores must be float32 with contiguous rows")
+    if out.dtype != torch.int32 or out.stride(1) != 1:
+        raise ValueError(f"{where}: out must be int32 with contiguous rows")
+    if n_valid is not None and (n_valid.dtype != torch.int32 or not n_valid.is_contiguous()):
+        raise ValueError(f"{where}: n_valid must be a contiguous int32 tensor")
+
+
 def topk(scores, k, n_valid=None, out=None, workspace=None, dev_status=None):
     """scores f32 [rows, n] -> int32 [rows, k], ascending indices, -1 padded."""
     rows, n = scores.shape
     if out is None:
         out = torch.empty(rows, k, dtype=torch.int32, device=scores.device)
+    _check_topk_tensors("topk", scores, out, n_valid)
     need = lib.csa2_topk_workspace_bytes(rows, n, k)
     ws = workspace if workspace is not None else _workspace(need, scores.device)
     _check(lib.csa2_topk(_ptr(scores), rows, n, scores.stride(0), _ptr(n_valid), k, _ptr(out),
@@ -287,6 +298,7 @@ def topk_noalloc(scores, k, n_valid=None, out=None, dev_status=None):
     rows, n = scores.shape
     if out is None:
         out = torch.empty(rows, k, dtype=torch.int32, device=scores.device)
+    _check_topk_tensors("topk_noalloc", scores, out, n_valid)
     _check(lib.csa2_topk_noalloc(_ptr(scores), rows, n, scores.stride(0), _ptr(n_valid), k,
                                  _ptr(out), out.stride(0), _ptr(dev_status), _stream()),
            "csa2_topk_noalloc")

@@ -53,10 +53,6 @@ int sm_count() {
   return cached[dev];
 }
 
-namespace {
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 // CSA2_FAULT_INJECT="<call>:<status>" makes the named entry point return
 // <status> before it enqueues anything (host-side failure injection for
 // tests of the callers' error paths).  <call> is the entry point's name
@@ -71,6 +67,10 @@ csa2_status injected(const char* call) {
   const int v = std::atoi(colon + 1);
   return (v > 0 && v <= CSA2_ERR_DEVICE_BOUNDS) ? (csa2_status)v : CSA2_OK;
 }
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 csa2_status check_quant(const csa2_quant_args* a) {
   if (!a || a->rows < 0 || a->d <= 0 || a->d % 32 != 0) return CSA2_ERR_INVALID_ARG;

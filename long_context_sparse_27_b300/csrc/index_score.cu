@@ -516,7 +516,7 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   p.keep_in_l2 = tune.keep_in_l2 ? 1 : 0;
   const int64_t total = p.groups * p.ktiles;
   if (total == 0) return CSA2_OK;
-  static uint64_t attr_done = 0;
+  static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
     return cudaFuncSetAttribute(idx_score_tc_kernel<QG>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/csa2.h"
 
 namespace csa2 {
@@ -12,6 +14,9 @@ namespace csa2 {
 // Round up to a multiple of 256 bytes (every workspace region starts aligned).
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Host-side failure injection: the status CSA2_FAULT_INJECT names for the
+// entry point `call` (its name without "csa2_"), else CSA2_OK.
+csa2_status injected(const char* call);
 // Records a failed CUDA call for csa2_last_cuda_error() and maps it to a status.
 csa2_status cuda_fail(cudaError_t e);
 // cudaGetLastError() after a launch, mapped to a status.
@@ -87,17 +92,19 @@ int sm_count();
 
 // Kernel attributes (the dynamic shared-memory limit) are per device: runs
 // `set` once for each device the calling thread makes current (bit d of
-// `done` records device d; devices past 63 run it every time).  A repeat
-// from a race is harmless: the attributes are idempotent.
+// `done` records device d; devices past 63 run it every time).  Host threads
+// may call concurrently: the mask is atomic, and two threads that both see
+// the bit clear both run `set`, which is harmless (the attributes are
+// idempotent).
 template <class F>
-cudaError_t once_per_device(uint64_t& done, F&& set) {
+cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& set) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t)1 << dev : 0;
-  if (bit && (done & bit)) return cudaSuccess;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
   e = set();
-  if (e == cudaSuccess) done |= bit;
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
   return e;
 }
 

@@ -64,11 +64,18 @@ __device__ __forceinline__ KeySrc key_source(const csa2_attn_args& a, int64_t qi
   return r;
 }
 
+// The query's window rows [ws, ws + wl).  A length above the launch's bound
+// win_max is clipped to it and raises CSA2_DEVFLAG_BOUNDS, like a row outside
+// [0, w_rows) (the launch only has room for win_max window keys).
 __device__ __forceinline__ void window_of(const csa2_attn_args& a, int64_t qi, int32_t& ws,
                                           int32_t& wl) {
   ws = a.win_start ? a.win_start[qi] : 0;
   wl = a.win_len ? a.win_len[qi] : a.w_rows;
   if (wl < 0) wl = 0;
+  if (wl > a.win_max) {
+    raise_flag(a.dev_status, CSA2_DEVFLAG_BOUNDS);
+    wl = a.win_max;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -88,7 +95,6 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const csa2_attn_args a) {
   for (int i = threadIdx.x; i < d; i += blockDim.x) sq[i] = qsrc[i];
   int32_t ws, wl;
   window_of(a, qi, ws, wl);
-  if (wl > a.win_max) wl = a.win_max;
   const int64_t nkeys = a.k + wl;
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -234,7 +240,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
   int32_t ws, wl;
   window_of(a, qi, ws, wl);
-  if (wl > a.win_max) wl = a.win_max;
   const int64_t nkeys = a.k + wl;
 
   // ---- 1. key sources; Q copy
@@ -597,7 +602,7 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(a.out, 0, (size_t)a.nq * a.hq * kD * sizeof(float), s);
     return e == cudaSuccess ? CSA2_OK : cuda_fail(e);
   }
-  static uint64_t attr_done = 0;
+  static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
     cudaError_t r = cudaFuncSetAttribute(attn_bf16_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);

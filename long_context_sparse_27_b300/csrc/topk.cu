@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kTkThreads)
   for (int i = m + tid; i < k; i += kTkThreads) o[i] = -1;
 }
 
-uint64_t g_select_attr = 0;  // devices on which the selector's attributes are set
+std::atomic<uint64_t> g_select_attr{0};  // devices on which the selector's attributes are set
 
 }  // namespace
 
@@ -647,10 +647,45 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;  // 4 MiB per device
 static __device__ __align__(256) uint8_t g_topk_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of the array, looked up once per device (host code cannot
-// use the array's name as a device pointer).
+// Device address of the array.  Host code cannot use the array's name as a
+// device pointer, so the address is looked up with cudaGetSymbolAddress,
+// with the device current, and kept per device together with the unique ID
+// of the CUDA context it was looked up in.  A call made in another context
+// (after cudaDeviceReset, or from a context other than the primary one)
+// looks it up again: the library's module, and with it the array, may then
+// sit at another address.  Context IDs are never reused within a process.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64] = {nullptr};
+unsigned long long g_noalloc_ctx[64] = {0};
+
+// Unique ID of the calling thread's current context (0 if there is none or
+// the driver cannot say).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    looked = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 }  // namespace
 }  // namespace csa2
@@ -665,6 +700,8 @@ extern "C" csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int6
   if (rows == 0) return CSA2_OK;
   if (!idx_out || (n > 0 && !scores)) return CSA2_ERR_INVALID_ARG;
   if (topk_workspace_bytes(rows, n, k) > kNoAllocScratchBytes) return CSA2_ERR_WORKSPACE;
+  csa2_status st = injected("topk_noalloc");
+  if (st != CSA2_OK) return st;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -672,14 +709,17 @@ extern "C" csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int6
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    unsigned long long ctx = current_context_id();
+    if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
       e = cudaGetSymbolAddress(&scratch, g_topk_noalloc_scratch);
       if (e != cudaSuccess) return cuda_fail(e);
       g_noalloc_ptr[dev] = scratch;
+      // the lookup made the context current if there was none
+      g_noalloc_ctx[dev] = ctx != 0 ? ctx : current_context_id();
     }
     scratch = g_noalloc_ptr[dev];
   }
-  // launch_topk clears the histograms of every row it uses
+  // launch_topk clears the parts of the scratch that must start at zero
   return launch_topk(scores, rows, n, ld, n_valid, k, idx_out, idx_ld, scratch, dev_status,
                      reinterpret_cast<cudaStream_t>(stream));
 }

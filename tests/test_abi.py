@@ -144,6 +144,10 @@ def test_fault_injection_stops_before_launch(csa2, monkeypatch):
     assert L.csa2_topk(FAKE, 4, 1000, 1000, None, 64, FAKE, 64, FAKE, ws, None, None) == 6
     # a bad argument is reported before the injected failure
     assert L.csa2_topk(FAKE, 4, 1000, 1000, None, 0, FAKE, 64, FAKE, ws, None, None) == 1
+    # the entry point without allocation takes its own injection name
+    monkeypatch.setenv("CSA2_FAULT_INJECT", "topk_noalloc:4")
+    assert L.csa2_topk_noalloc(FAKE, 4, 1000, 1000, None, 64, FAKE, 64, None, None) == 4
+    assert L.csa2_topk_noalloc(FAKE, 4, 1000, 1000, None, 0, FAKE, 64, None, None) == 1
 
 
 @no_gpu
@@ -283,3 +287,12 @@ def test_bindings_reject_strided_rows(csa2):
     with pytest.raises(ValueError):
         csa2.index_score_pool(torch.zeros(2, 64, 128, dtype=torch.bfloat16),
                               torch.zeros(2, 64), torch.zeros(1, 10, 128, dtype=torch.uint8), pool)
+    # top-k: a column-strided score view, a strided output, n_valid not int32
+    s = torch.zeros(3, 40)
+    for fn in (csa2.topk, csa2.topk_noalloc):
+        with pytest.raises(ValueError):
+            fn(s[:, ::2], 4)
+        with pytest.raises(ValueError):
+            fn(s, 4, out=torch.zeros(3, 8, dtype=torch.int32)[:, ::2])
+        with pytest.raises(ValueError):
+            fn(s, 4, n_valid=torch.full((3,), 40, dtype=torch.int64))

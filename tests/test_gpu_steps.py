@@ -405,3 +405,23 @@ def test_attn_bounds_flag(csa2):
     torch.cuda.synchronize()
     assert int(st.item()) & csa2.DEVFLAG_BOUNDS
     assert torch.isfinite(out).all()
+
+
+def test_attn_window_longer_than_bound_flags(csa2):
+    # a win_len above the launch bound win_max is clipped to win_max and
+    # reported, like any other window range the launch cannot hold
+    T, W, n, k, d, hq = 3, 4, 200, 16, 512, 16
+    codes, scales = make_cache(csa2, 1, n, d, 130)
+    q = dev(synth.normal((T, hq, d), 131))
+    idx = dev(synth.random_indices(T, k, n, 132))
+    win = dev(synth.normal((1, T + W, d), 133))
+    ws = dev(torch.arange(T, dtype=torch.int32))
+    for wl, flagged in (([W, W, W], False), ([W, W + 1, W], True)):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = csa2.sparse_attn(q, codes, scales, idx, win, 0.04, q_per_seq=T, win_start=ws,
+                               win_len=dev(torch.tensor(wl, dtype=torch.int32)), win_max=W,
+                               dev_status=st)
+        torch.cuda.synchronize()
+        assert bool(int(st.item()) & csa2.DEVFLAG_BOUNDS) == flagged
+        assert csa2.lib.csa2_status_from_device(int(st.item())) == (7 if flagged else 0)
+        assert torch.isfinite(out).all()

@@ -1,14 +1,15 @@
-"""csa2_topk_noalloc against csa2_topk, through the C ABI.
+"""csa2_topk_noalloc through the C ABI, against the oracle and csa2_topk.
 
 csa2_topk_noalloc serves callers that cannot allocate device memory (code
 running inside an allocator callback, a plugin whose host owns every device
 allocation, a process that must keep its footprint fixed after start-up):
 its scratch is a fixed array inside the library.  It must select exactly what
-csa2_topk selects -- top-k indices are compared bit for bit, the tolerance
-the other top-k tests use -- on two calls in a row (the second call must not
-see the first call's leftovers in the shared array), and it must refuse a
-problem larger than its fixed scratch.  This file is collected last so that
-a run stopping at the first failure has already run every other test.
+the oracle's top-k selects on the same float32 scores, and what csa2_topk
+selects -- indices are compared bit for bit, the tolerance the other top-k
+tests use -- on two calls in a row (the second call must not see the first
+call's leftovers in the shared array), and it must refuse a problem larger
+than its fixed scratch.  This file is collected last so that a run stopping
+at the first failure has already run every other test.
 """
 import ctypes
 
@@ -33,7 +34,7 @@ def call_noalloc(csa2, scores, k, n_valid=None):
     return st, out
 
 
-def test_noalloc_matches_topk_twice():
+def test_noalloc_matches_topk_twice(orc):
     csa2 = need_gpu()
     # first call: the 1M-context decode shape (8 rows of 262144 scores)
     s1 = synth.scores_with_ties(8, 262144, seed=901).cuda()
@@ -41,6 +42,7 @@ def test_noalloc_matches_topk_twice():
     assert st == 0
     ref1 = csa2.topk(s1, 512)
     torch.cuda.synchronize()
+    assert np.array_equal(got1.cpu().numpy(), orc.topk(s1.cpu().double().numpy(), 512))
     assert torch.equal(got1, ref1)
     # second call: other scores, many ties and ragged visibility; the shared
     # scratch still holds the first call's histograms and candidates
@@ -50,6 +52,8 @@ def test_noalloc_matches_topk_twice():
     assert st == 0
     ref2 = csa2.topk(s2, 512, n_valid=nv)
     torch.cuda.synchronize()
+    assert np.array_equal(got2.cpu().numpy(),
+                          orc.topk(s2.cpu().double().numpy(), 512, nv.cpu().numpy()))
     assert torch.equal(got2, ref2)
     assert not np.array_equal(got1.cpu().numpy()[:1], got2.cpu().numpy()[:1])
 
