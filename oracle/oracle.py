@@ -298,7 +298,37 @@ def pool_restrict(scores, pool):
     return scores
 
 
-def layer_stack(plan, layers, k, scale, q_per_seq=1, n_valid=None, pool=0):
+def block_summaries(k8, G):
+    """Block-level representations of the indexer keys, the first level of
+    the Hierarchical Sparse Indexer [P5 Method; P5 Related Work: hierarchical
+    approaches score token-level entries and prune them on block-level
+    representations].  Reading (the pages give no rule): the entries of each
+    sequence form blocks of G consecutive entries; a block's key is the sum
+    of its entries' decoded E4M3 keys divided by G (entries past the end of
+    the sequence count as zero), cast back to E4M3 like any indexer key.
+    k8 uint8 [B, n, di] -> uint8 [B, ceil(n / G), di]."""
+    kv = e4m3_decode(np.asarray(k8, dtype=np.uint8))
+    B, n, di = kv.shape
+    nb = -(-n // G)
+    padded = np.zeros((B, nb * G, di), dtype=np.float64)
+    padded[:, :n] = kv
+    return cast_e4m3(padded.reshape(B, nb, G, di).sum(axis=2) / G)
+
+
+def block_pool(blocks, G, n):
+    """The candidate pool of the chosen blocks: blocks int [rows, Bk]
+    (ascending block indices, -1 padded) -> pool int32 [rows, Bk * G], the
+    entries of block i in slots i*G .. i*G + G - 1 (ascending), -1 for a
+    padded block or an entry past n."""
+    blocks = np.asarray(blocks, dtype=np.int64)
+    rows, bk = blocks.shape
+    ent = blocks[:, :, None] * G + np.arange(G)[None, None, :]
+    ok = (blocks[:, :, None] >= 0) & (ent < n)
+    return np.where(ok, ent, -1).reshape(rows, bk * G).astype(np.int32)
+
+
+def layer_stack(plan, layers, k, scale, q_per_seq=1, n_valid=None, pool=0, block=0,
+                blocks_kept=0):
     """Run a static CSA2 schedule.
 
     plan: list of (mode, kv_src, idx_src).
@@ -313,6 +343,14 @@ def layer_stack(plan, layers, k, scale, q_per_seq=1, n_valid=None, pool=0):
     the pool of the Full layer whose KV it reads.  Readings: the pool is the
     earlier indexer's top-P under the top-k order; a Full layer's own top-k
     is unchanged (it lies inside its pool).
+    block > 0 (with blocks_kept = Bk) runs the Hierarchical Sparse Indexer
+    with block-level pruning first: a Full layer scores the block summaries
+    of its indexer keys (block_summaries, blocks of `block` entries) with
+    the same indexer formula, keeps its top-Bk blocks (the top-k order on
+    block indices), and scores at token level only the entries of those
+    blocks (block_pool), taking its top-k inside them; the Reindex layers
+    that read its KV score the same pool.  Readings as for the pool, plus
+    block_summaries.
     Returns (idx per layer, out per layer).
     """
     idx_of, out_of, pool_of = [], [], {}
@@ -324,9 +362,13 @@ def layer_stack(plan, layers, k, scale, q_per_seq=1, n_valid=None, pool=0):
                 s = index_score_fp8(L["idx_q"], L["idx_w"], src["k8"], q_per_seq, n_valid)
             else:
                 s = index_score(L["idx_q"], L["idx_w"], src["k_f32"], q_per_seq, n_valid)
-            if pool > 0 and mode == FULL:
+            if block > 0 and mode == FULL:
+                summ = block_summaries(src["k8"], block)
+                sb = index_score_fp8(L["idx_q"], L["idx_w"], summ, q_per_seq)
+                pool_of[l] = block_pool(topk(sb, blocks_kept), block, src["k8"].shape[1])
+            elif pool > 0 and mode == FULL:
                 pool_of[l] = topk(s, pool, n_valid)
-            if pool > 0 and mode == REINDEX:
+            if (pool > 0 and mode == REINDEX) or block > 0:
                 s = pool_restrict(s, pool_of[kv_src])
             idx = topk(s, k, n_valid)
         else:

@@ -376,3 +376,82 @@ def test_pages_feed_the_selection_unchanged(orc):
     ref = orc.topk(orc.index_score_fp8(q, w, k8[:, :n]), 16)
     got = orc.topk(orc.index_score_fp8(q, w, orc.gather_pages(pool, table, n)), 16)
     assert np.array_equal(got, ref)
+
+
+# ---- Hierarchical Sparse Indexer: block-level pruning ------------------------
+
+def test_block_summaries_hand_worked(orc):
+    # blocks of 2 entries over 5 entries (the last block has one entry and a
+    # zero): block key = E4M3((sum of the decoded keys) / 2).  Input codes:
+    # 1 = 0x38, 3 = 0x44, 2 = 0x40, 0.5 = 0x30, 448 = 0x7E, -1 = 0xB8,
+    # 1.125 = 0x39, -2 = 0xC0, -3 = 0xC4, 6 = 0x4C (E4M3: bias 7, 3 mantissa
+    # bits).  Expected: (1+3)/2 = 2 -> 0x40; (1+2)/2 = 1.5 -> 0x3C; (0.5+0)/2
+    # = 0.25 -> 0x28; 448 -> 0x7E; (-1+1)/2 = 0 -> 0x00; 1/2 -> 0x30;
+    # (1+1.125)/2 = 1.0625, halfway between 1 (0x38) and 1.125 (0x39): ties
+    # to the even mantissa -> 0x38; (-2-3)/2 = -2.5 -> 0xC2; 6/2 = 3 -> 0x44.
+    cols = [[0x38, 0x44, 0x38, 0x40, 0x30],
+            [0x7E, 0x7E, 0xB8, 0x38, 0x38],
+            [0x38, 0x39, 0xC0, 0xC4, 0x4C],
+            [0x00, 0x00, 0x00, 0x00, 0x00]]
+    k8 = np.array(cols, dtype=np.uint8).T[None]           # [1, 5, 4]
+    got = orc.block_summaries(k8, 2)
+    want = np.array([[0x40, 0x7E, 0x38, 0x00],
+                     [0x3C, 0x00, 0xC2, 0x00],
+                     [0x28, 0x30, 0x44, 0x00]], dtype=np.uint8)[None]
+    assert np.array_equal(got, want)
+
+
+def test_block_pool_expands_ascending_blocks(orc):
+    pool = orc.block_pool(np.array([[0, 2, -1], [1, 3, 4]]), 4, 18)
+    assert pool[0].tolist() == [0, 1, 2, 3, 8, 9, 10, 11, -1, -1, -1, -1]
+    assert pool[1].tolist() == [4, 5, 6, 7, 12, 13, 14, 15, 16, 17, -1, -1]
+
+
+def test_blocks_keeping_every_block_is_the_plain_schedule(orc):
+    modes = [F, RI, RU, RI]
+    layers = small_stack_layers(orc, modes, 94, n=300)
+    plain = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125)
+    blocked = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125, block=16,
+                              blocks_kept=19)   # 19 blocks of 16 cover 300 entries
+    for a, b in zip(plain[0] + plain[1], blocked[0] + blocked[1]):
+        assert np.array_equal(a, b)
+
+
+def test_single_entry_blocks_keep_the_full_top_k(orc):
+    # blocks of one entry: a block's key is the entry's own key, so the top-k
+    # blocks are the top-k entries and the Full layer selects as in the plain
+    # schedule; the Reindex layer then chooses inside those k entries
+    modes = [F, RI]
+    layers = small_stack_layers(orc, modes, 95, n=200)
+    plain, _ = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125)
+    blocked, _ = orc.layer_stack(orc.default_plan(modes), layers, k=32, scale=0.125, block=1,
+                                 blocks_kept=32)
+    assert np.array_equal(plain[0], blocked[0])
+    assert all(set(blocked[1][q]) == set(plain[0][q]) for q in range(2))
+
+
+def test_block_selection_by_sorting(orc):
+    # brute force with loops: block keys as means of decoded keys (cast by
+    # the E4M3 rule), block scores, the 3 best blocks by (score desc, block
+    # asc), then the 16 best entries of those blocks by (score desc, index asc)
+    modes = [F]
+    layers = small_stack_layers(orc, modes, 96, B=2, n=100)
+    G, Bk, k = 8, 3, 16
+    idx, _ = orc.layer_stack(orc.default_plan(modes), layers, k=k, scale=0.125, block=G,
+                             blocks_kept=Bk)
+    L = layers[0]
+    dec = orc.e4m3_decode(L["k8"])
+    nb = -(-100 // G)
+    summ = np.zeros((2, nb, 128))
+    for b in range(2):
+        for blk in range(nb):
+            for j in range(blk * G, min(100, blk * G + G)):
+                summ[b, blk] += dec[b, j]
+    summ = orc.cast_e4m3(summ / G)
+    sb = orc.index_score_fp8(L["idx_q"], L["idx_w"], summ)
+    s = orc.index_score_fp8(L["idx_q"], L["idx_w"], L["k8"])
+    for q in range(2):
+        keep = sorted(range(nb), key=lambda t: (-sb[q, t], t))[:Bk]
+        ents = [j for t in keep for j in range(t * G, min(100, t * G + G))]
+        best = sorted(ents, key=lambda j: (-s[q, j], j))[:k]
+        assert list(idx[0][q]) == sorted(best)
