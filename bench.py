@@ -144,6 +144,10 @@ class ClockSampler:
 def workload_desc(wl):
     """The workload as both arms name it in `config`."""
     pool = f", candidate pool {wl.pool}" if wl.pool else ""
+    if wl.page_rows:
+        pool += f", paged caches ({wl.page_rows}-entry pages, shuffled block table)"
+    if wl.block:
+        pool += f", block-level pruning (blocks of {wl.block}, {wl.blocks_kept} kept)"
     q = "" if wl.q_per_seq == 1 else f", {wl.q_per_seq} queries per sequence"
     return (f"{wl.name}: B={wl.B}, N={wl.N}{q}, layers={len(wl.modes)} "
             f"{''.join('FIU'[m] for m in wl.modes)}, indexer {wl.Hi}x{wl.Di} "
@@ -155,27 +159,51 @@ def workload_desc(wl):
 
 def launches_per_step(wl):
     """Kernels of this library per step (memsets are not counted).  Full:
-    new-row quantiser, indexer-Q quantiser, indexer score, top-k selection
-    and attention; Reindex: the same without the new rows; Reuse: attention.
-    A prefill chunk adds a top-k histogram pass per index layer (decode builds
-    it inside the indexer kernel); attention over more than 8 key chunks of
-    80 adds a merge kernel.  With a candidate pool a Full layer selects the
-    pool and then the top-k inside it (one kernel more) and a Reindex layer
-    runs the Q quantiser, the pooled scores, their selection and attention."""
-    per = {0: 5, 1: 4, 2: 1}
+    new-row quantiser, indexer score, top-k selection and attention; Reindex:
+    the same without the new rows; Reuse: attention.  Decode indexer launches
+    quantise their queries inside the indexer kernel; a prefill chunk runs
+    the indexer-Q quantiser as its own kernel and a top-k histogram pass per
+    index layer (decode builds the histogram inside the indexer kernel).
+    Attention over more than 8 key chunks of 80 adds a merge kernel.  With a
+    candidate pool a Full layer selects the pool and then the top-k inside it
+    (one kernel more) and a Reindex layer runs the Q quantiser, the pooled
+    scores, their selection and attention."""
+    per = {0: 4, 1: 3, 2: 1}
     n = 0
     for m in wl.modes:
-        if m == 1 and wl.pool:
+        if wl.block and m == 0:
+            # new rows, their block keys, Q quantiser, block scores, block
+            # selection (expanded to the pool), pooled scores, selection, attention
+            n += 8
+        elif m == 1 and (wl.pool or wl.block):
             n += 4  # Q quantiser, pooled scores, their selection, attention
         else:
             n += per[m]
             if m == 0 and wl.pool:
                 n += 1  # the pool's selection, then the top-k inside it
             if m != 2 and wl.q_per_seq > 1:
-                n += 1
+                n += 2  # separate Q quantiser, histogram pass
+            elif m != 2 and wl.fp32_indexer and wl.N > 4096:
+                n += 1  # the fp32 indexer builds no histogram: a histogram pass
         if (wl.k + wl.W + 79) // 80 > 8:
             n += 1
     return n
+
+
+class L2Flush:
+    """Empties L2 between timed iterations: writes a buffer four times the L2,
+    then reads another of the same size, so that the lines left in L2 are
+    clean.  Without the read the next timed kernel would first write back
+    ~126 MB of the flush's own dirty lines (5-12 us measured on a 268 MB
+    read stream), work that is not the kernel's."""
+
+    def __init__(self, device="cuda"):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
 
 
 def time_index_kernel(csa2, W, flush, reps=20):
@@ -195,7 +223,7 @@ def time_index_kernel(csa2, W, flush, reps=20):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(reps)]
     for a, b in ev:
-        flush.zero_()
+        flush()
         a.record(stream)
         csa2.index_score(q8, c, L0["idxk"], W.wl.q_per_seq, W.n_valid, scores)
         b.record(stream)
@@ -210,7 +238,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     wl = synth.WORKLOADS[args.workload]
     W = StackWorkload(wl, seed=100 + rank, gen_device="cuda")
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     stream = torch.cuda.current_stream()
 
     # warm-up (also sets kernel attributes before any capture)
@@ -241,7 +269,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for a, b in ev:
-            flush.zero_()
+            flush()
             a.record(stream)
             step()
             b.record(stream)
@@ -299,7 +327,7 @@ def run_ours(args, world, rank, local):
         if st >= 2:
             stream.wait_event(out_read[i])  # step st - 2's outputs have left block i
         if flush_e2e:
-            flush.zero_()
+            flush()
         io_graphs[i]()
         computed[i].record(stream)
         with torch.cuda.stream(d2h_stream):
@@ -368,10 +396,12 @@ def run_ours(args, world, rank, local):
         "config": {
             "workload": workload_desc(wl),
             "l2": ("inputs larger than L2 (%.2f GB per step); L2 flushed before every "
-                   "device-timed step, not in the pipelined end-to-end loop" % (alg / 1e9))
+                   "device-timed step (512 MB written, then 512 MB read so the lines left are "
+                   "clean), not in the pipelined end-to-end loop" % (alg / 1e9))
                   if alg >= 2 * L2_BYTES else
-                  ("inputs smaller than L2 (%.2f GB per step); L2 flushed before every step, "
-                   "device-timed and end-to-end" % (alg / 1e9)),
+                  ("inputs smaller than L2 (%.2f GB per step); L2 flushed before every step "
+                   "(512 MB written, then 512 MB read), device-timed and end-to-end"
+                   % (alg / 1e9)),
             "graph": graph is not None,
             "parallelism": f"replicas x{world}",
         },
@@ -508,7 +538,7 @@ def run_project(args):
     a prefill chunk's 1024 entries, hidden 4096, d 512, each timed with CUDA
     events over `steps` launches after `warmup`, L2 flushed before each."""
     from long_context_sparse_27_b300 import csa2, synth
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
     hidden, d = 4096, 512
     w = (synth.normal((d, hidden), 300, "cuda") * 0.05).to(torch.bfloat16)
@@ -521,7 +551,7 @@ def run_project(args):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         for a, b in ev:
-            flush.zero_()
+            flush()
             a.record(stream)
             csa2.project_fp4(h, w)
             b.record(stream)

@@ -30,7 +30,13 @@
  *     earlier kernels of the same call may have been enqueued.
  *   - `dev_status` (optional, device int32) collects errors that only the
  *     GPU can see: kernels OR CSA2_DEVFLAG_* bits into it.  The caller
- *     zeroes it and reads it after synchronising.
+ *     zeroes it and reads it after synchronising.  Every wait of the
+ *     tensor-core indexer's pipeline gives up after a limit (2 s, or the
+ *     environment variable CSA2_WAIT_LIMIT_NS in nanoseconds, read at each
+ *     launch), raises CSA2_DEVFLAG_TIMEOUT and ends the kernel cleanly (no
+ *     copy or MMA left in flight; the context stays usable).  Test hook:
+ *     CSA2_TEST_STALL_LOADS=1 makes that kernel issue no key loads, so its
+ *     waits run out.
  *   - Strides ("_ld" = between rows, "_seq_stride" = between sequences) are
  *     in elements of the tensor's own type (bytes for 8-bit tensors).
  *   - Query q belongs to sequence b = q / q_per_seq.  In decode q_per_seq is
@@ -87,6 +93,38 @@ int32_t csa2_last_cuda_error(void);
 csa2_status csa2_status_from_device(int32_t dev_status_word);
 
 /* ------------------------------------------------------------------------ */
+/* Paged caches (the serving layout)                                         */
+/* ------------------------------------------------------------------------ */
+/*
+ * The pages name serving stacks that run the model (vLLM, SGLang) ["Unlocking
+ * Extreme Context Scaling with DeepSeek-V4.1-Flash", "Deployment and
+ * Infrastructure"] but no cache layout.  This library's paged layout: the
+ * rows of a cache (FP4 codes, scales, indexer K) live in one pool of
+ * fixed-size pages of page_rows consecutive entries of one sequence; entry
+ * j of sequence b is pool row
+ *   block_table[b * bt_ld + j / page_rows] * page_rows + j % page_rows
+ * (a row of the pool is addressed with the cache's own row stride, *_ld).
+ * Every step computes exactly what it computes on the contiguous layout;
+ * only where rows live changes.
+ *
+ * block_table  device int32; NULL = not paged (the call's own layout)
+ * bt_ld        block-table row stride (>= ceil(n / page_rows) pages)
+ * page_rows    entries per page: a multiple of 64, >= 64
+ * num_pages    pages in the pool (the pool holds num_pages * page_rows rows)
+ * A page id outside [0, num_pages) reached by a step raises
+ * CSA2_DEVFLAG_BOUNDS, and its rows read as empty (a gathered row is
+ * skipped; an indexer tile reads zeros); a new row aimed at such a page is
+ * not written (csa2_quantize_fp4 has no dev_status: there it is only not
+ * written; the layer stack reports it).
+ */
+typedef struct csa2_pages {
+  const int32_t* block_table;
+  int64_t bt_ld;
+  int32_t page_rows;
+  int32_t num_pages;
+} csa2_pages;
+
+/* ------------------------------------------------------------------------ */
 /* a1: FP4 quantiser                                                         */
 /* ------------------------------------------------------------------------ */
 /*
@@ -109,7 +147,9 @@ csa2_status csa2_status_from_device(int32_t dev_status_word);
  * A strided destination lets one call write one new row per sequence of a
  * [B, N, ...] cache: pass the address of row N-1 of sequence 0 and the
  * sequence stride as the row stride.
- * Errors: INVALID_ARG (NULL, rows < 0, d % 32 != 0, strides too small),
+ * Errors: INVALID_ARG (NULL, rows < 0, d % 32 != 0, strides too small;
+ *         paged: page_rows not a positive multiple of 64, num_pages < 1,
+ *         rows_per_seq < 1, entry0 < 0),
  *         ALIGNMENT (x, x_ld not multiples of 8 elements; codes, codes_ld
  *         not multiples of 4 bytes; idxk / idxk_e4m3 rows not 8 / 4 aligned).
  */
@@ -127,6 +167,12 @@ typedef struct csa2_quant_args {
   int64_t idxk_ld;
   uint8_t* idxk_e4m3;
   int64_t idxk_e4m3_ld;
+  /* Paged destination (pages.block_table != NULL): codes / scales /
+   * idxk_e4m3 are pools, and row r of x is entry entry0 + r % rows_per_seq
+   * of sequence r / rows_per_seq, written through the block table. */
+  csa2_pages pages;
+  int64_t rows_per_seq;
+  int64_t entry0;
 } csa2_quant_args;
 
 csa2_status csa2_quantize_fp4(const csa2_quant_args* args, csa2_stream_t stream);
@@ -195,6 +241,9 @@ typedef struct csa2_index_args {
   void* workspace;
   size_t workspace_bytes;
   int32_t* dev_status;
+  /* Paged keys (pages.block_table != NULL): k is a pool of rows k_ld
+   * apart; k_seq_stride is not used. */
+  csa2_pages pages;
 } csa2_index_args;
 
 size_t csa2_index_score_workspace_bytes(const csa2_index_args* args);
@@ -220,6 +269,33 @@ csa2_status csa2_index_score(const csa2_index_args* args, csa2_stream_t stream);
 csa2_status csa2_index_score_pool(const csa2_index_args* args, const int32_t* pool,
                                   int64_t pool_ld, int32_t pool_n, csa2_stream_t stream);
 
+/*
+ * Block keys, the first level of the Hierarchical Sparse Indexer [P5
+ * Method: indexers restricted to a candidate pool selected by an earlier
+ * indexer; P5 Related Work: scoring token-level entries and pruning them on
+ * block-level representations].  This library's definition: the entries of
+ * a sequence form blocks of G consecutive entries, and block blk's key is
+ *   out[blk, i] = E4M3( (sum over the block's entries j < n of E4M3^-1(k8[j, i])) / G )
+ * (entries past n count as zero; E4M3 cast as everywhere: nearest, ties to
+ * even, saturating).  The sum is exact, so the cast is the only rounding.
+ * Computes blocks blk0 .. blk0 + nblk - 1 of every sequence b < B.
+ *
+ * k8     device E4M3 [B, n, 128]: row j of sequence b at k8 + b*k_seq_stride
+ *        + j*k_ld; or (pages non-NULL with a block table) a page pool of rows
+ *        k_ld apart.
+ * out    device u8: block blk of sequence b at out + b*out_seq_stride + blk*out_ld
+ * G      a power of two, 1 <= G <= 65536
+ * Errors: INVALID_ARG (NULL, negative sizes, G not a power of two, blocks
+ *         past ceil(n / G), strides below 128, a bad paged layout), CUDA.
+ * Device: CSA2_DEVFLAG_BOUNDS for a page outside the pool (its rows count
+ *         as zero).
+ */
+csa2_status csa2_index_block_keys(const uint8_t* k8, int64_t B, int64_t n, int64_t k_ld,
+                                  int64_t k_seq_stride, const csa2_pages* pages, int32_t G,
+                                  int64_t blk0, int64_t nblk, uint8_t* out, int64_t out_ld,
+                                  int64_t out_seq_stride, int32_t* dev_status,
+                                  csa2_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* a4: top-k                                                                 */
 /* ------------------------------------------------------------------------ */
@@ -232,12 +308,17 @@ csa2_status csa2_index_score_pool(const csa2_index_args* args, const int32_t* po
  *
  * scores  device f32, row r at scores + r * ld;  n_valid optional [rows]
  * idx_out device int32, row r at idx_out + r * idx_ld
- * 1 <= k <= 2048.  Workspace: csa2_topk_workspace_bytes(rows, n, k) =
- * rows * 16 KiB (one 4096-bin histogram per row, cleared by the call).
+ * 1 <= k <= 2048.  Workspace: csa2_topk_workspace_bytes(rows, n, k): one
+ * 4096-bin histogram per row (rows * 16 KiB) and, for rows longer than 4096,
+ * a counter per row and S candidate slots of 8 KiB per row (S = about 296 /
+ * rows, at most 64, at most one per 8192 entries); the call clears what must
+ * start at zero.
  * Kernels: rows of at most 4096 entries run one CTA per row with every key
  * in shared memory; longer rows a histogram pass over the scores, then one
- * selection kernel with a cluster of 8 CTAs per row (each owning 1/8 of the
- * row).
+ * selection kernel with S CTAs per row: each scans its slice once and keeps
+ * the entries of the histogram's threshold bin and above, and the row's
+ * last CTA to finish resolves the threshold among the kept entries (or, when
+ * a slice kept more than its slot holds, over the whole row again).
  * Errors: INVALID_ARG, UNSUPPORTED (k > 2048), WORKSPACE, CUDA.
  */
 size_t csa2_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k);
@@ -257,8 +338,9 @@ csa2_status csa2_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
  * The caller still passes the scores and idx_out buffers; the selector's
  * scratch comes from one fixed 4 MiB array compiled into the library, which
  * every GPU that loads the library keeps until the process exits.  Limit:
- * rows * csa2_topk_workspace_bytes(1, n, k) must not exceed 4 MiB (that is
- * 256 rows); larger calls return CSA2_ERR_WORKSPACE and enqueue nothing.  The call allocates nothing (no cudaMalloc / cudaFree).
+ * csa2_topk_workspace_bytes(rows, n, k) must not exceed 4 MiB (256 rows of
+ * at most 4096 entries; 8 rows of 262144); larger calls return
+ * CSA2_ERR_WORKSPACE and enqueue nothing.  The call allocates nothing (no cudaMalloc / cudaFree).
  * The first call on a device looks up the array's device address for that
  * device (with that device current), so make that first call before any
  * stream capture.  The address is looked up again whenever a call runs in
@@ -289,11 +371,14 @@ csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int64_t n, int6
  * dequant(row)[i] = E2M1(code_i) * 2^(scale_byte(i/32) - 127).
  *
  * Paths: q F32 (hq <= 64, d <= 256; CUDA cores) or q BF16 (hq % 16 == 0,
- * d == 512; bf16 tensor-core MMA, fp32 accumulation, probabilities split
- * into two bf16 terms).  The BF16 path cuts the k + win_max keys of a query
- * into chunks of 80; with at most 8 chunks (k + win_max <= 640) the chunks
- * of a query are merged on chip and the call needs no workspace, otherwise
- * it needs csa2_sparse_attn_workspace_bytes of it.
+ * d == 512; tcgen05 bf16 tensor-core MMA, fp32 accumulation in tensor
+ * memory, probabilities split into two bf16 terms).  The BF16 path cuts the
+ * k + win_max keys of a query into chunks of 80; each chunk writes its
+ * partial result (max, sum, unnormalised output per head) to the workspace,
+ * csa2_sparse_attn_workspace_bytes of it (nq * hq/16 * chunks * 32.9 KB).
+ * With at most 8 chunks (k + win_max <= 640) the chunks of a query form a
+ * thread-block cluster that merges the partials itself; with more, a second
+ * kernel merges them.
  * q        device [nq, hq, d] contiguous
  * codes    device u8: row j of sequence b at codes + b*codes_seq_stride + j*codes_ld
  * scales   device u8: likewise with scales_seq_stride / scales_ld
@@ -337,6 +422,9 @@ typedef struct csa2_attn_args {
   void* workspace;
   size_t workspace_bytes;
   int32_t* dev_status;
+  /* Paged main KV (pages.block_table != NULL): codes / scales are pools of
+   * rows codes_ld / scales_ld apart; the *_seq_stride fields are not used. */
+  csa2_pages pages;
 } csa2_attn_args;
 
 size_t csa2_sparse_attn_workspace_bytes(const csa2_attn_args* args);
@@ -444,6 +532,10 @@ typedef struct csa2_layer_desc {
   void* idxk;
   int32_t* topk_idx;
   float* out;
+  /* Full layers with block-level pruning (args->block > 0): the block keys
+   * of the layer's indexer K, [B, ceil(n / block), 128] E4M3 contiguous,
+   * kept current by the stack for the blocks its new rows touch. */
+  uint8_t* block_keys;
 } csa2_layer_desc;
 
 typedef struct csa2_stack_args {
@@ -468,6 +560,18 @@ typedef struct csa2_stack_args {
   int32_t* dev_status;
   int32_t pool;  /* candidate pool size P of the Hierarchical Sparse Indexer; 0 = off */
   int32_t win_max; /* host upper bound on win_len (0: w_rows); sizes the attention launch */
+  /* Paged caches: every Full layer's codes, scales and idxk are pools
+   * ([num_pages * page_rows] rows of d/2, d/32 and di) shared through this
+   * one block table; new rows are written through it. */
+  csa2_pages pages;
+  /* Block-level pruning of the Hierarchical Sparse Indexer (0 = off): blocks
+   * of `block` entries (a power of two); a Full layer scores the block keys,
+   * keeps its best blocks_kept blocks and scores at token level only their
+   * entries (the candidate pool, blocks_kept * block <= 2048 slots), taking
+   * its top-k there; Reindex layers score the same pool.  Decode shapes only
+   * (q_per_seq == 1, n_valid NULL), ceil(n / block) <= 4096, no `pool`. */
+  int32_t block;
+  int32_t blocks_kept;
 } csa2_stack_args;
 
 /* Checks a schedule (see above) without touching the GPU.  Returns CSA2_OK

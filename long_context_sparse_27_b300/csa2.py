@@ -23,11 +23,28 @@ _c_i32, _c_i64, _c_p, _c_f, _c_sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_vo
                                      ctypes.c_float, ctypes.c_size_t)
 
 
+class Pages(ctypes.Structure):
+    """csa2_pages: a paged cache's block table (block_table None = not paged)."""
+    _fields_ = [("block_table", _c_p), ("bt_ld", _c_i64), ("page_rows", _c_i32),
+                ("num_pages", _c_i32)]
+
+
+def pages(block_table=None, page_rows=0, num_pages=0):
+    """csa2_pages of a block table int32 [B, pages per sequence] (or none)."""
+    if block_table is None:
+        return Pages()
+    if block_table.dtype != torch.int32 or block_table.stride(1) != 1:
+        raise ValueError("pages: the block table must be int32 with contiguous rows")
+    return Pages(block_table=block_table.data_ptr(), bt_ld=block_table.stride(0),
+                 page_rows=page_rows, num_pages=num_pages)
+
+
 class QuantArgs(ctypes.Structure):
     _fields_ = [("x", _c_p), ("rows", _c_i64), ("d", _c_i32), ("x_ld", _c_i64),
                 ("codes", _c_p), ("codes_ld", _c_i64), ("scales", _c_p), ("scales_ld", _c_i64),
                 ("idxk", _c_p), ("di", _c_i32), ("idxk_ld", _c_i64), ("idxk_e4m3", _c_p),
-                ("idxk_e4m3_ld", _c_i64)]
+                ("idxk_e4m3_ld", _c_i64), ("pages", Pages), ("rows_per_seq", _c_i64),
+                ("entry0", _c_i64)]
 
 
 class IndexArgs(ctypes.Structure):
@@ -35,7 +52,7 @@ class IndexArgs(ctypes.Structure):
                 ("B", _c_i64), ("q_per_seq", _c_i64), ("hi", _c_i32), ("di", _c_i32),
                 ("n", _c_i64), ("k_ld", _c_i64), ("k_seq_stride", _c_i64), ("n_valid", _c_p),
                 ("scores", _c_p), ("scores_ld", _c_i64), ("workspace", _c_p),
-                ("workspace_bytes", _c_sz), ("dev_status", _c_p)]
+                ("workspace_bytes", _c_sz), ("dev_status", _c_p), ("pages", Pages)]
 
 
 class AttnArgs(ctypes.Structure):
@@ -46,7 +63,7 @@ class AttnArgs(ctypes.Structure):
                 ("window", _c_p), ("w_rows", _c_i32), ("win_ld", _c_i64),
                 ("win_seq_stride", _c_i64), ("win_start", _c_p), ("win_len", _c_p),
                 ("win_max", _c_i32), ("softmax_scale", _c_f), ("out", _c_p), ("workspace", _c_p),
-                ("workspace_bytes", _c_sz), ("dev_status", _c_p)]
+                ("workspace_bytes", _c_sz), ("dev_status", _c_p), ("pages", Pages)]
 
 
 class LayerDesc(ctypes.Structure):
@@ -54,7 +71,7 @@ class LayerDesc(ctypes.Structure):
                 ("new_idxk", _c_p), ("new_row", _c_i64), ("new_rows", _c_i64), ("idx_q", _c_p),
                 ("idx_w", _c_p),
                 ("attn_q", _c_p), ("window", _c_p), ("codes", _c_p), ("scales", _c_p),
-                ("idxk", _c_p), ("topk_idx", _c_p), ("out", _c_p)]
+                ("idxk", _c_p), ("topk_idx", _c_p), ("out", _c_p), ("block_keys", _c_p)]
 
 
 class ProjectArgs(ctypes.Structure):
@@ -69,7 +86,8 @@ class StackArgs(ctypes.Structure):
                 ("idx_q_dtype", _c_i32), ("idx_k_dtype", _c_i32), ("attn_q_dtype", _c_i32),
                 ("n_valid", _c_p), ("win_start", _c_p), ("win_len", _c_p),
                 ("softmax_scale", _c_f), ("workspace", _c_p), ("workspace_bytes", _c_sz),
-                ("dev_status", _c_p), ("pool", _c_i32), ("win_max", _c_i32)]
+                ("dev_status", _c_p), ("pool", _c_i32), ("win_max", _c_i32),
+                ("pages", Pages), ("block", _c_i32), ("blocks_kept", _c_i32)]
 
 
 EXPORTS = {
@@ -83,6 +101,9 @@ EXPORTS = {
     "csa2_index_score": (_c_i32, [ctypes.POINTER(IndexArgs), _c_p]),
     "csa2_index_score_pool": (_c_i32, [ctypes.POINTER(IndexArgs), _c_p, _c_i64, _c_i32, _c_p]),
     "csa2_project_fp4": (_c_i32, [ctypes.POINTER(ProjectArgs), _c_p]),
+    "csa2_index_block_keys": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_i64,
+                                       ctypes.POINTER(Pages), _c_i32, _c_i64, _c_i64, _c_p,
+                                       _c_i64, _c_i64, _c_p, _c_p]),
     "csa2_topk_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i32]),
     "csa2_topk": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_p, _c_sz,
                            _c_p, _c_p]),
@@ -160,10 +181,13 @@ def _aligned_ptr(ws):
 
 # ---- a1 / a2 ----------------------------------------------------------------
 
-def quantize_fp4(x, codes=None, scales=None, idxk=None, idxk_e4m3=None):
+def quantize_fp4(x, codes=None, scales=None, idxk=None, idxk_e4m3=None, pages=None,
+                 rows_per_seq=1, entry0=0):
     """x bf16 [rows, d] -> codes u8 [rows, d/2], scales u8 [rows, d/32];
     optional idxk bf16 [rows, di] -> idxk_e4m3 u8 [rows, di].  Row strides
-    of the given tensors are honoured (views into a cache work)."""
+    of the given tensors are honoured (views into a cache work).  pages (a
+    Pages): codes / scales / idxk_e4m3 are page pools and row r goes to
+    entry entry0 + r % rows_per_seq of sequence r // rows_per_seq."""
     rows, d = x.shape
     dev = x.device
     if codes is None:
@@ -172,6 +196,8 @@ def quantize_fp4(x, codes=None, scales=None, idxk=None, idxk_e4m3=None):
         scales = torch.empty(rows, d // 32, dtype=torch.uint8, device=dev)
     a = QuantArgs(x=_ptr(x), rows=rows, d=d, x_ld=x.stride(0), codes=_ptr(codes),
                   codes_ld=codes.stride(0), scales=_ptr(scales), scales_ld=scales.stride(0))
+    if pages is not None:
+        a.pages, a.rows_per_seq, a.entry0 = pages, rows_per_seq, entry0
     if idxk is not None:
         if idxk_e4m3 is None:
             idxk_e4m3 = torch.empty(rows, idxk.shape[1], dtype=torch.uint8, device=dev)
@@ -194,25 +220,36 @@ def quantize_index_q(q, w, q8=None, c=None):
 
 # ---- a3 ----------------------------------------------------------------------
 
-def index_args(q, w, k, q_per_seq=1, n_valid=None, scores=None, dev_status=None):
-    """q: f32, bf16, or uint8 / float8_e4m3fn (already quantised; w = c)."""
+def index_args(q, w, k, q_per_seq=1, n_valid=None, scores=None, dev_status=None, pages=None,
+               n=None):
+    """q: f32, bf16, or uint8 / float8_e4m3fn (already quantised; w = c).
+    k [B, n, di]; or, with pages, the pool [rows, di] and n given."""
     nq, hi, di = q.shape
-    B, n = k.shape[0], k.shape[1]
-    return IndexArgs(q=_ptr(q), q_dtype=_dtype_code(q), w=_ptr(w), k=_ptr(k),
-                     k_dtype=_dtype_code(k), B=B, q_per_seq=q_per_seq, hi=hi, di=di, n=n,
-                     k_ld=k.stride(1), k_seq_stride=k.stride(0), n_valid=_ptr(n_valid),
-                     scores=_ptr(scores), scores_ld=(scores.stride(0) if scores is not None else n),
-                     dev_status=_ptr(dev_status))
+    if pages is None:
+        B, n = k.shape[0], k.shape[1]
+        k_ld, k_seq = k.stride(1), k.stride(0)
+    else:
+        B, k_ld, k_seq = nq // q_per_seq, k.stride(0), 0
+    a = IndexArgs(q=_ptr(q), q_dtype=_dtype_code(q), w=_ptr(w), k=_ptr(k),
+                  k_dtype=_dtype_code(k), B=B, q_per_seq=q_per_seq, hi=hi, di=di, n=n,
+                  k_ld=k_ld, k_seq_stride=k_seq, n_valid=_ptr(n_valid),
+                  scores=_ptr(scores), scores_ld=(scores.stride(0) if scores is not None else n),
+                  dev_status=_ptr(dev_status))
+    if pages is not None:
+        a.pages = pages
+    return a
 
 
-def index_score(q, w, k, q_per_seq=1, n_valid=None, scores=None, dev_status=None):
+def index_score(q, w, k, q_per_seq=1, n_valid=None, scores=None, dev_status=None, pages=None,
+                n=None):
     """q [nq, hi, di] (f32 with f32 k, or bf16 with E4M3 k as uint8),
-    w f32 [nq, hi], k [B, n, di] -> scores f32 [nq, n]."""
+    w f32 [nq, hi], k [B, n, di] -> scores f32 [nq, n].  pages: k is a page
+    pool [rows, di] and n the entries per sequence."""
     nq = q.shape[0]
-    n = k.shape[1]
+    n = k.shape[1] if pages is None else n
     if scores is None:
         scores = torch.empty(nq, n, dtype=torch.float32, device=q.device)
-    a = index_args(q, w, k, q_per_seq, n_valid, scores, dev_status)
+    a = index_args(q, w, k, q_per_seq, n_valid, scores, dev_status, pages, n)
     need = lib.csa2_index_score_workspace_bytes(ctypes.byref(a))
     ws = _workspace(need, q.device) if need else None
     if ws is not None:
@@ -221,7 +258,8 @@ def index_score(q, w, k, q_per_seq=1, n_valid=None, scores=None, dev_status=None
     return scores
 
 
-def index_score_pool(q, w, k, pool, q_per_seq=1, scores=None, dev_status=None):
+def index_score_pool(q, w, k, pool, q_per_seq=1, scores=None, dev_status=None, pages=None,
+                     n=None):
     """The Hierarchical Sparse Indexer's restricted scoring: q bf16 [nq, 64,
     128] (or its E4M3 quantisation with w = c), w f32 [nq, 64], k E4M3 [B, n,
     128] as uint8, pool int32 [nq, P] (entry indices, -1 = empty slot) ->
@@ -231,7 +269,7 @@ def index_score_pool(q, w, k, pool, q_per_seq=1, scores=None, dev_status=None):
         raise ValueError("index_score_pool: rows of pool must be contiguous")
     if scores is None:
         scores = torch.empty(nq, P, dtype=torch.float32, device=q.device)
-    a = index_args(q, w, k, q_per_seq, None, scores, dev_status)
+    a = index_args(q, w, k, q_per_seq, None, scores, dev_status, pages, n)
     need = lib.csa2_index_score_workspace_bytes(ctypes.byref(a))
     ws = _workspace(need, q.device) if need else None
     if ws is not None:
@@ -259,6 +297,27 @@ def project_fp4(h, w, with_out=False):
                     out_ld=(out.stride(0) if out is not None else 0))
     _check(lib.csa2_project_fp4(ctypes.byref(a), _stream()), "csa2_project_fp4")
     return codes, scales, out
+
+
+def index_block_keys(k8, G, n=None, pages=None, B=None, blk0=0, nblk=None, out=None,
+                     dev_status=None):
+    """Block keys of the Hierarchical Sparse Indexer: k8 E4M3 [B, n, 128] as
+    uint8 (or, with pages, the pool [rows, 128] and B, n given) -> uint8
+    [B, ceil(n / G), 128]; blocks blk0 .. blk0 + nblk - 1 are computed."""
+    if pages is None:
+        B, n = k8.shape[0], k8.shape[1]
+        k_ld, k_seq = k8.stride(1), k8.stride(0)
+    else:
+        k_ld, k_seq = k8.stride(0), 0
+    nb = -(-n // G)
+    if out is None:
+        out = torch.zeros(B, nb, 128, dtype=torch.uint8, device=k8.device)
+    nblk = nb - blk0 if nblk is None else nblk
+    _check(lib.csa2_index_block_keys(_ptr(k8), B, n, k_ld, k_seq,
+                                     ctypes.byref(pages if pages is not None else Pages()), G,
+                                     blk0, nblk, _ptr(out), out.stride(1), out.stride(0),
+                                     _ptr(dev_status), _stream()), "csa2_index_block_keys")
+    return out
 
 
 # ---- a4 ----------------------------------------------------------------------
@@ -308,28 +367,38 @@ def topk_noalloc(scores, k, n_valid=None, out=None, dev_status=None):
 # ---- a5 ----------------------------------------------------------------------
 
 def attn_args(q, codes, scales, idx, window, softmax_scale, q_per_seq=1, win_start=None,
-              win_len=None, win_max=0, out=None, dev_status=None):
+              win_len=None, win_max=0, out=None, dev_status=None, pages=None, n=None):
     nq, hq, d = q.shape
-    return AttnArgs(q=_ptr(q), q_dtype=_dtype_code(q), nq=nq, q_per_seq=q_per_seq, hq=hq, d=d,
-                    codes=_ptr(codes), scales=_ptr(scales), n=codes.shape[1],
-                    codes_ld=codes.stride(1), codes_seq_stride=codes.stride(0),
-                    scales_ld=scales.stride(1), scales_seq_stride=scales.stride(0),
-                    idx=_ptr(idx), k=idx.shape[1], idx_ld=idx.stride(0), window=_ptr(window),
-                    w_rows=window.shape[1], win_ld=window.stride(1),
-                    win_seq_stride=window.stride(0), win_start=_ptr(win_start),
-                    win_len=_ptr(win_len), win_max=win_max, softmax_scale=softmax_scale,
-                    out=_ptr(out), dev_status=_ptr(dev_status))
+    if pages is None:
+        n = codes.shape[1]
+        c_ld, c_seq, s_ld, s_seq = codes.stride(1), codes.stride(0), scales.stride(1), \
+            scales.stride(0)
+    else:
+        c_ld, c_seq, s_ld, s_seq = codes.stride(0), 0, scales.stride(0), 0
+    a = AttnArgs(q=_ptr(q), q_dtype=_dtype_code(q), nq=nq, q_per_seq=q_per_seq, hq=hq, d=d,
+                 codes=_ptr(codes), scales=_ptr(scales), n=n,
+                 codes_ld=c_ld, codes_seq_stride=c_seq, scales_ld=s_ld, scales_seq_stride=s_seq,
+                 idx=_ptr(idx), k=idx.shape[1], idx_ld=idx.stride(0), window=_ptr(window),
+                 w_rows=window.shape[1], win_ld=window.stride(1),
+                 win_seq_stride=window.stride(0), win_start=_ptr(win_start),
+                 win_len=_ptr(win_len), win_max=win_max, softmax_scale=softmax_scale,
+                 out=_ptr(out), dev_status=_ptr(dev_status))
+    if pages is not None:
+        a.pages = pages
+    return a
 
 
 def sparse_attn(q, codes, scales, idx, window, softmax_scale, q_per_seq=1, win_start=None,
-                win_len=None, win_max=0, out=None, dev_status=None):
+                win_len=None, win_max=0, out=None, dev_status=None, pages=None, n=None):
     """q [nq, hq, d] f32 or bf16; codes u8 [B, n, d/2]; scales u8 [B, n, d/32];
-    idx int32 [nq, k]; window bf16 [B, w_rows, d] -> out f32 [nq, hq, d]."""
+    idx int32 [nq, k]; window bf16 [B, w_rows, d] -> out f32 [nq, hq, d].
+    pages: codes / scales are page pools [rows, d/2] / [rows, d/32] and n
+    the entries per sequence."""
     nq, hq, d = q.shape
     if out is None:
         out = torch.empty(nq, hq, d, dtype=torch.float32, device=q.device)
     a = attn_args(q, codes, scales, idx, window, softmax_scale, q_per_seq, win_start, win_len,
-                  win_max, out, dev_status)
+                  win_max, out, dev_status, pages, n)
     need = lib.csa2_sparse_attn_workspace_bytes(ctypes.byref(a))
     ws = _workspace(need, q.device) if need else None
     if ws is not None:
@@ -341,7 +410,7 @@ def sparse_attn(q, codes, scales, idx, window, softmax_scale, q_per_seq=1, win_s
 # ---- a6 ----------------------------------------------------------------------
 
 _DESC_KEYS = ("new_kv", "new_idxk", "idx_q", "idx_w", "attn_q", "window", "codes", "scales",
-              "idxk", "topk_idx", "out")
+              "idxk", "topk_idx", "out", "block_keys")
 
 
 def layer_descs(layers):
@@ -367,13 +436,16 @@ def validate_plan(layers):
 
 def stack_args(B, q_per_seq, n, hi, di, hq, d, k, w_rows, idx_q_dtype, idx_k_dtype,
                attn_q_dtype, softmax_scale, n_valid=None, win_start=None, win_len=None,
-               dev_status=None, pool=0, win_max=0):
-    return StackArgs(B=B, q_per_seq=q_per_seq, n=n, hi=hi, di=di, hq=hq, d=d, k=k,
-                     w_rows=w_rows, idx_q_dtype=idx_q_dtype, idx_k_dtype=idx_k_dtype,
-                     attn_q_dtype=attn_q_dtype, n_valid=_ptr(n_valid),
-                     win_start=_ptr(win_start), win_len=_ptr(win_len),
-                     softmax_scale=softmax_scale, dev_status=_ptr(dev_status), pool=pool,
-                     win_max=win_max)
+               dev_status=None, pool=0, win_max=0, pages=None, block=0, blocks_kept=0):
+    a = StackArgs(B=B, q_per_seq=q_per_seq, n=n, hi=hi, di=di, hq=hq, d=d, k=k,
+                  w_rows=w_rows, idx_q_dtype=idx_q_dtype, idx_k_dtype=idx_k_dtype,
+                  attn_q_dtype=attn_q_dtype, n_valid=_ptr(n_valid),
+                  win_start=_ptr(win_start), win_len=_ptr(win_len),
+                  softmax_scale=softmax_scale, dev_status=_ptr(dev_status), pool=pool,
+                  win_max=win_max, block=block, blocks_kept=blocks_kept)
+    if pages is not None:
+        a.pages = pages
+    return a
 
 
 def layer_stack_workspace_bytes(sargs):

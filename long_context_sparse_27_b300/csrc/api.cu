@@ -72,6 +72,16 @@ namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// A paged layout for rows of n entries: pages of a positive multiple of 64
+// entries, a pool of at least one page addressable with 32-bit row numbers,
+// and block-table rows that cover n entries.
+bool pages_ok(const csa2_pages& pg, int64_t n) {
+  if (!pg.block_table) return true;
+  if (pg.page_rows < 64 || pg.page_rows % 64 != 0 || pg.num_pages < 1) return false;
+  if ((int64_t)pg.num_pages * pg.page_rows > ((int64_t)1 << 31) - 1) return false;
+  return pg.bt_ld >= (n + pg.page_rows - 1) / pg.page_rows;
+}
+
 csa2_status check_quant(const csa2_quant_args* a) {
   if (!a || a->rows < 0 || a->d <= 0 || a->d % 32 != 0) return CSA2_ERR_INVALID_ARG;
   if (a->rows == 0) return CSA2_OK;
@@ -81,6 +91,11 @@ csa2_status check_quant(const csa2_quant_args* a) {
   if (!aligned(a->x, 16) || a->x_ld % 8 != 0 || !aligned(a->codes, 4) || a->codes_ld % 4 != 0)
     return CSA2_ERR_ALIGNMENT;
   if ((a->idxk == nullptr) != (a->idxk_e4m3 == nullptr)) return CSA2_ERR_INVALID_ARG;
+  if (a->pages.block_table &&
+      (!pages_ok(a->pages, 0) || a->rows_per_seq < 1 || a->entry0 < 0 ||
+       a->pages.bt_ld < (a->entry0 + a->rows_per_seq + a->pages.page_rows - 1) /
+                            a->pages.page_rows))
+    return CSA2_ERR_INVALID_ARG;
   if (a->idxk) {
     if (a->di <= 0 || a->di % 8 != 0 || a->idxk_ld < a->di || a->idxk_e4m3_ld < a->di)
       return CSA2_ERR_INVALID_ARG;
@@ -118,7 +133,9 @@ csa2_status check_index(const csa2_index_args* a) {
   if (nq == 0 || a->n == 0) return CSA2_OK;
   if (!a->q || !a->w || !a->k || !a->scores) return CSA2_ERR_INVALID_ARG;
   if (a->k_ld < a->di || a->k_seq_stride < 0 || a->scores_ld < a->n) return CSA2_ERR_INVALID_ARG;
-  if (a->B > 1 && a->k_seq_stride < a->k_ld * a->n) return CSA2_ERR_INVALID_ARG;
+  if (!pages_ok(a->pages, a->n)) return CSA2_ERR_INVALID_ARG;
+  const bool paged = a->pages.block_table != nullptr;
+  if (!paged && a->B > 1 && a->k_seq_stride < a->k_ld * a->n) return CSA2_ERR_INVALID_ARG;
   if (fp8_path(a)) {
     if (a->hi != 64 || a->di != 128) return CSA2_ERR_UNSUPPORTED;
     if (!aligned(a->k, 16) || a->k_ld % 16 != 0 || a->k_seq_stride % 16 != 0)
@@ -145,6 +162,9 @@ csa2_status run_index(const csa2_index_args& a, uint32_t* hist1, IndexTuning tun
   if (!fp8_path(&a)) return launch_index_score_f32(a, s);
   if (a.q_dtype == CSA2_E4M3)
     return launch_index_score_fp8(a, static_cast<const uint8_t*>(a.q), a.w, hist1, tune, s);
+  // decode: the indexer kernel quantises its queries itself (one launch)
+  const csa2_status fused = launch_index_score_bf16q(a, hist1, tune, s);
+  if (fused != CSA2_ERR_UNSUPPORTED) return fused;
   const int64_t nq = a.B * a.q_per_seq;
   uint8_t* q8 = static_cast<uint8_t*>(a.workspace);
   float* c = reinterpret_cast<float*>(q8 + align256((size_t)nq * a.hi * a.di));
@@ -175,6 +195,7 @@ csa2_status check_attn(const csa2_attn_args* a) {
     return CSA2_ERR_INVALID_ARG;
   if (a->w_rows > 0 && !a->window) return CSA2_ERR_INVALID_ARG;
   if (a->codes_ld < a->d / 2 || a->scales_ld < a->d / 32) return CSA2_ERR_INVALID_ARG;
+  if (!pages_ok(a->pages, a->n)) return CSA2_ERR_INVALID_ARG;
   if (a->window && a->win_ld < a->d) return CSA2_ERR_INVALID_ARG;
   if (a->q_dtype == CSA2_F32) {
     if (a->hq > 65535 || a->d > 256) return CSA2_ERR_UNSUPPORTED;
@@ -205,9 +226,15 @@ struct StackPieces {
   size_t total() const { return scores + tk + pl + std::max(ix, at); }
 };
 
-// slots of the Hierarchical Sparse Indexer's candidate pool (0 = off)
+// slots of the Hierarchical Sparse Indexer's candidate pool (0 = off): the
+// top-P pool, or the entries of the kept blocks under block-level pruning
 int64_t pool_slots(const csa2_stack_args& s) {
+  if (s.block > 0) return (int64_t)s.blocks_kept * s.block;
   return s.pool > 0 ? std::min<int64_t>(s.pool, s.n) : 0;
+}
+
+int64_t stack_blocks(const csa2_stack_args& s) {
+  return s.block > 0 ? (s.n + s.block - 1) / s.block : 0;
 }
 
 csa2_index_args stack_index_args(const csa2_stack_args& s, const csa2_layer_desc& L,
@@ -233,6 +260,7 @@ csa2_index_args stack_index_args(const csa2_stack_args& s, const csa2_layer_desc
   a.workspace = ws;
   a.workspace_bytes = ws_bytes;
   a.dev_status = s.dev_status;
+  a.pages = s.pages;
   return a;
 }
 
@@ -269,6 +297,7 @@ csa2_attn_args stack_attn_args(const csa2_stack_args& s, const csa2_layer_desc& 
   a.workspace = ws;
   a.workspace_bytes = ws_bytes;
   a.dev_status = s.dev_status;
+  a.pages = s.pages;
   return a;
 }
 
@@ -280,6 +309,31 @@ csa2_status quantize_new_rows(const csa2_stack_args& s, const csa2_layer_desc& d
                               cudaStream_t cs) {
   const int64_t nr = d.new_rows > 0 ? d.new_rows : 1;
   const bool e4m3 = s.idx_k_dtype == CSA2_E4M3;
+  if (s.pages.block_table) {
+    // paged caches: one launch writes every sequence's new rows through the
+    // block table (the fp32 indexer keys are not paged: checked before)
+    csa2_quant_args q;
+    std::memset(&q, 0, sizeof(q));
+    q.x = d.new_kv;
+    q.rows = s.B * nr;
+    q.d = s.d;
+    q.x_ld = s.d;
+    q.codes = d.codes;
+    q.codes_ld = s.d / 2;
+    q.scales = d.scales;
+    q.scales_ld = s.d / 32;
+    q.idxk = d.new_idxk;
+    q.di = s.di;
+    q.idxk_ld = s.di;
+    q.idxk_e4m3 = static_cast<uint8_t*>(d.idxk);
+    q.idxk_e4m3_ld = s.di;
+    q.pages = s.pages;
+    q.rows_per_seq = nr;
+    q.entry0 = d.new_row;
+    csa2_status st = check_quant(&q);
+    if (st != CSA2_OK) return st;
+    return launch_quantize_fp4(q, cs, s.dev_status);
+  }
   const int64_t per_call = nr == 1 ? 1 : s.B;  // number of calls
   for (int64_t b = 0; b < per_call; ++b) {
     csa2_quant_args q;
@@ -302,7 +356,7 @@ csa2_status quantize_new_rows(const csa2_stack_args& s, const csa2_layer_desc& d
     }
     csa2_status st = check_quant(&q);
     if (st != CSA2_OK) return st;
-    if ((st = launch_quantize_fp4(q, cs)) != CSA2_OK) return st;
+    if ((st = launch_quantize_fp4(q, cs, s.dev_status)) != CSA2_OK) return st;
     if (!e4m3) {
       // fp32 indexer keys are stored as given
       const size_t row_bytes = (size_t)s.di * sizeof(float);
@@ -436,6 +490,26 @@ csa2_status csa2_project_fp4(const csa2_project_args* a, csa2_stream_t stream) {
   return launch_project_fp4(*a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+csa2_status csa2_index_block_keys(const uint8_t* k8, int64_t B, int64_t n, int64_t k_ld,
+                                  int64_t k_seq_stride, const csa2_pages* pages, int32_t G,
+                                  int64_t blk0, int64_t nblk, uint8_t* out, int64_t out_ld,
+                                  int64_t out_seq_stride, int32_t* dev_status,
+                                  csa2_stream_t stream) {
+  if (B < 0 || n < 0 || G < 1 || G > 65536 || (G & (G - 1)) != 0 || blk0 < 0 || nblk < 0)
+    return CSA2_ERR_INVALID_ARG;
+  const csa2_pages pg = pages ? *pages : csa2_pages{nullptr, 0, 0, 0};
+  if (!pages_ok(pg, n)) return CSA2_ERR_INVALID_ARG;
+  if (blk0 + nblk > (n + G - 1) / G) return CSA2_ERR_INVALID_ARG;
+  if (B == 0 || nblk == 0) return CSA2_OK;
+  if (!k8 || !out || k_ld < 128 || out_ld < 128) return CSA2_ERR_INVALID_ARG;
+  if (!pg.block_table && B > 1 && (k_seq_stride < k_ld * n || out_seq_stride < out_ld * nblk))
+    return CSA2_ERR_INVALID_ARG;
+  csa2_status st = injected("index_block_keys");
+  if (st != CSA2_OK) return st;
+  return launch_block_keys(k8, B, n, k_ld, k_seq_stride, pg, G, blk0, nblk, out, out_ld,
+                           out_seq_stride, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t csa2_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k) {
   if (rows < 0 || k < 1) return 0;
   return topk_workspace_bytes(rows, n, k);
@@ -512,6 +586,19 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
     if (s->pool < s->k) return CSA2_ERR_INVALID_ARG;
     if (s->pool > 2048 || s->idx_k_dtype != CSA2_E4M3) return CSA2_ERR_UNSUPPORTED;
   }
+  if (!pages_ok(s->pages, s->n)) return CSA2_ERR_INVALID_ARG;
+  // paged caches hold E4M3 indexer keys (the new rows are cast into them)
+  if (s->pages.block_table && s->idx_k_dtype != CSA2_E4M3) return CSA2_ERR_UNSUPPORTED;
+  if (s->block < 0 || s->blocks_kept < 0) return CSA2_ERR_INVALID_ARG;
+  if (s->block > 0) {
+    if ((s->block & (s->block - 1)) != 0 || s->block > 65536 || s->blocks_kept < 1 ||
+        s->pool > 0 || (int64_t)s->blocks_kept * s->block < s->k)
+      return CSA2_ERR_INVALID_ARG;
+    if (s->idx_k_dtype != CSA2_E4M3 || s->q_per_seq != 1 || s->n_valid ||
+        (int64_t)s->blocks_kept * s->block > 2048 || stack_blocks(*s) > kTopkShortRow ||
+        s->blocks_kept > 2048)
+      return CSA2_ERR_UNSUPPORTED;
+  }
   // workspace: scores | per-row top-k histograms | the candidate pool |
   // scratch of the index (quantised Q) or attention (chunk partials) step
   const StackPieces p = stack_pieces(*s);
@@ -531,6 +618,7 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
     const csa2_layer_desc& kv = L[d.kv_src];
     if (d.mode == CSA2_MODE_FULL) {
       if (!d.codes || !d.scales || !d.idxk) return CSA2_ERR_INVALID_ARG;
+      if (s->block > 0 && !d.block_keys) return CSA2_ERR_INVALID_ARG;
       if ((d.new_kv == nullptr) != (d.new_idxk == nullptr)) return CSA2_ERR_INVALID_ARG;
       const int64_t nr = d.new_rows > 0 ? d.new_rows : 1;
       if (d.new_kv && (d.new_row < 0 || d.new_rows < 0 || d.new_row + nr > s->n))
@@ -567,14 +655,54 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
   };
   // the top-k histograms start at zero; every selection leaves them zeroed,
   // so one clear serves the whole stack (and keeps the launches back to back)
-  if ((st = clear_topk_hist(hist, nq, cs)) != CSA2_OK) return st;
+  if ((st = clear_topk_hist(hist, nq, s->n, cs)) != CSA2_OK) return st;
   for (int32_t l = 0; l < n_layers; ++l) {
     const csa2_layer_desc& d = L[l];
     const csa2_layer_desc& kv = L[d.kv_src];
     if (d.mode == CSA2_MODE_FULL && d.new_kv) {
       if ((st = quantize_new_rows(*s, d, cs)) != CSA2_OK) return st;
+      if (s->block > 0) {
+        // the block keys of the blocks the new rows fall in
+        const int64_t nr = d.new_rows > 0 ? d.new_rows : 1;
+        const int64_t b0 = d.new_row / s->block, b1 = (d.new_row + nr - 1) / s->block;
+        const bool paged = s->pages.block_table != nullptr;
+        if ((st = launch_block_keys(static_cast<const uint8_t*>(d.idxk), s->B, s->n, s->di,
+                                    paged ? 0 : s->n * s->di, s->pages, s->block, b0,
+                                    b1 - b0 + 1, d.block_keys, 128, stack_blocks(*s) * 128,
+                                    s->dev_status, cs)) != CSA2_OK)
+          return st;
+      }
     }
-    if (d.mode == CSA2_MODE_REINDEX && P > 0) {
+    if (d.mode == CSA2_MODE_FULL && s->block > 0) {
+      // block-level pruning: score the block keys, keep the best blocks, score
+      // only their entries at token level and select the top-k among them
+      csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
+      uint8_t* wq = static_cast<uint8_t*>(scratch);
+      float* wc = reinterpret_cast<float*>(wq + align256((size_t)nq * s->hi * s->di));
+      if ((st = launch_quantize_index_q(ia.q, ia.w, nq, s->hi, s->di, wq, wc, cs)) != CSA2_OK)
+        return st;
+      const int64_t nb = stack_blocks(*s);
+      csa2_index_args ib = ia;
+      ib.k = d.block_keys;
+      ib.n = nb;
+      ib.k_ld = 128;
+      ib.k_seq_stride = nb * 128;
+      ib.scores_ld = nb;
+      ib.n_valid = nullptr;
+      std::memset(&ib.pages, 0, sizeof(ib.pages));  // block keys are contiguous
+      if ((st = launch_index_score_fp8(ib, wq, wc, nullptr, IndexTuning{}, cs)) != CSA2_OK)
+        return st;
+      if ((st = launch_topk_small(scores, nb, nullptr, 0, nq, (int32_t)nb, nullptr,
+                                  s->blocks_kept, nullptr, 0, pool, P, cs, s->block, s->n)) !=
+          CSA2_OK)
+        return st;
+      if ((st = launch_index_score_pool(ia, wq, wc, pool, P, (int32_t)P, scores, P, cs)) !=
+          CSA2_OK)
+        return st;
+      if ((st = launch_topk_small(scores, P, nullptr, 0, nq, (int32_t)P, nullptr, s->k, pool, P,
+                                  d.topk_idx, s->k, cs)) != CSA2_OK)
+        return st;
+    } else if (d.mode == CSA2_MODE_REINDEX && P > 0) {
       // Hierarchical Sparse Indexer: score the last Full layer's pool only,
       // then its top-k (pool positions mapped back to entry indices)
       csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
@@ -596,9 +724,12 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
         return st;
     } else if (d.mode != CSA2_MODE_REUSE) {
       csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
-      // decode: the indexer kernel also builds the top-k's first-level
-      // histograms; otherwise a histogram pass over the scores does
-      const bool fused = index_fuses_topk_hist(ia);
+      // long rows: the indexer kernel also builds the top-k's first-level
+      // histograms in decode, a histogram pass over the scores otherwise;
+      // short rows are selected with every key in shared memory (no
+      // histogram, so none is accumulated)
+      const bool long_rows = s->n > kTopkShortRow;
+      const bool fused = long_rows && index_fuses_topk_hist(ia);
       IndexTuning tune;
       if (d.kv_src < 64) {
         tune.reverse = reverse_next[d.kv_src];
@@ -606,27 +737,33 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
         reverse_next[d.kv_src] = !tune.reverse;
       }
       if ((st = run_index(ia, fused ? hist : nullptr, tune, cs)) != CSA2_OK) return st;
-      if (!fused &&
+      if (long_rows && !fused &&
           (st = launch_topk_hist(scores, nq, s->n, s->n, s->n_valid, hist, cs)) != CSA2_OK)
         return st;
+      // the k (or, for the pool, P) best of each row
+      auto select = [&](int32_t kk, int32_t* out, int64_t out_ld) {
+        return long_rows ? launch_topk_select(scores, nq, s->n, s->n, s->n_valid, kk, hist, out,
+                                              out_ld, cs)
+                         : launch_topk_small(scores, s->n, nullptr, 0, nq, (int32_t)s->n,
+                                             s->n_valid, kk, nullptr, 0, out, out_ld, cs);
+      };
       if (P > 0 && d.mode == CSA2_MODE_FULL) {
         // a Full layer of the Hierarchical Sparse Indexer keeps its top-P as
         // the pool, then takes its top-k inside the pool (the same entries
         // as the top-k of the whole row: the pool holds them)
-        if ((st = launch_topk_select(scores, nq, s->n, s->n, s->n_valid, (int32_t)P, hist, pool,
-                                     P, cs)) != CSA2_OK)
-          return st;
+        if ((st = select((int32_t)P, pool, P)) != CSA2_OK) return st;
         if ((st = launch_topk_small(scores, s->n, pool, P, nq, (int32_t)P, nullptr, s->k, pool,
                                     P, d.topk_idx, s->k, cs)) != CSA2_OK)
           return st;
-      } else if ((st = launch_topk_select(scores, nq, s->n, s->n, s->n_valid, s->k, hist,
-                                          d.topk_idx, s->k, cs)) != CSA2_OK) {
+      } else if ((st = select(s->k, d.topk_idx, s->k)) != CSA2_OK) {
         return st;
       }
     }
     const int32_t* idx = L[d.mode == CSA2_MODE_REUSE ? d.idx_src : l].topk_idx;
     csa2_attn_args aa = stack_attn_args(*s, d, kv, idx, scratch, scratch_bytes);
-    if ((st = launch_sparse_attn(aa, cs)) != CSA2_OK) return st;
+    // the attention queries are inputs of the call: the kernels before this
+    // one in the stack never write them, so they may load before its wait
+    if ((st = launch_sparse_attn(aa, cs, true)) != CSA2_OK) return st;
   }
   return CSA2_OK;
 }

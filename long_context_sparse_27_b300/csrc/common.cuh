@@ -60,6 +60,19 @@ __device__ __forceinline__ float e2m1_value(uint32_t c) {
 // UE8M0 scale byte -> 2^(s - 127) as a float (s = 0 gives the subnormal 2^-127).
 __device__ __forceinline__ float ue8m0_value(uint32_t s) { return exp2_int((int)s - 127); }
 
+// Exponent e of the indexer-Q scale 2^e for a head whose largest magnitude
+// is amax > 0: the smallest e (>= -126) with amax / 2^e <= 448 = 1.75 * 2^8.
+// With amax = m 2^E (m in [1, 2)), e = E - 8 when m <= 1.75, else E - 7.
+__device__ __forceinline__ int index_q_exponent(float amax) {
+  const int E = floor_log2_pos(amax);
+  // fraction bits of m, normalising a subnormal amax first
+  const uint32_t u = __float_as_uint(amax);
+  uint32_t frac = u & 0x7FFFFFu;
+  if (((u >> 23) & 0xFFu) == 0) frac = (frac << (__clz(frac) - 8)) & 0x7FFFFFu;
+  const int e = (frac <= 0x600000u) ? E - 8 : E - 7;  // 0x600000: fraction of 1.75
+  return e < -126 ? -126 : e;
+}
+
 // E4M3 with round-to-nearest-even and saturation to +-448.
 __device__ __forceinline__ uint32_t e4m3_encode(float x) {
   return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
@@ -104,6 +117,19 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 __device__ __forceinline__ void raise_flag(int32_t* dev_status, int32_t flag) {
   if (dev_status) atomicOr(dev_status, flag);
+}
+
+// Pool row of entry j of sequence b in a paged cache (csa2_pages), or -1
+// with CSA2_DEVFLAG_BOUNDS raised when the block table names a page outside
+// [0, num_pages).
+__device__ __forceinline__ int64_t paged_row(const csa2_pages& pg, int64_t b, int64_t j,
+                                             int32_t* dev_status) {
+  const int32_t page = pg.block_table[b * pg.bt_ld + j / pg.page_rows];
+  if (page < 0 || page >= pg.num_pages) {
+    raise_flag(dev_status, CSA2_DEVFLAG_BOUNDS);
+    return -1;
+  }
+  return (int64_t)page * pg.page_rows + j % pg.page_rows;
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -261,6 +287,22 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
+// swizzle layout: 64 consecutive MN elements (128 bytes) per row of the
+// swizzle atom, 8 K rows 128 bytes apart per atom; `lbo` = bytes between
+// atoms adjacent along MN, `sbo` = bytes between atoms adjacent along K (8
+// K rows).  Atoms are 1024-byte aligned (base offset 0).
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t smem_addr, uint32_t lbo,
+                                                   uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f8f6f4 with E4M3 A and B, f32 accumulate,
 // both operands K-major: D format (bits 4-5) = 1, A / B format (7-9 /
 // 10-12) = 0, transpose bits 15 / 16 = 0, N >> 3 at 17-22, M >> 4 at 24-28.
@@ -269,10 +311,20 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
 }
 
 // Instruction descriptor, kind::f16 with BF16 A and B (format 1), f32
-// accumulate, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// accumulate; B K-major, A K-major or (a_mn) MN-major (bit 15).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -312,6 +364,49 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 8 / 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Generic-proxy writes to shared memory (st.shared, cp.async) made visible
+// to the async proxy (tcgen05.mma operand reads); each writing thread
+// executes it before the barrier that precedes the MMA issue.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Thread-block-cluster barrier in two halves: arrive (release: this
+// thread's earlier writes, global ones included, are ordered before) and
+// wait (acquire).  Every thread of every CTA of the cluster executes both.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

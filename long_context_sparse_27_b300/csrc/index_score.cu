@@ -22,6 +22,8 @@
 //    chunk (QG = 4, 4 queries x 64 heads per MMA) it is a dense contraction,
 //    one CTA per SM with a 6-stage ring.
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.h"
@@ -42,7 +44,8 @@ __global__ void __launch_bounds__(kF32Warps * 32)
                          const float* __restrict__ k, int64_t q_per_seq, int32_t hi, int32_t di,
                          int64_t n, int64_t k_ld, int64_t k_seq_stride,
                          const int32_t* __restrict__ n_valid, float* __restrict__ scores,
-                         int64_t scores_ld, int64_t per_block) {
+                         int64_t scores_ld, int64_t per_block, const csa2_pages pages,
+                         int32_t* dev_status) {
   extern __shared__ float sq[];  // [hi * di] query, then [hi] weights
   pdl_wait();
   const int64_t qi = blockIdx.y;
@@ -52,7 +55,8 @@ __global__ void __launch_bounds__(kF32Warps * 32)
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int64_t nv = n_valid ? (int64_t)n_valid[qi] : n;
-  const float* kseq = k + (qi / q_per_seq) * k_seq_stride;
+  const int64_t b = qi / q_per_seq;
+  const float* kseq = k + b * k_seq_stride;
   const int64_t j0 = (int64_t)blockIdx.x * per_block;
   const int64_t j1 = min(n, j0 + per_block);
   for (int64_t j = j0 + warp; j < j1; j += kF32Warps) {
@@ -61,9 +65,13 @@ __global__ void __launch_bounds__(kF32Warps * 32)
       continue;
     }
     const float* kj = kseq + j * k_ld;
+    if (pages.block_table) {  // paged keys: the entry's row in the pool
+      const int64_t row = paged_row(pages, b, j, dev_status);
+      kj = row < 0 ? nullptr : k + row * k_ld;
+    }
     float kv[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) kv[t] = (lane + 32 * t < di) ? kj[lane + 32 * t] : 0.f;
+    for (int t = 0; t < 8; ++t) kv[t] = (kj && lane + 32 * t < di) ? kj[lane + 32 * t] : 0.f;
     float s = 0.f;
     for (int h = 0; h < hi; ++h) {
       float dot = 0.f;
@@ -90,7 +98,7 @@ csa2_status launch_index_score_f32(const csa2_index_args& a, cudaStream_t s) {
   return launch_kernel(idx_score_f32_kernel, grid, dim3(kF32Warps * 32), smem, s, 1,
                        static_cast<const float*>(a.q), a.w, static_cast<const float*>(a.k),
                        a.q_per_seq, a.hi, a.di, a.n, a.k_ld, a.k_seq_stride, a.n_valid, a.scores,
-                       a.scores_ld, per_block);
+                       a.scores_ld, per_block, a.pages, a.dev_status);
 }
 
 // ===========================================================================
@@ -100,6 +108,31 @@ csa2_status launch_index_score_f32(const csa2_index_args& a, cudaStream_t s) {
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
+
+// Limit of the pipeline waits of one launch: 2 s, or CSA2_WAIT_LIMIT_NS
+// when set (read at every launch; a test hook that makes the waits run out
+// and the kernel return CSA2_DEVFLAG_TIMEOUT).  Waits for copies or MMAs
+// already in flight keep fixed limits, so a CTA never leaves with either
+// outstanding.
+uint64_t pipeline_wait_ns() {
+  const char* e = std::getenv("CSA2_WAIT_LIMIT_NS");
+  if (!e || !*e) return kWaitLimitNs;
+  const unsigned long long v = std::strtoull(e, nullptr, 10);
+  return v > 0 ? (uint64_t)v : kWaitLimitNs;
+}
+
+// CSA2_TEST_STALL_LOADS=1 (read at every launch; a test hook): the TMA
+// producer issues no key loads, so the MMA and epilogue waits wait for data
+// that never comes and run out after pipeline_wait_ns(); no copy or MMA is
+// ever in flight, and the launch ends with CSA2_DEVFLAG_TIMEOUT.
+bool stall_loads() {
+  const char* e = std::getenv("CSA2_TEST_STALL_LOADS");
+  return e && e[0] == '1';
+}
+
+constexpr int kPageLookahead = 8;  // paged keys: tiles whose page ids are in flight ahead
+constexpr int kPageRing = 16;      // tiles in the page-id ring (two ids each)
+static_assert(kPageRing >= kPageLookahead + 1, "a ring slot is not rewritten while in use");
 
 template <int QG>
 struct TcCfg {
@@ -126,14 +159,16 @@ struct TcCfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_Q = OFF_K + STAGES * KTILE;
   static constexpr int OFF_C = OFF_Q + 2 * QTILE;             // float [EPI_WARPS][2][BN]
+  static constexpr int OFF_CQ = OFF_C + EPI_WARPS * 2 * BN * 4;  // float [2][BN], fused Q
   // fused first-level top-k histogram (decode): two group slots of 4096 bins
-  static constexpr int OFF_H = OFF_C + EPI_WARPS * 2 * BN * 4;
+  static constexpr int OFF_H = OFF_CQ + (QG == 1 ? 2 * BN * 4 : 0);
   static constexpr int HIST_BYTES = QG == 1 ? 2 * kTopkBins * 4 : 0;
   static constexpr int OFF_BAR = OFF_H + HIST_BYTES;
   // barriers: full[S], empty[S], qfull[2], qempty[2], tfull[NACC], tempty[NACC], fin
   static constexpr int NBAR = 2 * STAGES + 4 + 2 * NACC + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem slot, abort flag
-  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr int OFF_PG = OFF_MISC + 16;                // int32 [kPageRing][2] page ids
+  static constexpr int SMEM = OFF_PG + kPageRing * 2 * 4;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
   static_assert(NACC % STREAMS == 0 && QG % SPLIT == 0,
                 "accumulator a is drained by the warpgroups of stream a % STREAMS");
@@ -144,7 +179,12 @@ struct TcCfg {
 };
 
 struct TcParams {
-  const float* c;          // [nq, 64] head weights (w * sigma)
+  const float* c;          // [nq, 64] head weights (w * sigma); unused when qbf is set
+  // decode with the indexer-Q quantiser fused in: bf16 Q [nq, 64, 128] and
+  // raw weights w [nq, 64]; the kernel quantises the (at most two) query
+  // groups of each CTA itself instead of loading q8 by TMA
+  const uint16_t* qbf;
+  const float* w;
   const int32_t* n_valid;  // [nq] or null
   float* scores;
   int64_t scores_ld;
@@ -156,7 +196,13 @@ struct TcParams {
   uint32_t* hist1;         // QG = 1: [nq][4096] first-level top-k histograms to add to, or null
   int reverse;             // walk each CTA's tile range from its end
   int keep_in_l2;          // load keys with the normal L2 policy instead of evict-first
+  // paged keys (pages.block_table set): kmap is a 2-D map over the pool
+  // with 64-row boxes; a tile is two boxes, each inside one page
+  csa2_pages pages;
+  uint64_t wait_ns;        // limit of each pipeline wait (drain waits keep their own)
+  int stall_loads;         // test hook: the producer issues no loads (waits run out)
 };
+
 
 // (group, tile within the group) of the CTA's tiles, moved without 64-bit
 // divisions: tile t is group t / ktiles, tile t % ktiles.
@@ -210,7 +256,8 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&qfull[i], 1);
+      // fused Q: every epilogue warp arrives once its share of the slot is written
+      mbar_init(&qfull[i], p.qbf ? C::EPI_WARPS : 1);
       mbar_init(&qempty[i], 1);
     }
     for (int i = 0; i < C::NACC; ++i) {
@@ -221,7 +268,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&kmap);
-    tma_prefetch_desc(&qmap);
+    if (!p.qbf) tma_prefetch_desc(&qmap);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   if constexpr (QG == 1) {
@@ -236,7 +283,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0 && t_begin < t_end) {
+    if (lane == 0 && t_begin < t_end && !p.stall_loads) {
       const uint64_t pol_k = p.keep_in_l2 ? l2_policy_evict_normal() : l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
       int stage = 0;
@@ -245,12 +292,39 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       bool ok = true;
       const int64_t dir = p.reverse ? -1 : 1;
       TileCursor cur(p.reverse ? t_end - 1 : t_begin, p.ktiles);
-      for (int64_t i = 0; i < t_end - t_begin; ++i, cur.advance(dir)) {
+      // paged keys: the page ids of tile i (two 64-row halves) are copied by
+      // cp.async into ring slot i % kPageRing, kPageLookahead tiles before
+      // the tile's loads are issued (one commit group per tile)
+      const bool paged = p.pages.block_table != nullptr;
+      const int64_t ntiles = t_end - t_begin;
+      int32_t* pg = reinterpret_cast<int32_t*>(smem + C::OFF_PG);
+      TileCursor ahead(p.reverse ? t_end - 1 : t_begin, p.ktiles);
+      int64_t ahead_i = 0;
+      auto page_ids_ahead = [&](int64_t upto) {  // issue tiles ahead_i .. upto - 1
+        for (; ahead_i < upto; ++ahead_i) {
+          if (ahead_i < ntiles) {
+            const int64_t bb = (ahead.g * QG) / p.q_per_seq;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int64_t j = ahead.kt * C::BM + 64 * h;
+              if (j < p.n)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                                 smem_u32(pg + (ahead_i % kPageRing) * 2 + h)),
+                             "l"(p.pages.block_table + bb * p.pages.bt_ld + j / p.pages.page_rows)
+                             : "memory");
+            }
+            ahead.advance(dir);
+          }
+          asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+      };
+      if (paged) page_ids_ahead(kPageLookahead);
+      for (int64_t i = 0; i < ntiles; ++i, cur.advance(dir)) {
         const int64_t g = cur.g, kt = cur.kt;
-        if (g != g_prev) {
+        if (g != g_prev && !p.qbf) {
           const int qs = (int)(qcount & 1);
           const uint32_t qph = (uint32_t)((qcount >> 1) & 1);
-          if (!mbar_wait(&qempty[qs], qph ^ 1, abort_flag, p.dev_status, kWaitLimitNs)) {
+          if (!mbar_wait(&qempty[qs], qph ^ 1, abort_flag, p.dev_status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -259,20 +333,49 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
           ++qcount;
           g_prev = g;
         }
-        if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, p.dev_status, kWaitLimitNs)) {
+        if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, p.dev_status, p.wait_ns)) {
           ok = false;
           break;
         }
         const int64_t b = (g * QG) / p.q_per_seq;
-        mbar_arrive_expect_tx(&full[stage], C::KTILE);
-        tma_load_3d(&kmap, &full[stage], kbuf + stage * C::KTILE, 0, (int32_t)(kt * C::BM),
-                    (int32_t)b, pol_k);
+        if (!paged) {
+          mbar_arrive_expect_tx(&full[stage], C::KTILE);
+          tma_load_3d(&kmap, &full[stage], kbuf + stage * C::KTILE, 0, (int32_t)(kt * C::BM),
+                      (int32_t)b, pol_k);
+        } else {
+          // this tile's page ids (loaded kPageLookahead tiles ago) have landed
+          page_ids_ahead(i + kPageLookahead);
+          asm volatile("cp.async.wait_group %0;" ::"n"(kPageLookahead) : "memory");
+          const int32_t* ids = pg + (i % kPageRing) * 2;
+          int32_t y[2];
+          uint32_t bytes = 0;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int64_t j = kt * C::BM + 64 * h;
+            y[h] = -1;
+            if (j >= p.n) continue;  // past the rows: never looked up, stays stale (masked)
+            const int32_t page = ids[h];
+            if (page < 0 || page >= p.pages.num_pages) {
+              raise_flag(p.dev_status, CSA2_DEVFLAG_BOUNDS);
+              continue;
+            }
+            y[h] = (int32_t)((int64_t)page * p.pages.page_rows + j % p.pages.page_rows);
+            bytes += C::KTILE / 2;
+          }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            if (y[h] >= 0)
+              tma_load_2d(&kmap, &full[stage], kbuf + stage * C::KTILE + h * (C::KTILE / 2), 0,
+                          y[h], pol_k);
+        }
         ++issued;
         if (++stage == C::STAGES) {
           stage = 0;
           ph ^= 1;
         }
       }
+      if (paged) asm volatile("cp.async.wait_all;" ::: "memory");  // page ids in flight
       if (!ok) {
         // let the copies already in flight land before the CTA's shared
         // memory goes away: wait (bounded, ignoring the abort flag) for the
@@ -304,14 +407,14 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
           if (g_prev >= 0) tc_commit(&qempty[qs]);  // old Q free once its MMAs finish
           qs = (int)(qcount & 1);
           if (!mbar_wait(&qfull[qs], (uint32_t)((qcount >> 1) & 1), abort_flag, p.dev_status,
-                         kWaitLimitNs))
+                         p.wait_ns))
             break;
           ++qcount;
           g_prev = g;
         }
-        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.dev_status, kWaitLimitNs)) break;
+        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, p.dev_status, p.wait_ns)) break;
         tc_fence_after();
-        if (!mbar_wait(&full[stage], ph, abort_flag, p.dev_status, kWaitLimitNs)) break;
+        if (!mbar_wait(&full[stage], ph, abort_flag, p.dev_status, p.wait_ns)) break;
         tc_fence_after();
         const uint64_t adesc = sdesc_k_sw128(smem_u32(kbuf + stage * C::KTILE));
         const uint64_t bdesc = sdesc_k_sw128(smem_u32(qbuf + qs * C::QTILE));
@@ -353,6 +456,68 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     // each warp keeps its own double-buffered copy of the group's head weights
     float* my_c = cbuf + ew * 2 * C::BN;
     int cb = 1;
+    // fused Q (decode): slot 0 holds the first group in processing order,
+    // slot 1 the other end of the CTA's range (the host launches this form
+    // only when no range spans more than two groups)
+    const int64_t gq0 = (p.reverse ? t_end - 1 : t_begin) / p.ktiles;
+    // [2][BN] folded weights c = w * sigma of the two slots
+    float* cq = reinterpret_cast<float*>(smem + C::OFF_CQ);
+    if constexpr (QG == 1) {  // (the prefill form has no room for cq and never fuses)
+      if (p.qbf && t_begin < t_end) {
+        const int64_t gq1 = (p.reverse ? t_begin : t_end - 1) / p.ktiles;
+        // warp ew quantises heads 8 ew .. 8 ew + 7; lanes 4h'.. 4h'+3 hold
+        // the four 32-element quarters of head 8 ew + h'
+        const int h = (C::BN / C::EPI_WARPS) * ew + (lane >> 2), part = lane & 3;
+        for (int slot = 0; slot < 2; ++slot) {
+          const int64_t g = slot == 0 ? gq0 : gq1;
+          if (slot == 1 && gq1 == gq0) break;
+          const uint4* src =
+              reinterpret_cast<const uint4*>(p.qbf + (g * C::BN + h) * C::BK + part * 32);
+          uint4 raw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t wv[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              v[8 * i + 2 * j] = bf16_bits_to_float(wv[j] & 0xFFFFu);
+              v[8 * i + 2 * j + 1] = bf16_bits_to_float(wv[j] >> 16);
+            }
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          const int e = amax > 0.f ? index_q_exponent(amax) : 0;
+          const float inv = exp2_int(-e);
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t wd = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              wd |= (amax > 0.f ? e4m3_encode(v[4 * i + j] * inv) : 0u) << (8 * j);
+            pk[i] = wd;
+          }
+          // bytes 32 part .. of row h: 16-byte pieces 2 part, 2 part + 1 of
+          // the 128-byte swizzle row (piece index XOR h % 8), as TMA writes
+          uint8_t* qrow = qbuf + slot * C::QTILE + h * C::BK;
+          *reinterpret_cast<uint4*>(qrow + (((2 * part) ^ (h & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(qrow + (((2 * part + 1) ^ (h & 7)) << 4)) =
+              make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          if (part == 0) cq[slot * C::BN + h] = p.w[g * C::BN + h] * exp2_int(e);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&qfull[slot]);
+        }
+        // every epilogue warp's share of cq is written
+        asm volatile("bar.sync 1, %0;" ::"n"(C::EPI_WARPS * 32) : "memory");
+      }
+    }
     int64_t nv[C::QPW];
     // li counts tiles in processing order (from the range's end when reversed)
     const int64_t dir = p.reverse ? -1 : 1;
@@ -365,7 +530,11 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       if (g != g_prev) {
         cb ^= 1;
         __syncwarp();
-        for (int i = lane; i < C::BN; i += 32) my_c[cb * C::BN + i] = p.c[g * C::BN + i];
+        if (p.qbf)
+          for (int i = lane; i < C::BN; i += 32)
+            my_c[cb * C::BN + i] = cq[(g == gq0 ? 0 : 1) * C::BN + i];
+        else
+          for (int i = lane; i < C::BN; i += 32) my_c[cb * C::BN + i] = p.c[g * C::BN + i];
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < C::QPW; ++i)
@@ -374,7 +543,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       }
       // every lane waits; the warp goes on only if all of them saw the phase
       // complete, so the warp-collective loads below never run diverged
-      const bool got = mbar_wait(&tfull[acc], aph, abort_flag, p.dev_status, kWaitLimitNs);
+      const bool got = mbar_wait(&tfull[acc], aph, abort_flag, p.dev_status, p.wait_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(lq * 32) << 16) + (uint32_t)(acc * C::BN);
@@ -473,6 +642,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// CTAs of a launch over `total` tiles (at most CTAS_PER_SM per SM).
+template <int QG>
+int64_t tc_grid(int64_t total) {
+  return std::min<int64_t>(total, (int64_t)TcCfg<QG>::CTAS_PER_SM * sm_count());
+}
+
+// q8 / c: the quantised queries; or, both null, bf16 queries a.q and raw
+// weights a.w quantised inside the kernel (decode only, see TcParams::qbf).
 template <int QG>
 csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* c,
                       uint32_t* hist1, IndexTuning tune, cudaStream_t s) {
@@ -480,8 +657,21 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cuda_fail(cudaErrorNotSupported);
   const int64_t nq = a.B * a.q_per_seq;
+  const bool fuse_q = q8 == nullptr;
   CUtensorMap kmap, qmap;
-  {
+  std::memset(&qmap, 0, sizeof(qmap));
+  if (a.pages.block_table) {
+    // the page pool as rows of 128 bytes, loaded in 64-row boxes
+    cuuint64_t dims[2] = {(cuuint64_t)a.di,
+                          (cuuint64_t)a.pages.num_pages * (cuuint64_t)a.pages.page_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)a.k_ld};
+    cuuint32_t box[2] = {128, 64};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.k), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return CSA2_ERR_INVALID_ARG;
+  } else {
     cuuint64_t dims[3] = {(cuuint64_t)a.di, (cuuint64_t)a.n, (cuuint64_t)a.B};
     cuuint64_t strides[2] = {(cuuint64_t)a.k_ld, (cuuint64_t)a.k_seq_stride};
     cuuint32_t box[3] = {128, 128, 1};
@@ -491,7 +681,7 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return CSA2_ERR_INVALID_ARG;
   }
-  {
+  if (!fuse_q) {
     cuuint64_t dims[2] = {(cuuint64_t)a.di, (cuuint64_t)(nq * a.hi)};
     cuuint64_t strides[1] = {(cuuint64_t)a.di};
     cuuint32_t box[2] = {128, (cuuint32_t)C::BN};
@@ -503,6 +693,8 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   }
   TcParams p;
   p.c = c;
+  p.qbf = fuse_q ? static_cast<const uint16_t*>(a.q) : nullptr;
+  p.w = fuse_q ? a.w : nullptr;
   p.n_valid = a.n_valid;
   p.scores = a.scores;
   p.scores_ld = a.scores_ld;
@@ -514,6 +706,9 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   p.hist1 = QG == 1 ? hist1 : nullptr;
   p.reverse = tune.reverse ? 1 : 0;
   p.keep_in_l2 = tune.keep_in_l2 ? 1 : 0;
+  p.pages = a.pages;
+  p.wait_ns = pipeline_wait_ns();
+  p.stall_loads = stall_loads() ? 1 : 0;
   const int64_t total = p.groups * p.ktiles;
   if (total == 0) return CSA2_OK;
   static std::atomic<uint64_t> attr_done{0};
@@ -522,7 +717,7 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   });
   if (e != cudaSuccess) return cuda_fail(e);
-  const int grid = (int)std::min<int64_t>(total, (int64_t)C::CTAS_PER_SM * sm_count());
+  const int grid = (int)tc_grid<QG>(total);
   return launch_kernel(idx_score_tc_kernel<QG>, dim3(grid), dim3(C::THREADS),
                        (size_t)C::SMEM_ALLOC, s, 1, kmap, qmap, p);
 }
@@ -535,6 +730,22 @@ csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, 
   if (a.B * a.q_per_seq == 0 || a.n == 0) return CSA2_OK;
   if (a.q_per_seq % 4 == 0) return launch_tc<4>(a, q8, c, nullptr, tune, s);
   return launch_tc<1>(a, q8, c, hist1, tune, s);
+}
+
+csa2_status launch_index_score_bf16q(const csa2_index_args& a, uint32_t* hist1, IndexTuning tune,
+                                     cudaStream_t s) {
+  if (a.hi != 64 || a.di != 128 || a.q_dtype != CSA2_BF16 || a.k_dtype != CSA2_E4M3 ||
+      a.q_per_seq % 4 == 0)
+    return CSA2_ERR_UNSUPPORTED;
+  const int64_t nq = a.B * a.q_per_seq;
+  if (nq == 0 || a.n == 0) return CSA2_OK;
+  // every CTA's tile range must span at most two query groups
+  const int64_t ktiles = (a.n + TcCfg<1>::BM - 1) / TcCfg<1>::BM;
+  const int64_t total = nq * ktiles;
+  const int64_t grid = tc_grid<1>(total);
+  if ((total + grid - 1) / grid > ktiles + 1) return CSA2_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(a.q) & 15) != 0) return CSA2_ERR_UNSUPPORTED;
+  return launch_tc<1>(a, nullptr, nullptr, hist1, tune, s);
 }
 
 bool index_fuses_topk_hist(const csa2_index_args& a) {

@@ -22,8 +22,9 @@ csa2_status cuda_fail(cudaError_t e);
 // cudaGetLastError() after a launch, mapped to a status.
 csa2_status check_launch();
 
-// a1
-csa2_status launch_quantize_fp4(const csa2_quant_args& a, cudaStream_t s);
+// a1 (dev_status: where a paged destination outside the pool is reported)
+csa2_status launch_quantize_fp4(const csa2_quant_args& a, cudaStream_t s,
+                                int32_t* dev_status = nullptr);
 // a2
 csa2_status launch_quantize_index_q(const void* q, const float* w, int64_t nq, int32_t hi,
                                     int32_t di, uint8_t* q8, float* c, cudaStream_t s);
@@ -44,6 +45,12 @@ struct IndexTuning {
 // keys to (see index_fuses_topk_hist).
 csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, const float* c,
                                    uint32_t* hist1, IndexTuning tune, cudaStream_t s);
+// The same with bf16 queries and raw weights (a.q, a.w), quantised inside
+// the indexer kernel (decode shapes: hi 64, di 128, q_per_seq not a
+// multiple of 4); CSA2_ERR_UNSUPPORTED (nothing launched) when the launch
+// cannot take that form, and the caller quantises separately.
+csa2_status launch_index_score_bf16q(const csa2_index_args& a, uint32_t* hist1, IndexTuning tune,
+                                     cudaStream_t s);
 // Scores of a candidate pool (the Hierarchical Sparse Indexer): for every
 // query q and slot i < pool_n, scores[q * scores_ld + i] = the FP8 indexer
 // score of entry pool[q * pool_ld + i] of q's sequence (-inf for a slot
@@ -54,16 +61,31 @@ csa2_status launch_index_score_pool(const csa2_index_args& a, const uint8_t* q8,
                                     float* scores, int64_t scores_ld, cudaStream_t s);
 // whether launch_index_score_fp8 builds the top-k histograms for `a`
 bool index_fuses_topk_hist(const csa2_index_args& a);
-// a4: the workspace holds one 4096-bin first-level histogram per row
+// a4: rows of at most kTopkShortRow entries are selected by
+// launch_topk_small (every key in shared memory, no histogram); longer rows
+// by launch_topk_select from their level-1 histograms.
+constexpr int64_t kTopkShortRow = 4096;
+// the workspace holds one 4096-bin first-level histogram per row (the
+// first rows * 16 KiB), then for rows longer than 4096 a counter and the
+// slices' candidate slots per row
 size_t topk_workspace_bytes(int64_t rows, int64_t n, int32_t k);
 csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
                         const int32_t* n_valid, int32_t k, int32_t* idx_out, int64_t idx_ld,
                         void* ws, int32_t* dev_status, cudaStream_t s);
-// the pieces of launch_topk: zero the histograms; select from scores whose
-// histograms are complete (the selection leaves the histograms zeroed)
-csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s);
+// the pieces of launch_topk: zero the histograms (and the counters of a
+// long-row workspace for rows of n); select from scores whose histograms are
+// complete (the selection leaves histograms and counters zeroed)
+csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, int64_t n, cudaStream_t s);
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
                              const int32_t* n_valid, uint32_t* hist1, cudaStream_t s);
+// Block keys of the Hierarchical Sparse Indexer's first level: for blocks
+// blk0 .. blk0 + nblk - 1 of every sequence b < B, out[b * out_seq_stride +
+// blk * out_ld + i] = E4M3((sum of the di = 128 key bytes i of the block's
+// entries, decoded) / G) (G a power of two, entries past n count as zero).
+csa2_status launch_block_keys(const uint8_t* k8, int64_t B, int64_t n, int64_t k_ld,
+                              int64_t k_seq_stride, const csa2_pages& pages, int32_t G,
+                              int64_t blk0, int64_t nblk, uint8_t* out, int64_t out_ld,
+                              int64_t out_seq_stride, int32_t* dev_status, cudaStream_t s);
 // The decoder's global KV: h [rows, hidden] x w [d, hidden]^T quantised to
 // FP4 (codes / scales), the fp32 projection optionally to out.
 csa2_status launch_project_fp4(const csa2_project_args& a, cudaStream_t s);
@@ -71,10 +93,14 @@ csa2_status launch_project_fp4(const csa2_project_args& a, cudaStream_t s);
 // scores[r * ld + i], or with gather scores[r * ld + gather[r * gather_ld +
 // i]] (an index < 0 is an empty slot, below every value); positions are
 // written ascending as remap[r * remap_ld + i] (or i), padded with -1.
+// expand = G > 0: position p (a block) written at output slot s is written
+// as the G entries p * G .. p * G + G - 1 into slots s * G .., those at or
+// past expand_n as -1 (the row then holds k * G slots).
 csa2_status launch_topk_small(const float* scores, int64_t ld, const int32_t* gather,
                               int64_t gather_ld, int64_t rows, int32_t n, const int32_t* n_valid,
                               int32_t k, const int32_t* remap, int64_t remap_ld, int32_t* idx_out,
-                              int64_t idx_ld, cudaStream_t s);
+                              int64_t idx_ld, cudaStream_t s, int32_t expand = 0,
+                              int64_t expand_n = 0);
 // remap (optional): entry j of row r is written as remap[r * remap_ld + j]
 // (positions in a candidate pool -> entry indices); clear_hist = false
 // leaves the histograms for another selection from the same scores.
@@ -84,8 +110,11 @@ csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int
                                const int32_t* remap = nullptr, int64_t remap_ld = 0,
                                bool clear_hist = true);
 // a5
+// q_ready: the attention queries may be read before the kernel's
+// programmatic-launch wait (no kernel still running on the stream writes
+// them); set by the layer stack, whose preceding kernels never do.
 size_t attn_workspace_bytes(const csa2_attn_args& a);
-csa2_status launch_sparse_attn(const csa2_attn_args& a, cudaStream_t s);
+csa2_status launch_sparse_attn(const csa2_attn_args& a, cudaStream_t s, bool q_ready = false);
 
 // number of SMs of the current device (cached per device)
 int sm_count();

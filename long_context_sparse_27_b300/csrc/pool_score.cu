@@ -45,11 +45,11 @@ __global__ void __launch_bounds__(kPThreads)
                       const uint8_t* __restrict__ k, int64_t k_ld, int64_t k_seq_stride,
                       int64_t q_per_seq, int64_t n, const int32_t* __restrict__ pool,
                       int64_t pool_ld, int32_t pool_n, float* __restrict__ scores,
-                      int64_t scores_ld, int32_t* dev_status) {
+                      int64_t scores_ld, int32_t* dev_status, const csa2_pages pages) {
   __shared__ __align__(16) uint8_t sk[kPSlots * kPRow];
   __shared__ __align__(16) uint8_t sq[kPHeads * kPRow];
   __shared__ float sc[kPHeads];
-  __shared__ int32_t sj[kPSlots];
+  __shared__ int64_t sj[kPSlots];  // byte offset of the slot's key row from k, -1: empty
   pdl_wait();
   const int64_t qi = blockIdx.x;
   const int s0 = blockIdx.y * kPSlots;
@@ -63,7 +63,16 @@ __global__ void __launch_bounds__(kPThreads)
       raise_flag(dev_status, CSA2_DEVFLAG_BOUNDS);
       j = -1;
     }
-    sj[tid] = j;
+    int64_t off = -1;
+    if (j >= 0) {
+      if (pages.block_table) {  // paged keys: the entry's row in the pool
+        const int64_t row = paged_row(pages, b, j, dev_status);
+        off = row < 0 ? -1 : row * k_ld;
+      } else {
+        off = b * k_seq_stride + (int64_t)j * k_ld;
+      }
+    }
+    sj[tid] = off;
   }
   if (tid < kPHeads) sc[tid] = c[qi * kPHeads + tid];
   for (int i = tid; i < kPHeads * (kPDim / 16); i += kPThreads) {
@@ -71,13 +80,12 @@ __global__ void __launch_bounds__(kPThreads)
     cp_async16(sq + h * kPRow + p * 16, q8 + (qi * kPHeads + h) * kPDim + p * 16);
   }
   __syncthreads();
-  const uint8_t* kseq = k + b * k_seq_stride;
   for (int i = tid; i < kPSlots * (kPDim / 16); i += kPThreads) {
     const int r = i / (kPDim / 16), p = i % (kPDim / 16);
-    const int32_t j = sj[r];
+    const int64_t off = sj[r];
     uint8_t* dst = sk + r * kPRow + p * 16;
-    if (j >= 0)
-      cp_async16(dst, kseq + (int64_t)j * k_ld + p * 16);
+    if (off >= 0)
+      cp_async16(dst, k + off + p * 16);
     else
       *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
   }
@@ -142,7 +150,7 @@ csa2_status launch_index_score_pool(const csa2_index_args& a, const uint8_t* q8,
   const dim3 grid((unsigned)nq, (unsigned)((pool_n + kPSlots - 1) / kPSlots));
   return launch_kernel(pool_score_kernel, grid, dim3(kPThreads), 0, s, 1, q8, c,
                        static_cast<const uint8_t*>(a.k), a.k_ld, a.k_seq_stride, a.q_per_seq,
-                       a.n, pool, pool_ld, pool_n, scores, scores_ld, a.dev_status);
+                       a.n, pool, pool_ld, pool_n, scores, scores_ld, a.dev_status, a.pages);
 }
 
 }  // namespace csa2

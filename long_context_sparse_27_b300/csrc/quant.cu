@@ -26,8 +26,15 @@ __global__ void __launch_bounds__(kQuantThreads)
                      uint8_t* __restrict__ codes, int64_t codes_ld, uint8_t* __restrict__ scales,
                      int64_t scales_ld, const uint16_t* __restrict__ kx, int32_t di,
                      int64_t k_ld, uint8_t* __restrict__ k8, int64_t k8_ld, int64_t kv_threads,
-                     int64_t k_begin) {
+                     int64_t k_begin, const csa2_pages pages, int64_t rows_per_seq,
+                     int64_t entry0, int32_t* dev_status) {
   pdl_wait();
+  // destination row of source row r: r itself, or its entry's row in the
+  // page pool (-1: a page outside the pool, nothing written)
+  auto dst_row = [&](int64_t r) -> int64_t {
+    if (!pages.block_table) return r;
+    return paged_row(pages, r / rows_per_seq, entry0 + r % rows_per_seq, dev_status);
+  };
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid < k_begin) {
     const int64_t per_row = d / 8;
@@ -49,6 +56,8 @@ __global__ void __launch_bounds__(kQuantThreads)
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     if (!live) return;
+    const int64_t drow = dst_row(row);
+    if (drow < 0) return;
     uint32_t packed = 0, sbyte = 0;
     if (amax > 0.f) {
       int e = floor_log2_pos(amax) - 2;
@@ -58,13 +67,15 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
       for (int i = 0; i < 8; ++i) packed |= e2m1_encode(v[i] * inv) << (4 * i);
     }
-    *reinterpret_cast<uint32_t*>(codes + row * codes_ld + part * 4) = packed;
-    if ((part & 3) == 0) scales[row * scales_ld + part / 4] = (uint8_t)sbyte;
+    *reinterpret_cast<uint32_t*>(codes + drow * codes_ld + part * 4) = packed;
+    if ((part & 3) == 0) scales[drow * scales_ld + part / 4] = (uint8_t)sbyte;
   } else {
     const int64_t t = gid - k_begin;
     const int64_t per_row = di / 8;
     if (t >= rows * per_row) return;
     const int64_t row = t / per_row, part = t % per_row;
+    const int64_t drow = dst_row(row);
+    if (drow < 0) return;
     const uint4 raw = *reinterpret_cast<const uint4*>(kx + row * k_ld + part * 8);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
     uint32_t lo = 0, hi = 0;
@@ -75,7 +86,7 @@ __global__ void __launch_bounds__(kQuantThreads)
       hi |= e4m3_encode(bf16_bits_to_float(w[i + 2] & 0xFFFFu)) << (16 * i);
       hi |= e4m3_encode(bf16_bits_to_float(w[i + 2] >> 16)) << (16 * i + 8);
     }
-    *reinterpret_cast<uint2*>(k8 + row * k8_ld + part * 8) = make_uint2(lo, hi);
+    *reinterpret_cast<uint2*>(k8 + drow * k8_ld + part * 8) = make_uint2(lo, hi);
   }
 }
 
@@ -98,18 +109,7 @@ __global__ void __launch_bounds__(256)
   for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  int e = 0;
-  if (amax > 0.f) {
-    // smallest e with amax / 2^e <= 448 = 1.75 * 2^8: with amax = m 2^E
-    // (m in [1, 2)), e = E - 8 when m <= 1.75, else E - 7.
-    const int E = floor_log2_pos(amax);
-    // fraction bits of m, normalising a subnormal amax first
-    const uint32_t u = __float_as_uint(amax);
-    uint32_t frac = u & 0x7FFFFFu;
-    if (((u >> 23) & 0xFFu) == 0) frac = (frac << (__clz(frac) - 8)) & 0x7FFFFFu;
-    e = (frac <= 0x600000u) ? E - 8 : E - 7;  // 0x600000: fraction of 1.75
-    e = max(e, -126);
-  }
+  const int e = amax > 0.f ? index_q_exponent(amax) : 0;
   const float inv = exp2_int(-e);
   uint8_t out[PER];
 #pragma unroll
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-csa2_status launch_quantize_fp4(const csa2_quant_args& a, cudaStream_t s) {
+csa2_status launch_quantize_fp4(const csa2_quant_args& a, cudaStream_t s, int32_t* dev_status) {
   if (a.rows == 0) return CSA2_OK;
   const int64_t kv_threads = a.rows * (a.d / 8);
   const int64_t k_begin = (kv_threads + 31) / 32 * 32;
@@ -131,7 +131,8 @@ csa2_status launch_quantize_fp4(const csa2_quant_args& a, cudaStream_t s) {
   return launch_kernel(quant_fp4_kernel, dim3((unsigned)blocks), dim3(kQuantThreads), 0, s, 1,
                        static_cast<const uint16_t*>(a.x), a.rows, a.d, a.x_ld, a.codes,
                        a.codes_ld, a.scales, a.scales_ld, static_cast<const uint16_t*>(a.idxk),
-                       a.di, a.idxk_ld, a.idxk_e4m3, a.idxk_e4m3_ld, kv_threads, k_begin);
+                       a.di, a.idxk_ld, a.idxk_e4m3, a.idxk_e4m3_ld, kv_threads, k_begin,
+                       a.pages, a.rows_per_seq, a.entry0, dev_status);
 }
 
 csa2_status launch_quantize_index_q(const void* q, const float* w, int64_t nq, int32_t hi,

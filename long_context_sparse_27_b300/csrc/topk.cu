@@ -5,24 +5,25 @@
 // (CSA2)").  Order is (score descending, index ascending); the output row
 // holds the chosen indices ascending, padded with -1.
 //
-// Radix select on an order-preserving 32-bit key (+0 and -0 share a key),
-// one row per thread-block cluster of kTkCluster CTAs, each CTA owning a
-// contiguous chunk of the row:
-//   level 1   the row's 4096-bin histogram of the key's top 12 bits comes
-//             from global memory (topk_hist_kernel, or the indexer epilogue
-//             that produced the scores); every CTA finds the threshold bin
-//             T1 itself and keeps its entries in bins >= T1, in index order;
-//   level 2/3 if bin T1 holds more entries than are still needed, the CTAs
-//             histogram the next 12 (then 8) key bits of those entries and
-//             combine the histograms through distributed shared memory;
-//   ties      entries whose whole key equals the threshold key are taken in
-//             index order, CTA by CTA;
-//   output    each CTA learns how many entries the CTAs before it keep and
-//             writes its own ascending, so the row needs no final sort.
-// Every CTA of a cluster takes the same branches (they derive the same
-// thresholds from the same histograms), so the cluster barriers match.
-#include <cooperative_groups.h>
-
+// Radix select on an order-preserving 32-bit key (+0 and -0 share a key).
+// Level 1 is the row's 4096-bin histogram of the key's top 12 bits; it comes
+// from global memory (topk_hist_kernel, or the indexer epilogue that
+// produced the scores).  Its threshold bin T1 splits the row into entries
+// surely selected (bins above T1), candidates (bin T1) and the rest.
+//
+// Long rows (topk_scan_kernel): a row is cut into S slices, one CTA each.
+// Every CTA finds T1 from the histogram, scans its slice once and keeps the
+// entries in bins >= T1, in index order, in shared memory; with S > 1 it
+// publishes them to its slot in the workspace and the last CTA of the row to
+// finish (an atomic counter) gathers every slot.  That CTA then resolves the
+// threshold bin among the gathered entries (next 12, then 8 key bits, then
+// ties on the whole key in index order) and writes the selection ascending.
+// A slice with more kept entries than its slot holds (massive ties, sorted
+// rows) makes the last CTA run the same levels as passes over the whole row
+// in global memory instead: slower, same result.
+//
+// Short rows (topk_small_kernel, n <= 4096): one CTA per row with every key
+// in shared memory, the same levels.
 #include <mutex>
 
 #include "common.cuh"
@@ -32,27 +33,26 @@ namespace csa2 {
 
 namespace {
 
-namespace cg = cooperative_groups;
-
 constexpr int kBins = kTopkBins;    // 12-bit digits (levels 1 and 2)
 constexpr int kBins3 = 256;         // 8-bit digit (level 3)
 constexpr int kMaxK = 2048;
 constexpr int kTkThreads = 512;
 constexpr int kTkWarps = kTkThreads / 32;
-constexpr int kTkCluster = 8;       // CTAs per row (portable cluster size)
-constexpr int kLCap = 512;          // per-warp ordered list of entries in bins >= T1
-constexpr int kTkDynSmem = 2 * kTkWarps * kLCap * 4;  // keys + indices
 constexpr int kHistThreads = 512;
+constexpr int kRound = kTkThreads * 4;        // scores per round: one float4 per thread
+constexpr int kRounds = 4;                    // rounds whose loads are in flight together
+constexpr int kBatch = kRound * kRounds;      // 8192 scores per batch
+constexpr int kCandCap = 4096;                // kept entries a CTA holds in shared memory
+constexpr int kSlotCap = 1024;                // kept entries a slice may publish
+constexpr int kMaxSlices = 64;
+constexpr int kSliceTarget = 296;             // CTAs of one launch to aim for (2 per SM)
+constexpr int kSmallN = (int)kTopkShortRow;   // longest row of topk_small_kernel
+// dynamic shared memory of topk_scan_kernel: histogram | keys | indices
+constexpr int kScanSmem = (kBins + 2 * kCandCap) * 4;
 
 __device__ __forceinline__ int64_t row_nvalid(const int32_t* n_valid, int64_t row, int64_t n) {
   int64_t nv = n_valid ? (int64_t)n_valid[row] : n;
   return nv < 0 ? 0 : (nv > n ? n : nv);
-}
-
-__device__ __forceinline__ uint32_t lanemask_lt() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
 }
 
 // ---------------------------------------------------------------------------
@@ -95,17 +95,15 @@ __global__ void __launch_bounds__(kHistThreads)
 }
 
 // ---------------------------------------------------------------------------
-// selection
+// block-wide pieces of the selection (kTkThreads threads)
 // ---------------------------------------------------------------------------
 
 struct TkTmp {
-  uint32_t wsum[kTkWarps];
-  uint32_t tot[kTkCluster];
+  uint32_t wsum[kTkWarps * kRounds];
   int t;            // find_top: bin
   uint32_t above;   // find_top: entries in higher bins
-  int R;            // cluster_top: slice holding the threshold
-  uint32_t cum;     // cluster_top: entries in higher slices
-  uint32_t T, A, cnt;  // cluster_top results: bin, entries above it, entries in it
+  uint32_t total;   // scans: running count
+  uint32_t flag;
 };
 
 // Largest bin t with sum(h[t .. nb)) >= target, and above = sum(h[t+1 ..
@@ -144,99 +142,313 @@ __device__ void find_top(const uint32_t* h, int nb, uint32_t target, TkTmp* tmp)
   __syncthreads();
 }
 
-// The cluster-wide histogram is the sum of every CTA's `hist` (nb bins).
-// CTA r reduces bins [r*sl, (r+1)*sl) (sl = nb / C) into `slice`; then every
-// CTA finds the slice that holds the target-th largest entry and the bin in
-// it.  All CTAs end with the same tmp->T / A / cnt.  `hist` is overwritten.
-template <int C>
-__device__ void cluster_top(cg::cluster_group& cluster, uint32_t* hist, uint32_t* slice,
-                            uint32_t* s_tot, int nb, uint32_t target, TkTmp* tmp) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = (int)cluster.block_rank();
-  const int sl = nb / C;
-  cluster.sync();  // every CTA's histogram is complete
-  uint32_t part = 0;
-  for (int i = tid; i < sl; i += kTkThreads) {
-    uint32_t v = 0;
-#pragma unroll
-    for (int c = 0; c < C; ++c) v += *cluster.map_shared_rank(hist + r * sl + i, c);
-    slice[i] = v;
-    part += v;
+// The threshold below level 1: among the entries whose top 12 key bits equal
+// T1 (cnt1 of them), `need` more are selected.  Resolves the next 12 and 8
+// key bits through histograms built by `each` (each(f) calls f(key) for
+// every entry) and returns depth / thr: depth 1, 2, 3 -> an entry is selected
+// iff (key >> shift) > thr or == thr (shift 20, 8, 0); depth 4 -> (key > thr)
+// or (key == thr and it is among the first `need` such entries in index
+// order).  `hist` is overwritten.
+struct Threshold {
+  int depth;
+  uint32_t thr, need;
+  __device__ int shift() const { return depth == 1 ? 20 : (depth == 2 ? 8 : 0); }
+  __device__ bool sure(uint32_t key) const {
+    const uint32_t x = key >> shift();
+    return x > thr || (depth <= 3 && x == thr);
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if (lane == 0) tmp->wsum[warp] = part;
+  __device__ bool tie(uint32_t key) const { return depth == 4 && key == thr; }
+};
+
+template <class Each>
+__device__ Threshold resolve_threshold(uint32_t T1, uint32_t need, uint32_t cnt1, uint32_t* hist,
+                                       TkTmp* tmp, Each&& each) {
+  const int tid = threadIdx.x;
+  Threshold th{1, T1, need};
+  if (cnt1 == need) return th;
   __syncthreads();
-  if (tid == 0) {
-    uint32_t t = 0;
-    for (int w = 0; w < kTkWarps; ++w) t += tmp->wsum[w];
-    *s_tot = t;
-  }
-  cluster.sync();  // every slice and slice total is complete
-  if (tid < C) tmp->tot[tid] = *cluster.map_shared_rank(s_tot, tid);
+  for (int i = tid; i < kBins; i += kTkThreads) hist[i] = 0;
   __syncthreads();
-  if (tid == 0) {
-    uint32_t cum = 0;
-    int R = C - 1;
-    for (; R > 0; --R) {
-      if (cum + tmp->tot[R] >= target) break;
-      cum += tmp->tot[R];
-    }
-    tmp->R = R;
-    tmp->cum = cum;
-  }
+  each([&](uint32_t key) {
+    if ((key >> 20) == T1) atomicAdd(&hist[(key >> 8) & (kBins - 1)], 1u);
+  });
   __syncthreads();
-  const int R = tmp->R;
-  // the other CTAs no longer read this CTA's `hist`: reuse it for slice R
-  for (int i = tid; i < sl; i += kTkThreads) hist[i] = *cluster.map_shared_rank(slice + i, R);
+  find_top(hist, kBins, th.need, tmp);
+  th.need -= tmp->above;
+  th.thr = (T1 << 12) | (uint32_t)tmp->t;
+  th.depth = 2;
+  if (hist[tmp->t] == th.need) return th;
   __syncthreads();
-  find_top(hist, sl, target - tmp->cum, tmp);
-  if (tid == 0) {
-    tmp->T = (uint32_t)(R * sl + tmp->t);
-    tmp->A = tmp->cum + tmp->above;
-    tmp->cnt = hist[tmp->t];
-  }
+  for (int i = tid; i < kBins3; i += kTkThreads) hist[i] = 0;
   __syncthreads();
+  const uint32_t t12 = th.thr;
+  each([&](uint32_t key) {
+    if ((key >> 8) == t12) atomicAdd(&hist[key & (kBins3 - 1)], 1u);
+  });
+  __syncthreads();
+  find_top(hist, kBins3, th.need, tmp);
+  th.need -= tmp->above;
+  th.thr = (th.thr << 8) | (uint32_t)tmp->t;
+  th.depth = hist[tmp->t] != th.need ? 4 : 3;
+  __syncthreads();
+  return th;
 }
 
-template <int C>
-__global__ void __launch_bounds__(kTkThreads, 1)
-    topk_select_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
-                       const int32_t* __restrict__ n_valid, int32_t k,
-                       uint32_t* __restrict__ hist1, int32_t* __restrict__ idx_out,
-                       int64_t idx_ld, int vec, const int32_t* __restrict__ remap,
-                       int64_t remap_ld, int clear) {
-  cg::cluster_group cluster = cg::this_cluster();
-  extern __shared__ __align__(16) uint8_t dyn[];
-  uint32_t* lkey = reinterpret_cast<uint32_t*>(dyn);
-  int32_t* lj = reinterpret_cast<int32_t*>(dyn + kTkWarps * kLCap * 4);
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t slice[kBins / C];
+// Scores [j0, j1) of row s in index order, kBatch at a time (each thread a
+// float4 per round, the rounds' loads in flight together).  cls(key, j)
+// returns 0 (skip), 1 (take) or 2 (a tie: taken while fewer than `quota`
+// ties precede it in index order).  emit(pos, key, j) receives every taken
+// entry with its rank among taken entries.  Returns the number taken.
+// Block-wide (every thread calls it with the same arguments).
+template <class Cls, class Emit>
+__device__ uint32_t ordered_take(const float* __restrict__ s, int64_t j0, int64_t j1, int vec,
+                                 uint32_t quota, TkTmp* tmp, Cls&& cls, Emit&& emit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t taken1 = 0, ties = 0;  // block-uniform: class-1 entries and ties of earlier batches
+  for (int64_t b0 = j0; b0 < j1; b0 += kBatch) {
+    float4 x[kRounds];
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const int64_t j = b0 + (int64_t)u * kRound + tid * 4;
+      if (vec && j + 3 < j1) {
+        x[u] = __ldcs(reinterpret_cast<const float4*>(s + j));
+      } else {
+        x[u].x = j < j1 ? s[j] : 0.f;
+        x[u].y = j + 1 < j1 ? s[j + 1] : 0.f;
+        x[u].z = j + 2 < j1 ? s[j + 2] : 0.f;
+        x[u].w = j + 3 < j1 ? s[j + 3] : 0.f;
+      }
+    }
+    uint32_t c[kRounds], incl[kRounds];
+    uint32_t cl[kRounds];  // 2 bits per element: its class
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const int64_t j = b0 + (int64_t)u * kRound + tid * 4;
+      const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+      uint32_t packed = 0, cnt = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t k2 = (j + e < j1) ? cls(score_key(xv[e]), j + e) : 0u;
+        packed |= k2 << (2 * e);
+        cnt += (k2 == 1u) + ((k2 == 2u) << 16);  // low half: takes, high half: ties
+      }
+      cl[u] = packed;
+      c[u] = cnt;
+      uint32_t v = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      incl[u] = v;
+      if (lane == 31) tmp->wsum[u * kTkWarps + warp] = v;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // exclusive prefix over (round, warp) in index order; ties are capped
+      // by the quota only when positions are assigned below
+      uint32_t v[kRounds * kTkWarps / 32];
+      uint32_t run = 0;
+#pragma unroll
+      for (int i = 0; i < kRounds * kTkWarps / 32; ++i) {
+        const uint32_t w = tmp->wsum[i * 32 + lane];
+        uint32_t sc = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, sc, o);
+          if (lane >= o) sc += y;
+        }
+        v[i] = run + sc - w;
+        run += __shfl_sync(0xffffffffu, sc, 31);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < kRounds * kTkWarps / 32; ++i) tmp->wsum[i * 32 + lane] = v[i];
+      if (lane == 0) tmp->total = run;
+    }
+    __syncthreads();
+    const uint32_t batch_total = tmp->total;
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      if (__ballot_sync(0xffffffffu, c[u] != 0) == 0) continue;
+      // rank among taken entries: class-1 entries before it plus the ties
+      // before it, capped by the quota
+      const uint32_t before = tmp->wsum[u * kTkWarps + warp] + incl[u] - c[u];
+      uint32_t t_before = ties + (before >> 16);
+      uint32_t c1 = taken1 + (before & 0xFFFFu);
+      const int64_t j = b0 + (int64_t)u * kRound + tid * 4;
+      const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t k2 = (cl[u] >> (2 * e)) & 3u;
+        if (k2 == 1u || (k2 == 2u && t_before < quota))
+          emit(c1 + min(t_before, quota), score_key(xv[e]), j + e);
+        c1 += k2 == 1u;
+        t_before += k2 == 2u;
+      }
+    }
+    taken1 += batch_total & 0xFFFFu;
+    ties += batch_total >> 16;
+    __syncthreads();  // tmp->wsum is rewritten by the next batch
+  }
+  return taken1 + min(ties, quota);
+}
+
+// Every key of the row, in any order (histogram passes of the fallback).
+template <class F>
+__device__ __forceinline__ void for_each_key(const float* __restrict__ s, int64_t nv, int vec,
+                                             const F& f) {
+  const int tid = threadIdx.x;
+  for (int64_t b0 = 0; b0 < nv; b0 += kBatch) {
+    float4 x[kRounds];
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const int64_t j = b0 + (int64_t)u * kRound + tid * 4;
+      if (vec && j + 3 < nv) {
+        x[u] = __ldcs(reinterpret_cast<const float4*>(s + j));
+      } else {
+        x[u].x = j < nv ? s[j] : 0.f;
+        x[u].y = j + 1 < nv ? s[j + 1] : 0.f;
+        x[u].z = j + 2 < nv ? s[j + 2] : 0.f;
+        x[u].w = j + 3 < nv ? s[j + 3] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const int64_t j = b0 + (int64_t)u * kRound + tid * 4;
+      if (j < nv) f(score_key(x[u].x));
+      if (j + 1 < nv) f(score_key(x[u].y));
+      if (j + 2 < nv) f(score_key(x[u].z));
+      if (j + 3 < nv) f(score_key(x[u].w));
+    }
+  }
+}
+
+// Writes the entries of key[0..nc) (positions in index order) that `th`
+// selects, ascending by position, as map(position) to o[0..m), and -1 to
+// o[m..k).  Thread t owns positions [t * per, (t + 1) * per).
+// expand = G > 0: each selected position p goes out as the G entries p * G
+// + t (t < G; -1 from expand_n on) in slots pos * G + t; o holds k * G slots.
+template <class Map>
+__device__ void write_selected(const uint32_t* key, int nc, const Threshold& th, uint32_t m,
+                               int32_t k, int32_t* o, TkTmp* tmp, Map&& map, int32_t expand = 0,
+                               int64_t expand_n = 0) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (nc + kTkThreads - 1) / kTkThreads;
+  const int i0 = min(nc, tid * per), i1 = min(nc, i0 + per);
+  uint32_t g = 0, t = 0;
+  for (int i = i0; i < i1; ++i) {
+    g += th.sure(key[i]);
+    t += th.tie(key[i]);
+  }
+  uint32_t ig = g, it = t;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t vg = __shfl_up_sync(0xffffffffu, ig, d);
+    const uint32_t vt = __shfl_up_sync(0xffffffffu, it, d);
+    if (lane >= d) {
+      ig += vg;
+      it += vt;
+    }
+  }
+  __syncthreads();
+  if (lane == 31) {
+    tmp->wsum[warp] = ig;
+    tmp->wsum[kTkWarps + warp] = it;
+  }
+  __syncthreads();
+  uint32_t bg = 0, bt = 0;
+  for (int w = 0; w < warp; ++w) {
+    bg += tmp->wsum[w];
+    bt += tmp->wsum[kTkWarps + w];
+  }
+  uint32_t tpre = bt + it - t;
+  uint32_t pos = bg + ig - g + min(tpre, th.need);
+  for (int i = i0; i < i1; ++i) {
+    bool sel = th.sure(key[i]);
+    if (!sel && th.tie(key[i])) sel = tpre++ < th.need;
+    if (sel) {
+      if (pos < m) {
+        if (expand > 0) {
+          const int64_t e0 = (int64_t)map(i) * expand;
+          for (int t = 0; t < expand; ++t)
+            o[(int64_t)pos * expand + t] = e0 + t < expand_n ? (int32_t)(e0 + t) : -1;
+        } else {
+          o[pos] = map(i);
+        }
+      }
+      ++pos;
+    }
+  }
+  const int64_t per_slot = expand > 0 ? expand : 1;
+  for (int64_t i = (int64_t)m * per_slot + tid; i < (int64_t)k * per_slot; i += kTkThreads)
+    o[i] = -1;
+}
+
+// ---------------------------------------------------------------------------
+// long rows
+// ---------------------------------------------------------------------------
+
+// Workspace of a long-row selection: per row its level-1 histogram, a
+// counter (the slices done) and S slots of (count, kSlotCap keys, kSlotCap
+// indices).
+struct ScanLayout {
+  int64_t rows;
+  int S;
+  __host__ __device__ size_t hist_bytes() const { return (size_t)rows * kBins * 4; }
+  __host__ __device__ size_t counter_off() const { return hist_bytes(); }
+  __host__ __device__ size_t slot_off() const {
+    return align256_hd(counter_off() + (size_t)rows * 16);
+  }
+  static constexpr size_t kSlotBytes = 16 + (size_t)kSlotCap * 8;
+  __host__ __device__ size_t total() const {
+    return S > 0 ? slot_off() + (size_t)rows * S * kSlotBytes : hist_bytes();
+  }
+  __host__ __device__ static size_t align256_hd(size_t x) { return (x + 255) & ~(size_t)255; }
+};
+
+// Slices per row: about kSliceTarget CTAs per launch, each slice at least a
+// batch, at most kMaxSlices.  0 for short rows.
+int scan_slices(int64_t rows, int64_t n) {
+  if (n <= kSmallN || rows <= 0) return 0;
+  const int64_t want = (kSliceTarget + rows - 1) / rows;
+  const int64_t most = std::min<int64_t>(kMaxSlices, (n + kBatch - 1) / kBatch);
+  return (int)std::max<int64_t>(1, std::min(want, most));
+}
+
+__global__ void __launch_bounds__(kTkThreads, 2)
+    topk_scan_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
+                     const int32_t* __restrict__ n_valid, int32_t k,
+                     uint32_t* __restrict__ hist1, uint32_t* __restrict__ counters,
+                     uint8_t* __restrict__ slots, int S, int64_t slice,
+                     int32_t* __restrict__ idx_out, int64_t idx_ld, int vec,
+                     const int32_t* __restrict__ remap, int64_t remap_ld, int clear) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  uint32_t* hist = dyn;                                     // [kBins]
+  uint32_t* ckey = dyn + kBins;                             // [kCandCap] kept keys
+  int32_t* cidx = reinterpret_cast<int32_t*>(dyn + kBins + kCandCap);  // their indices
   __shared__ TkTmp tmp;
-  __shared__ uint32_t s_tot, s_gt, s_tie, s_off, s_quota;
-  __shared__ uint32_t wgt[kTkWarps], wtie[kTkWarps];
+  __shared__ uint32_t s_last, s_base[kMaxSlices + 1];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();
-  const int r = (int)cluster.block_rank();
-  const int64_t row = blockIdx.x / C;
+  const int64_t row = blockIdx.x / S;
+  const int sl = (int)(blockIdx.x % S);
   const int64_t nv = row_nvalid(n_valid, row, n);
+  const uint32_t m = (uint32_t)(nv < (int64_t)k ? nv : (int64_t)k);
   int32_t* out = idx_out + row * idx_ld;
-  // The row's histogram goes back to zero once read (unless the caller
-  // selects from it again), ready for the next selection that uses the same
-  // workspace: CTA r clears bins r*512 .. (after every CTA has read them).
-  // With `remap`, entry j of the row stands for remap[row * remap_ld + j]
-  // (its position in a candidate pool) and that is what is written.
   uint32_t* hrow = hist1 + row * kBins;
   const int32_t* rmap = remap ? remap + row * remap_ld : nullptr;
-  if (nv <= k) {  // every visible entry is selected (the whole cluster returns here)
-    for (int64_t i = (int64_t)r * kTkThreads + tid; i < k; i += (int64_t)C * kTkThreads)
-      out[i] = i < nv ? (rmap ? rmap[i] : (int32_t)i) : -1;
-    if (clear)
-      for (int i = tid; i < kBins / C; i += kTkThreads) hrow[r * (kBins / C) + i] = 0;
+  const float* s = scores + row * ld;
+  if (nv <= k) {  // every visible entry is selected; slice 0 writes the row
+    if (sl == 0) {
+      for (int64_t i = tid; i < k; i += kTkThreads)
+        out[i] = i < nv ? (rmap ? rmap[i] : (int32_t)i) : -1;
+      if (clear)
+        for (int i = tid; i < kBins; i += kTkThreads) hrow[i] = 0;
+    }
     return;
   }
-  const float* s = scores + row * ld;
 
   // ---- level 1: threshold bin from the row's histogram (all loads in flight)
   {
@@ -247,219 +459,148 @@ __global__ void __launch_bounds__(kTkThreads, 1)
     for (int u = 0; u < kBins / kTkThreads; ++u) hist[tid + u * kTkThreads] = hv[u];
   }
   __syncthreads();
-  find_top(hist, kBins, (uint32_t)k, &tmp);
+  find_top(hist, kBins, m, &tmp);
   const uint32_t T1 = (uint32_t)tmp.t;
-  uint32_t need = (uint32_t)k - tmp.above;
+  const uint32_t need = m - tmp.above;
   const uint32_t cnt1 = hist[T1];
 
-  // ---- this CTA's chunk; warp w scans its contiguous segment in order and
-  // keeps (key, index) of every entry in a bin >= T1
-  const int64_t chunk = (((nv + C - 1) / C) + 31) & ~(int64_t)31;
-  const int64_t j0 = min(nv, (int64_t)r * chunk), j1 = min(nv, j0 + chunk);
-  const int64_t seg = (((chunk + kTkWarps - 1) / kTkWarps) + 31) & ~(int64_t)31;
-  const int64_t wj0 = min(j1, j0 + warp * seg), wj1 = min(j1, wj0 + seg);
-  uint32_t* mykey = lkey + warp * kLCap;
-  int32_t* myj = lj + warp * kLCap;
-  uint32_t cnt = 0;
-  {
-    constexpr int U = 8;  // 8 x 4 scores per lane in flight
-    for (int64_t base = wj0; base < wj1; base += 128 * U) {
-      float4 x[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t j = base + u * 128 + lane * 4;
-        if (vec && j + 3 < wj1) {
-          x[u] = __ldcs(reinterpret_cast<const float4*>(s + j));
-        } else {
-          x[u].x = j < wj1 ? s[j] : 0.f;
-          x[u].y = j + 1 < wj1 ? s[j + 1] : 0.f;
-          x[u].z = j + 2 < wj1 ? s[j + 2] : 0.f;
-          x[u].w = j + 3 < wj1 ? s[j + 3] : 0.f;
+  // ---- this slice: keep (key, index) of every entry in a bin >= T1
+  const int64_t j0 = min(nv, (int64_t)sl * slice), j1 = min(nv, j0 + slice);
+  const uint32_t kept = ordered_take(
+      s, j0, j1, vec, 0u, &tmp, [&](uint32_t key, int64_t) { return (key >> 20) >= T1 ? 1u : 0u; },
+      [&](uint32_t pos, uint32_t key, int64_t j) {
+        if (pos < (uint32_t)kCandCap) {
+          ckey[pos] = key;
+          cidx[pos] = (int32_t)j;
         }
+      });
+  __syncthreads();
+
+  bool overflow;
+  int nc;
+  if (S == 1) {
+    overflow = kept > (uint32_t)kCandCap;
+    nc = (int)min(kept, (uint32_t)kCandCap);
+  } else {
+    // publish this slice's entries, then count the slice as done; the last
+    // slice of the row to finish gathers every slot
+    uint8_t* slot = slots + ((size_t)row * S + sl) * ScanLayout::kSlotBytes;
+    const uint32_t np = min(kept, (uint32_t)kSlotCap);
+    uint32_t* sk = reinterpret_cast<uint32_t*>(slot + 16);
+    int32_t* sj = reinterpret_cast<int32_t*>(slot + 16 + (size_t)kSlotCap * 4);
+    for (uint32_t i = tid; i < np; i += kTkThreads) {
+      sk[i] = ckey[i];
+      sj[i] = cidx[i];
+    }
+    if (tid == 0) *reinterpret_cast<uint32_t*>(slot) = kept;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&counters[row * 4], 1u) == (uint32_t)(S - 1);
+    __syncthreads();
+    if (!s_last) {
+      pdl_trigger();
+      return;
+    }
+    __threadfence();
+    // slot counts -> offsets (slice order = index order): warp 0 loads every
+    // count at once (two per lane) and scans them
+    if (warp == 0) {
+      uint32_t cnt[2], ovf = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        cnt[h] = c < S ? __ldcg(reinterpret_cast<const uint32_t*>(
+                             slots + ((size_t)row * S + c) * ScanLayout::kSlotBytes))
+                       : 0u;
+        ovf |= cnt[h] > (uint32_t)kSlotCap;
       }
+      uint32_t run = 0;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t j = base + u * 128 + lane * 4;
-        const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-        uint32_t key[4];
-        bool p[4];
-        uint32_t c = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          key[e] = score_key(xv[e]);
-          p[e] = (j + e < wj1) && (key[e] >> 20) >= T1;
-          c += p[e];
-        }
-        // most steps hold no entry in the top bins: skip the lane scan
-        if (__ballot_sync(0xffffffffu, c != 0) == 0) continue;
-        uint32_t incl = c;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t incl = cnt[h];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
-        uint32_t pos = cnt + incl - c;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (p[e]) {
-            if (pos < (uint32_t)kLCap) {
-              mykey[pos] = key[e];
-              myj[pos] = (int32_t)(j + e);
-            }
-            ++pos;
-          }
-        cnt += __shfl_sync(0xffffffffu, incl, 31);
+        const int c = lane + 32 * h;
+        if (c < S) s_base[c] = run + incl - cnt[h];
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      ovf = __any_sync(0xffffffffu, ovf != 0);
+      if (lane == 0) {
+        s_base[S] = run;
+        tmp.flag = ovf || run > (uint32_t)kCandCap;
+        counters[row * 4] = 0;  // ready for the next selection on this workspace
       }
     }
-  }
-  // A warp whose list overflowed re-reads its segment instead (rare: it needs
-  // more than kLCap entries in the top bins of one segment).
-  const bool ovf = cnt > (uint32_t)kLCap;
-  // f(key, index, valid) over the warp's kept entries in index order; all
-  // lanes take the same number of steps.
-  auto walk = [&](auto&& f) {
-    if (!ovf) {
-      for (uint32_t base = 0; base < cnt; base += 32) {
-        const uint32_t i = base + lane;
-        const bool v = i < cnt;
-        f(v ? mykey[i] : 0u, v ? myj[i] : 0, v);
-      }
-    } else {
-      for (int64_t base = wj0; base < wj1; base += 32) {
-        const int64_t j = base + lane;
-        bool v = j < wj1;
-        const uint32_t key = v ? score_key(s[j]) : 0u;
-        v = v && (key >> 20) >= T1;
-        f(key, (int32_t)j, v);
+    __syncthreads();
+    overflow = tmp.flag != 0;
+    nc = (int)s_base[S];
+    if (!overflow) {
+      // warp w gathers slots w, w + 16, ..: their loads are in flight together
+      for (int c = warp; c < S; c += kTkWarps) {
+        const uint32_t b = s_base[c], cnt = s_base[c + 1] - b;
+        const uint8_t* sc = slots + ((size_t)row * S + c) * ScanLayout::kSlotBytes;
+        const uint32_t* sk2 = reinterpret_cast<const uint32_t*>(sc + 16);
+        const int32_t* sj2 = reinterpret_cast<const int32_t*>(sc + 16 + (size_t)kSlotCap * 4);
+        for (uint32_t i = lane; i < cnt; i += 32) {
+          ckey[b + i] = __ldcg(sk2 + i);
+          cidx[b + i] = __ldcg(sj2 + i);
+        }
       }
     }
-  };
-  __syncwarp();
-
-  // ---- levels 2 and 3 (only while the threshold bin holds surplus entries)
-  int depth = 1;        // key digits resolved: 1 -> 12 bits, 2 -> 24, 3/4 -> 32
-  uint32_t thr = T1;    // threshold key prefix
-  if (cnt1 != need) {
     __syncthreads();
-    for (int i = tid; i < kBins; i += kTkThreads) hist[i] = 0;
-    __syncthreads();
-    walk([&](uint32_t key, int32_t, bool v) {
-      if (v && (key >> 20) == T1) atomicAdd(&hist[(key >> 8) & (kBins - 1)], 1u);
-    });
-    __syncthreads();
-    cluster_top<C>(cluster, hist, slice, &s_tot, kBins, need, &tmp);
-    need -= tmp.A;
-    depth = 2;
-    thr = (T1 << 12) | tmp.T;
-    if (tmp.cnt != need) {
-      for (int i = tid; i < kBins3; i += kTkThreads) hist[i] = 0;
-      __syncthreads();
-      const uint32_t t12 = thr;
-      walk([&](uint32_t key, int32_t, bool v) {
-        if (v && (key >> 8) == t12) atomicAdd(&hist[key & (kBins3 - 1)], 1u);
-      });
-      __syncthreads();
-      cluster_top<C>(cluster, hist, slice, &s_tot, kBins3, need, &tmp);
-      need -= tmp.A;
-      thr = (thr << 8) | tmp.T;
-      depth = tmp.cnt != need ? 4 : 3;
-    }
   }
-  const int shift = depth == 1 ? 20 : (depth == 2 ? 8 : 0);
-  // g: kept for sure; t: a tie on the full key, kept in index order up to `need`
-  auto is_g = [&](uint32_t key) {
-    return (key >> shift) > thr || (depth <= 3 && (key >> shift) == thr);
-  };
-  auto is_t = [&](uint32_t key) { return depth == 4 && key == thr; };
-
-  // ---- counts, offsets, output
-  uint32_t ng = 0, nt = 0;
-  walk([&](uint32_t key, int32_t, bool v) {
-    ng += __popc(__ballot_sync(0xffffffffu, v && is_g(key)));
-    nt += __popc(__ballot_sync(0xffffffffu, v && is_t(key)));
-  });
-  if (lane == 0) {
-    wgt[warp] = ng;
-    wtie[warp] = nt;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t g = 0, t = 0;
-    for (int w = 0; w < kTkWarps; ++w) {
-      g += wgt[w];
-      t += wtie[w];
-    }
-    s_gt = g;
-    s_tie = t;
-  }
-  cluster.sync();  // every CTA's counts are visible
-  if (tid < C) {  // every CTA's counts, one remote load per thread
-    tmp.tot[tid] = *cluster.map_shared_rank(&s_gt, tid);
-    tmp.wsum[tid] = *cluster.map_shared_rank(&s_tie, tid);
-  }
-  cluster.sync();  // no CTA reads another's shared memory after this point
-  // every CTA read the row's histogram at its start: clear this CTA's share
-  if (clear)
-    for (int i = tid; i < kBins / C; i += kTkThreads) hrow[r * (kBins / C) + i] = 0;
-  if (tid == 0) {
-    uint32_t pre_sel = 0, pre_tie = 0;
-    for (int c = 0; c < r; ++c) {
-      const uint32_t qc = min(tmp.wsum[c], need > pre_tie ? need - pre_tie : 0u);
-      pre_tie += tmp.wsum[c];
-      pre_sel += tmp.tot[c] + qc;
-    }
-    s_quota = min(s_tie, need > pre_tie ? need - pre_tie : 0u);
-    s_off = pre_sel;
-  }
-  __syncthreads();
-  uint32_t woff = s_off, tq = s_quota;
-  for (int w = 0; w < warp; ++w) {
-    const uint32_t qw = min(wtie[w], tq);
-    tq -= qw;
-    woff += wgt[w] + qw;
-  }
-  const uint32_t myq = min(wtie[warp], tq);
   pdl_trigger();
-  uint32_t run_sel = 0, run_tie = 0;
-  const uint32_t lt = lanemask_lt();
-  walk([&](uint32_t key, int32_t j, bool v) {
-    const bool g = v && is_g(key);
-    const bool t = v && is_t(key);
-    const uint32_t tm = __ballot_sync(0xffffffffu, t);
-    const bool sel = g || (t && run_tie + __popc(tm & lt) < myq);
-    const uint32_t sm = __ballot_sync(0xffffffffu, sel);
-    const uint32_t pos = woff + run_sel + __popc(sm & lt);
-    if (sel && pos < (uint32_t)k) out[pos] = rmap ? rmap[j] : j;
-    run_sel += __popc(sm);
-    run_tie += __popc(tm);
-  });
+
+  if (!overflow) {
+    // every entry of bins >= T1 is in shared memory, in index order
+    const Threshold th = resolve_threshold(T1, need, cnt1, hist, &tmp, [&](const auto& f) {
+      for (int i = tid; i < nc; i += kTkThreads) f(ckey[i]);
+    });
+    write_selected(ckey, nc, th, m, k, out, &tmp,
+                   [&](int i) { return rmap ? rmap[cidx[i]] : cidx[i]; });
+  } else {
+    // some slice kept more than its slot: the same levels over the whole row
+    const Threshold th = resolve_threshold(T1, need, cnt1, hist, &tmp, [&](const auto& f) {
+      for_each_key(s, nv, vec, f);
+    });
+    const uint32_t taken = ordered_take(
+        s, 0, nv, vec, th.need, &tmp,
+        [&](uint32_t key, int64_t) { return th.sure(key) ? 1u : (th.tie(key) ? 2u : 0u); },
+        [&](uint32_t pos, uint32_t, int64_t j) {
+          if (pos < m) out[pos] = rmap ? rmap[j] : (int32_t)j;
+        });
+    (void)taken;
+    for (int i = (int)m + tid; i < k; i += kTkThreads) out[i] = -1;
+  }
+  if (clear)  // every slice read the histogram before counting itself done
+    for (int i = tid; i < kBins; i += kTkThreads) hrow[i] = 0;
 }
 
 // ---------------------------------------------------------------------------
 // short rows (a candidate pool): one CTA per row, every key in shared memory
 
-constexpr int kSmallN = 4096;  // longest row
-
 // Row r of n <= kSmallN values (the first n_valid[r] of them when n_valid
 // is given): value i is scores[r * ld + i], or with `gather` scores[r * ld +
 // gather[r * gather_ld + i]] (an index < 0 is an empty slot, below every
-// value).  The k largest (value descending, position
-// ascending) are written ascending by position to out[r * out_ld ..] as
-// remap[r * remap_ld + i] (remap may be null: i), padded with -1.  The
-// same radix select as topk_select_kernel, on one CTA: 12 / 12 / 8-bit
-// digits, then ties on the whole key in position order.
+// value).  The k largest (value descending, position ascending) are written
+// ascending by position to out[r * out_ld ..] as remap[r * remap_ld + i]
+// (remap may be null: i), padded with -1.  The same levels as the long
+// rows: 12 / 12 / 8-bit digits, then ties on the whole key in position order.
 __global__ void __launch_bounds__(kTkThreads)
     topk_small_kernel(const float* __restrict__ scores, int64_t ld,
                       const int32_t* __restrict__ gather, int64_t gather_ld, int32_t n_row,
                       const int32_t* __restrict__ n_valid, int32_t k,
                       const int32_t* __restrict__ remap, int64_t remap_ld,
-                      int32_t* __restrict__ out, int64_t out_ld) {
+                      int32_t* __restrict__ out, int64_t out_ld, int32_t expand,
+                      int64_t expand_n) {
   __shared__ uint32_t key[kSmallN];
   __shared__ uint32_t hist[kBins];
   __shared__ TkTmp tmp;
-  __shared__ uint32_t wg[kTkWarps], wt[kTkWarps];
   pdl_wait();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int64_t row = blockIdx.x;
   const int n = (int)row_nvalid(n_valid, row, n_row);  // positions >= n_valid[row] do not exist
   const float* s = scores + row * ld;
@@ -480,103 +621,40 @@ __global__ void __launch_bounds__(kTkThreads)
     atomicAdd(&hist[kk >> 20], 1u);
   }
   __syncthreads();
-  const int m = min(k, n);
+  const uint32_t m = (uint32_t)min(k, n);
   if (m == 0) {  // an empty row (the whole CTA returns here)
-    for (int i = tid; i < k; i += kTkThreads) o[i] = -1;
+    const int64_t slots = (int64_t)k * (expand > 0 ? expand : 1);
+    for (int64_t i = tid; i < slots; i += kTkThreads) o[i] = -1;
     return;
   }
-  // threshold: depth 1 (12 bits), 2 (24), 3 (32) or 4 (32 bits, ties)
-  find_top(hist, kBins, (uint32_t)m, &tmp);
-  uint32_t thr = (uint32_t)tmp.t;
-  uint32_t need = (uint32_t)m - tmp.above;
-  uint32_t cnt = hist[thr];
-  int depth = 1;
-  if (cnt != need) {
-    __syncthreads();
-    for (int i = tid; i < kBins; i += kTkThreads) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += kTkThreads)
-      if ((key[i] >> 20) == thr) atomicAdd(&hist[(key[i] >> 8) & (kBins - 1)], 1u);
-    __syncthreads();
-    find_top(hist, kBins, need, &tmp);
-    need -= tmp.above;
-    thr = (thr << 12) | (uint32_t)tmp.t;
-    cnt = hist[tmp.t];
-    depth = 2;
-    if (cnt != need) {
-      __syncthreads();
-      for (int i = tid; i < kBins3; i += kTkThreads) hist[i] = 0;
-      __syncthreads();
-      for (int i = tid; i < n; i += kTkThreads)
-        if ((key[i] >> 8) == thr) atomicAdd(&hist[key[i] & (kBins3 - 1)], 1u);
-      __syncthreads();
-      find_top(hist, kBins3, need, &tmp);
-      need -= tmp.above;
-      thr = (thr << 8) | (uint32_t)tmp.t;
-      cnt = hist[tmp.t];
-      depth = cnt != need ? 4 : 3;
-    }
-  }
-  const int shift = depth == 1 ? 20 : (depth == 2 ? 8 : 0);
-  // thread t owns positions [t * per, (t + 1) * per): counts, then offsets
-  const int per = (n + kTkThreads - 1) / kTkThreads;
-  const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
-  uint32_t g = 0, t = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t x = key[i] >> shift;
-    g += x > thr || (depth <= 3 && x == thr);
-    t += depth == 4 && key[i] == thr;
-  }
-  // block-wide exclusive scans of g and t
-  uint32_t ig = g, it = t;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint32_t vg = __shfl_up_sync(0xffffffffu, ig, d);
-    const uint32_t vt = __shfl_up_sync(0xffffffffu, it, d);
-    if (lane >= d) {
-      ig += vg;
-      it += vt;
-    }
-  }
-  if (lane == 31) {
-    wg[warp] = ig;
-    wt[warp] = it;
-  }
-  __syncthreads();
-  uint32_t bg = 0, bt = 0;
-  for (int w = 0; w < warp; ++w) {
-    bg += wg[w];
-    bt += wt[w];
-  }
-  uint32_t gpre = bg + ig - g, tpre = bt + it - t;  // before this thread's range
-  // ties before this range taken (at most need), so positions before it
-  uint32_t pos = gpre + min(tpre, need);
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t x = key[i] >> shift;
-    bool sel = x > thr || (depth <= 3 && x == thr);
-    if (!sel && depth == 4 && key[i] == thr) sel = tpre++ < need;
-    if (sel) {
-      if (pos < (uint32_t)m) o[pos] = rm ? rm[i] : i;
-      ++pos;
-    }
-  }
+  find_top(hist, kBins, m, &tmp);
+  const uint32_t T1 = (uint32_t)tmp.t;
+  const uint32_t need = m - tmp.above;
+  const uint32_t cnt1 = hist[T1];
+  const Threshold th = resolve_threshold(T1, need, cnt1, hist, &tmp, [&](const auto& f) {
+    for (int i = tid; i < n; i += kTkThreads) f(key[i]);
+  });
   pdl_trigger();
-  for (int i = m + tid; i < k; i += kTkThreads) o[i] = -1;
+  write_selected(key, n, th, m, k, o, &tmp, [&](int i) { return rm ? rm[i] : i; }, expand,
+                 expand_n);
 }
 
-std::atomic<uint64_t> g_select_attr{0};  // devices on which the selector's attributes are set
+std::atomic<uint64_t> g_scan_attr{0};  // devices on which the scan kernel's attributes are set
 
 }  // namespace
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n, int32_t k) {
-  (void)n;
   (void)k;
-  return (size_t)rows * kBins * sizeof(uint32_t);
+  ScanLayout L{rows, scan_slices(rows, n)};
+  return L.total();
 }
 
-csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, cudaStream_t s) {
+csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, int64_t n, cudaStream_t s) {
   if (rows == 0) return CSA2_OK;
-  cudaError_t e = cudaMemsetAsync(hist1, 0, (size_t)rows * kBins * sizeof(uint32_t), s);
+  ScanLayout L{rows, scan_slices(rows, n)};
+  // the histograms and (long rows) the per-row counters start at zero
+  const size_t bytes = L.S > 0 ? L.slot_off() : L.hist_bytes();
+  cudaError_t e = cudaMemsetAsync(hist1, 0, bytes, s);
   return e == cudaSuccess ? CSA2_OK : cuda_fail(e);
 }
 
@@ -585,25 +663,33 @@ csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int
                                int32_t* idx_out, int64_t idx_ld, cudaStream_t s,
                                const int32_t* remap, int64_t remap_ld, bool clear_hist) {
   if (rows == 0) return CSA2_OK;
-  cudaError_t e = once_per_device(g_select_attr, [] {
-    return cudaFuncSetAttribute(topk_select_kernel<kTkCluster>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kTkDynSmem);
+  ScanLayout L{rows, scan_slices(rows, n)};
+  if (L.S == 0) return CSA2_ERR_UNSUPPORTED;  // short rows take topk_small_kernel
+  cudaError_t e = once_per_device(g_scan_attr, [] {
+    return cudaFuncSetAttribute(topk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kScanSmem);
   });
   if (e != cudaSuccess) return cuda_fail(e);
   const int vec = (ld % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) % 16) == 0) ? 1 : 0;
-  return launch_kernel(topk_select_kernel<kTkCluster>, dim3((unsigned)(rows * kTkCluster)),
-                       dim3(kTkThreads), (size_t)kTkDynSmem, s, kTkCluster, scores, n, ld, n_valid,
-                       k, hist1, idx_out, idx_ld, vec, remap, remap_ld, clear_hist ? 1 : 0);
+  // slices are whole rounds long, so every float4 of a slice is aligned
+  const int64_t per = (n + L.S - 1) / L.S;
+  const int64_t slice = (per + kRound - 1) / kRound * kRound;
+  uint8_t* base = reinterpret_cast<uint8_t*>(hist1);
+  return launch_kernel(topk_scan_kernel, dim3((unsigned)(rows * L.S)), dim3(kTkThreads),
+                       (size_t)kScanSmem, s, 1, scores, n, ld, n_valid, k, hist1,
+                       reinterpret_cast<uint32_t*>(base + L.counter_off()), base + L.slot_off(),
+                       L.S, slice, idx_out, idx_ld, vec, remap, remap_ld, clear_hist ? 1 : 0);
 }
 
 csa2_status launch_topk_small(const float* scores, int64_t ld, const int32_t* gather,
                               int64_t gather_ld, int64_t rows, int32_t n, const int32_t* n_valid,
                               int32_t k, const int32_t* remap, int64_t remap_ld, int32_t* idx_out,
-                              int64_t idx_ld, cudaStream_t s) {
+                              int64_t idx_ld, cudaStream_t s, int32_t expand, int64_t expand_n) {
   if (rows == 0) return CSA2_OK;
-  if (n < 0 || n > kSmallN || k < 1 || k > kMaxK) return CSA2_ERR_UNSUPPORTED;
+  if (n < 0 || n > kSmallN || k < 1 || k > kMaxK || expand < 0) return CSA2_ERR_UNSUPPORTED;
   return launch_kernel(topk_small_kernel, dim3((unsigned)rows), dim3(kTkThreads), 0, s, 1, scores,
-                       ld, gather, gather_ld, n, n_valid, k, remap, remap_ld, idx_out, idx_ld);
+                       ld, gather, gather_ld, n, n_valid, k, remap, remap_ld, idx_out, idx_ld,
+                       expand, expand_n);
 }
 
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
@@ -628,7 +714,7 @@ csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld
     return launch_topk_small(scores, ld, nullptr, 0, rows, (int32_t)n, n_valid, k, nullptr, 0,
                              idx_out, idx_ld, s);
   uint32_t* hist1 = static_cast<uint32_t*>(ws);
-  csa2_status st = clear_topk_hist(hist1, rows, s);
+  csa2_status st = clear_topk_hist(hist1, rows, n, s);
   if (st != CSA2_OK) return st;
   if ((st = launch_topk_hist(scores, rows, n, ld, n_valid, hist1, s)) != CSA2_OK) return st;
   return launch_topk_select(scores, rows, n, ld, n_valid, k, hist1, idx_out, idx_ld, s);

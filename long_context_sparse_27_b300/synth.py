@@ -50,6 +50,9 @@ class Workload:
     modes: tuple      # static layer schedule
     pos0: int = -1    # prefill: absolute token position of the first query
     pool: int = 0     # Hierarchical Sparse Indexer candidate pool (0 = off)
+    page_rows: int = 0  # paged caches: entries per page (0 = contiguous caches)
+    block: int = 0        # block-level pruning: entries per block (0 = off)
+    blocks_kept: int = 0  # blocks a Full layer keeps
 
     @property
     def nq(self):
@@ -81,12 +84,37 @@ C1M_GROUP = replace(C1M, name="1m4", modes=C1M.modes[:4])
 C1M_POOL = replace(C1M, name="1m-pool", pool=2048)
 
 C1M_POOL_GROUP = replace(C1M_POOL, name="1m4-pool", modes=C1M.modes[:4])
+
+# the 1m stack over paged caches: pages of 256 entries (1024 tokens), the
+# pages of every sequence scattered over one pool in a seeded random order
+C1M_PAGED = replace(C1M, name="1m-paged", page_rows=256)
+C1M_PAGED_GROUP = replace(C1M_PAGED, name="1m4-paged", modes=C1M.modes[:4])
+
+# the 1m stack with the Hierarchical Sparse Indexer's block-level pruning:
+# blocks of 64 entries, a Full layer keeps its 32 best blocks (a 2048-entry
+# pool) and scores only their entries
+C1M_BLOCK = replace(C1M, name="1m-block", block=64, blocks_kept=32)
+C1M_BLOCK_GROUP = replace(C1M_BLOCK, name="1m4-block", modes=C1M.modes[:4])
 # a quarter of the prefill chunk (1024 queries): the same kernels with a
 # quarter of the score scratch (profiling captures)
 PREFILL_1K = replace(PREFILL, name="prefill1k", q_per_seq=1024, pos0=1048576 - 1024)
 
 WORKLOADS = {w.name: w for w in (TINY, C128K, GROUP3, C1M, C1M_GROUP, PREFILL, C1M_POOL,
-                                 C1M_POOL_GROUP, PREFILL_1K)}
+                                 C1M_POOL_GROUP, PREFILL_1K, C1M_PAGED, C1M_PAGED_GROUP,
+                                 C1M_BLOCK, C1M_BLOCK_GROUP)}
+
+
+def block_table(B, n, page_rows, seed, device="cpu", spare=None):
+    """A paged layout's block table int32 [B, ceil(n / page_rows)]: every
+    sequence's pages drawn without repetition, in a seeded random order, from
+    a pool with `spare` (default B) pages no sequence uses.  Returns (table,
+    pages in the pool)."""
+    pps = (n + page_rows - 1) // page_rows
+    spare = B if spare is None else spare
+    num_pages = B * pps + spare
+    g = _gen(seed, "cpu")
+    perm = torch.randperm(num_pages, generator=g)[: B * pps]
+    return perm.reshape(B, pps).to(torch.int32).to(device), num_pages
 
 
 def scaled(w: Workload, **kw) -> Workload:

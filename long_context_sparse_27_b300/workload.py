@@ -58,6 +58,12 @@ class StackWorkload:
         self.device = device
         gen = gen_device or device
         self.plan = sources or default_sources(wl.modes)
+        self.pages = None
+        if wl.page_rows:
+            # one block table shared by every Full layer's pools
+            self.block_table, self.num_pages = synth.block_table(
+                wl.B, wl.N, wl.page_rows, seed * 1000 + 999, device)
+            self.pages = csa2.pages(self.block_table, wl.page_rows, self.num_pages)
         self.layers = []
         self.bf16 = []
         B, N = wl.B, wl.N
@@ -82,6 +88,14 @@ class StackWorkload:
                     host["kk"] = kk.cpu()
                 self._fill_cache(L, kv.to(device), kk.to(device))
                 del kv, kk
+                if wl.block:
+                    # block keys of the cache as filled (the step refreshes the
+                    # block its new row falls in)
+                    if self.pages is not None:
+                        L["block_keys"] = csa2.index_block_keys(
+                            L["idxk"], wl.block, n=N, pages=self.pages, B=B)
+                    else:
+                        L["block_keys"] = csa2.index_block_keys(L["idxk"], wl.block)
             self.layers.append(L)
             self.bf16.append(host)
         self.n_valid = None
@@ -100,6 +114,8 @@ class StackWorkload:
     def _fill_cache(self, L, kv, kk):
         wl = self.wl
         B, N = wl.B, wl.N
+        if self.pages is not None:
+            return self._fill_pages(L, kv, kk)
         L["codes"] = torch.zeros(B, N, wl.D // 2, dtype=torch.uint8, device=self.device)
         L["scales"] = torch.zeros(B, N, wl.D // 32, dtype=torch.uint8, device=self.device)
         if wl.fp32_indexer:
@@ -123,6 +139,27 @@ class StackWorkload:
         L["new_row"] = old
         L["new_rows"] = rows_new
 
+    def _fill_pages(self, L, kv, kk):
+        """Paged caches: pools of num_pages * page_rows rows, entries 0 ..
+        N - 2 of every sequence quantised into them through the block table
+        (one launch of the paged quantiser); entry N - 1 is the step's new
+        row, as in the contiguous layout."""
+        wl = self.wl
+        B, N = wl.B, wl.N
+        rows = self.num_pages * wl.page_rows
+        L["codes"] = torch.zeros(rows, wl.D // 2, dtype=torch.uint8, device=self.device)
+        L["scales"] = torch.zeros(rows, wl.D // 32, dtype=torch.uint8, device=self.device)
+        L["idxk"] = torch.zeros(rows, wl.Di, dtype=torch.uint8, device=self.device)
+        rows_new = 1 if wl.q_per_seq == 1 else wl.q_per_seq // 4
+        old = N - rows_new
+        csa2.quantize_fp4(kv[:, :old].reshape(B * old, wl.D), L["codes"], L["scales"],
+                          kk[:, :old].reshape(B * old, wl.Di), L["idxk"], pages=self.pages,
+                          rows_per_seq=old, entry0=0)
+        L["new_kv"] = kv[:, old:].contiguous()
+        L["new_idxk"] = kk[:, old:].contiguous()
+        L["new_row"] = old
+        L["new_rows"] = rows_new
+
     def stack_args(self):
         wl = self.wl
         return csa2.stack_args(
@@ -133,7 +170,8 @@ class StackWorkload:
             attn_q_dtype=csa2.F32 if wl.attn_q_fp32 else csa2.BF16,
             softmax_scale=1.0 / math.sqrt(wl.D), n_valid=self.n_valid,
             win_start=self.win_start, win_len=self.win_len, dev_status=self.dev_status,
-            pool=wl.pool, win_max=wl.W if self.win_len is not None else 0)
+            pool=wl.pool, win_max=wl.W if self.win_len is not None else 0, pages=self.pages,
+            block=wl.block, blocks_kept=wl.blocks_kept)
 
     def run(self):
         """Enqueue one step on the current stream."""
@@ -184,13 +222,24 @@ class StackWorkload:
         queries = (nq * wl.Hi * wl.Di * (4 if wl.fp32_indexer else 2)
                    + nq * wl.Hi * 4 + nq * wl.k * 4)
         full_index = wl.B * wl.N * wl.Di * (4 if wl.fp32_indexer else 1) + queries
+        if wl.page_rows:
+            # paged caches: the indexer reads each sequence's block table (and
+            # every selected entry looks up its page, below)
+            full_index += wl.B * (-(-wl.N // wl.page_rows)) * 4
         # a pooled Reindex layer reads its pool and the pool's indexer-K rows
-        P = min(wl.pool, wl.N)
+        P = wl.blocks_kept * wl.block if wl.block else min(wl.pool, wl.N)
         reindex = full_index if P == 0 else nq * P * (wl.Di + 4) + queries
+        if wl.block:
+            # block-level pruning: a Full layer reads the block keys and the
+            # kept blocks' indexer-K rows instead of every entry
+            full_index = (wl.B * (-(-wl.N // wl.block)) * wl.Di + nq * P * (wl.Di + 4)
+                          + queries)
         n_full = sum(1 for m in wl.modes if m == FULL)
         n_re = sum(1 for m in wl.modes if m == REINDEX)
         per_layer = (nq * wl.k * (wl.D // 2 + wl.D // 32) + nq * wl.W * wl.D * 2
                      + nq * wl.Hq * wl.D * (4 if wl.attn_q_fp32 else 2) + nq * wl.Hq * wl.D * 4)
+        if wl.page_rows:
+            per_layer += nq * wl.k * 4
         return n_full * full_index + n_re * reindex + len(wl.modes) * per_layer
 
     def visible_pairs(self):

@@ -132,6 +132,29 @@ def test_index_score_fp8_decode(csa2, orc, B, n):
     assert score_close(s.cpu().numpy(), ref) <= 1.0
 
 
+@pytest.mark.parametrize("B,n", [(8, 262144), (3, 1000), (2, 130), (600, 128)])
+def test_index_score_fused_q_matches_separate_quantiser(csa2, orc, B, n):
+    # decode launches quantise the bf16 indexer queries inside the indexer
+    # kernel; the scores must equal, bit for bit, those of the same kernel
+    # fed the separately quantised q8 and c (csa2_quantize_index_q, itself
+    # bit-exact against the oracle).  600 queries of 128 entries give CTAs
+    # spanning more than two queries: that launch takes the separate path.
+    wl = synth.scaled(synth.C128K, B=B, N=n)
+    q = synth.index_q(wl, 34 + n, "cuda")
+    q[0, 5] = 0.0                              # an all-zero head
+    q[min(1, B - 1), 7, 3] = 3.0e38            # saturating magnitudes
+    w = synth.index_w(wl, 35 + n, "cuda")
+    k8 = torch.randint(0, 0x7F, (B, n, 128), dtype=torch.uint8, device="cuda",
+                       generator=torch.Generator(device="cuda").manual_seed(36 + n))
+    fused = csa2.index_score(q, w, k8)
+    q8, c = csa2.quantize_index_q(q, w)
+    sep = csa2.index_score(q8, c, k8)
+    torch.cuda.synchronize()
+    assert torch.equal(fused.view(torch.int32), sep.view(torch.int32))
+    rq8, rc = orc.quantize_index_q(f64(q), f64(w))
+    assert np.array_equal(q8.cpu().numpy(), rq8)
+
+
 def test_index_score_fp8_prefill_causal(csa2, orc):
     # 8 queries of one sequence at the end of a 4x-compressed context
     wl = synth.scaled(synth.PREFILL, q_per_seq=8, N=700, pos0=4 * 700 - 8)
@@ -243,7 +266,8 @@ def test_project_fp4_exact_small_integers(csa2, orc):
 
 @pytest.mark.parametrize("rows,n,k,levels", [
     (3, 5000, 64, 0), (4, 4096, 512, 0), (5, 3000, 512, 40), (2, 262144, 512, 0),
-    (2, 70000, 512, 3), (6, 1000, 2048, 0), (1, 100, 512, 0), (9, 1, 1, 0)])
+    (2, 70000, 512, 3), (6, 1000, 2048, 0), (1, 100, 512, 0), (9, 1, 1, 0),
+    (4, 8000, 512, 1), (300, 5000, 256, 0), (37, 40000, 512, 0), (3, 262144, 2048, 5)])
 def test_topk_bit_exact(csa2, orc, rows, n, k, levels):
     s = synth.scores_with_ties(rows, n, seed=60 + rows + k, levels=levels)
     g = torch.Generator().manual_seed(61)
@@ -425,3 +449,30 @@ def test_attn_window_longer_than_bound_flags(csa2):
         assert bool(int(st.item()) & csa2.DEVFLAG_BOUNDS) == flagged
         assert csa2.lib.csa2_status_from_device(int(st.item())) == (7 if flagged else 0)
         assert torch.isfinite(out).all()
+
+
+def test_index_wait_timeout_returns_a_status(csa2, monkeypatch):
+    # the device-side failure path: the indexer's producer issues no loads
+    # (test hook), its MMA and epilogue waits run out after 1 ms, the kernel
+    # returns with CSA2_DEVFLAG_TIMEOUT, and the context stays usable: the
+    # same launch without the hook gives the scores of a clean run
+    B, n = 4, 20000
+    wl = synth.scaled(synth.C128K, B=B, N=n)
+    q8, c = csa2.quantize_index_q(synth.index_q(wl, 140, "cuda"), synth.index_w(wl, 141, "cuda"))
+    k8 = torch.randint(0, 0x7F, (B, n, 128), dtype=torch.uint8, device="cuda",
+                       generator=torch.Generator(device="cuda").manual_seed(142))
+    ref = csa2.index_score(q8, c, k8)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    monkeypatch.setenv("CSA2_TEST_STALL_LOADS", "1")
+    monkeypatch.setenv("CSA2_WAIT_LIMIT_NS", "1000000")
+    csa2.index_score(q8, c, k8, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & csa2.DEVFLAG_TIMEOUT
+    assert csa2.lib.csa2_status_from_device(int(st.item())) == 6
+    monkeypatch.delenv("CSA2_TEST_STALL_LOADS")
+    monkeypatch.delenv("CSA2_WAIT_LIMIT_NS")
+    st.zero_()
+    again = csa2.index_score(q8, c, k8, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(again.view(torch.int32), ref.view(torch.int32))
