@@ -157,18 +157,38 @@ def workload_desc(wl):
 
 # ---------------------------------------------------------------- our arm
 
+def prefill_selects(wl):
+    """Whether the layer stack selects this prefill chunk's top-k without its
+    score matrix (sampled threshold, candidates, exact selection among them)."""
+    return (wl.q_per_seq > 1 and wl.q_per_seq % 4 == 0 and wl.N > 4096 and not wl.pool
+            and not wl.block and not wl.fp32_indexer and wl.Hi == 64 and wl.Di == 128
+            and wl.k <= 8192)
+
+
+def fuses_new_rows(wl):
+    """Whether a decode Full layer's indexer launch also quantises the step's
+    new cache rows (E4M3 keys, one query per sequence, 256-element KV parts,
+    no block-level pruning)."""
+    return (not wl.fp32_indexer and wl.q_per_seq == 1 and wl.Hi == 64 and wl.Di == 128
+            and wl.D % 256 == 0 and not wl.block)
+
+
 def launches_per_step(wl):
     """Kernels of this library per step (memsets are not counted).  Full:
     new-row quantiser, indexer score, top-k selection and attention; Reindex:
     the same without the new rows; Reuse: attention.  Decode indexer launches
-    quantise their queries inside the indexer kernel; a prefill chunk runs
+    quantise their queries (and a Full layer's new rows) inside the indexer
+    kernel; a prefill chunk runs
     the indexer-Q quantiser as its own kernel and a top-k histogram pass per
-    index layer (decode builds the histogram inside the indexer kernel).
+    index layer (decode builds the histogram inside the indexer kernel), or,
+    when it selects without the score matrix, the kernels of that selection.
     Attention over more than 8 key chunks of 80 adds a merge kernel.  With a
     candidate pool a Full layer selects the pool and then the top-k inside it
     (one kernel more) and a Reindex layer runs the Q quantiser, the pooled
     scores, their selection and attention."""
-    per = {0: 4, 1: 3, 2: 1}
+    # a decode Full layer on the plain path quantises its new rows inside its
+    # indexer launch
+    per = {0: 3 if fuses_new_rows(wl) else 4, 1: 3, 2: 1}
     n = 0
     for m in wl.modes:
         if wl.block and m == 0:
@@ -181,7 +201,12 @@ def launches_per_step(wl):
             n += per[m]
             if m == 0 and wl.pool:
                 n += 1  # the pool's selection, then the top-k inside it
-            if m != 2 and wl.q_per_seq > 1:
+            if m != 2 and wl.q_per_seq > 1 and prefill_selects(wl):
+                # Q quantiser, sampled scores, two histogram passes and two
+                # threshold kernels, the emitting scores; the candidate
+                # selector takes the top-k's place
+                n += 6
+            elif m != 2 and wl.q_per_seq > 1:
                 n += 2  # separate Q quantiser, histogram pass
             elif m != 2 and wl.fp32_indexer and wl.N > 4096:
                 n += 1  # the fp32 indexer builds no histogram: a histogram pass
@@ -206,26 +231,50 @@ class L2Flush:
         self.r.max()
 
 
+def index_launch_form(wl):
+    """How the timed indexer launch takes its queries: "f32" (the CUDA-core
+    fp32 indexer), "bf16" (decode: bf16 queries quantised inside the launch,
+    the form the layer stack runs) or "q8" (a prefill chunk: queries
+    quantised beforehand, so the launch holds only the indexer kernel)."""
+    if wl.fp32_indexer:
+        return "f32"
+    return "bf16" if wl.q_per_seq % 4 != 0 else "q8"
+
+
+def index_launch_bytes(W):
+    """Algorithmic bytes of one timed indexer launch: the keys, the queries
+    in the form the launch reads them, the head weights and, over paged
+    caches, the block table."""
+    wl = W.wl
+    q_bytes = {"f32": 4, "bf16": 2, "q8": 1}[index_launch_form(wl)]
+    n = W.indexer_bytes_per_layer() + wl.nq * wl.Hi * (wl.Di * q_bytes + 4)
+    if wl.page_rows:
+        n += wl.B * (-(-wl.N // wl.page_rows)) * 4
+    return n
+
+
 def time_index_kernel(csa2, W, flush, reps=20):
     """Average device time of one launch of the indexer kernel (FP8 tensor
     core, or fp32 CUDA cores for an fp32 indexer) on the workload's first Full
-    layer (already-quantised queries, so the launch holds only that kernel),
-    with L2 flushed before each launch."""
+    layer, one kernel per launch (see index_launch_form), with L2 flushed
+    before each launch."""
     L0 = W.layers[0]
-    if W.wl.fp32_indexer:  # the CUDA-core fp32 indexer takes the queries as they are
-        q8, c = L0["idx_q"], L0["idx_w"]
+    wl = W.wl
+    if index_launch_form(wl) == "q8":
+        q, c = csa2.quantize_index_q(L0["idx_q"], L0["idx_w"])
     else:
-        q8, c = csa2.quantize_index_q(L0["idx_q"], L0["idx_w"])
-    scores = torch.empty(W.wl.nq, W.wl.N, dtype=torch.float32, device=q8.device)
+        q, c = L0["idx_q"], L0["idx_w"]
+    kw = {} if W.pages is None else {"pages": W.pages, "n": wl.N}
+    scores = torch.empty(wl.nq, wl.N, dtype=torch.float32, device=q.device)
     for _ in range(3):
-        csa2.index_score(q8, c, L0["idxk"], W.wl.q_per_seq, W.n_valid, scores)
+        csa2.index_score(q, c, L0["idxk"], wl.q_per_seq, W.n_valid, scores, **kw)
     stream = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(reps)]
     for a, b in ev:
         flush()
         a.record(stream)
-        csa2.index_score(q8, c, L0["idxk"], W.wl.q_per_seq, W.n_valid, scores)
+        csa2.index_score(q, c, L0["idxk"], wl.q_per_seq, W.n_valid, scores, **kw)
         b.record(stream)
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in ev) / reps * 1e-3  # seconds
@@ -351,7 +400,7 @@ def run_ours(args, world, rank, local):
     # ---- dominant kernel, timed live (roofline)
     k_s = time_index_kernel(csa2, W, flush)
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
-    k_bytes = W.indexer_bytes_per_layer() + wl.nq * wl.Hi * (wl.Di + 4)
+    k_bytes = index_launch_bytes(W)
     if wl.q_per_seq > 1:
         # a prefill chunk: the indexer is a dense FP8 contraction; algorithmic
         # FLOPs = 2 * Hi * Di per visible (query, entry) pair (causal)
@@ -412,6 +461,11 @@ def run_ours(args, world, rank, local):
             "unit": "tokens/s",
             "h2d_bytes_per_step": h2d_bytes,
             "d2h_bytes_per_step": d2h_bytes,
+            "note": ("host-to-device per step: new KV and indexer-K rows, indexer Q and weights, "
+                     "attention Q; the caches and the sliding-window rows stay on the device "
+                     "(a step's new window rows, %d bytes, are not copied)"
+                     % (len(wl.modes) * wl.B * (1 if wl.q_per_seq == 1 else wl.q_per_seq)
+                        * wl.D * 2)),
         },
         "gpu_launches": launches_per_step(wl) * args.steps,
         "clocks": clk.summary(),

@@ -63,12 +63,15 @@ typedef enum csa2_status {
   CSA2_ERR_CUDA = 4,           /* a CUDA call failed: csa2_last_cuda_error() */
   CSA2_ERR_WORKSPACE = 5,      /* workspace NULL or smaller than required */
   CSA2_ERR_DEVICE_TIMEOUT = 6, /* reported through dev_status only */
-  CSA2_ERR_DEVICE_BOUNDS = 7   /* reported through dev_status only */
+  CSA2_ERR_DEVICE_BOUNDS = 7,  /* reported through dev_status only */
+  CSA2_ERR_DEVICE_CAPACITY = 8 /* reported through dev_status only */
 } csa2_status;
 
 /* Bits a kernel ORs into *dev_status. */
 #define CSA2_DEVFLAG_TIMEOUT 0x1 /* a pipeline wait gave up (kernel returned early) */
 #define CSA2_DEVFLAG_BOUNDS 0x2  /* an index outside [-1, n) was skipped */
+#define CSA2_DEVFLAG_CAPACITY 0x4 /* a bounded candidate buffer overflowed: the
+                                     selection of that row is not exact */
 
 typedef enum csa2_dtype {
   CSA2_F32 = 0,
@@ -89,7 +92,8 @@ const char* csa2_status_string(int32_t status);
 /* The cudaError_t of the most recent CSA2_ERR_CUDA on the calling thread. */
 int32_t csa2_last_cuda_error(void);
 /* Turns a dev_status word read back by the caller into a status:
- * CSA2_OK, CSA2_ERR_DEVICE_TIMEOUT or CSA2_ERR_DEVICE_BOUNDS. */
+ * CSA2_OK, CSA2_ERR_DEVICE_TIMEOUT, CSA2_ERR_DEVICE_BOUNDS or
+ * CSA2_ERR_DEVICE_CAPACITY (in that order of precedence). */
 csa2_status csa2_status_from_device(int32_t dev_status_word);
 
 /* ------------------------------------------------------------------------ */
@@ -309,7 +313,8 @@ csa2_status csa2_index_block_keys(const uint8_t* k8, int64_t B, int64_t n, int64
  * scores  device f32, row r at scores + r * ld;  n_valid optional [rows]
  * idx_out device int32, row r at idx_out + r * idx_ld
  * 1 <= k <= 2048.  Workspace: csa2_topk_workspace_bytes(rows, n, k): one
- * 4096-bin histogram per row (rows * 16 KiB) and, for rows longer than 4096,
+ * histogram per row of 4096 fine and 64 coarse bins (rows * 16,640 bytes)
+ * and, for rows longer than 4096,
  * a counter per row and S candidate slots of 8 KiB per row (S = about 296 /
  * rows, at most 64, at most one per 8192 entries); the call clears what must
  * start at zero.
@@ -338,7 +343,7 @@ csa2_status csa2_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
  * The caller still passes the scores and idx_out buffers; the selector's
  * scratch comes from one fixed 4 MiB array compiled into the library, which
  * every GPU that loads the library keeps until the process exits.  Limit:
- * csa2_topk_workspace_bytes(rows, n, k) must not exceed 4 MiB (256 rows of
+ * csa2_topk_workspace_bytes(rows, n, k) must not exceed 4 MiB (252 rows of
  * at most 4096 entries; 8 rows of 262144); larger calls return
  * CSA2_ERR_WORKSPACE and enqueue nothing.  The call allocates nothing (no cudaMalloc / cudaFree).
  * The first call on a device looks up the array's device address for that
@@ -375,7 +380,7 @@ csa2_status csa2_topk_noalloc(const float* scores, int64_t rows, int64_t n, int6
  * memory, probabilities split into two bf16 terms).  The BF16 path cuts the
  * k + win_max keys of a query into chunks of 80; each chunk writes its
  * partial result (max, sum, unnormalised output per head) to the workspace,
- * csa2_sparse_attn_workspace_bytes of it (nq * hq/16 * chunks * 32.9 KB).
+ * csa2_sparse_attn_workspace_bytes of it (nq * ceil(hq/32) * chunks * 65.8 KB).
  * With at most 8 chunks (k + win_max <= 640) the chunks of a query form a
  * thread-block cluster that merges the partials itself; with more, a second
  * kernel merges them.

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 
 F32, BF16, E4M3 = 0, 1, 2
 FULL, REINDEX, REUSE = 0, 1, 2
-DEVFLAG_TIMEOUT, DEVFLAG_BOUNDS = 0x1, 0x2
+DEVFLAG_TIMEOUT, DEVFLAG_BOUNDS, DEVFLAG_CAPACITY = 0x1, 0x2, 0x4
 
 _c_i32, _c_i64, _c_p, _c_f, _c_sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
                                      ctypes.c_float, ctypes.c_size_t)

@@ -65,7 +65,7 @@ csa2_status injected(const char* call) {
   const size_t len = (size_t)(colon - env);
   if (std::strlen(call) != len || std::strncmp(env, call, len) != 0) return CSA2_OK;
   const int v = std::atoi(colon + 1);
-  return (v > 0 && v <= CSA2_ERR_DEVICE_BOUNDS) ? (csa2_status)v : CSA2_OK;
+  return (v > 0 && v <= CSA2_ERR_DEVICE_CAPACITY) ? (csa2_status)v : CSA2_OK;
 }
 
 namespace {
@@ -222,9 +222,29 @@ csa2_status check_attn(const csa2_attn_args* a) {
 // ---- layer stack ----
 
 struct StackPieces {
-  size_t scores, ix, tk, pl, at;
-  size_t total() const { return scores + tk + pl + std::max(ix, at); }
+  size_t scores, ix, tk, pl, at, sel;
+  size_t total() const { return scores + tk + pl + sel + std::max(ix, at); }
 };
+
+// The selection of a prefill chunk without its score matrix (see
+// IndexSelect): a sample of every kSampleStride-th tile of 128 entries gives
+// each query a threshold no entry of its top k lies below; the full pass then
+// keeps only the entries at or above it, at most kCandCap per query.
+constexpr int kSampleStride = 8;
+constexpr int64_t kCandCap = 8192;
+
+bool prefill_select(const csa2_stack_args& s) {
+  return s.q_per_seq > 1 && s.q_per_seq % 4 == 0 && s.n > kTopkShortRow && s.pool == 0 &&
+         s.block == 0 && s.idx_k_dtype == CSA2_E4M3 &&
+         (s.idx_q_dtype == CSA2_BF16 || s.idx_q_dtype == CSA2_E4M3) && s.hi == 64 &&
+         s.di == 128 && s.k <= kCandCap && topk_cand_fits(kCandCap, s.n);
+}
+
+// compact sample columns of a prefill selection
+int64_t sample_cols(const csa2_stack_args& s) {
+  const int64_t ktiles = (s.n + 127) / 128;
+  return (ktiles + kSampleStride - 1) / kSampleStride * 128;
+}
 
 // slots of the Hierarchical Sparse Indexer's candidate pool (0 = off): the
 // top-P pool, or the entries of the kept blocks under block-level pruning
@@ -373,7 +393,11 @@ csa2_status quantize_new_rows(const csa2_stack_args& s, const csa2_layer_desc& d
 StackPieces stack_pieces(const csa2_stack_args& s) {
   StackPieces p;
   const int64_t nq = s.B * s.q_per_seq;
-  p.scores = align256((size_t)nq * s.n * sizeof(float));
+  const bool psel = prefill_select(s);
+  // scores: the whole [nq, n] matrix, or a prefill selection's sample of it
+  p.scores = align256((size_t)nq * (psel ? sample_cols(s) : s.n) * sizeof(float));
+  // a prefill selection's thresholds, candidate counters and candidates
+  p.sel = psel ? align256((size_t)nq * 8) + align256((size_t)nq * kCandCap * sizeof(uint2)) : 0;
   csa2_layer_desc dummy;
   std::memset(&dummy, 0, sizeof(dummy));
   csa2_index_args ia = stack_index_args(s, dummy, dummy, nullptr, nullptr, 0);
@@ -404,6 +428,7 @@ const char* csa2_status_string(int32_t st) {
     case CSA2_ERR_WORKSPACE: return "CSA2_ERR_WORKSPACE";
     case CSA2_ERR_DEVICE_TIMEOUT: return "CSA2_ERR_DEVICE_TIMEOUT";
     case CSA2_ERR_DEVICE_BOUNDS: return "CSA2_ERR_DEVICE_BOUNDS";
+    case CSA2_ERR_DEVICE_CAPACITY: return "CSA2_ERR_DEVICE_CAPACITY";
     default: return "CSA2_ERR_UNKNOWN";
   }
 }
@@ -413,6 +438,7 @@ int32_t csa2_last_cuda_error(void) { return g_last_cuda_error; }
 csa2_status csa2_status_from_device(int32_t w) {
   if (w & CSA2_DEVFLAG_TIMEOUT) return CSA2_ERR_DEVICE_TIMEOUT;
   if (w & CSA2_DEVFLAG_BOUNDS) return CSA2_ERR_DEVICE_BOUNDS;
+  if (w & CSA2_DEVFLAG_CAPACITY) return CSA2_ERR_DEVICE_CAPACITY;
   return CSA2_OK;
 }
 
@@ -608,8 +634,13 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
   uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(s->workspace) + p.scores);
   int32_t* pool = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(s->workspace) + p.scores +
                                              p.tk);
-  void* scratch = static_cast<uint8_t*>(s->workspace) + p.scores + p.tk + p.pl;
-  const size_t scratch_bytes = s->workspace_bytes - p.scores - p.tk - p.pl;
+  uint8_t* selw = static_cast<uint8_t*>(s->workspace) + p.scores + p.tk + p.pl;
+  uint32_t* theta = reinterpret_cast<uint32_t*>(selw);
+  uint32_t* cand_cnt = theta + s->B * s->q_per_seq;
+  uint2* cand = reinterpret_cast<uint2*>(selw + align256((size_t)s->B * s->q_per_seq * 8));
+  void* scratch = selw + p.sel;
+  const size_t scratch_bytes = s->workspace_bytes - p.scores - p.tk - p.pl - p.sel;
+  const bool psel = prefill_select(*s);
   const int64_t nq = s->B * s->q_per_seq;
   const int64_t P = pool_slots(*s);
   // check every call's arguments before anything is enqueued
@@ -659,7 +690,23 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
   for (int32_t l = 0; l < n_layers; ++l) {
     const csa2_layer_desc& d = L[l];
     const csa2_layer_desc& kv = L[d.kv_src];
-    if (d.mode == CSA2_MODE_FULL && d.new_kv) {
+    // a decode Full layer on the plain path quantises its new rows inside its
+    // indexer launch (the CTA that loads a new row's tile writes it first)
+    NewRows nrows;
+    bool fuse_new = false;
+    if (d.mode == CSA2_MODE_FULL && d.new_kv && s->block == 0 && !psel) {
+      nrows.kv = static_cast<const uint16_t*>(d.new_kv);
+      nrows.idxk = static_cast<const uint16_t*>(d.new_idxk);
+      nrows.row0 = d.new_row;
+      nrows.rows = (int32_t)(d.new_rows > 0 ? d.new_rows : 1);
+      nrows.d = s->d;
+      nrows.codes = d.codes;
+      nrows.scales = d.scales;
+      nrows.k8 = static_cast<uint8_t*>(d.idxk);
+      const csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
+      fuse_new = index_bf16q_supported(ia, &nrows);
+    }
+    if (d.mode == CSA2_MODE_FULL && d.new_kv && !fuse_new) {
       if ((st = quantize_new_rows(*s, d, cs)) != CSA2_OK) return st;
       if (s->block > 0) {
         // the block keys of the blocks the new rows fall in
@@ -702,6 +749,41 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
       if ((st = launch_topk_small(scores, P, nullptr, 0, nq, (int32_t)P, nullptr, s->k, pool, P,
                                   d.topk_idx, s->k, cs)) != CSA2_OK)
         return st;
+    } else if (d.mode != CSA2_MODE_REUSE && psel) {
+      // a prefill chunk: sampled scores -> thresholds -> candidates -> top-k
+      csa2_index_args ia = stack_index_args(*s, d, kv, scores, scratch, scratch_bytes);
+      const uint8_t* q8 = static_cast<const uint8_t*>(ia.q);
+      const float* c = ia.w;
+      if (ia.q_dtype != CSA2_E4M3) {
+        uint8_t* wq = static_cast<uint8_t*>(scratch);
+        float* wc = reinterpret_cast<float*>(wq + align256((size_t)nq * s->hi * s->di));
+        if ((st = launch_quantize_index_q(ia.q, ia.w, nq, s->hi, s->di, wq, wc, cs)) != CSA2_OK)
+          return st;
+        q8 = wq;
+        c = wc;
+      }
+      const int64_t ns = sample_cols(*s);
+      csa2_index_args is = ia;
+      is.scores_ld = ns;
+      IndexSelect sample;
+      sample.tile_stride = kSampleStride;
+      if ((st = launch_index_select_prefill(is, q8, c, sample, cs)) != CSA2_OK) return st;
+      // the sample's k-th largest key to 24 bits: its level-1 bin, then the
+      // next 12 bits within that bin
+      if ((st = launch_topk_hist(scores, nq, ns, ns, nullptr, hist, cs)) != CSA2_OK) return st;
+      if ((st = launch_topk_theta(hist, nq, s->k, theta, cand_cnt, 0, cs)) != CSA2_OK) return st;
+      if ((st = launch_topk_hist(scores, nq, ns, ns, nullptr, hist, cs, theta)) != CSA2_OK)
+        return st;
+      if ((st = launch_topk_theta(hist, nq, s->k, theta, cand_cnt, 1, cs)) != CSA2_OK) return st;
+      IndexSelect emit;
+      emit.theta = theta;
+      emit.cand_cnt = cand_cnt;
+      emit.cand = cand;
+      emit.cand_cap = kCandCap;
+      if ((st = launch_index_select_prefill(ia, q8, c, emit, cs)) != CSA2_OK) return st;
+      if ((st = launch_topk_cand(cand, cand_cnt, kCandCap, nq, s->n, s->n_valid, s->k, d.topk_idx,
+                                 s->k, s->dev_status, cs)) != CSA2_OK)
+        return st;
     } else if (d.mode == CSA2_MODE_REINDEX && P > 0) {
       // Hierarchical Sparse Indexer: score the last Full layer's pool only,
       // then its top-k (pool positions mapped back to entry indices)
@@ -736,7 +818,9 @@ csa2_status csa2_layer_stack(const csa2_layer_desc* L, int32_t n_layers,
         tune.keep_in_l2 = read_again(l, d.kv_src);
         reverse_next[d.kv_src] = !tune.reverse;
       }
-      if ((st = run_index(ia, fused ? hist : nullptr, tune, cs)) != CSA2_OK) return st;
+      st = fuse_new ? launch_index_score_bf16q(ia, fused ? hist : nullptr, tune, cs, &nrows)
+                    : run_index(ia, fused ? hist : nullptr, tune, cs);
+      if (st != CSA2_OK) return st;
       if (long_rows && !fused &&
           (st = launch_topk_hist(scores, nq, s->n, s->n, s->n_valid, hist, cs)) != CSA2_OK)
         return st;

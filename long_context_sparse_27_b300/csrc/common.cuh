@@ -78,6 +78,49 @@ __device__ __forceinline__ uint32_t e4m3_encode(float x) {
   return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
 }
 
+// Eight bf16 values (a 16-byte load) as floats, element i of the load in v[i].
+__device__ __forceinline__ void bf16x8_to_float(uint4 raw, float v[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+    v[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+  }
+}
+
+// a1: eight consecutive elements of a 32-element block whose largest
+// magnitude is amax -> eight E2M1 codes (element i in nibble i) and the
+// block's UE8M0 scale byte: X = 2^(floor(log2 amax) - 2), exponent clamped
+// to [-127, 127]; an all-zero block has scale byte 0 and zero codes.
+__device__ __forceinline__ uint32_t fp4_encode8(const float v[8], float amax, uint32_t& sbyte) {
+  uint32_t packed = 0;
+  sbyte = 0;
+  if (amax > 0.f) {
+    int e = floor_log2_pos(amax) - 2;
+    e = max(-127, min(127, e));
+    sbyte = (uint32_t)(e + 127);
+    const float inv = exp2_int(-e);  // -e in [-127, 127]: exact power of two
+#pragma unroll
+    for (int i = 0; i < 8; ++i) packed |= e2m1_encode(v[i] * inv) << (4 * i);
+  }
+  return packed;
+}
+
+// a1, indexer keys: eight bf16 values (a 16-byte load) -> eight E4M3 bytes,
+// element i in byte i.
+__device__ __forceinline__ uint2 e4m3_encode8(uint4 raw) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    lo |= e4m3_encode(bf16_bits_to_float(w[i] & 0xFFFFu)) << (16 * i);
+    lo |= e4m3_encode(bf16_bits_to_float(w[i] >> 16)) << (16 * i + 8);
+    hi |= e4m3_encode(bf16_bits_to_float(w[i + 2] & 0xFFFFu)) << (16 * i);
+    hi |= e4m3_encode(bf16_bits_to_float(w[i + 2] >> 16)) << (16 * i + 8);
+  }
+  return make_uint2(lo, hi);
+}
+
 // ---------------------------------------------------------------------------
 // top-k keys and histograms
 // ---------------------------------------------------------------------------
@@ -91,6 +134,11 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 }
 
 constexpr int kTopkBins = 4096;  // first-level digit: the key's top 12 bits
+// A row's level-1 histogram in global memory: the 4096 fine bins, then 64
+// coarse bins (the key's top 6 bits; coarse bin c = fine bins 64c .. 64c+63),
+// so that a reader can find the threshold bin from 128 counts.
+constexpr int kTopkCoarse = 64;
+constexpr int kTopkHistStride = kTopkBins + kTopkCoarse;
 
 // ---------------------------------------------------------------------------
 // programmatic dependent launch
@@ -287,44 +335,11 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t smem_addr) {
   return d;
 }
 
-// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
-// swizzle layout: 64 consecutive MN elements (128 bytes) per row of the
-// swizzle atom, 8 K rows 128 bytes apart per atom; `lbo` = bytes between
-// atoms adjacent along MN, `sbo` = bytes between atoms adjacent along K (8
-// K rows).  Atoms are 1024-byte aligned (base offset 0).
-__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t smem_addr, uint32_t lbo,
-                                                   uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
 // Instruction descriptor, kind::f8f6f4 with E4M3 A and B, f32 accumulate,
 // both operands K-major: D format (bits 4-5) = 1, A / B format (7-9 /
 // 10-12) = 0, transpose bits 15 / 16 = 0, N >> 3 at 17-22, M >> 4 at 24-28.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// Instruction descriptor, kind::f16 with BF16 A and B (format 1), f32
-// accumulate; B K-major, A K-major or (a_mn) MN-major (bit 15).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -364,32 +379,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 8 / 16 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr)
-               : "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Generic-proxy writes to shared memory (st.shared, cp.async) made visible

@@ -162,10 +162,13 @@ struct TcCfg {
   static constexpr int OFF_CQ = OFF_C + EPI_WARPS * 2 * BN * 4;  // float [2][BN], fused Q
   // fused first-level top-k histogram (decode): two group slots of 4096 bins
   static constexpr int OFF_H = OFF_CQ + (QG == 1 ? 2 * BN * 4 : 0);
-  static constexpr int HIST_BYTES = QG == 1 ? 2 * kTopkBins * 4 : 0;
+  // decode: the first HSLOTS groups of a CTA's range keep their histograms
+  // in shared memory (later ones add to the global histogram directly)
+  static constexpr int HSLOTS = QG == 1 ? 2 : 0;
+  static constexpr int HIST_BYTES = HSLOTS * kTopkBins * 4;
   static constexpr int OFF_BAR = OFF_H + HIST_BYTES;
-  // barriers: full[S], empty[S], qfull[2], qempty[2], tfull[NACC], tempty[NACC], fin
-  static constexpr int NBAR = 2 * STAGES + 4 + 2 * NACC + 1;
+  // barriers: full[S], empty[S], qfull[2], qempty[2], tfull[NACC], tempty[NACC], fin, nrdy
+  static constexpr int NBAR = 2 * STAGES + 4 + 2 * NACC + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem slot, abort flag
   static constexpr int OFF_PG = OFF_MISC + 16;                // int32 [kPageRing][2] page ids
   static constexpr int SMEM = OFF_PG + kPageRing * 2 * 4;
@@ -201,6 +204,22 @@ struct TcParams {
   csa2_pages pages;
   uint64_t wait_ns;        // limit of each pipeline wait (drain waits keep their own)
   int stall_loads;         // test hook: the producer issues no loads (waits run out)
+  // sampled launches: the cursor's tile kt is key tile kt * tile_stride, and
+  // its scores go to columns kt * 128 .. of the (compact) score rows
+  int tile_stride;
+  // emitting launches (cand set): no scores are stored; every visible entry
+  // whose order-preserving key is >= theta[q] is appended to query q's
+  // candidates cand[q * cand_cap ..] as (key, entry) through the counter
+  // cand_cnt[q] (which may end above cand_cap: the overflow is the reader's
+  // to detect)
+  const uint32_t* theta;
+  uint32_t* cand_cnt;
+  uint2* cand;
+  int64_t cand_cap;
+  // decode Full layers (one query per sequence): the step's new rows, which
+  // the epilogue warps quantise first; the producer waits for them (nrdy)
+  // before loading a tile that holds one (nr.kv null: none)
+  NewRows nr;
 };
 
 
@@ -241,6 +260,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
   uint64_t* tfull = qempty + 2;
   uint64_t* tempty = tfull + C::NACC;
   uint64_t* fin = tempty + C::NACC;
+  uint64_t* nrdy = fin + 1;  // the CTA's new rows are in the caches
   uint32_t* hslot = reinterpret_cast<uint32_t*>(smem + C::OFF_H);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -265,6 +285,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       mbar_init(&tempty[i], 4 * C::SPLIT);  // the warps of the warpgroups that share a tile
     }
     mbar_init(fin, 1);
+    mbar_init(nrdy, C::EPI_WARPS);  // every epilogue warp, once its new-row share is written
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&kmap);
@@ -272,7 +293,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   if constexpr (QG == 1) {
-    for (int i = threadIdx.x; i < 2 * kTopkBins; i += C::THREADS) hslot[i] = 0;
+    for (int i = threadIdx.x; i < C::HSLOTS * kTopkBins; i += C::THREADS) hslot[i] = 0;
   }
   const int64_t g_first = total > 0 ? t_begin / p.ktiles : 0;
   tc_fence_before();
@@ -289,7 +310,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       int stage = 0;
       uint32_t ph = 0;
       int64_t g_prev = -1, qcount = 0, issued = 0;
-      bool ok = true;
+      bool ok = true, nr_seen = false;
       const int64_t dir = p.reverse ? -1 : 1;
       TileCursor cur(p.reverse ? t_end - 1 : t_begin, p.ktiles);
       // paged keys: the page ids of tile i (two 64-row halves) are copied by
@@ -306,7 +327,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
             const int64_t bb = (ahead.g * QG) / p.q_per_seq;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const int64_t j = ahead.kt * C::BM + 64 * h;
+              const int64_t j = ahead.kt * p.tile_stride * C::BM + 64 * h;
               if (j < p.n)
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                                  smem_u32(pg + (ahead_i % kPageRing) * 2 + h)),
@@ -320,7 +341,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       };
       if (paged) page_ids_ahead(kPageLookahead);
       for (int64_t i = 0; i < ntiles; ++i, cur.advance(dir)) {
-        const int64_t g = cur.g, kt = cur.kt;
+        const int64_t g = cur.g, kt = cur.kt * p.tile_stride;  // the key tile
         if (g != g_prev && !p.qbf) {
           const int qs = (int)(qcount & 1);
           const uint32_t qph = (uint32_t)((qcount >> 1) & 1);
@@ -336,6 +357,16 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, p.dev_status, p.wait_ns)) {
           ok = false;
           break;
+        }
+        if (p.nr.kv && !nr_seen && kt * C::BM < p.nr.row0 + p.nr.rows &&
+            (kt + 1) * C::BM > p.nr.row0) {
+          // this tile holds new rows: the epilogue warps have written them
+          // (their proxy fence orders the stores before this TMA load)
+          if (!mbar_wait(nrdy, 0, abort_flag, p.dev_status, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          nr_seen = true;
         }
         const int64_t b = (g * QG) / p.q_per_seq;
         if (!paged) {
@@ -517,8 +548,58 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         // every epilogue warp's share of cq is written
         asm volatile("bar.sync 1, %0;" ::"n"(C::EPI_WARPS * 32) : "memory");
       }
+      if (p.nr.kv && t_begin < t_end) {
+        // a1 for the new rows inside this CTA's tiles: work items (sequence,
+        // row, piece), piece < d / 256 a 256-element part of the main-KV row
+        // (lane l: elements 8 l .. 8 l + 7; a 32-element block in 4 lanes),
+        // the last piece the 128-element indexer key (lanes 0 .. 15); item
+        // u goes to epilogue warp u % EPI_WARPS
+        const int kvp = p.nr.d / 256;
+        const int64_t g_lo = t_begin / p.ktiles, g_hi = (t_end - 1) / p.ktiles;
+        int u = 0;
+        for (int64_t b = g_lo; b <= g_hi; ++b) {
+          for (int r = 0; r < p.nr.rows; ++r) {
+            const int64_t j = p.nr.row0 + r;
+            const int64_t t = b * p.ktiles + j / C::BM;
+            if (t < t_begin || t >= t_end || j >= p.n) continue;
+            for (int piece = 0; piece <= kvp; ++piece, ++u) {
+              if (u % C::EPI_WARPS != ew) continue;
+              const int64_t crow =
+                  p.pages.block_table ? paged_row(p.pages, b, j, p.dev_status) : b * p.n + j;
+              const int64_t src = b * p.nr.rows + r;
+              if (piece < kvp) {
+                const int e0 = 256 * piece + 8 * lane;
+                float v[8];
+                bf16x8_to_float(
+                    __ldg(reinterpret_cast<const uint4*>(p.nr.kv + src * p.nr.d + e0)), v);
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                uint32_t sbyte;
+                const uint32_t packed = fp4_encode8(v, amax, sbyte);
+                if (crow >= 0) {
+                  *reinterpret_cast<uint32_t*>(p.nr.codes + crow * (p.nr.d / 2) + e0 / 2) = packed;
+                  if ((lane & 3) == 0) p.nr.scales[crow * (p.nr.d / 32) + e0 / 32] = (uint8_t)sbyte;
+                }
+              } else if (lane < C::BK / 8 && crow >= 0) {
+                const uint4 raw =
+                    __ldg(reinterpret_cast<const uint4*>(p.nr.idxk + src * C::BK + 8 * lane));
+                *reinterpret_cast<uint2*>(p.nr.k8 + crow * C::BK + 8 * lane) = e4m3_encode8(raw);
+              }
+            }
+          }
+        }
+        // the key stores are ordered before the producer's TMA loads (async
+        // proxy) of their tiles, which wait for every warp's arrival
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(nrdy);
+      }
     }
     int64_t nv[C::QPW];
+    uint32_t th[C::QPW];
     // li counts tiles in processing order (from the range's end when reversed)
     const int64_t dir = p.reverse ? -1 : 1;
     TileCursor cur(p.reverse ? t_end - 1 - stream : t_begin + stream, p.ktiles);
@@ -538,7 +619,10 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < C::QPW; ++i)
+        {
           nv[i] = p.n_valid ? (int64_t)p.n_valid[g * QG + q0 + i] : p.n;
+          th[i] = p.cand ? p.theta[g * QG + q0 + i] : 0u;
+        }
         g_prev = g;
       }
       // every lane waits; the warp goes on only if all of them saw the phase
@@ -578,12 +662,33 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         }
         sc[qq] = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
       }
-      const int64_t j = kt * C::BM + row;
-      if (j < p.n) {
+      const int64_t jc = kt * C::BM + row;          // score column (compact when sampled)
+      const int64_t j = jc + kt * (p.tile_stride - 1) * C::BM;  // the entry
+      if (p.cand) {
+        // candidates of the exact selection: warp-aggregated appends
+        const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
         for (int qq = 0; qq < C::QPW; ++qq) {
           const int64_t qi = g * QG + q0 + qq;
-          p.scores[qi * p.scores_ld + j] = (j < nv[qq]) ? sc[qq] : -INFINITY;
+          const uint32_t key = score_key(sc[qq]);
+          const bool take = j < p.n && j < nv[qq] && key >= th[qq];
+          const uint32_t mask = __ballot_sync(0xffffffffu, take);
+          if (mask) {
+            const int leader = __ffs(mask) - 1;
+            uint32_t base = 0;
+            if (lane == leader) base = atomicAdd(&p.cand_cnt[qi], (uint32_t)__popc(mask));
+            base = __shfl_sync(0xffffffffu, base, leader);
+            const uint32_t pos = base + __popc(mask & lt);
+            if (take && pos < (uint64_t)p.cand_cap)
+              p.cand[qi * p.cand_cap + pos] = make_uint2(key, (uint32_t)j);
+          }
+        }
+      } else if (j < p.n || p.tile_stride > 1) {
+        // (a sampled row is compact: its columns past the entries read -inf)
+#pragma unroll
+        for (int qq = 0; qq < C::QPW; ++qq) {
+          const int64_t qi = g * QG + q0 + qq;
+          p.scores[qi * p.scores_ld + jc] = (j < p.n && j < nv[qq]) ? sc[qq] : -INFINITY;
         }
       }
       if constexpr (QG == 1) {
@@ -593,10 +698,13 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         if (p.hist1 && j < p.n && j < nv[0]) {
           const uint32_t bin = score_key(sc[0]) >> 20;
           const int64_t slot = g - g_first;
-          if (slot < 2)
+          if (slot < C::HSLOTS)
             atomicAdd(hslot + slot * kTopkBins + bin, 1u);
           else
-            atomicAdd(p.hist1 + g * kTopkBins + bin, 1u);
+          {
+            atomicAdd(p.hist1 + g * kTopkHistStride + bin, 1u);
+            atomicAdd(p.hist1 + g * kTopkHistStride + kTopkBins + (bin >> 6), 1u);
+          }
         }
       }
     }
@@ -613,10 +721,19 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
   if constexpr (QG == 1) {
     if (p.hist1 && t_end > t_begin) {
       const int64_t g_last = (t_end - 1) / p.ktiles;
-      for (int sl = 0; sl < 2 && g_first + sl <= g_last; ++sl)
-        for (int i = threadIdx.x; i < kTopkBins; i += C::THREADS) {
-          const uint32_t v = hslot[sl * kTopkBins + i];
-          if (v) atomicAdd(&p.hist1[(g_first + sl) * kTopkBins + i], v);
+      for (int sl = 0; sl < C::HSLOTS && g_first + sl <= g_last; ++sl)
+        {
+          uint32_t* hrow = p.hist1 + (g_first + sl) * kTopkHistStride;
+          for (int i = threadIdx.x; i < kTopkBins; i += C::THREADS) {
+            const uint32_t v = hslot[sl * kTopkBins + i];
+            if (v) atomicAdd(&hrow[i], v);
+          }
+          if (threadIdx.x < kTopkCoarse) {  // coarse bin t: fine bins 64t .. 64t + 63
+            uint32_t v = 0;
+            for (int i = 0; i < kTopkBins / kTopkCoarse; ++i)
+              v += hslot[sl * kTopkBins + threadIdx.x * (kTopkBins / kTopkCoarse) + i];
+            if (v) atomicAdd(&hrow[kTopkBins + threadIdx.x], v);
+          }
         }
     }
   }
@@ -652,7 +769,8 @@ int64_t tc_grid(int64_t total) {
 // weights a.w quantised inside the kernel (decode only, see TcParams::qbf).
 template <int QG>
 csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* c,
-                      uint32_t* hist1, IndexTuning tune, cudaStream_t s) {
+                      uint32_t* hist1, IndexTuning tune, cudaStream_t s,
+                      const IndexSelect* sel = nullptr, const NewRows* nr = nullptr) {
   using C = TcCfg<QG>;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cuda_fail(cudaErrorNotSupported);
@@ -702,6 +820,8 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   p.q_per_seq = a.q_per_seq;
   p.groups = nq / QG;
   p.ktiles = (a.n + C::BM - 1) / C::BM;
+  if (sel && sel->tile_stride > 1)  // sampled: every tile_stride-th tile
+    p.ktiles = (p.ktiles + sel->tile_stride - 1) / sel->tile_stride;
   p.dev_status = a.dev_status;
   p.hist1 = QG == 1 ? hist1 : nullptr;
   p.reverse = tune.reverse ? 1 : 0;
@@ -709,6 +829,12 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   p.pages = a.pages;
   p.wait_ns = pipeline_wait_ns();
   p.stall_loads = stall_loads() ? 1 : 0;
+  p.tile_stride = sel && sel->tile_stride > 1 ? sel->tile_stride : 1;
+  p.theta = sel ? sel->theta : nullptr;
+  p.cand_cnt = sel ? sel->cand_cnt : nullptr;
+  p.cand = sel ? sel->cand : nullptr;
+  p.cand_cap = sel ? sel->cand_cap : 0;
+  if (nr) p.nr = *nr;
   const int64_t total = p.groups * p.ktiles;
   if (total == 0) return CSA2_OK;
   static std::atomic<uint64_t> attr_done{0};
@@ -732,20 +858,49 @@ csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, 
   return launch_tc<1>(a, q8, c, hist1, tune, s);
 }
 
-csa2_status launch_index_score_bf16q(const csa2_index_args& a, uint32_t* hist1, IndexTuning tune,
-                                     cudaStream_t s) {
+bool index_bf16q_supported(const csa2_index_args& a, const NewRows* nr) {
   if (a.hi != 64 || a.di != 128 || a.q_dtype != CSA2_BF16 || a.k_dtype != CSA2_E4M3 ||
       a.q_per_seq % 4 == 0)
-    return CSA2_ERR_UNSUPPORTED;
+    return false;
+  const int64_t nq = a.B * a.q_per_seq;
+  if (nq > 0 && a.n > 0) {
+    // every CTA's tile range must span at most two query groups
+    const int64_t ktiles = (a.n + TcCfg<1>::BM - 1) / TcCfg<1>::BM;
+    const int64_t total = nq * ktiles;
+    const int64_t grid = tc_grid<1>(total);
+    if ((total + grid - 1) / grid > ktiles + 1) return false;
+  }
+  if ((reinterpret_cast<uintptr_t>(a.q) & 15) != 0) return false;
+  if (nr) {
+    // one query per sequence (each key tile read by one CTA), a few new rows
+    // of whole 256-element parts, 16-byte rows, inside the caches
+    if (a.q_per_seq != 1 || nr->rows < 1 || nr->rows > 128 || nr->d < 256 || nr->d % 256 != 0)
+      return false;
+    if (nr->row0 < 0 || nr->row0 + nr->rows > a.n) return false;
+    if (!nr->kv || !nr->idxk || !nr->codes || !nr->scales || !nr->k8) return false;
+    if (((reinterpret_cast<uintptr_t>(nr->kv) | reinterpret_cast<uintptr_t>(nr->idxk) |
+          reinterpret_cast<uintptr_t>(nr->k8)) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(nr->codes) & 3) != 0)
+      return false;
+    if (nr->k8 != a.k || a.k_ld != 128 || (!a.pages.block_table && a.k_seq_stride != a.n * 128))
+      return false;  // the keys the launch reads are the cache the new rows go to
+  }
+  return true;
+}
+
+csa2_status launch_index_score_bf16q(const csa2_index_args& a, uint32_t* hist1, IndexTuning tune,
+                                     cudaStream_t s, const NewRows* nr) {
+  if (!index_bf16q_supported(a, nr)) return CSA2_ERR_UNSUPPORTED;
   const int64_t nq = a.B * a.q_per_seq;
   if (nq == 0 || a.n == 0) return CSA2_OK;
-  // every CTA's tile range must span at most two query groups
-  const int64_t ktiles = (a.n + TcCfg<1>::BM - 1) / TcCfg<1>::BM;
-  const int64_t total = nq * ktiles;
-  const int64_t grid = tc_grid<1>(total);
-  if ((total + grid - 1) / grid > ktiles + 1) return CSA2_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(a.q) & 15) != 0) return CSA2_ERR_UNSUPPORTED;
-  return launch_tc<1>(a, nullptr, nullptr, hist1, tune, s);
+  return launch_tc<1>(a, nullptr, nullptr, hist1, tune, s, nullptr, nr);
+}
+
+csa2_status launch_index_select_prefill(const csa2_index_args& a, const uint8_t* q8,
+                                        const float* c, const IndexSelect& sel, cudaStream_t s) {
+  if (a.hi != 64 || a.di != 128 || a.q_per_seq % 4 != 0) return CSA2_ERR_UNSUPPORTED;
+  if (a.B * a.q_per_seq == 0 || a.n == 0) return CSA2_OK;
+  return launch_tc<4>(a, q8, c, nullptr, IndexTuning{}, s, &sel);
 }
 
 bool index_fuses_topk_hist(const csa2_index_args& a) {

@@ -40,17 +40,54 @@ struct IndexTuning {
   bool keep_in_l2 = false;
 };
 
+// The forms of a prefill indexer launch (q_per_seq a multiple of 4) that
+// feed a selection without the full score matrix:
+//   sampled  (tile_stride = R > 1, theta null): only every R-th tile of 128
+//            entries is scored, its scores written compactly (tile t of the
+//            sample to columns 128 t ..) into a.scores / a.scores_ld;
+//   emitting (theta set, tile_stride 1): every tile is scored, nothing is
+//            stored but the (key, entry) pairs of the visible entries whose
+//            order-preserving key is >= theta[q], appended to cand[q *
+//            cand_cap ..] through the counter cand_cnt[q] (zero before).
+struct IndexSelect {
+  int tile_stride = 1;
+  const uint32_t* theta = nullptr;
+  uint32_t* cand_cnt = nullptr;
+  uint2* cand = nullptr;
+  int64_t cand_cap = 0;
+};
+csa2_status launch_index_select_prefill(const csa2_index_args& a, const uint8_t* q8,
+                                        const float* c, const IndexSelect& sel, cudaStream_t s);
 // a3, FP8 tensor-core path: q8 / c already quantised.  hist1 (nullable):
 // [nq][4096] first-level top-k histograms the decode kernel adds its scores'
 // keys to (see index_fuses_topk_hist).
 csa2_status launch_index_score_fp8(const csa2_index_args& a, const uint8_t* q8, const float* c,
                                    uint32_t* hist1, IndexTuning tune, cudaStream_t s);
+// A decode Full layer's new cache rows (a1), quantised inside the indexer
+// launch that reads them: the CTA whose tiles hold a new row writes its FP4
+// codes and scales and its E4M3 indexer key before that CTA loads the tile.
+// Row j of sequence b goes to cache row b * n + j, or through the block
+// table when the caches are paged.
+struct NewRows {
+  const uint16_t* kv = nullptr;    // bf16 [B, rows, d]
+  const uint16_t* idxk = nullptr;  // bf16 [B, rows, 128]
+  int64_t row0 = 0;                // first new entry of every sequence
+  int32_t rows = 0;
+  int32_t d = 0;                   // a multiple of 256
+  uint8_t* codes = nullptr;        // FP4 codes [B * n (or pool rows), d / 2]
+  uint8_t* scales = nullptr;       // UE8M0 scales [.., d / 32]
+  uint8_t* k8 = nullptr;           // E4M3 indexer keys [.., 128]
+};
 // The same with bf16 queries and raw weights (a.q, a.w), quantised inside
 // the indexer kernel (decode shapes: hi 64, di 128, q_per_seq not a
 // multiple of 4); CSA2_ERR_UNSUPPORTED (nothing launched) when the launch
-// cannot take that form, and the caller quantises separately.
+// cannot take that form, and the caller quantises separately.  nr
+// (optional, one query per sequence): new rows quantised in the launch.
 csa2_status launch_index_score_bf16q(const csa2_index_args& a, uint32_t* hist1, IndexTuning tune,
-                                     cudaStream_t s);
+                                     cudaStream_t s, const NewRows* nr = nullptr);
+// Whether launch_index_score_bf16q takes this launch, and also its new rows
+// when nr is given.
+bool index_bf16q_supported(const csa2_index_args& a, const NewRows* nr = nullptr);
 // Scores of a candidate pool (the Hierarchical Sparse Indexer): for every
 // query q and slot i < pool_n, scores[q * scores_ld + i] = the FP8 indexer
 // score of entry pool[q * pool_ld + i] of q's sequence (-inf for a slot
@@ -65,9 +102,9 @@ bool index_fuses_topk_hist(const csa2_index_args& a);
 // launch_topk_small (every key in shared memory, no histogram); longer rows
 // by launch_topk_select from their level-1 histograms.
 constexpr int64_t kTopkShortRow = 4096;
-// the workspace holds one 4096-bin first-level histogram per row (the
-// first rows * 16 KiB), then for rows longer than 4096 a counter and the
-// slices' candidate slots per row
+// the workspace holds one first-level histogram per row (the first rows *
+// kTopkHistStride words: 4096 fine and 64 coarse bins), then for rows longer
+// than 4096 a counter and the slices' candidate slots per row
 size_t topk_workspace_bytes(int64_t rows, int64_t n, int32_t k);
 csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
                         const int32_t* n_valid, int32_t k, int32_t* idx_out, int64_t idx_ld,
@@ -76,8 +113,29 @@ csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld
 // long-row workspace for rows of n); select from scores whose histograms are
 // complete (the selection leaves histograms and counters zeroed)
 csa2_status clear_topk_hist(uint32_t* hist1, int64_t rows, int64_t n, cudaStream_t s);
+// The selection of a prefill chunk without its score matrix: theta[r], the
+// lowest key of the 24-bit key prefix holding the k-th largest key of a
+// sample of row r's scores (so no entry of the row's top k lies below it),
+// in two levels over the row's histogram: level 0 reads the 12-bit
+// histogram, sets theta[r] = T1 << 20 and keeps in cand_cnt[r] how many of
+// the k fall in bin T1; level 1 reads the histogram of the next 12 bits of
+// the keys in bin T1, completes theta[r] and zeroes cand_cnt[r].  Each level
+// clears the histogram.  Then the exact top k of each row among its
+// candidates (see IndexSelect), written ascending, -1 padded (more than cap
+// candidates: CSA2_DEVFLAG_CAPACITY).
+csa2_status launch_topk_theta(uint32_t* hist1, int64_t rows, int32_t k, uint32_t* theta,
+                              uint32_t* cand_cnt, int level, cudaStream_t s);
+size_t topk_cand_smem(int64_t cap, int64_t n);
+// whether a candidate selection of `cap` slots over rows of n entries fits a CTA
+bool topk_cand_fits(int64_t cap, int64_t n);
+csa2_status launch_topk_cand(const uint2* cand, const uint32_t* cand_cnt, int64_t cap,
+                             int64_t rows, int64_t n, const int32_t* n_valid, int32_t k,
+                             int32_t* out, int64_t out_ld, int32_t* dev_status, cudaStream_t s);
+// within (optional, per row): count only the keys in level-1 bin
+// within[r] >> 20, binned by their next 12 bits
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
-                             const int32_t* n_valid, uint32_t* hist1, cudaStream_t s);
+                             const int32_t* n_valid, uint32_t* hist1, cudaStream_t s,
+                             const uint32_t* within = nullptr);
 // Block keys of the Hierarchical Sparse Indexer's first level: for blocks
 // blk0 .. blk0 + nblk - 1 of every sequence b < B, out[b * out_seq_stride +
 // blk * out_ld + i] = E4M3((sum of the di = 128 key bytes i of the block's

@@ -44,12 +44,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     uint4 raw = make_uint4(0, 0, 0, 0);
     if (live) raw = *reinterpret_cast<const uint4*>(x + row * x_ld + part * 8);
     float v[8];
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
-      v[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
-    }
+    bf16x8_to_float(raw, v);
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
@@ -58,15 +53,8 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (!live) return;
     const int64_t drow = dst_row(row);
     if (drow < 0) return;
-    uint32_t packed = 0, sbyte = 0;
-    if (amax > 0.f) {
-      int e = floor_log2_pos(amax) - 2;
-      e = max(-127, min(127, e));
-      sbyte = (uint32_t)(e + 127);
-      const float inv = exp2_int(-e);  // -e in [-127, 127]: exact power of two
-#pragma unroll
-      for (int i = 0; i < 8; ++i) packed |= e2m1_encode(v[i] * inv) << (4 * i);
-    }
+    uint32_t sbyte;
+    const uint32_t packed = fp4_encode8(v, amax, sbyte);
     *reinterpret_cast<uint32_t*>(codes + drow * codes_ld + part * 4) = packed;
     if ((part & 3) == 0) scales[drow * scales_ld + part / 4] = (uint8_t)sbyte;
   } else {
@@ -77,16 +65,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     const int64_t drow = dst_row(row);
     if (drow < 0) return;
     const uint4 raw = *reinterpret_cast<const uint4*>(kx + row * k_ld + part * 8);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      lo |= e4m3_encode(bf16_bits_to_float(w[i] & 0xFFFFu)) << (16 * i);
-      lo |= e4m3_encode(bf16_bits_to_float(w[i] >> 16)) << (16 * i + 8);
-      hi |= e4m3_encode(bf16_bits_to_float(w[i + 2] & 0xFFFFu)) << (16 * i);
-      hi |= e4m3_encode(bf16_bits_to_float(w[i + 2] >> 16)) << (16 * i + 8);
-    }
-    *reinterpret_cast<uint2*>(k8 + drow * k8_ld + part * 8) = make_uint2(lo, hi);
+    *reinterpret_cast<uint2*>(k8 + drow * k8_ld + part * 8) = e4m3_encode8(raw);
   }
 }
 

@@ -9,19 +9,21 @@
 // both key and value.
 //
 // attn_f32_kernel    fp32 queries, one CTA per (query, head), CUDA cores.
-// attn_tc_kernel     bf16 queries, d = 512: one CTA per (80-key chunk, 16
+// attn_bf16_kernel   bf16 queries, d = 512: one CTA per (80-key chunk, 16
 //                    heads, query).  The chunk's rows are gathered and
 //                    dequantised into shared memory as bf16 (exact: every
 //                    E2M1 value times a UE8M0 scale is a bf16 value), then
-//                    S^T = K Q^T and O^T = V^T P^T run on the tcgen05
-//                    tensor cores (bf16 operands, fp32 accumulators in
-//                    tensor memory); P is split into two bf16 terms (p = hi
-//                    + lo) so the probabilities keep ~16 bits.  Each chunk
-//                    writes its (max, sum, unnormalised O) to the
-//                    workspace; the chunks of one (query, head group) form
-//                    a thread-block cluster and, after one cluster barrier,
-//                    each merges a slice of the output.  With more than 8
-//                    chunks attn_combine_kernel merges instead.
+//                    S = Q K^T and O = P V run as m16n8k16 bf16 MMAs with
+//                    fp32 accumulation (at 16 heads the operands are too
+//                    thin for the tcgen05 path: every tcgen05 MMA would
+//                    re-read a 4 KB key tile from shared memory); P is split
+//                    into two bf16 terms (p = hi + lo) so the probabilities
+//                    keep ~16 bits.  Each chunk writes its (max, sum,
+//                    unnormalised O) to the workspace; the chunks of one
+//                    (query, head group) form a thread-block cluster and,
+//                    after one cluster barrier, each merges a slice of the
+//                    output.  With more than 8 chunks attn_combine_kernel
+//                    merges instead.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -170,39 +172,35 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const csa2_attn_args a) {
 }
 
 // ---------------------------------------------------------------------------
-// bf16 tensor-core path (d = 512): tcgen05, accumulators in tensor memory
+// bf16 tensor-core path (d = 512, 16 heads per CTA, 80 keys per chunk)
 // ---------------------------------------------------------------------------
 
 constexpr int kD = 512;
-constexpr int kHG = 16;                  // heads per CTA (MMA N)
-constexpr int kKC = 80;                  // keys per chunk (S: MMA M = 128, rows 80.. unused)
+// 16 heads per CTA keep two CTAs on an SM (about 104 KB of shared memory
+// each), so the 8-CTA clusters of a 1M-context decode step all run at once.
+constexpr int kHG = 16;                  // heads per CTA
+constexpr int kKC = 80;                  // keys per chunk
+constexpr int kPairs = kKC / 16;         // key pairs of 16 (two n8 tiles)
 constexpr int kAttnWarps = 8;
 constexpr int kAttnThreads = 32 * kAttnWarps;
+constexpr int kSWarps = kPairs;          // S = Q K^T: warp w < kSWarps owns keys 16w .. 16w + 15
+constexpr int kPVSlice = kD / kAttnWarps;  // O = P V: warp w owns 64 dims
 constexpr int kMaxClusterChunks = 8;     // portable cluster size
-constexpr int kDBlocks = kD / 64;        // 64-element (128-byte) swizzle atoms along d
-constexpr int kKBlockBytes = kKC * 128;  // one d-block of the K tile: kKC rows of 128 bytes
-// shared memory (offsets from a 1024-byte aligned base)
-constexpr int kOffK = 0;                              // K tile [d-block][key][128 B], swizzled
-constexpr int kOffQ = kOffK + kDBlocks * kKBlockBytes;  // Q [d-block][head][128 B]
-constexpr int kOffP = kOffQ + kDBlocks * kHG * 128;   // P hi, P lo: [key-block][head][128 B]
-constexpr int kPBytes = 2 * kHG * 128;                // keys 0..127 in two 64-key blocks
-constexpr int kAttnSmem = kOffP + 2 * kPBytes + 1024;  // + alignment slack
-constexpr int kTmemCols = 128;           // S^T: 16 columns; O^T: 4 x 16 columns
-constexpr int kTmemO = kHG;              // first O^T column
+constexpr int kRowBytes = kD * 2 + 16;   // padded bf16 row (conflict-free ldmatrix)
+constexpr int kPRow = kKC * 2 + 16;      // padded P row
+constexpr int kSmemQ = kHG * kRowBytes;
+constexpr int kSmemK = kKC * kRowBytes;
+constexpr int kSmemP = 2 * kHG * kPRow;  // P split into bf16 hi and lo
+constexpr int kAttnSmem = kSmemQ + kSmemK + kSmemP;
 constexpr int kPieces = kD / 8;          // 16-byte pieces of a bf16 row (8 elements)
 constexpr int kBlocks = kD / 32;         // 32-element blocks of a row (16 code bytes each)
 constexpr int kBItems = kKC * kBlocks / kAttnThreads;  // K-tile blocks per thread
 constexpr int kQItems = kHG * kPieces / kAttnThreads;  // Q-tile pieces per thread
-constexpr uint64_t kAttnWaitNs = 2000000000ull;        // far beyond any legal wait
 static_assert(kKC * kBlocks % kAttnThreads == 0 && kAttnThreads % kBlocks == 0 &&
                   kHG * kPieces % kAttnThreads == 0,
               "tiles split evenly over the threads, one block column per thread");
-static_assert(kKC % 16 == 0 && kKC <= 128 && kKC > 64, "keys per chunk: PV K steps of 16");
-static_assert(kKBlockBytes % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0,
-              "swizzle atoms start on 1024-byte boundaries");
-static_assert((128 - kKC) * 128 <= kDBlocks * kHG * 128,
-              "rows kKC..127 of the last d-block (read by the M = 128 MMA, unused) stay "
-              "inside the Q tile");
+static_assert(kSWarps <= kAttnWarps && kKC % 16 == 0, "S tiling");
+static_assert(kPVSlice == 64, "PV tiling");
 
 struct PartialLayout {
   // per (query, head group, chunk): O [kHG][512] f32 (unnormalised), then m [kHG], l [kHG]
@@ -216,22 +214,54 @@ struct ChunkRows {
   const uint16_t* win[kKC];
 };
 
-// Byte offset of the 16-byte piece `piece` (0..7) of row `row` inside a
-// 128-byte swizzle atom: the piece index is XORed with row % 8.
-__device__ __forceinline__ uint32_t swz(int row, int piece) {
-  return (uint32_t)(row * 128 + ((piece ^ (row & 7)) << 4));
+// Dequantises 32 E2M1 codes (16 bytes, element 2i in the low nibble of byte
+// i) with scale byte sb into four 16-byte bf16 pieces at d0 .. d3 (piece v =
+// elements 8v .. 8v + 7).  Exact: every E2M1 value times a UE8M0 scale in
+// [2^-127, 2^125] is a bf16 value.  Out of line: the instruction cache holds
+// one copy of this code, whatever the number of call sites.
+__device__ __noinline__ void dequant_block(uint4 cw, uint32_t sb, uint8_t* d0, uint8_t* d1,
+                                           uint8_t* d2, uint8_t* d3) {
+  // scale 2^(sb - 127) in [2^-119, 2^123]: every product is a normal bf16,
+  // so the bf16x2 multiply is exact; other scales take fp32
+  if (sb >= 8 && sb <= 250) {
+    const __nv_bfloat16 sc1 = __float2bfloat16_rn(ue8m0_value(sb));
+    const __nv_bfloat162 sc2 = __halves2bfloat162(sc1, sc1);
+    uint32_t p[4];
+    e2m1x8_to_bf16(cw.x, sc2, p);
+    *reinterpret_cast<uint4*>(d0) = make_uint4(p[0], p[1], p[2], p[3]);
+    e2m1x8_to_bf16(cw.y, sc2, p);
+    *reinterpret_cast<uint4*>(d1) = make_uint4(p[0], p[1], p[2], p[3]);
+    e2m1x8_to_bf16(cw.z, sc2, p);
+    *reinterpret_cast<uint4*>(d2) = make_uint4(p[0], p[1], p[2], p[3]);
+    e2m1x8_to_bf16(cw.w, sc2, p);
+    *reinterpret_cast<uint4*>(d3) = make_uint4(p[0], p[1], p[2], p[3]);
+    return;
+  }
+  const float scf = ue8m0_value(sb);
+  auto slow = [&](uint32_t word, uint8_t* dst) {
+    uint32_t p[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t byte = (word >> (8 * b)) & 0xFFu;
+      p[b] = pack_bf16x2(e2m1_value(byte & 15u) * scf, e2m1_value(byte >> 4) * scf);
+    }
+    *reinterpret_cast<uint4*>(dst) = make_uint4(p[0], p[1], p[2], p[3]);
+  };
+  slow(cw.x, d0);
+  slow(cw.y, d1);
+  slow(cw.z, d2);
+  slow(cw.w, d3);
 }
 
-// One CTA = (key chunk, 16 heads, query).  Phases:
-//  1. key sources of the chunk (idx reads); Q copied into its swizzled tile;
-//  2. K tile: window rows copy with cp.async; FP4 rows load their code and
-//     scale bytes into registers (all loads in flight), then dequantise
-//     exactly to bf16; keys without a row are zero rows;
-//  3. S^T = K Q^T: 32 MMAs (M = 128 keys, N = 16 heads, K = 16) into tensor
-//     memory; the chunk's softmax statistics (m, l) per head and P = e^(s-m)
-//     split into bf16 hi + lo, written as the K-major B operand of
-//  4. O^T = V^T P^T: the K tile read MN-major as V^T (M = 128 dims x 4, K =
-//     keys), 2 x 5 MMAs per 128 dims;
+// One CTA = (key chunk, 16 heads, query), 8 warps, two CTAs per SM.  Phases:
+//  1. key sources of the chunk (idx reads); Q rows copying by cp.async;
+//  2. K tile: window rows by cp.async; FP4 rows load their code and scale
+//     bytes into registers (every load in flight), then dequantise exactly
+//     to bf16; keys without a row are zero rows;
+//  3. S = Q K^T (warps 0..4, m16n8k16 bf16 MMA, fp32 accumulate), the
+//     chunk's softmax statistics per head, P = e^(S - m) split into bf16 hi +
+//     lo (~16 significant bits);
+//  4. O = P V (8 warps, 64 dims each);
 //  5. the unnormalised O, m and l go to this chunk's partial in the
 //     workspace.  CLUSTER: the chunks of one (query, head group) are a
 //     thread-block cluster; after one cluster barrier each CTA merges
@@ -241,49 +271,35 @@ __device__ __forceinline__ uint32_t swz(int row, int piece) {
 // the kernels still running on the stream do not write it).
 template <bool CLUSTER>
 __global__ void __launch_bounds__(kAttnThreads, 2)
-    attn_tc_kernel(const csa2_attn_args a, int nchunks, float* __restrict__ partial, int pre) {
-  extern __shared__ uint8_t sm_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* sK = smem + kOffK;
-  uint8_t* sQ = smem + kOffQ;
-  uint8_t* sPh = smem + kOffP;
-  uint8_t* sPl = sPh + kPBytes;
+    attn_bf16_kernel(const csa2_attn_args a, int nchunks, float* __restrict__ partial, int pre) {
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  uint8_t* sQ = sm_raw;
+  uint8_t* sK = sm_raw + kSmemQ;
+  uint8_t* sPh = sK + kSmemK;
+  uint8_t* sPl = sPh + kHG * kPRow;
   __shared__ ChunkRows rows;
-  __shared__ __align__(8) uint64_t bar_s, bar_o;
-  __shared__ uint32_t tmem_slot;
-  __shared__ float red_m[3][kHG], red_l[3][kHG];
-  __shared__ float s_m[kHG], s_l[kHG];
-  __shared__ int s_abort;
+  __shared__ float red_m[kPairs][kHG], red_l[kPairs][kHG];
 
   const int chunk = blockIdx.x, hg = blockIdx.y;
   const int64_t qi = blockIdx.z;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
-  const int ngroups = a.hq / kHG;
-
-  if (tid == 0) {
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_o, 1);
-    s_abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
-  // Q [16 heads x 512] -> [d-block][head][128 B], swizzled
-  const uint8_t* qsrc =
-      static_cast<const uint8_t*>(a.q) + ((qi * a.hq + (int64_t)hg * kHG) * kD) * 2;
+  const int ngroups = (a.hq + kHG - 1) / kHG;
+  // heads of this group that exist (hq may be an odd multiple of 16)
+  const int hvalid = min(kHG, a.hq - hg * kHG);
   auto load_q = [&] {
+    const uint8_t* qsrc = static_cast<const uint8_t*>(a.q) +
+                          ((qi * a.hq + (int64_t)hg * kHG) * kD) * 2;
 #pragma unroll
     for (int u = 0; u < kQItems; ++u) {
       const int i = tid + u * kAttnThreads;
-      const int h = i / kPieces, c = i % kPieces;
-      cp_async16(sQ + (c >> 3) * (kHG * 128) + swz(h, c & 7), qsrc + h * kD * 2 + c * 16);
+      const int r = i / kPieces, c = i % kPieces;
+      if (r < hvalid)
+        cp_async16(sQ + r * kRowBytes + c * 16, qsrc + r * kD * 2 + c * 16);
+      else
+        *reinterpret_cast<uint4*>(sQ + r * kRowBytes + c * 16) = make_uint4(0, 0, 0, 0);
     }
   };
   if (pre) load_q();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_slot;
   pdl_wait();
   if (!pre) load_q();
 
@@ -302,15 +318,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   }
   __syncthreads();
 
-  // ---- 2. K tile: item = (key r, 32-element block c) = 16 code bytes -> 64
-  // bf16 bytes = 4 pieces of the d-block c / 2; thread t takes block c = t %
-  // 16 of keys t / 16 + 16u.  A thread's four pieces go out in the order
-  // (v + rot) % 4 so that the lanes of a warp spread over the bank groups.
+  // ---- 2. K tile: item = (row r, 32-element block c) = 16 code bytes -> 64
+  // bf16 bytes; thread t always takes block c = t % 16 of rows t / 16 + 16u.
+  // FP4 items load their 16 code bytes and scale byte into registers first
+  // (every load in flight at once); window items copy 64 bytes with
+  // cp.async.  An item's four 16-byte output pieces go out in the order
+  // (v + t / 2) % 4, so each group of 8 lanes covers all 8 bank quads of its
+  // 128-byte wavefront.
   {
     const int c = tid % kBlocks;
     const int rot = (tid >> 1) & 3;
-    uint8_t* kblk = sK + (c >> 1) * kKBlockBytes;
-    const int p0 = (c & 1) * 4;  // first piece of the block inside its 128-byte row
     uint4 cw[kBItems];
     uint32_t sb[kBItems];
 #pragma unroll
@@ -319,183 +336,175 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const uint8_t* cp = rows.codes[r];
       cw[u] = cp ? __ldg(reinterpret_cast<const uint4*>(cp) + c) : make_uint4(0, 0, 0, 0);
       sb[u] = cp ? (uint32_t)__ldg(rows.scales[r] + c) : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < kBItems; ++u) {
-      const int r = tid / kBlocks + u * (kAttnThreads / kBlocks);
-      const uint16_t* wrow = rows.win[r];
-      if (wrow) {
+      if (const uint16_t* wrow = rows.win[r]) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int vv = (v + rot) & 3;
-          cp_async16(kblk + swz(r, p0 + vv), wrow + c * 32 + vv * 8);
+          cp_async16(sK + r * kRowBytes + c * 64 + vv * 16, wrow + c * 32 + vv * 8);
         }
       }
     }
-#pragma unroll
+#pragma unroll  // small: the dequantiser is one out-of-line copy
     for (int u = 0; u < kBItems; ++u) {
       const int r = tid / kBlocks + u * (kAttnThreads / kBlocks);
       if (rows.win[r]) continue;  // copied by cp.async
-      const bool fp4 = rows.codes[r] != nullptr;  // else: no key, zero row (P is 0 there)
-      // scale 2^(sb - 127) in [2^-119, 2^123]: every product is a normal
-      // bf16, so the bf16x2 multiply is exact; other scales take fp32
-      const bool fast = sb[u] >= 8 && sb[u] <= 250;
-      const float scf = ue8m0_value(sb[u]);
-      const __nv_bfloat16 sc1 = __float2bfloat16_rn(fast ? scf : 1.f);
-      const __nv_bfloat162 sc2 = __halves2bfloat162(sc1, sc1);
+      uint8_t* row = sK + r * kRowBytes + c * 64;
+      if (rows.codes[r]) {
+        // piece v (code word v) always lands at row + 16 v; the words are
+        // handed over starting at piece rot, so the stores go out in the
+        // rotated order
+        const uint4 w = cw[u];
+        auto word = [&](int v) {
+          v &= 3;
+          return v == 0 ? w.x : (v == 1 ? w.y : (v == 2 ? w.z : w.w));
+        };
+        dequant_block(make_uint4(word(rot), word(rot + 1), word(rot + 2), word(rot + 3)), sb[u],
+                      row + ((0 + rot) & 3) * 16, row + ((1 + rot) & 3) * 16,
+                      row + ((2 + rot) & 3) * 16, row + ((3 + rot) & 3) * 16);
+      } else {  // no key: a zero row (finite values where P is 0)
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int vv = (v + rot) & 3;
-        const uint32_t word =
-            vv == 0 ? cw[u].x : (vv == 1 ? cw[u].y : (vv == 2 ? cw[u].z : cw[u].w));
-        uint32_t packed[4] = {0u, 0u, 0u, 0u};
-        if (fast) {
-          e2m1x8_to_bf16(word, sc2, packed);
-        } else if (fp4) {
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const uint32_t byte = (word >> (8 * p)) & 0xFFu;
-            packed[p] = pack_bf16x2(e2m1_value(byte & 15u) * scf, e2m1_value(byte >> 4) * scf);
-          }
-        }
-        *reinterpret_cast<uint4*>(kblk + swz(r, p0 + vv)) =
-            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        for (int v = 0; v < 4; ++v)
+          *reinterpret_cast<uint4*>(row + v * 16) = make_uint4(0, 0, 0, 0);
       }
     }
   }
   cp_async_wait_all();
-  fence_proxy_async_smem();
   __syncthreads();
 
-  // ---- 3. S^T = K Q^T (one thread issues; K = 512 in 32 steps of 16)
-  if (tid == 0) {
-    tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16_f32(128, kHG);
-    const uint32_t kb = smem_u32(sK), qb = smem_u32(sQ);
-#pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
-      const uint32_t in = (uint32_t)(kk & 3) * 32;  // 16 bf16 = 32 bytes along the atom
-      tc_mma_bf16(tmem, sdesc_k_sw128(kb + (kk >> 2) * kKBlockBytes + in),
-                  sdesc_k_sw128(qb + (kk >> 2) * (kHG * 128) + in), idesc, kk > 0 ? 1u : 0u);
+  // ---- 3. S = Q K^T and the chunk softmax (warps 0 .. kSWarps-1)
+  const int r0 = lane >> 2;
+  if (warp < kSWarps) {
+    const int pr = warp;
+    // two independent accumulator chains per n-tile: dims 0..255 and 256..511
+    float s1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const uint32_t qbase = smem_u32(sQ) + (lane & 15) * kRowBytes + (lane >> 4) * 16;
+    const int krow = pr * 16 + (lane & 7) + ((lane >> 4) << 3);
+    const uint32_t kbase = smem_u32(sK) + krow * kRowBytes + ((lane >> 3) & 1) * 16;
+#pragma unroll 4
+    for (int ks = 0; ks < kD / 32; ++ks) {
+      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+      uint32_t c0, c1, c2, c3, d0, d1, d2, d3;
+      ldmatrix_x4(qbase + ks * 32, a0, a1, a2, a3);
+      ldmatrix_x4(kbase + ks * 32, b0, b1, b2, b3);
+      ldmatrix_x4(qbase + (ks + kD / 32) * 32, c0, c1, c2, c3);
+      ldmatrix_x4(kbase + (ks + kD / 32) * 32, d0, d1, d2, d3);
+      mma_bf16_16816(s1[0], a0, a1, a2, a3, b0, b1);
+      mma_bf16_16816(s1[1], a0, a1, a2, a3, b2, b3);
+      mma_bf16_16816(s2[0], c0, c1, c2, c3, d0, d1);
+      mma_bf16_16816(s2[1], c0, c1, c2, c3, d2, d3);
     }
-    tc_commit(&bar_s);
+    // rows (heads) r0 (e = 0, 1) and r0 + 8 (e = 2, 3); keys 16pr + 8nt + 2(lane%4) + (e&1)
+    float sc[2][4];
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = pr * 16 + nt * 8 + 2 * (lane & 3) + (e & 1);
+        const bool valid = rows.codes[key] || rows.win[key];
+        sc[nt][e] = valid ? (s1[nt][e] + s2[nt][e]) * a.softmax_scale : -INFINITY;
+        if (e < 2)
+          m0 = fmaxf(m0, sc[nt][e]);
+        else
+          m1 = fmaxf(m1, sc[nt][e]);
+      }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+    if ((lane & 3) == 0) {
+      red_m[pr][r0] = m0;
+      red_m[pr][r0 + 8] = m1;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kSWarps * 32) : "memory");  // S warps only
+    m0 = m1 = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kPairs; ++w) {
+      m0 = fmaxf(m0, red_m[w][r0]);
+      m1 = fmaxf(m1, red_m[w][r0 + 8]);
+    }
+    float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float m = e < 2 ? m0 : m1;
+        p[e] = (sc[nt][e] == -INFINITY) ? 0.f : __expf(sc[nt][e] - m);
+      }
+      l0 += p[0] + p[1];
+      l1 += p[2] + p[3];
+      const int col = pr * 16 + nt * 8 + 2 * (lane & 3);
+      // p = hi + lo with hi = bf16(p), lo = bf16(p - hi): ~16 significant bits
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
+      const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
+      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+      *reinterpret_cast<__nv_bfloat162*>(sPh + r0 * kPRow + col * 2) = h01;
+      *reinterpret_cast<__nv_bfloat162*>(sPh + (r0 + 8) * kPRow + col * 2) = h23;
+      *reinterpret_cast<uint32_t*>(sPl + r0 * kPRow + col * 2) =
+          pack_bf16x2(p[0] - f01.x, p[1] - f01.y);
+      *reinterpret_cast<uint32_t*>(sPl + (r0 + 8) * kPRow + col * 2) =
+          pack_bf16x2(p[2] - f23.x, p[3] - f23.y);
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    if ((lane & 3) == 0) {
+      red_l[pr][r0] = l0;
+      red_l[pr][r0 + 8] = l1;
+    }
   }
-  // softmax over the chunk's keys: warps of TMEM lane quarters 0..2 (keys
-  // 0..95; keys >= kKC are not in the chunk), warp w takes heads 8 (w / 4) ..
-  const int qtr = warp & 3;
-  const int h0 = (warp >> 2) * 8;
-  const bool smx = qtr < 3;
-  const int key = qtr * 32 + lane;
-  bool ok = mbar_wait(&bar_s, 0, &s_abort, a.dev_status, kAttnWaitNs);
-  ok = __all_sync(0xffffffffu, ok);
-  tc_fence_after();
-  float sv[8];
-  if (smx) {
-    if (ok) {
-      tmem_ld8(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)h0, sv);
-      tmem_ld_wait();
-    }
-    const bool valid = ok && key < kKC && (rows.codes[key] || rows.win[key]);
+  __syncthreads();
+
+  // ---- 4. O = P V: dims d0 .. d0+63 (8 n-tiles), keys as the K dimension
+  const int d0 = warp * kPVSlice;
+  float o[8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      sv[i] = valid ? sv[i] * a.softmax_scale : -INFINITY;
-      // max over the warp's 32 keys on order-preserving integer keys
-      const uint32_t mk = __reduce_max_sync(0xffffffffu, score_key(sv[i]));
-      if (lane == 0) {
-        const uint32_t u = (mk & 0x80000000u) ? (mk & 0x7FFFFFFFu) : ~mk;
-        red_m[qtr][h0 + i] = __uint_as_float(u);
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  {
+    const uint32_t pbase_h = smem_u32(sPh) + (lane & 15) * kPRow + (lane >> 4) * 16;
+    const uint32_t pbase_l = smem_u32(sPl) + (lane & 15) * kPRow + (lane >> 4) * 16;
+    const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t vbase = smem_u32(sK) + vrow * kRowBytes + (d0 + (lane >> 4) * 8) * 2;
+#pragma unroll
+    for (int ks = 0; ks < kKC / 16; ++ks) {
+      uint32_t h0r, h1r, h2r, h3r, l0r, l1r, l2r, l3r;
+      ldmatrix_x4(pbase_h + ks * 32, h0r, h1r, h2r, h3r);
+      ldmatrix_x4(pbase_l + ks * 32, l0r, l1r, l2r, l3r);
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(vbase + ks * 16 * kRowBytes + np * 32, b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * np], h0r, h1r, h2r, h3r, b0, b1);
+        mma_bf16_16816(o[2 * np], l0r, l1r, l2r, l3r, b0, b1);
+        mma_bf16_16816(o[2 * np + 1], h0r, h1r, h2r, h3r, b2, b3);
+        mma_bf16_16816(o[2 * np + 1], l0r, l1r, l2r, l3r, b2, b3);
       }
     }
   }
-  __syncthreads();
-  if (smx) {
-    float l8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float m = fmaxf(fmaxf(red_m[0][h0 + i], red_m[1][h0 + i]), red_m[2][h0 + i]);
-      const float p = (sv[i] == -INFINITY) ? 0.f : expf(sv[i] - m);
-      float l = p;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      l8[i] = l;
-      // P = hi + lo with hi = bf16(p), lo = bf16(p - hi): ~16 significant
-      // bits.  Element (head h, key t) of the K-major operand.
-      if (key < kKC) {
-        const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-        const int h = h0 + i;
-        const uint32_t off = (uint32_t)((key >> 6) * (kHG * 128)) + swz(h, (key & 63) >> 3) +
-                             (uint32_t)((key & 7) * 2);
-        *reinterpret_cast<__nv_bfloat16*>(sPh + off) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(sPl + off) = lo;
-      }
-    }
-    if (lane == 0)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) red_l[qtr][h0 + i] = l8[i];
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  if (tid < kHG) {
-    s_m[tid] = fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]), red_m[2][tid]);
-    s_l[tid] = red_l[0][tid] + red_l[1][tid] + red_l[2][tid];
-  }
 
-  // ---- 4. O^T = V^T P^T: dims 128 mb .. as M (two d-blocks, MN-major), keys as K
-  if (tid == 0 && ok) {
-    tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16_f32(128, kHG, true);
-    const uint32_t kb = smem_u32(sK), ph = smem_u32(sPh), pl = smem_u32(sPl);
-#pragma unroll
-    for (int mb = 0; mb < kD / 128; ++mb)
-#pragma unroll
-      for (int ks = 0; ks < kKC / 16; ++ks) {
-        const uint64_t ad = sdesc_mn_sw128(kb + (2 * mb) * kKBlockBytes + ks * 2048,
-                                           kKBlockBytes, 1024);
-        const uint32_t pof = (uint32_t)((ks >> 2) * (kHG * 128) + (ks & 3) * 32);
-        const uint32_t dt = tmem + (uint32_t)(kTmemO + kHG * mb);
-        tc_mma_bf16(dt, ad, sdesc_k_sw128(ph + pof), idesc, ks > 0 ? 1u : 0u);
-        tc_mma_bf16(dt, ad, sdesc_k_sw128(pl + pof), idesc, 1u);
-      }
-    tc_commit(&bar_o);
-  }
-
-  // ---- 5. this chunk's partial: O (unnormalised), m, l
+  // ---- 5. this chunk's partial: O (unnormalised), then m and l per head
   float* part = partial + ((qi * ngroups + hg) * (int64_t)nchunks + chunk) *
                               PartialLayout::kFloats;
-  {
-    bool got = ok && mbar_wait(&bar_o, 0, &s_abort, a.dev_status, kAttnWaitNs);
-    got = __all_sync(0xffffffffu, got);
-    tc_fence_after();
-    // warp w: TMEM lane quarter w % 4 (dims 32 (w % 4) + lane of each block
-    // of 128), blocks 2 (w / 4) and 2 (w / 4) + 1
 #pragma unroll
-    for (int bb = 0; bb < 2; ++bb) {
-      const int mb = 2 * (warp >> 2) + bb;
-      float o[16];
-      if (got) {
-        tmem_ld16(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)(kTmemO + kHG * mb), o);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = 0.f;
-      }
-      const int dd = mb * 128 + qtr * 32 + lane;
-#pragma unroll
-      for (int h = 0; h < kHG; ++h) part[h * kD + dd] = o[h];
-    }
-    __syncthreads();  // s_m / s_l are set
-    if (tid < kHG) {
-      part[kHG * kD + tid] = ok ? s_m[tid] : -INFINITY;
-      part[kHG * kD + kHG + tid] = ok ? s_l[tid] : 0.f;
-    }
+  for (int nt = 0; nt < 8; ++nt) {
+    const int col = d0 + nt * 8 + 2 * (lane & 3);
+    *reinterpret_cast<float2*>(part + r0 * kD + col) = make_float2(o[nt][0], o[nt][1]);
+    *reinterpret_cast<float2*>(part + (r0 + 8) * kD + col) = make_float2(o[nt][2], o[nt][3]);
   }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+  if (tid < kHG) {
+    float m = -INFINITY, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPairs; ++w) {
+      m = fmaxf(m, red_m[w][tid]);
+      l += red_l[w][tid];
+    }
+    part[kHG * kD + tid] = m;
+    part[kHG * kD + kHG + tid] = l;
   }
 
   if constexpr (CLUSTER) {
@@ -510,6 +519,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const int v0 = rank * kVec / nchunks, v1 = (rank + 1) * kVec / nchunks;
     for (int v = v0 + tid; v < v1; v += kAttnThreads) {
       const int h = (v * 4) / kD, d = (v * 4) % kD;
+      if (h >= hvalid) break;  // v grows with h
       float2 ml[kMaxClusterChunks];
       float4 x[kMaxClusterChunks];
 #pragma unroll
@@ -529,7 +539,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       float L = 0.f, f[kMaxClusterChunks];
 #pragma unroll
       for (int c = 0; c < kMaxClusterChunks; ++c) {
-        f[c] = (ml[c].x == -INFINITY) ? 0.f : expf(ml[c].x - M);
+        f[c] = (ml[c].x == -INFINITY) ? 0.f : __expf(ml[c].x - M);
         L += f[c] * ml[c].y;
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -617,21 +627,21 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s, bool q_
   }
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
-    cudaError_t r = cudaFuncSetAttribute(attn_tc_kernel<true>,
+    cudaError_t r = cudaFuncSetAttribute(attn_bf16_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(attn_tc_kernel<false>,
+      r = cudaFuncSetAttribute(attn_bf16_kernel<false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     return r;
   });
   if (e != cudaSuccess) return cuda_fail(e);
-  const dim3 grid((unsigned)nchunks, (unsigned)(a.hq / kHG), (unsigned)a.nq);
+  const dim3 grid((unsigned)nchunks, (unsigned)((a.hq + kHG - 1) / kHG), (unsigned)a.nq);
   float* partial = static_cast<float*>(a.workspace);
   const int pre = q_ready ? 1 : 0;
   if (nchunks <= kMaxClusterChunks)
-    return launch_kernel(attn_tc_kernel<true>, grid, dim3(kAttnThreads), (size_t)kAttnSmem, s,
+    return launch_kernel(attn_bf16_kernel<true>, grid, dim3(kAttnThreads), (size_t)kAttnSmem, s,
                          (unsigned)nchunks, a, nchunks, partial, pre);
-  csa2_status st = launch_kernel(attn_tc_kernel<false>, grid, dim3(kAttnThreads),
+  csa2_status st = launch_kernel(attn_bf16_kernel<false>, grid, dim3(kAttnThreads),
                                  (size_t)kAttnSmem, s, 1, a, nchunks, partial, pre);
   if (st != CSA2_OK) return st;
   return launch_kernel(attn_combine_kernel, dim3((unsigned)a.hq, (unsigned)a.nq), dim3(128), 0, s,

@@ -42,7 +42,7 @@ constexpr int kHistThreads = 512;
 constexpr int kRound = kTkThreads * 4;        // scores per round: one float4 per thread
 constexpr int kRounds = 4;                    // rounds whose loads are in flight together
 constexpr int kBatch = kRound * kRounds;      // 8192 scores per batch
-constexpr int kCandCap = 4096;                // kept entries a CTA holds in shared memory
+constexpr int kCandCap = 8192;                // kept entries a CTA holds in shared memory
 constexpr int kSlotCap = 1024;                // kept entries a slice may publish
 constexpr int kMaxSlices = 64;
 constexpr int kSliceTarget = 296;             // CTAs of one launch to aim for (2 per SM)
@@ -63,7 +63,7 @@ __device__ __forceinline__ int64_t row_nvalid(const int32_t* n_valid, int64_t ro
 __global__ void __launch_bounds__(kHistThreads)
     topk_hist_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
                      const int32_t* __restrict__ n_valid, uint32_t* __restrict__ hist1,
-                     int64_t chunk) {
+                     int64_t chunk, const uint32_t* __restrict__ within) {
   __shared__ uint32_t h[kBins];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < kBins; i += kHistThreads) h[i] = 0;
@@ -74,6 +74,10 @@ __global__ void __launch_bounds__(kHistThreads)
   const int64_t j0 = (int64_t)blockIdx.x * chunk;
   const int64_t j1 = min(nv, j0 + chunk);
   const float* s = scores + row * ld;
+  // level 1: every key by its top 12 bits; within a bin: that bin's keys by
+  // their next 12 bits
+  const bool sub = within != nullptr;
+  const uint32_t t1 = sub ? within[row] >> 20 : 0u;
   constexpr int U = 4;
   for (int64_t base = j0 + warp * 32; base < j1; base += (int64_t)kHistThreads * U) {
     float x[U];
@@ -85,13 +89,21 @@ __global__ void __launch_bounds__(kHistThreads)
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t j = base + u * kHistThreads + lane;
-      if (j < j1) atomicAdd(&h[score_key(x[u]) >> 20], 1u);
+      const uint32_t key = score_key(x[u]);
+      if (j < j1 && (!sub || (key >> 20) == t1))
+        atomicAdd(&h[sub ? (key >> 8) & (kBins - 1) : key >> 20], 1u);
     }
   }
   __syncthreads();
   pdl_trigger();
+  uint32_t* hrow = hist1 + row * kTopkHistStride;
   for (int i = tid; i < kBins; i += kHistThreads)
-    if (h[i]) atomicAdd(&hist1[row * kBins + i], h[i]);
+    if (h[i]) atomicAdd(&hrow[i], h[i]);
+  if (tid < kTopkCoarse) {  // coarse bin t: fine bins 64t .. 64t + 63
+    uint32_t v = 0;
+    for (int i = 0; i < kBins / kTopkCoarse; ++i) v += h[tid * (kBins / kTopkCoarse) + i];
+    if (v) atomicAdd(&hrow[kBins + tid], v);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -124,8 +136,15 @@ __device__ void find_top(const uint32_t* h, int nb, uint32_t target, TkTmp* tmp)
   }
   if (lane == 31) tmp->wsum[warp] = incl;
   __syncthreads();
-  uint32_t woff = 0;
-  for (int w = 0; w < warp; ++w) woff += tmp->wsum[w];
+  // exclusive prefix of the warp totals: lane w < kTkWarps of every warp
+  // scans them (kTkWarps <= 32)
+  uint32_t wv = lane < kTkWarps ? tmp->wsum[lane] : 0u;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, wv, o);
+    if (lane >= o) wv += y;
+  }
+  const uint32_t woff = __shfl_sync(0xffffffffu, wv, (warp + 31) & 31) * (warp > 0);
   const uint32_t before = woff + incl - local;
   if (local > 0 && before < target && before + local >= target) {
     uint32_t cum = before;
@@ -200,6 +219,24 @@ __device__ Threshold resolve_threshold(uint32_t T1, uint32_t need, uint32_t cnt1
 // ties precede it in index order).  emit(pos, key, j) receives every taken
 // entry with its rank among taken entries.  Returns the number taken.
 // Block-wide (every thread calls it with the same arguments).
+// This thread's float4s of the batch starting at b0 (scores [b0, j1)).
+__device__ __forceinline__ void load_batch(const float* __restrict__ s, int64_t b0, int64_t j1,
+                                           int vec, float4* x) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int u = 0; u < kRounds; ++u) {
+    const int64_t j = b0 + (int64_t)u * kRound + tid * 4;
+    if (vec && j + 3 < j1) {
+      x[u] = __ldcs(reinterpret_cast<const float4*>(s + j));
+    } else {
+      x[u].x = j < j1 ? s[j] : 0.f;
+      x[u].y = j + 1 < j1 ? s[j + 1] : 0.f;
+      x[u].z = j + 2 < j1 ? s[j + 2] : 0.f;
+      x[u].w = j + 3 < j1 ? s[j + 3] : 0.f;
+    }
+  }
+}
+
 template <class Cls, class Emit>
 __device__ uint32_t ordered_take(const float* __restrict__ s, int64_t j0, int64_t j1, int vec,
                                  uint32_t quota, TkTmp* tmp, Cls&& cls, Emit&& emit) {
@@ -207,18 +244,7 @@ __device__ uint32_t ordered_take(const float* __restrict__ s, int64_t j0, int64_
   uint32_t taken1 = 0, ties = 0;  // block-uniform: class-1 entries and ties of earlier batches
   for (int64_t b0 = j0; b0 < j1; b0 += kBatch) {
     float4 x[kRounds];
-#pragma unroll
-    for (int u = 0; u < kRounds; ++u) {
-      const int64_t j = b0 + (int64_t)u * kRound + tid * 4;
-      if (vec && j + 3 < j1) {
-        x[u] = __ldcs(reinterpret_cast<const float4*>(s + j));
-      } else {
-        x[u].x = j < j1 ? s[j] : 0.f;
-        x[u].y = j + 1 < j1 ? s[j + 1] : 0.f;
-        x[u].z = j + 2 < j1 ? s[j + 2] : 0.f;
-        x[u].w = j + 3 < j1 ? s[j + 3] : 0.f;
-      }
-    }
+    load_batch(s, b0, j1, vec, x);
     uint32_t c[kRounds], incl[kRounds];
     uint32_t cl[kRounds];  // 2 bits per element: its class
 #pragma unroll
@@ -235,10 +261,12 @@ __device__ uint32_t ordered_take(const float* __restrict__ s, int64_t j0, int64_
       cl[u] = packed;
       c[u] = cnt;
       uint32_t v = cnt;
+      if (__ballot_sync(0xffffffffu, cnt != 0)) {  // most rounds of a warp keep nothing
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += y;
+        }
       }
       incl[u] = v;
       if (lane == 31) tmp->wsum[u * kTkWarps + warp] = v;
@@ -395,7 +423,7 @@ __device__ void write_selected(const uint32_t* key, int nc, const Threshold& th,
 struct ScanLayout {
   int64_t rows;
   int S;
-  __host__ __device__ size_t hist_bytes() const { return (size_t)rows * kBins * 4; }
+  __host__ __device__ size_t hist_bytes() const { return (size_t)rows * kTopkHistStride * 4; }
   __host__ __device__ size_t counter_off() const { return hist_bytes(); }
   __host__ __device__ size_t slot_off() const {
     return align256_hd(counter_off() + (size_t)rows * 16);
@@ -428,7 +456,7 @@ __global__ void __launch_bounds__(kTkThreads, 2)
   uint32_t* ckey = dyn + kBins;                             // [kCandCap] kept keys
   int32_t* cidx = reinterpret_cast<int32_t*>(dyn + kBins + kCandCap);  // their indices
   __shared__ TkTmp tmp;
-  __shared__ uint32_t s_last, s_base[kMaxSlices + 1];
+  __shared__ uint32_t s_last, s_base[kMaxSlices + 1], s_cnt[kMaxSlices];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();
@@ -437,7 +465,7 @@ __global__ void __launch_bounds__(kTkThreads, 2)
   const int64_t nv = row_nvalid(n_valid, row, n);
   const uint32_t m = (uint32_t)(nv < (int64_t)k ? nv : (int64_t)k);
   int32_t* out = idx_out + row * idx_ld;
-  uint32_t* hrow = hist1 + row * kBins;
+  uint32_t* hrow = hist1 + row * kTopkHistStride;
   const int32_t* rmap = remap ? remap + row * remap_ld : nullptr;
   const float* s = scores + row * ld;
   if (nv <= k) {  // every visible entry is selected; slice 0 writes the row
@@ -445,27 +473,58 @@ __global__ void __launch_bounds__(kTkThreads, 2)
       for (int64_t i = tid; i < k; i += kTkThreads)
         out[i] = i < nv ? (rmap ? rmap[i] : (int32_t)i) : -1;
       if (clear)
-        for (int i = tid; i < kBins; i += kTkThreads) hrow[i] = 0;
+        for (int i = tid; i < kTopkHistStride; i += kTkThreads) hrow[i] = 0;
     }
     return;
   }
 
-  // ---- level 1: threshold bin from the row's histogram (all loads in flight)
-  {
-    uint32_t hv[kBins / kTkThreads];
+  // the slice's first scores move into L1 while the histogram is read and
+  // searched (a prefetch holds no registers)
+  const int64_t j0 = min(nv, (int64_t)sl * slice), j1 = min(nv, j0 + slice);
 #pragma unroll
-    for (int u = 0; u < kBins / kTkThreads; ++u) hv[u] = hrow[tid + u * kTkThreads];
+  for (int u = 0; u < kRounds; ++u) {
+    const int64_t j = j0 + (int64_t)u * kRound + tid * 4;
+    if (j < j1) asm volatile("prefetch.global.L1 [%0];" ::"l"(s + j));
+  }
+
+  // ---- level 1: the threshold bin from the row's coarse bins, then the 64
+  // fine bins under the chosen coarse bin (warp 0; two rounds of loads)
+  if (warp == 0) {
+    // lane l holds bins 63 - 2l and 62 - 2l: suffix counts in descending order
+    auto pick = [&](const uint32_t* bins, uint32_t target, uint32_t& bin, uint32_t& above) {
+      const uint32_t hi = __ldcg(bins + 63 - 2 * lane), lo = __ldcg(bins + 62 - 2 * lane);
+      uint32_t incl = hi + lo;
 #pragma unroll
-    for (int u = 0; u < kBins / kTkThreads; ++u) hist[tid + u * kTkThreads] = hv[u];
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t before = incl - hi - lo;
+      const bool here = before < target && incl >= target;
+      const uint32_t who = __ballot_sync(0xffffffffu, here);
+      const int src = who ? __ffs(who) - 1 : 31;
+      const uint32_t b = before + hi >= target ? 63 - 2 * lane : 62 - 2 * lane;
+      const uint32_t ab = before + hi >= target ? before : before + hi;
+      bin = who ? __shfl_sync(0xffffffffu, b, src) : 0u;
+      above = who ? __shfl_sync(0xffffffffu, ab, src) : 0u;
+      return __shfl_sync(0xffffffffu, before + hi >= target ? hi : lo, src);
+    };
+    uint32_t cbin, cabove, fbin, fabove;
+    pick(hrow + kBins, m, cbin, cabove);
+    const uint32_t cnt = pick(hrow + cbin * (kBins / kTopkCoarse), m - cabove, fbin, fabove);
+    if (lane == 0) {
+      tmp.t = (int)(cbin * (kBins / kTopkCoarse) + fbin);
+      tmp.above = cabove + fabove;
+      tmp.total = cnt;
+    }
   }
   __syncthreads();
-  find_top(hist, kBins, m, &tmp);
   const uint32_t T1 = (uint32_t)tmp.t;
   const uint32_t need = m - tmp.above;
-  const uint32_t cnt1 = hist[T1];
+  const uint32_t cnt1 = tmp.total;
+  __syncthreads();  // tmp is rewritten by the scan
 
   // ---- this slice: keep (key, index) of every entry in a bin >= T1
-  const int64_t j0 = min(nv, (int64_t)sl * slice), j1 = min(nv, j0 + slice);
   const uint32_t kept = ordered_take(
       s, j0, j1, vec, 0u, &tmp, [&](uint32_t key, int64_t) { return (key >> 20) >= T1 ? 1u : 0u; },
       [&](uint32_t pos, uint32_t key, int64_t j) {
@@ -493,38 +552,56 @@ __global__ void __launch_bounds__(kTkThreads, 2)
       sj[i] = cidx[i];
     }
     if (tid == 0) *reinterpret_cast<uint32_t*>(slot) = kept;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&counters[row * 4], 1u) == (uint32_t)(S - 1);
+    __syncthreads();  // the CTA's slot writes happen before thread 0's fence
+    if (tid == 0) {
+      __threadfence();
+      s_last = atomicAdd(&counters[row * 4], 1u) == (uint32_t)(S - 1);
+      if (s_last) __threadfence();  // every other slice's writes are visible from here
+    }
     __syncthreads();
     if (!s_last) {
       pdl_trigger();
       return;
     }
-    __threadfence();
-    // slot counts -> offsets (slice order = index order): warp 0 loads every
-    // count at once (two per lane) and scans them
+    // every slot's count and its first 32 (key, index) pairs in one round
+    // of cp.async copies into shared memory (the histogram's space is free
+    // until the threshold is resolved): slot c's pairs land at hist[64 c ..]
+    static_assert(kMaxSlices * 64 <= kBins, "staging fits in the histogram");
+    for (int c = warp; c < S; c += kTkWarps) {
+      const uint8_t* sc = slots + ((size_t)row * S + c) * ScanLayout::kSlotBytes;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(hist + 64 * c + lane)),
+                   "l"(sc + 16 + lane * 4) : "memory");
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                       smem_u32(hist + 64 * c + 32 + lane)),
+                   "l"(sc + 16 + (size_t)kSlotCap * 4 + lane * 4) : "memory");
+      if (lane == 0)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&s_base[c])),
+                     "l"(sc) : "memory");
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // counts -> offsets (slice order = index order)
     if (warp == 0) {
-      uint32_t cnt[2], ovf = 0;
+      uint32_t cc[2], ovf = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c = lane + 32 * h;
-        cnt[h] = c < S ? __ldcg(reinterpret_cast<const uint32_t*>(
-                             slots + ((size_t)row * S + c) * ScanLayout::kSlotBytes))
-                       : 0u;
-        ovf |= cnt[h] > (uint32_t)kSlotCap;
+        cc[h] = c < S ? s_base[c] : 0u;
+        ovf |= cc[h] > (uint32_t)kSlotCap;
       }
+      __syncwarp();
       uint32_t run = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t incl = cnt[h];
+        uint32_t incl = cc[h];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
         const int c = lane + 32 * h;
-        if (c < S) s_base[c] = run + incl - cnt[h];
+        if (c < S) s_cnt[c] = cc[h];
+        if (c < S) s_base[c] = run + incl - cc[h];
         run += __shfl_sync(0xffffffffu, incl, 31);
       }
       ovf = __any_sync(0xffffffffu, ovf != 0);
@@ -538,15 +615,20 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     overflow = tmp.flag != 0;
     nc = (int)s_base[S];
     if (!overflow) {
-      // warp w gathers slots w, w + 16, ..: their loads are in flight together
       for (int c = warp; c < S; c += kTkWarps) {
-        const uint32_t b = s_base[c], cnt = s_base[c + 1] - b;
-        const uint8_t* sc = slots + ((size_t)row * S + c) * ScanLayout::kSlotBytes;
-        const uint32_t* sk2 = reinterpret_cast<const uint32_t*>(sc + 16);
-        const int32_t* sj2 = reinterpret_cast<const int32_t*>(sc + 16 + (size_t)kSlotCap * 4);
-        for (uint32_t i = lane; i < cnt; i += 32) {
-          ckey[b + i] = __ldcg(sk2 + i);
-          cidx[b + i] = __ldcg(sj2 + i);
+        const uint32_t b = s_base[c], cnt = s_cnt[c];
+        if ((uint32_t)lane < cnt) {
+          ckey[b + lane] = hist[64 * c + lane];
+          cidx[b + lane] = (int32_t)hist[64 * c + 32 + lane];
+        }
+        if (cnt > 32) {  // the rest of a long slot
+          const uint8_t* sc = slots + ((size_t)row * S + c) * ScanLayout::kSlotBytes;
+          const uint32_t* sk2 = reinterpret_cast<const uint32_t*>(sc + 16);
+          const int32_t* sj2 = reinterpret_cast<const int32_t*>(sc + 16 + (size_t)kSlotCap * 4);
+          for (uint32_t i = 32 + lane; i < cnt; i += 32) {
+            ckey[b + i] = __ldcg(sk2 + i);
+            cidx[b + i] = __ldcg(sj2 + i);
+          }
         }
       }
     }
@@ -576,7 +658,7 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     for (int i = (int)m + tid; i < k; i += kTkThreads) out[i] = -1;
   }
   if (clear)  // every slice read the histogram before counting itself done
-    for (int i = tid; i < kBins; i += kTkThreads) hrow[i] = 0;
+    for (int i = tid; i < kTopkHistStride; i += kTkThreads) hrow[i] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -639,7 +721,184 @@ __global__ void __launch_bounds__(kTkThreads)
                  expand_n);
 }
 
+// ---------------------------------------------------------------------------
+// selection from candidates (a prefill chunk without its score matrix)
+// ---------------------------------------------------------------------------
+
+// Lane l of the calling warp holds bins 63 - 2l and 62 - 2l of a 64-bin
+// row: the largest bin b whose count from the top reaches target, the
+// count above it (above) and its own count (returned).  bin = 0 / above = 0
+// when the bins hold fewer than target entries.
+__device__ uint32_t pick64(const uint32_t* bins, uint32_t target, uint32_t& bin,
+                          uint32_t& above) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t hi = __ldcg(bins + 63 - 2 * lane), lo = __ldcg(bins + 62 - 2 * lane);
+  uint32_t incl = hi + lo;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t before = incl - hi - lo;
+  const uint32_t who = __ballot_sync(0xffffffffu, before < target && incl >= target);
+  const int src = who ? __ffs(who) - 1 : 31;
+  const bool in_hi = before + hi >= target;
+  const uint32_t b = in_hi ? 63 - 2 * lane : 62 - 2 * lane;
+  const uint32_t ab = in_hi ? before : before + hi;
+  bin = who ? __shfl_sync(0xffffffffu, b, src) : 0u;
+  above = who ? __shfl_sync(0xffffffffu, ab, src) : 0u;
+  return __shfl_sync(0xffffffffu, in_hi ? hi : lo, src);
+}
+
+// The k-th largest key of a sample of row r (its histogram in hist1), one
+// warp per row, in two levels of 12 bits.  Level 0: T1 = the level-1 bin
+// holding it; theta[r] = T1 << 20, cand_cnt[r] = its rank among the keys of
+// bin T1.  Level 1 (the histogram now holds bin T1's keys by their next 12
+// bits): T2 = the sub-bin holding that rank; theta[r] |= T2 << 8, the lowest
+// key of the 24-bit prefix, and cand_cnt[r] = 0 for the emitting pass.
+// theta[r] is at most the sample's k-th largest key, so no entry of the
+// row's top k lies below it.  A sample of fewer than k keys (in either
+// level) gives bin 0: every visible entry becomes a candidate.  Each level
+// clears the row's histogram.
+__global__ void __launch_bounds__(128)
+    topk_theta_kernel(uint32_t* __restrict__ hist1, int64_t rows, int32_t k,
+                      uint32_t* __restrict__ theta, uint32_t* __restrict__ cand_cnt, int level) {
+  pdl_wait();
+  const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (row >= rows) return;  // whole warps leave together
+  const int lane = threadIdx.x & 31;
+  uint32_t* hrow = hist1 + row * kTopkHistStride;
+  const uint32_t target = level == 0 ? (uint32_t)k : cand_cnt[row];
+  uint32_t cbin, cabove, fbin, fabove;
+  pick64(hrow + kTopkBins, target, cbin, cabove);
+  pick64(hrow + cbin * (kTopkBins / kTopkCoarse), target - cabove, fbin, fabove);
+  const uint32_t bin = cbin * (kTopkBins / kTopkCoarse) + fbin;
+  __syncwarp();
+  if (lane == 0) {
+    if (level == 0) {
+      theta[row] = bin << 20;
+      cand_cnt[row] = target - cabove - fabove;  // >= 1 when the bin holds the k-th
+    } else {
+      theta[row] |= bin << 8;
+      cand_cnt[row] = 0;
+    }
+  }
+  for (int i = lane; i < kTopkHistStride; i += 32) hrow[i] = 0;
+  pdl_trigger();
+}
+
+// Row r's candidates cand[r * cap .. + min(cand_cnt[r], cap)) as (key,
+// entry), in any order: the m = min(k, n_valid[r], candidates) largest by
+// (key descending, entry ascending), written ascending to out[r * out_ld ..],
+// padded with -1.  The same radix levels as the other selectors resolve the
+// threshold; the output is read off a bitmap of the row's n entries in
+// entry order (ties at the threshold key through a second bitmap, the
+// lowest entries first).  More candidates than cap raise
+// CSA2_DEVFLAG_CAPACITY (the selection is then among the first cap).
+__global__ void __launch_bounds__(kTkThreads)
+    topk_cand_kernel(const uint2* __restrict__ cand, const uint32_t* __restrict__ cand_cnt,
+                     int64_t cap, int64_t n, const int32_t* __restrict__ n_valid, int32_t k,
+                     int32_t* __restrict__ out, int64_t out_ld, int32_t* dev_status) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  uint32_t* hist = dyn;                                 // [kBins]
+  uint32_t* ckey = dyn + kBins;                         // [cap]
+  uint32_t* cidx = ckey + cap;                          // [cap]
+  const int64_t words = (n + 31) / 32;
+  uint32_t* selb = cidx + cap;                          // [words] selected entries
+  uint32_t* tieb = selb + words;                        // [words] ties at the threshold key
+  __shared__ TkTmp tmp;
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  int32_t* o = out + row * out_ld;
+  const uint32_t total = cand_cnt[row];
+  if (total > (uint64_t)cap && tid == 0) raise_flag(dev_status, CSA2_DEVFLAG_CAPACITY);
+  const int nc = (int)min((uint64_t)total, (uint64_t)cap);
+  const int64_t nv = row_nvalid(n_valid, row, n);
+  const uint32_t m = (uint32_t)min((int64_t)min(k, nc), nv);
+  for (int i = tid; i < kBins; i += kTkThreads) hist[i] = 0;
+  for (int64_t i = tid; i < 2 * words; i += kTkThreads) selb[i] = 0;
+  __syncthreads();
+  const uint2* cr = cand + row * cap;
+  for (int i = tid; i < nc; i += kTkThreads) {
+    const uint2 c = __ldcg(cr + i);
+    ckey[i] = c.x;
+    cidx[i] = c.y;
+    atomicAdd(&hist[c.x >> 20], 1u);
+  }
+  __syncthreads();
+  if (m > 0) {
+    find_top(hist, kBins, m, &tmp);
+    const uint32_t T1 = (uint32_t)tmp.t;
+    const uint32_t need = m - tmp.above;
+    const uint32_t cnt1 = hist[T1];
+    const Threshold th = resolve_threshold(T1, need, cnt1, hist, &tmp, [&](const auto& f) {
+      for (int i = tid; i < nc; i += kTkThreads) f(ckey[i]);
+    });
+    for (int i = tid; i < nc; i += kTkThreads) {
+      const uint32_t key = ckey[i], j = cidx[i];
+      if (th.sure(key))
+        atomicOr(&selb[j >> 5], 1u << (j & 31));
+      else if (th.tie(key))
+        atomicOr(&tieb[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+    // thread t owns words [t * per, (t + 1) * per) of both bitmaps
+    const int64_t per = (words + kTkThreads - 1) / kTkThreads;
+    const int64_t w0 = min(words, (int64_t)tid * per), w1 = min(words, w0 + per);
+    auto block_excl = [&](uint32_t v) {  // block-wide exclusive prefix in thread order
+      uint32_t incl = v;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o2);
+        if (lane >= o2) incl += y;
+      }
+      __syncthreads();
+      if (lane == 31) tmp.wsum[warp] = incl;
+      __syncthreads();
+      uint32_t wv = lane < kTkWarps ? tmp.wsum[lane] : 0u;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, wv, o2);
+        if (lane >= o2) wv += y;
+      }
+      const uint32_t woff = __shfl_sync(0xffffffffu, wv, (warp + 31) & 31) * (warp > 0);
+      return woff + incl - v;
+    };
+    if (th.depth == 4) {
+      // ties: the first `need` tie entries in entry order join the selection
+      uint32_t t = 0;
+      for (int64_t w = w0; w < w1; ++w) t += __popc(tieb[w]);
+      uint32_t rank = block_excl(t);
+      for (int64_t w = w0; w < w1; ++w) {
+        uint32_t bits = tieb[w];
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (rank++ < th.need) selb[w] |= 1u << b;
+        }
+      }
+      __syncthreads();
+    }
+    uint32_t c = 0;
+    for (int64_t w = w0; w < w1; ++w) c += __popc(selb[w]);
+    uint32_t pos = block_excl(c);
+    for (int64_t w = w0; w < w1; ++w) {
+      uint32_t bits = selb[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (pos < m) o[pos] = (int32_t)(w * 32 + b);
+        ++pos;
+      }
+    }
+  }
+  pdl_trigger();
+  for (int i = (int)m + tid; i < k; i += kTkThreads) o[i] = -1;
+}
+
 std::atomic<uint64_t> g_scan_attr{0};  // devices on which the scan kernel's attributes are set
+std::atomic<uint64_t> g_cand_attr{0};  // the same for the candidate selector
 
 }  // namespace
 
@@ -692,8 +951,43 @@ csa2_status launch_topk_small(const float* scores, int64_t ld, const int32_t* ga
                        expand, expand_n);
 }
 
+csa2_status launch_topk_theta(uint32_t* hist1, int64_t rows, int32_t k, uint32_t* theta,
+                              uint32_t* cand_cnt, int level, cudaStream_t s) {
+  if (rows == 0) return CSA2_OK;
+  return launch_kernel(topk_theta_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, s, 1,
+                       hist1, rows, k, theta, cand_cnt, level);
+}
+
+size_t topk_cand_smem(int64_t cap, int64_t n) {
+  return (size_t)(kBins + 2 * cap + 2 * ((n + 31) / 32)) * 4;
+}
+
+// Dynamic shared memory the candidate selector may take: a CTA holds at most
+// 227 KB of static and dynamic shared memory together, and the kernel's
+// static part (its TkTmp) is well under the 1 KB kept back here.
+constexpr size_t kCandDynMax = 227 * 1024 - 1024;
+static_assert(sizeof(TkTmp) <= 1024, "static shared memory of the candidate selector");
+
+bool topk_cand_fits(int64_t cap, int64_t n) { return topk_cand_smem(cap, n) <= kCandDynMax; }
+
+csa2_status launch_topk_cand(const uint2* cand, const uint32_t* cand_cnt, int64_t cap,
+                             int64_t rows, int64_t n, const int32_t* n_valid, int32_t k,
+                             int32_t* out, int64_t out_ld, int32_t* dev_status, cudaStream_t s) {
+  if (rows == 0) return CSA2_OK;
+  const size_t smem = topk_cand_smem(cap, n);
+  if (smem > kCandDynMax || k < 1 || k > kMaxK) return CSA2_ERR_UNSUPPORTED;
+  cudaError_t e = once_per_device(g_cand_attr, [] {
+    return cudaFuncSetAttribute(topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kCandDynMax);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  return launch_kernel(topk_cand_kernel, dim3((unsigned)rows), dim3(kTkThreads), smem, s, 1, cand,
+                       cand_cnt, cap, n, n_valid, k, out, out_ld, dev_status);
+}
+
 csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64_t ld,
-                             const int32_t* n_valid, uint32_t* hist1, cudaStream_t s) {
+                             const int32_t* n_valid, uint32_t* hist1, cudaStream_t s,
+                             const uint32_t* within) {
   if (rows == 0 || n == 0) return CSA2_OK;
   // enough CTAs to cover the GPU about twice
   const int64_t want = (2 * (int64_t)sm_count() + rows - 1) / rows;
@@ -701,7 +995,8 @@ csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64
   const int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(want, max_chunks));
   const int64_t chunk = (n + chunks - 1) / chunks;
   return launch_kernel(topk_hist_kernel, dim3((unsigned)chunks, (unsigned)rows),
-                       dim3(kHistThreads), 0, s, 1, scores, n, ld, n_valid, hist1, chunk);
+                       dim3(kHistThreads), 0, s, 1, scores, n, ld, n_valid, hist1, chunk,
+                       within);
 }
 
 csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,

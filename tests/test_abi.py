@@ -76,15 +76,18 @@ def test_status_strings(csa2):
     assert csa2.lib.csa2_status_from_device(0) == 0
     assert csa2.lib.csa2_status_from_device(csa2.DEVFLAG_BOUNDS) == 7
     assert csa2.lib.csa2_status_from_device(csa2.DEVFLAG_TIMEOUT | csa2.DEVFLAG_BOUNDS) == 6
+    assert csa2.lib.csa2_status_from_device(csa2.DEVFLAG_CAPACITY) == 8
+    assert csa2.lib.csa2_status_from_device(csa2.DEVFLAG_CAPACITY | csa2.DEVFLAG_BOUNDS) == 7
+    assert csa2.lib.csa2_status_string(8) == b"CSA2_ERR_DEVICE_CAPACITY"
     assert csa2.version().count(".") == 2
 
 
 def topk_ws(rows, n):
-    # one 4096-bin u32 histogram per row; rows longer than 4096 add a 16-byte
-    # counter per row (from a 256-byte boundary) and, per row, S slices of a
-    # 16-byte count + 1024 (key, index) pairs, S = about 296 CTAs per launch,
-    # at most 64, at most one slice per 8192 entries
-    hist = rows * 4096 * 4
+    # one u32 histogram of 4096 fine and 64 coarse bins per row; rows longer
+    # than 4096 add a 16-byte counter per row (from a 256-byte boundary) and,
+    # per row, S slices of a 16-byte count + 1024 (key, index) pairs, S =
+    # about 296 CTAs per launch, at most 64, at most one slice per 8192 entries
+    hist = rows * 4160 * 4
     if n <= 4096:
         return hist
     S = max(1, min(-(-296 // rows), 64, -(-n // 8192)))
@@ -95,7 +98,7 @@ def test_workspace_sizes(csa2):
     for rows, n, k in ((8, 262144, 512), (3, 100, 2048), (4096, 262144, 512), (20, 30000, 512),
                        (1, 4097, 1)):
         assert csa2.topk_workspace_bytes(rows, n, k) == topk_ws(rows, n)
-    assert topk_ws(8, 262144) == 131328 + 8 * 32 * 8208
+    assert topk_ws(8, 262144) == 133376 + 8 * 32 * 8208
     a = csa2.IndexArgs(q_dtype=csa2.BF16, k_dtype=csa2.E4M3, B=8, q_per_seq=1, hi=64, di=128,
                        n=262144)
     assert csa2.lib.csa2_index_score_workspace_bytes(ctypes.byref(a)) == 8 * 64 * 128 + 8 * 64 * 4
@@ -191,7 +194,7 @@ def test_attn_and_quant_validation(csa2, monkeypatch):
                       scales=FAKE, n=100, codes_ld=256, codes_seq_stride=25600, scales_ld=16,
                       scales_seq_stride=1600, idx=FAKE, k=64, idx_ld=64, window=FAKE, w_rows=8,
                       win_ld=512, win_seq_stride=4096, softmax_scale=0.04, out=FAKE)
-    # 64 + 8 keys: one 80-key chunk; every chunk's partial (16 heads x 512
+    # 64 + 8 keys: one 80-key chunk; every chunk's partial (32 heads x 512
     # + max and sum per head, f32) goes through the workspace
     assert L.csa2_sparse_attn_workspace_bytes(ctypes.byref(a)) == 2 * 4 * 1 * (16 * 512 + 32) * 4
     assert L.csa2_sparse_attn(ctypes.byref(a), None) == 5

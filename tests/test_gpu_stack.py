@@ -331,3 +331,77 @@ def test_full_size_1m_pool_sampled(csa2, orc):
         assert rel_l2(R1["out"][q:q + 1].cpu().numpy(), ref) <= 2e-3, q
         checked += 1
     assert checked > 0
+
+
+def test_stack_prefill_selection_without_the_score_matrix(csa2, orc):
+    # a prefill chunk of 64 queries over 20000 entries (long rows): the stack
+    # scores a sample of the tiles, derives each query's threshold, keeps
+    # the entries at or above it and selects among them; the result must be,
+    # bit for bit, the top-k of the full score matrix of the same kernel
+    wl = synth.scaled(synth.PREFILL, q_per_seq=64, N=20000, pos0=4 * 20000 - 64)
+    W = build(wl, 6)
+    run_stack(W)
+    assert int(W.dev_status.item()) == 0
+    L = W.layers[0]
+    scores = csa2.index_score(L["idx_q"], L["idx_w"], L["idxk"], q_per_seq=wl.q_per_seq,
+                              n_valid=W.n_valid)
+    ref = csa2.topk(scores, wl.k, n_valid=W.n_valid)
+    torch.cuda.synchronize()
+    assert torch.equal(L["topk_idx"], ref)
+    assert np.array_equal(L["topk_idx"].cpu().numpy(),
+                          orc.topk(scores.cpu().double().numpy(), wl.k, W.n_valid.cpu().numpy()))
+    compare(orc, W)
+
+
+def test_stack_prefill_candidate_overflow_is_flagged(csa2):
+    # every indexer key equal: every visible entry reaches the sample's
+    # threshold, far more than a query's candidate buffer holds; the
+    # selection reports CSA2_DEVFLAG_CAPACITY instead of failing silently
+    wl = synth.scaled(synth.PREFILL, q_per_seq=8, N=20000, pos0=4 * 20000 - 8)
+    W = build(wl, 7)
+    W.layers[0]["idxk"][:] = 0x38                    # E4M3 1.0 everywhere
+    W.layers[0]["new_idxk"][:] = 1.0
+    W.dev_status.zero_()
+    W.run()
+    torch.cuda.synchronize()
+    assert int(W.dev_status.item()) & csa2.DEVFLAG_CAPACITY
+    assert csa2.lib.csa2_status_from_device(int(W.dev_status.item())) == 8
+
+
+@pytest.mark.parametrize("page_rows", [0, 64])
+def test_stack_new_rows_quantised_before_they_are_scored(csa2, orc, page_rows):
+    # a decode Full layer quantises the step's new rows inside its indexer
+    # launch, in the CTA that loads their tile and before that load.  Each
+    # new indexer key is made its sequence's best entry (200 x the direction
+    # of the query's weighted head sum), so a load that ran ahead of the
+    # write (a zero key, score 0) would drop entry N - 1 from the selection
+    wl = synth.scaled(synth.C1M, B=3, N=9000, modes=synth.C1M.modes[:4], page_rows=page_rows)
+    W = build(wl, 23)
+    N = wl.N
+    for L, host in zip(W.layers, W.bf16):
+        if L["mode"] != synth.FULL:
+            continue
+        v = (L["idx_w"].float()[:, :, None] * L["idx_q"].float()).sum(1)
+        k = (v / v.abs().amax(1, keepdim=True) * 200).to(torch.bfloat16)
+        L["new_idxk"].copy_(k[:, None, :])
+        host["kk"][:, N - 1] = k.cpu()
+    run_stack(W)
+    for L, host in zip(W.layers, W.bf16):
+        if L["mode"] != synth.FULL:
+            continue
+        idx = L["topk_idx"].cpu().numpy()
+        assert all(N - 1 in idx[b] for b in range(wl.B))
+        # the rows the launch wrote: the oracle's quantisation of the same bf16 rows
+        if page_rows:
+            bt = W.block_table.cpu().numpy()
+            rows = [int(bt[b, (N - 1) // page_rows]) * page_rows + (N - 1) % page_rows
+                    for b in range(wl.B)]
+        else:
+            rows = [b * N + N - 1 for b in range(wl.B)]
+        codes = L["codes"].reshape(-1, wl.D // 2)[rows].cpu().numpy()
+        scales = L["scales"].reshape(-1, wl.D // 32)[rows].cpu().numpy()
+        k8 = L["idxk"].reshape(-1, wl.Di)[rows].cpu().numpy()
+        c, s = orc.quantize_fp4(f64(host["kv"][:, N - 1]))
+        assert np.array_equal(codes, c) and np.array_equal(scales, s)
+        assert np.array_equal(k8, orc.cast_e4m3(f64(host["kk"][:, N - 1])))
+    compare(orc, W)
