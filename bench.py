@@ -257,7 +257,8 @@ def time_index_kernel(csa2, W, flush, reps=20):
     """Average device time of one launch of the indexer kernel (FP8 tensor
     core, or fp32 CUDA cores for an fp32 indexer) on the workload's first Full
     layer, one kernel per launch (see index_launch_form), with L2 flushed
-    before each launch."""
+    before each launch.  A prefill chunk that the stack selects without its
+    score matrix is timed in that form (csa2_index_candidates)."""
     L0 = W.layers[0]
     wl = W.wl
     if index_launch_form(wl) == "q8":
@@ -268,13 +269,35 @@ def time_index_kernel(csa2, W, flush, reps=20):
     scores = torch.empty(wl.nq, wl.N, dtype=torch.float32, device=q.device)
     for _ in range(3):
         csa2.index_score(q, c, L0["idxk"], wl.q_per_seq, W.n_valid, scores, **kw)
+    launch = lambda: csa2.index_score(q, c, L0["idxk"], wl.q_per_seq, W.n_valid, scores, **kw)
+    if wl.q_per_seq > 1 and prefill_selects(wl):
+        # the pass the stack runs: no score matrix, the candidates at or above
+        # each query's threshold; thresholds at the key of each query's 8k-th
+        # largest score, the candidate volume of the stack's sampled threshold
+        kth = torch.topk(scores, 8 * wl.k, dim=1).values[:, -1].contiguous()
+        u = kth.view(torch.int32).clone()
+        u[u == -2147483648] = 0  # -0 counts as +0
+        theta = torch.where(u < 0, ~u, u ^ -2147483648)
+        cap = 8192
+        cand = torch.empty(wl.nq, cap, dtype=torch.int64, device=q.device)
+        cnt = torch.zeros(wl.nq, dtype=torch.int32, device=q.device)
+        del scores
+
+        def launch():
+            csa2.index_candidates(q, c, L0["idxk"], theta, cap, wl.q_per_seq, W.n_valid, cand,
+                                  cnt, **kw)
+        for _ in range(3):
+            cnt.zero_()
+            launch()
     stream = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(reps)]
     for a, b in ev:
         flush()
+        if wl.q_per_seq > 1 and prefill_selects(wl):
+            cnt.zero_()
         a.record(stream)
-        csa2.index_score(q, c, L0["idxk"], wl.q_per_seq, W.n_valid, scores, **kw)
+        launch()
         b.record(stream)
     torch.cuda.synchronize()
     return sum(a.elapsed_time(b) for a, b in ev) / reps * 1e-3  # seconds

@@ -274,6 +274,31 @@ csa2_status csa2_index_score_pool(const csa2_index_args* args, const int32_t* po
                                   int64_t pool_ld, int32_t pool_n, csa2_stream_t stream);
 
 /*
+ * The scoring pass of a prefill chunk's fused score -> top-k step, which
+ * stores no score matrix (the pass the layer stack runs after its sampled
+ * threshold; the threshold reading is the library's, see csa2_layer_stack).
+ * For every query q, every visible entry j whose score s[q, j] (exactly as
+ * csa2_index_score computes it) has an order-preserving key >= theta[q] is
+ * appended to q's candidates as cand[q * cand_cap + i] = key | (uint64_t)j
+ * << 32.  The kernel reserves slots 32 at a time through cand_cnt[q]; a
+ * reserved slot it does not fill holds 0xFFFFFFFF00000000 (entry
+ * 0xFFFFFFFF).  Candidates are in no particular order.  The key of a float
+ * x with bits u is u ^ 0x80000000 for x >= 0 (-0 counts as +0) and ~u
+ * otherwise, so a larger score has a larger key.
+ * Only the prefill form of the FP8 path: q_per_seq a multiple of 4, q BF16
+ * or E4M3, k E4M3, hi == 64, di == 128.  scores / scores_ld are not read.
+ * theta    device uint32 [nq]
+ * cand_cnt device uint32 [nq], zero on entry; on exit the slots reserved
+ *          (above cand_cap: the candidates past cand_cap were dropped)
+ * cand     device uint64 [nq, cand_cap], 8-byte aligned
+ * Workspace: csa2_index_score_workspace_bytes(args) (the quantised Q).
+ * Errors: as csa2_index_score; UNSUPPORTED for another path or form.
+ */
+csa2_status csa2_index_candidates(const csa2_index_args* args, const uint32_t* theta,
+                                  uint32_t* cand_cnt, uint64_t* cand, int64_t cand_cap,
+                                  csa2_stream_t stream);
+
+/*
  * Block keys, the first level of the Hierarchical Sparse Indexer [P5
  * Method: indexers restricted to a candidate pool selected by an earlier
  * indexer; P5 Related Work: scoring token-level entries and pruning them on

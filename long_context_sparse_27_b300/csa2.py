@@ -100,6 +100,8 @@ EXPORTS = {
     "csa2_index_score_workspace_bytes": (_c_sz, [ctypes.POINTER(IndexArgs)]),
     "csa2_index_score": (_c_i32, [ctypes.POINTER(IndexArgs), _c_p]),
     "csa2_index_score_pool": (_c_i32, [ctypes.POINTER(IndexArgs), _c_p, _c_i64, _c_i32, _c_p]),
+    "csa2_index_candidates": (_c_i32, [ctypes.POINTER(IndexArgs), _c_p, _c_p, _c_p, _c_i64,
+                                       _c_p]),
     "csa2_project_fp4": (_c_i32, [ctypes.POINTER(ProjectArgs), _c_p]),
     "csa2_index_block_keys": (_c_i32, [_c_p, _c_i64, _c_i64, _c_i64, _c_i64,
                                        ctypes.POINTER(Pages), _c_i32, _c_i64, _c_i64, _c_p,
@@ -277,6 +279,30 @@ def index_score_pool(q, w, k, pool, q_per_seq=1, scores=None, dev_status=None, p
     _check(lib.csa2_index_score_pool(ctypes.byref(a), _ptr(pool), pool.stride(0), P, _stream()),
            "csa2_index_score_pool")
     return scores
+
+
+def index_candidates(q, w, k, theta, cand_cap, q_per_seq, n_valid=None, cand=None,
+                     cand_cnt=None, dev_status=None, pages=None, n=None):
+    """The prefill chunk's scoring pass that stores no scores: q [nq, 64, 128]
+    (bf16, or its E4M3 quantisation with w = c), k E4M3 [B, n, 128] as uint8,
+    theta uint32 [nq] (order-preserving keys, as int32) -> (cand int64 [nq,
+    cand_cap]: key | entry << 32, cand_cnt int32 [nq]: slots reserved)."""
+    nq = q.shape[0]
+    n = k.shape[1] if pages is None else n
+    if theta.dtype != torch.int32 or theta.numel() != nq:
+        raise ValueError("index_candidates: theta must be int32 [nq]")
+    if cand is None:
+        cand = torch.empty(nq, cand_cap, dtype=torch.int64, device=q.device)
+    if cand_cnt is None:
+        cand_cnt = torch.zeros(nq, dtype=torch.int32, device=q.device)
+    a = index_args(q, w, k, q_per_seq, n_valid, None, dev_status, pages, n)
+    need = lib.csa2_index_score_workspace_bytes(ctypes.byref(a))
+    ws = _workspace(need, q.device) if need else None
+    if ws is not None:
+        a.workspace, a.workspace_bytes = _aligned_ptr(ws), need
+    _check(lib.csa2_index_candidates(ctypes.byref(a), _ptr(theta), _ptr(cand_cnt), _ptr(cand),
+                                     cand_cap, _stream()), "csa2_index_candidates")
+    return cand, cand_cnt
 
 
 def project_fp4(h, w, with_out=False):

@@ -499,6 +499,42 @@ csa2_status csa2_index_score_pool(const csa2_index_args* args, const int32_t* po
                                  args->scores_ld, cs);
 }
 
+csa2_status csa2_index_candidates(const csa2_index_args* args, const uint32_t* theta,
+                                  uint32_t* cand_cnt, uint64_t* cand, int64_t cand_cap,
+                                  csa2_stream_t stream) {
+  if (!args) return CSA2_ERR_INVALID_ARG;
+  // the checks of csa2_index_score (no score matrix is written)
+  csa2_index_args chk = *args;
+  chk.scores = reinterpret_cast<float*>(cand);
+  chk.scores_ld = std::max(chk.scores_ld, chk.n);
+  csa2_status st = check_index(&chk);
+  if (st != CSA2_OK) return st;
+  if (!fp8_path(args) || args->q_per_seq % 4 != 0) return CSA2_ERR_UNSUPPORTED;
+  const int64_t nq = args->B * args->q_per_seq;
+  if (nq == 0 || args->n == 0) return CSA2_OK;
+  if (!theta || !cand_cnt || !cand || cand_cap < 1) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(cand, 8)) return CSA2_ERR_ALIGNMENT;
+  if ((st = injected("index_candidates")) != CSA2_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const uint8_t* q8 = static_cast<const uint8_t*>(args->q);
+  const float* c = args->w;
+  if (args->q_dtype != CSA2_E4M3) {
+    uint8_t* wq = static_cast<uint8_t*>(args->workspace);
+    float* wc = reinterpret_cast<float*>(wq + align256((size_t)nq * args->hi * args->di));
+    if ((st = launch_quantize_index_q(args->q, args->w, nq, args->hi, args->di, wq, wc, cs)) !=
+        CSA2_OK)
+      return st;
+    q8 = wq;
+    c = wc;
+  }
+  IndexSelect emit;
+  emit.theta = theta;
+  emit.cand_cnt = cand_cnt;
+  emit.cand = reinterpret_cast<uint2*>(cand);
+  emit.cand_cap = cand_cap;
+  return launch_index_select_prefill(*args, q8, c, emit, cs);
+}
+
 csa2_status csa2_project_fp4(const csa2_project_args* a, csa2_stream_t stream) {
   if (!a || a->rows < 0 || a->hidden < 32 || a->hidden % 32 != 0 || a->d < 64 || a->d % 64 != 0)
     return CSA2_ERR_INVALID_ARG;

@@ -172,12 +172,15 @@ __device__ __forceinline__ void raise_flag(int32_t* dev_status, int32_t flag) {
 // [0, num_pages).
 __device__ __forceinline__ int64_t paged_row(const csa2_pages& pg, int64_t b, int64_t j,
                                              int32_t* dev_status) {
-  const int32_t page = pg.block_table[b * pg.bt_ld + j / pg.page_rows];
+  // entries fit 32 bits (indices are int32): 32-bit division
+  const uint32_t jj = (uint32_t)j, pr = (uint32_t)pg.page_rows;
+  const uint32_t pi = jj / pr;
+  const int32_t page = pg.block_table[b * pg.bt_ld + pi];
   if (page < 0 || page >= pg.num_pages) {
     raise_flag(dev_status, CSA2_DEVFLAG_BOUNDS);
     return -1;
   }
-  return (int64_t)page * pg.page_rows + j % pg.page_rows;
+  return (int64_t)page * pg.page_rows + (jj - pi * pr);
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

@@ -200,8 +200,11 @@ struct TcParams {
   int reverse;             // walk each CTA's tile range from its end
   int keep_in_l2;          // load keys with the normal L2 policy instead of evict-first
   // paged keys (pages.block_table set): kmap is a 2-D map over the pool
-  // with 64-row boxes; a tile is two boxes, each inside one page
+  // with boxes of pg_box rows (128 when pages hold a multiple of 128
+  // entries, so a tile lies in one page; else 64); a tile is 128 / pg_box
+  // boxes, each inside one page
   csa2_pages pages;
+  int pg_box;
   uint64_t wait_ns;        // limit of each pipeline wait (drain waits keep their own)
   int stall_loads;         // test hook: the producer issues no loads (waits run out)
   // sampled launches: the cursor's tile kt is key tile kt * tile_stride, and
@@ -209,9 +212,10 @@ struct TcParams {
   int tile_stride;
   // emitting launches (cand set): no scores are stored; every visible entry
   // whose order-preserving key is >= theta[q] is appended to query q's
-  // candidates cand[q * cand_cap ..] as (key, entry) through the counter
-  // cand_cnt[q] (which may end above cand_cap: the overflow is the reader's
-  // to detect)
+  // candidates cand[q * cand_cap ..] as (key, entry), in slots reserved 32 at
+  // a time through the counter cand_cnt[q]; reserved slots left unused hold
+  // (0, 0xFFFFFFFF).  The counter may end above cand_cap: the overflow is
+  // the reader's to detect
   const uint32_t* theta;
   uint32_t* cand_cnt;
   uint2* cand;
@@ -321,17 +325,28 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       int32_t* pg = reinterpret_cast<int32_t*>(smem + C::OFF_PG);
       TileCursor ahead(p.reverse ? t_end - 1 : t_begin, p.ktiles);
       int64_t ahead_i = 0;
+      // (the producer is one thread: no 64-bit divisions per tile; the
+      // sequence of a group changes rarely, and rows, page sizes and query
+      // counts fit 32 bits)
+      const uint32_t pr = paged ? (uint32_t)p.pages.page_rows : 1u;
+      const uint32_t qps = (uint32_t)p.q_per_seq;
+      int64_t ahead_gprev = -1;
+      const int32_t* bt_row = nullptr;
       auto page_ids_ahead = [&](int64_t upto) {  // issue tiles ahead_i .. upto - 1
         for (; ahead_i < upto; ++ahead_i) {
           if (ahead_i < ntiles) {
-            const int64_t bb = (ahead.g * QG) / p.q_per_seq;
+            if (ahead.g != ahead_gprev) {
+              ahead_gprev = ahead.g;
+              bt_row = p.pages.block_table +
+                       (int64_t)((uint32_t)(ahead.g * QG) / qps) * p.pages.bt_ld;
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int64_t j = ahead.kt * p.tile_stride * C::BM + 64 * h;
-              if (j < p.n)
+              if (j < p.n && (h == 0 || p.pg_box == 64))
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                                  smem_u32(pg + (ahead_i % kPageRing) * 2 + h)),
-                             "l"(p.pages.block_table + bb * p.pages.bt_ld + j / p.pages.page_rows)
+                             "l"(bt_row + (uint32_t)j / pr)
                              : "memory");
             }
             ahead.advance(dir);
@@ -340,8 +355,13 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         }
       };
       if (paged) page_ids_ahead(kPageLookahead);
+      int64_t b_of = -1, b = 0;  // the sequence of group b_of
       for (int64_t i = 0; i < ntiles; ++i, cur.advance(dir)) {
         const int64_t g = cur.g, kt = cur.kt * p.tile_stride;  // the key tile
+        if (g != b_of) {
+          b_of = g;
+          b = (uint32_t)(g * QG) / qps;
+        }
         if (g != g_prev && !p.qbf) {
           const int qs = (int)(qcount & 1);
           const uint32_t qph = (uint32_t)((qcount >> 1) & 1);
@@ -368,30 +388,32 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
           }
           nr_seen = true;
         }
-        const int64_t b = (g * QG) / p.q_per_seq;
         if (!paged) {
           mbar_arrive_expect_tx(&full[stage], C::KTILE);
           tma_load_3d(&kmap, &full[stage], kbuf + stage * C::KTILE, 0, (int32_t)(kt * C::BM),
                       (int32_t)b, pol_k);
         } else {
-          // this tile's page ids (loaded kPageLookahead tiles ago) have landed
+          // tiles i .. i + kPageLookahead - 1 have their page ids in flight;
+          // the kPageLookahead - 1 groups after tile i's may stay pending
           page_ids_ahead(i + kPageLookahead);
-          asm volatile("cp.async.wait_group %0;" ::"n"(kPageLookahead) : "memory");
+          asm volatile("cp.async.wait_group %0;" ::"n"(kPageLookahead - 1) : "memory");
           const int32_t* ids = pg + (i % kPageRing) * 2;
           int32_t y[2];
           uint32_t bytes = 0;
+          const int boxes = C::BM / p.pg_box;
+          const uint32_t box_bytes = (uint32_t)p.pg_box * C::BK;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int64_t j = kt * C::BM + 64 * h;
             y[h] = -1;
-            if (j >= p.n) continue;  // past the rows: never looked up, stays stale (masked)
+            if (h >= boxes || j >= p.n) continue;  // past the rows: never looked up (masked)
             const int32_t page = ids[h];
             if (page < 0 || page >= p.pages.num_pages) {
               raise_flag(p.dev_status, CSA2_DEVFLAG_BOUNDS);
               continue;
             }
-            y[h] = (int32_t)((int64_t)page * p.pages.page_rows + j % p.pages.page_rows);
-            bytes += C::KTILE / 2;
+            y[h] = (int32_t)((int64_t)page * pr + (uint32_t)j % pr);
+            bytes += box_bytes;
           }
           mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
@@ -600,6 +622,22 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     }
     int64_t nv[C::QPW];
     uint32_t th[C::QPW];
+    // emitting launches: each (warp, query) stream reserves its candidate
+    // slots 32 at a time (one atomic per 32 candidates); slots [cpos, cend)
+    // of the current chunk are still free, and are filled with the empty
+    // candidate (entry 0xFFFFFFFF) when the stream leaves the query
+    uint32_t cpos[C::QPW], cend[C::QPW];
+#pragma unroll
+    for (int i = 0; i < C::QPW; ++i) cpos[i] = cend[i] = 0;
+    auto flush_chunks = [&](int64_t gq) {
+#pragma unroll
+      for (int qq = 0; qq < C::QPW; ++qq) {
+        const uint32_t pos = cpos[qq] + lane;
+        if (pos < cend[qq] && pos < (uint64_t)p.cand_cap)
+          p.cand[(gq * QG + q0 + qq) * p.cand_cap + pos] = make_uint2(0u, 0xFFFFFFFFu);
+        cpos[qq] = cend[qq] = 0;
+      }
+    };
     // li counts tiles in processing order (from the range's end when reversed)
     const int64_t dir = p.reverse ? -1 : 1;
     TileCursor cur(p.reverse ? t_end - 1 - stream : t_begin + stream, p.ktiles);
@@ -609,6 +647,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       const int acc = (int)(li % C::NACC);
       const uint32_t aph = (uint32_t)((li / C::NACC) & 1);
       if (g != g_prev) {
+        if (p.cand && g_prev >= 0) flush_chunks(g_prev);
         cb ^= 1;
         __syncwarp();
         if (p.qbf)
@@ -665,7 +704,8 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       const int64_t jc = kt * C::BM + row;          // score column (compact when sampled)
       const int64_t j = jc + kt * (p.tile_stride - 1) * C::BM;  // the entry
       if (p.cand) {
-        // candidates of the exact selection: warp-aggregated appends
+        // candidates of the exact selection: the warp's takes fill its
+        // current chunk, then (one atomic) a new chunk of 32
         const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
         for (int qq = 0; qq < C::QPW; ++qq) {
@@ -674,11 +714,19 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
           const bool take = j < p.n && j < nv[qq] && key >= th[qq];
           const uint32_t mask = __ballot_sync(0xffffffffu, take);
           if (mask) {
-            const int leader = __ffs(mask) - 1;
-            uint32_t base = 0;
-            if (lane == leader) base = atomicAdd(&p.cand_cnt[qi], (uint32_t)__popc(mask));
-            base = __shfl_sync(0xffffffffu, base, leader);
-            const uint32_t pos = base + __popc(mask & lt);
+            const uint32_t cnt = __popc(mask), r = __popc(mask & lt);
+            const uint32_t avail = cend[qq] - cpos[qq];
+            uint32_t pos = cpos[qq] + r;
+            if (cnt <= avail) {
+              cpos[qq] += cnt;
+            } else {
+              uint32_t nb = 0;
+              if (lane == 0) nb = atomicAdd(&p.cand_cnt[qi], 32u);
+              nb = __shfl_sync(0xffffffffu, nb, 0);
+              if (r >= avail) pos = nb + (r - avail);
+              cpos[qq] = nb + (cnt - avail);
+              cend[qq] = nb + 32;
+            }
             if (take && pos < (uint64_t)p.cand_cap)
               p.cand[qi * p.cand_cap + pos] = make_uint2(key, (uint32_t)j);
           }
@@ -708,6 +756,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         }
       }
     }
+    if (p.cand && g_prev >= 0) flush_chunks(g_prev);
   }
 
   tc_fence_before();
@@ -783,7 +832,7 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
     cuuint64_t dims[2] = {(cuuint64_t)a.di,
                           (cuuint64_t)a.pages.num_pages * (cuuint64_t)a.pages.page_rows};
     cuuint64_t strides[1] = {(cuuint64_t)a.k_ld};
-    cuuint32_t box[2] = {128, 64};
+    cuuint32_t box[2] = {128, (cuuint32_t)(a.pages.page_rows % 128 == 0 ? 128 : 64)};
     cuuint32_t es[2] = {1, 1};
     if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.k), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -827,6 +876,7 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   p.reverse = tune.reverse ? 1 : 0;
   p.keep_in_l2 = tune.keep_in_l2 ? 1 : 0;
   p.pages = a.pages;
+  p.pg_box = a.pages.page_rows % 128 == 0 ? 128 : 64;
   p.wait_ns = pipeline_wait_ns();
   p.stall_loads = stall_loads() ? 1 : 0;
   p.tile_stride = sel && sel->tile_stride > 1 ? sel->tile_stride : 1;

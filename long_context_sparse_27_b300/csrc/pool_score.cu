@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kPThreads)
   const int64_t qi = blockIdx.x;
   const int s0 = blockIdx.y * kPSlots;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t b = qi / q_per_seq;
+  const int64_t b = (uint32_t)qi / (uint32_t)q_per_seq;  // queries fit 32 bits
 
   if (tid < kPSlots) {
     const int slot = s0 + tid;

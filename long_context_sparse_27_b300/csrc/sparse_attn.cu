@@ -43,7 +43,7 @@ struct KeySrc {
 __device__ __forceinline__ KeySrc key_source(const csa2_attn_args& a, int64_t qi, int64_t t,
                                              int32_t ws, int32_t wl) {
   KeySrc r{nullptr, nullptr, nullptr};
-  const int64_t b = qi / a.q_per_seq;
+  const int64_t b = (uint32_t)qi / (uint32_t)a.q_per_seq;  // queries fit 32 bits
   if (t < a.k) {
     const int32_t j = a.idx[qi * a.idx_ld + t];
     if (j < -1 || j >= a.n) {
@@ -271,7 +271,8 @@ __device__ __noinline__ void dequant_block(uint4 cw, uint32_t sb, uint8_t* d0, u
 // the kernels still running on the stream do not write it).
 template <bool CLUSTER>
 __global__ void __launch_bounds__(kAttnThreads, 2)
-    attn_bf16_kernel(const csa2_attn_args a, int nchunks, float* __restrict__ partial, int pre) {
+    attn_bf16_kernel(const csa2_attn_args a, int nchunks, int fk, float* __restrict__ partial,
+                     int pre) {
   extern __shared__ __align__(16) uint8_t sm_raw[];
   uint8_t* sQ = sm_raw;
   uint8_t* sK = sm_raw + kSmemQ;
@@ -307,11 +308,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   window_of(a, qi, ws, wl);
   const int64_t nkeys = a.k + wl;
 
-  // ---- 1. key sources
+  // ---- 1. key sources.  fk > 0: chunk c holds selected keys fk c .. fk c +
+  // fk - 1 and window rows (kKC - fk) c .., so every chunk gathers the same
+  // mix (the softmax is over the set of keys, in any order); fk = 0: keys
+  // t = kKC c .. of the list (selected keys, then the window)
   if (tid < kKC) {
-    const int64_t t = (int64_t)chunk * kKC + tid;
+    int64_t t = -1;  // no key
+    if (fk > 0) {
+      if (tid < fk) {
+        const int64_t i = (int64_t)chunk * fk + tid;
+        if (i < a.k) t = i;
+      } else {
+        const int64_t u = (int64_t)chunk * (kKC - fk) + (tid - fk);
+        if (u < wl) t = a.k + u;
+      }
+    } else {
+      t = (int64_t)chunk * kKC + tid;
+      if (t >= nkeys) t = -1;
+    }
     KeySrc src{nullptr, nullptr, nullptr};
-    if (t < nkeys) src = key_source(a, qi, t, ws, wl);
+    if (t >= 0) src = key_source(a, qi, t, ws, wl);
     rows.codes[tid] = src.codes;
     rows.scales[tid] = src.scales;
     rows.win[tid] = src.win;
@@ -638,11 +654,16 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s, bool q_
   const dim3 grid((unsigned)nchunks, (unsigned)((a.hq + kHG - 1) / kHG), (unsigned)a.nq);
   float* partial = static_cast<float*>(a.workspace);
   const int pre = q_ready ? 1 : 0;
+  // spread the selected keys and the window rows evenly over the chunks when
+  // the split holds every key (the window rows' bf16 loads are four times
+  // an FP4 row's bytes: a chunk of window rows alone would finish last)
+  int fk = (int)((a.k + nchunks - 1) / nchunks);
+  if (fk > kKC || (int64_t)(kKC - fk) * nchunks < a.win_max) fk = 0;
   if (nchunks <= kMaxClusterChunks)
     return launch_kernel(attn_bf16_kernel<true>, grid, dim3(kAttnThreads), (size_t)kAttnSmem, s,
-                         (unsigned)nchunks, a, nchunks, partial, pre);
+                         (unsigned)nchunks, a, nchunks, fk, partial, pre);
   csa2_status st = launch_kernel(attn_bf16_kernel<false>, grid, dim3(kAttnThreads),
-                                 (size_t)kAttnSmem, s, 1, a, nchunks, partial, pre);
+                                 (size_t)kAttnSmem, s, 1, a, nchunks, fk, partial, pre);
   if (st != CSA2_OK) return st;
   return launch_kernel(attn_combine_kernel, dim3((unsigned)a.hq, (unsigned)a.nq), dim3(128), 0, s,
                        1, static_cast<const float*>(partial), nchunks, (int)a.hq, a.out);

@@ -417,6 +417,31 @@ __device__ void write_selected(const uint32_t* key, int nc, const Threshold& th,
 // long rows
 // ---------------------------------------------------------------------------
 
+// Lane l of the calling warp holds bins 63 - 2l and 62 - 2l of a 64-bin
+// row: the largest bin b whose count from the top reaches target, the
+// count above it (above) and its own count (returned).  bin = 0 / above = 0
+// when the bins hold fewer than target entries.
+__device__ uint32_t pick64(const uint32_t* bins, uint32_t target, uint32_t& bin,
+                          uint32_t& above) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t hi = __ldcg(bins + 63 - 2 * lane), lo = __ldcg(bins + 62 - 2 * lane);
+  uint32_t incl = hi + lo;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t before = incl - hi - lo;
+  const uint32_t who = __ballot_sync(0xffffffffu, before < target && incl >= target);
+  const int src = who ? __ffs(who) - 1 : 31;
+  const bool in_hi = before + hi >= target;
+  const uint32_t b = in_hi ? 63 - 2 * lane : 62 - 2 * lane;
+  const uint32_t ab = in_hi ? before : before + hi;
+  bin = who ? __shfl_sync(0xffffffffu, b, src) : 0u;
+  above = who ? __shfl_sync(0xffffffffu, ab, src) : 0u;
+  return __shfl_sync(0xffffffffu, in_hi ? hi : lo, src);
+}
+
 // Workspace of a long-row selection: per row its level-1 histogram, a
 // counter (the slices done) and S slots of (count, kSlotCap keys, kSlotCap
 // indices).
@@ -478,61 +503,154 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     return;
   }
 
-  // the slice's first scores move into L1 while the histogram is read and
-  // searched (a prefetch holds no registers)
   const int64_t j0 = min(nv, (int64_t)sl * slice), j1 = min(nv, j0 + slice);
+  uint8_t* slot = slots + ((size_t)row * S + sl) * ScanLayout::kSlotBytes;
+  uint32_t T1, need, cnt1, kept;
+  if (S > 1) {
+    // ---- a slice: in each batch of kBatch scores warp w takes the
+    // contiguous 512 from b0 + 512 w (lane l the float4 at 128 u + 4 l, u <
+    // kRounds).  Every warp issues its first loads before warp 0 reads the
+    // threshold bin (coarse, then fine bins: one reader per CTA, since a
+    // row's 32 or so CTAs all read the same histogram lines); the entries in
+    // bins >= T1 go straight to the slot in index order, the only block-wide
+    // step per batch being the prefix over the 16 warps' counts
+    // (double-buffered: one barrier per batch).
+    uint32_t* sk = reinterpret_cast<uint32_t*>(slot + 16);
+    int32_t* sj = reinterpret_cast<int32_t*>(slot + 16 + (size_t)kSlotCap * 4);
+    uint32_t* wtot = tmp.wsum;  // [2][kTkWarps] per-warp counts of a batch
+    uint32_t base = 0;          // entries kept by earlier batches (block-uniform)
+    int par = 0;
+    bool first = true;
+    T1 = 0;
+    need = cnt1 = 0;
+    for (int64_t b0 = j0; b0 < j1; b0 += kBatch, first = false) {
+      const int64_t wb = b0 + (int64_t)warp * (kBatch / kTkWarps);
+      float4 x[kRounds];
 #pragma unroll
-  for (int u = 0; u < kRounds; ++u) {
-    const int64_t j = j0 + (int64_t)u * kRound + tid * 4;
-    if (j < j1) asm volatile("prefetch.global.L1 [%0];" ::"l"(s + j));
-  }
-
-  // ---- level 1: the threshold bin from the row's coarse bins, then the 64
-  // fine bins under the chosen coarse bin (warp 0; two rounds of loads)
-  if (warp == 0) {
-    // lane l holds bins 63 - 2l and 62 - 2l: suffix counts in descending order
-    auto pick = [&](const uint32_t* bins, uint32_t target, uint32_t& bin, uint32_t& above) {
-      const uint32_t hi = __ldcg(bins + 63 - 2 * lane), lo = __ldcg(bins + 62 - 2 * lane);
-      uint32_t incl = hi + lo;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t before = incl - hi - lo;
-      const bool here = before < target && incl >= target;
-      const uint32_t who = __ballot_sync(0xffffffffu, here);
-      const int src = who ? __ffs(who) - 1 : 31;
-      const uint32_t b = before + hi >= target ? 63 - 2 * lane : 62 - 2 * lane;
-      const uint32_t ab = before + hi >= target ? before : before + hi;
-      bin = who ? __shfl_sync(0xffffffffu, b, src) : 0u;
-      above = who ? __shfl_sync(0xffffffffu, ab, src) : 0u;
-      return __shfl_sync(0xffffffffu, before + hi >= target ? hi : lo, src);
-    };
-    uint32_t cbin, cabove, fbin, fabove;
-    pick(hrow + kBins, m, cbin, cabove);
-    const uint32_t cnt = pick(hrow + cbin * (kBins / kTopkCoarse), m - cabove, fbin, fabove);
-    if (lane == 0) {
-      tmp.t = (int)(cbin * (kBins / kTopkCoarse) + fbin);
-      tmp.above = cabove + fabove;
-      tmp.total = cnt;
-    }
-  }
-  __syncthreads();
-  const uint32_t T1 = (uint32_t)tmp.t;
-  const uint32_t need = m - tmp.above;
-  const uint32_t cnt1 = tmp.total;
-  __syncthreads();  // tmp is rewritten by the scan
-
-  // ---- this slice: keep (key, index) of every entry in a bin >= T1
-  const uint32_t kept = ordered_take(
-      s, j0, j1, vec, 0u, &tmp, [&](uint32_t key, int64_t) { return (key >> 20) >= T1 ? 1u : 0u; },
-      [&](uint32_t pos, uint32_t key, int64_t j) {
-        if (pos < (uint32_t)kCandCap) {
-          ckey[pos] = key;
-          cidx[pos] = (int32_t)j;
+      for (int u = 0; u < kRounds; ++u) {
+        const int64_t j = wb + 128 * u + 4 * lane;
+        if (vec && j + 3 < j1) {
+          x[u] = __ldcs(reinterpret_cast<const float4*>(s + j));
+        } else {
+          x[u].x = j < j1 ? s[j] : 0.f;
+          x[u].y = j + 1 < j1 ? s[j + 1] : 0.f;
+          x[u].z = j + 2 < j1 ? s[j + 2] : 0.f;
+          x[u].w = j + 3 < j1 ? s[j + 3] : 0.f;
         }
-      });
+      }
+      if (first) {  // warp 0 reads the threshold bin (one reader per CTA)
+        if (warp == 0) {
+          uint32_t cbin, cabove, fbin, fabove;
+          pick64(hrow + kBins, m, cbin, cabove);
+          const uint32_t c1 = pick64(hrow + cbin * (kBins / kTopkCoarse), m - cabove, fbin, fabove);
+          if (lane == 0) {
+            tmp.t = (int)(cbin * (kBins / kTopkCoarse) + fbin);
+            tmp.above = cabove + fabove;
+            tmp.total = c1;
+          }
+        }
+        __syncthreads();
+        T1 = (uint32_t)tmp.t;
+        need = m - tmp.above;
+        cnt1 = tmp.total;
+      }
+      // 4 bits per float4: which of its scores are kept
+      uint32_t bits[kRounds], cnt = 0;
+#pragma unroll
+      for (int u = 0; u < kRounds; ++u) {
+        const int64_t j = wb + 128 * u + 4 * lane;
+        const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+        uint32_t b = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          b |= (uint32_t)(j + e < j1 && (score_key(xv[e]) >> 20) >= T1) << e;
+        bits[u] = b;
+        cnt += __popc(b);
+      }
+      uint32_t wsum = cnt;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+      if (lane == 0) wtot[par * kTkWarps + warp] = wsum;
+      __syncthreads();
+      uint32_t pos = base, batch = 0;
+#pragma unroll
+      for (int w = 0; w < kTkWarps; ++w) {
+        const uint32_t c = wtot[par * kTkWarps + w];
+        pos += w < warp ? c : 0u;
+        batch += c;
+      }
+      if (wsum) {
+#pragma unroll
+        for (int u = 0; u < kRounds; ++u) {
+          const uint32_t c = __popc(bits[u]);
+          if (!__ballot_sync(0xffffffffu, c != 0)) continue;
+          uint32_t incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          uint32_t p = pos + incl - c;
+          const int64_t j = wb + 128 * u + 4 * lane;
+          const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if ((bits[u] >> e) & 1u) {
+              if (p < (uint32_t)kSlotCap) {
+                sk[p] = score_key(xv[e]);
+                sj[p] = (int32_t)(j + e);
+              }
+              ++p;
+            }
+          }
+          pos += __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      base += batch;
+      par ^= 1;
+    }
+    kept = base;
+    if (j0 >= j1) {  // an empty slice still reports the threshold
+      uint32_t cbin, cabove, fbin, fabove;
+      pick64(hrow + kBins, m, cbin, cabove);
+      cnt1 = pick64(hrow + cbin * (kBins / kTopkCoarse), m - cabove, fbin, fabove);
+      T1 = cbin * (kBins / kTopkCoarse) + fbin;
+      need = m - cabove - fabove;
+    }
+  } else {
+    // ---- one CTA per row: the row's first scores move into L1 (a prefetch
+    // holds no registers) while warp 0 finds the threshold bin; the entries
+    // in bins >= T1 are kept in shared memory in index order
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const int64_t j = j0 + (int64_t)u * kRound + tid * 4;
+      if (j < j1) asm volatile("prefetch.global.L1 [%0];" ::"l"(s + j));
+    }
+    if (warp == 0) {
+      uint32_t cbin, cabove, fbin, fabove;
+      pick64(hrow + kBins, m, cbin, cabove);
+      const uint32_t cnt = pick64(hrow + cbin * (kBins / kTopkCoarse), m - cabove, fbin, fabove);
+      if (lane == 0) {
+        tmp.t = (int)(cbin * (kBins / kTopkCoarse) + fbin);
+        tmp.above = cabove + fabove;
+        tmp.total = cnt;
+      }
+    }
+    __syncthreads();
+    T1 = (uint32_t)tmp.t;
+    need = m - tmp.above;
+    cnt1 = tmp.total;
+    __syncthreads();  // tmp is rewritten by the scan
+    kept = ordered_take(
+        s, j0, j1, vec, 0u, &tmp,
+        [&](uint32_t key, int64_t) { return (key >> 20) >= T1 ? 1u : 0u; },
+        [&](uint32_t pos, uint32_t key, int64_t j) {
+          if (pos < (uint32_t)kCandCap) {
+            ckey[pos] = key;
+            cidx[pos] = (int32_t)j;
+          }
+        });
+  }
   __syncthreads();
 
   bool overflow;
@@ -541,16 +659,8 @@ __global__ void __launch_bounds__(kTkThreads, 2)
     overflow = kept > (uint32_t)kCandCap;
     nc = (int)min(kept, (uint32_t)kCandCap);
   } else {
-    // publish this slice's entries, then count the slice as done; the last
+    // the slice's entries are in its slot: count the slice as done; the last
     // slice of the row to finish gathers every slot
-    uint8_t* slot = slots + ((size_t)row * S + sl) * ScanLayout::kSlotBytes;
-    const uint32_t np = min(kept, (uint32_t)kSlotCap);
-    uint32_t* sk = reinterpret_cast<uint32_t*>(slot + 16);
-    int32_t* sj = reinterpret_cast<int32_t*>(slot + 16 + (size_t)kSlotCap * 4);
-    for (uint32_t i = tid; i < np; i += kTkThreads) {
-      sk[i] = ckey[i];
-      sj[i] = cidx[i];
-    }
     if (tid == 0) *reinterpret_cast<uint32_t*>(slot) = kept;
     __syncthreads();  // the CTA's slot writes happen before thread 0's fence
     if (tid == 0) {
@@ -725,30 +835,6 @@ __global__ void __launch_bounds__(kTkThreads)
 // selection from candidates (a prefill chunk without its score matrix)
 // ---------------------------------------------------------------------------
 
-// Lane l of the calling warp holds bins 63 - 2l and 62 - 2l of a 64-bin
-// row: the largest bin b whose count from the top reaches target, the
-// count above it (above) and its own count (returned).  bin = 0 / above = 0
-// when the bins hold fewer than target entries.
-__device__ uint32_t pick64(const uint32_t* bins, uint32_t target, uint32_t& bin,
-                          uint32_t& above) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t hi = __ldcg(bins + 63 - 2 * lane), lo = __ldcg(bins + 62 - 2 * lane);
-  uint32_t incl = hi + lo;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  const uint32_t before = incl - hi - lo;
-  const uint32_t who = __ballot_sync(0xffffffffu, before < target && incl >= target);
-  const int src = who ? __ffs(who) - 1 : 31;
-  const bool in_hi = before + hi >= target;
-  const uint32_t b = in_hi ? 63 - 2 * lane : 62 - 2 * lane;
-  const uint32_t ab = in_hi ? before : before + hi;
-  bin = who ? __shfl_sync(0xffffffffu, b, src) : 0u;
-  above = who ? __shfl_sync(0xffffffffu, ab, src) : 0u;
-  return __shfl_sync(0xffffffffu, in_hi ? hi : lo, src);
-}
 
 // The k-th largest key of a sample of row r (its histogram in hist1), one
 // warp per row, in two levels of 12 bits.  Level 0: T1 = the level-1 bin
@@ -788,7 +874,7 @@ __global__ void __launch_bounds__(128)
 }
 
 // Row r's candidates cand[r * cap .. + min(cand_cnt[r], cap)) as (key,
-// entry), in any order: the m = min(k, n_valid[r], candidates) largest by
+// entry), in any order (entry 0xFFFFFFFF: an empty slot): the m = min(k, n_valid[r], candidates) largest by
 // (key descending, entry ascending), written ascending to out[r * out_ld ..],
 // padded with -1.  The same radix levels as the other selectors resolve the
 // threshold; the output is read off a bitmap of the row's n entries in
@@ -813,20 +899,38 @@ __global__ void __launch_bounds__(kTkThreads)
   int32_t* o = out + row * out_ld;
   const uint32_t total = cand_cnt[row];
   if (total > (uint64_t)cap && tid == 0) raise_flag(dev_status, CSA2_DEVFLAG_CAPACITY);
-  const int nc = (int)min((uint64_t)total, (uint64_t)cap);
+  const int slots = (int)min((uint64_t)total, (uint64_t)cap);
   const int64_t nv = row_nvalid(n_valid, row, n);
-  const uint32_t m = (uint32_t)min((int64_t)min(k, nc), nv);
+  __shared__ uint32_t s_nc;
   for (int i = tid; i < kBins; i += kTkThreads) hist[i] = 0;
   for (int64_t i = tid; i < 2 * words; i += kTkThreads) selb[i] = 0;
+  if (tid == 0) s_nc = 0;
   __syncthreads();
+  // the filled slots (an unused reserved slot holds entry 0xFFFFFFFF),
+  // compacted in any order
   const uint2* cr = cand + row * cap;
-  for (int i = tid; i < nc; i += kTkThreads) {
-    const uint2 c = __ldcg(cr + i);
-    ckey[i] = c.x;
-    cidx[i] = c.y;
-    atomicAdd(&hist[c.x >> 20], 1u);
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int i0 = 0; i0 < slots; i0 += kTkThreads) {
+    const int i = i0 + tid;
+    uint2 c = make_uint2(0u, 0xFFFFFFFFu);
+    if (i < slots) c = __ldcg(cr + i);
+    const bool ok = c.y != 0xFFFFFFFFu;
+    const uint32_t mask = __ballot_sync(0xffffffffu, ok);
+    if (mask) {
+      uint32_t b = 0;
+      if (lane == 0) b = atomicAdd(&s_nc, (uint32_t)__popc(mask));
+      b = __shfl_sync(0xffffffffu, b, 0);
+      if (ok) {
+        const uint32_t pos = b + __popc(mask & lt);
+        ckey[pos] = c.x;
+        cidx[pos] = c.y;
+        atomicAdd(&hist[c.x >> 20], 1u);
+      }
+    }
   }
   __syncthreads();
+  const int nc = (int)s_nc;
+  const uint32_t m = (uint32_t)min((int64_t)min(k, nc), nv);
   if (m > 0) {
     find_top(hist, kBins, m, &tmp);
     const uint32_t T1 = (uint32_t)tmp.t;

@@ -171,6 +171,55 @@ def test_index_score_fp8_prefill_causal(csa2, orc):
     assert score_close(s.cpu().numpy(), ref) <= 1.0
 
 
+def _score_keys(s):
+    """Order-preserving uint32 keys of float32 scores (-0 counts as +0)."""
+    u = np.ascontiguousarray(s, dtype=np.float32).view(np.uint32).copy()
+    u[u == 0x80000000] = 0
+    return np.where(u & 0x80000000, ~u, u | 0x80000000).astype(np.uint32)
+
+
+def test_index_candidates_are_the_scores_at_or_above_theta(csa2):
+    # the prefill scoring pass that stores no scores keeps exactly the
+    # visible entries whose score key is >= theta[q], with the keys of
+    # csa2_index_score's scores; reserved slots left unused hold entry
+    # 0xFFFFFFFF; a buffer too small for a query's candidates reports more
+    # slots than it holds
+    T, n = 16, 5000
+    wl = synth.scaled(synth.PREFILL, q_per_seq=T, N=n, pos0=4 * n - T)
+    q = synth.index_q(wl, 320, "cuda")
+    w = synth.index_w(wl, 321, "cuda")
+    k8 = torch.randint(0, 0x7F, (1, n, 128), dtype=torch.uint8, device="cuda",
+                       generator=torch.Generator(device="cuda").manual_seed(322))
+    nv = synth.prefill_n_valid(wl, "cuda")
+    s = csa2.index_score(q, w, k8, q_per_seq=T, n_valid=nv).cpu().numpy()
+    keys = _score_keys(s)
+    nvh = nv.cpu().numpy()
+    theta = np.zeros(T, np.uint32)
+    for t in range(T):
+        theta[t] = np.sort(keys[t, :nvh[t]])[::-1][min(299, nvh[t] - 1)]
+    theta[3] = 0            # every visible entry
+    theta[5] = 0xFFFFFFFF   # none (no score reaches the largest key)
+    th = torch.from_numpy(theta.view(np.int32)).cuda()
+    cap = n + 1024
+    cand, cnt = csa2.index_candidates(q, w, k8, th, cap, T, n_valid=nv)
+    cand, cnt = cand.cpu().numpy().view(np.uint64), cnt.cpu().numpy().view(np.uint32)
+    for t in range(T):
+        assert cnt[t] <= cap and cnt[t] % 32 == 0
+        c = cand[t, :cnt[t]]
+        ent = (c >> np.uint64(32)).astype(np.uint32)
+        key = (c & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+        filled = ent != 0xFFFFFFFF
+        assert np.all(key[~filled] == 0)
+        want = np.nonzero(keys[t, :nvh[t]] >= theta[t])[0]
+        got = np.sort(ent[filled])
+        assert np.array_equal(got, want), t
+        assert np.array_equal(key[filled], keys[t, ent[filled]]), t
+    assert cnt[5] == 0 and (cnt[3] >= nvh[3])
+    # a buffer of 64 slots: the counter still counts every reservation
+    cand2, cnt2 = csa2.index_candidates(q, w, k8, th, 64, T, n_valid=nv)
+    assert int(cnt2.cpu().numpy().view(np.uint32)[3]) >= nvh[3] > 64
+
+
 def test_index_score_fp8_exact_small_integers(csa2, orc):
     # q and k with small-integer E4M3 values (q8 in {0, +-64, 448}, k in
     # {0, +-1}): every product and partial sum is an integer below 2^14, so
