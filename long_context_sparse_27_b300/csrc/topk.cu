@@ -47,8 +47,9 @@ constexpr int kSlotCap = 1024;                // kept entries a slice may publis
 constexpr int kMaxSlices = 64;
 constexpr int kSliceTarget = 296;             // CTAs of one launch to aim for (2 per SM)
 constexpr int kSmallN = (int)kTopkShortRow;   // longest row of topk_small_kernel
-// dynamic shared memory of topk_scan_kernel: histogram | keys | indices
-constexpr int kScanSmem = (kBins + 2 * kCandCap) * 4;
+// dynamic shared memory of topk_scan_kernel: histogram (fine and coarse
+// bins) | keys | indices
+constexpr int kScanSmem = (kTopkHistStride + 2 * kCandCap) * 4;
 
 __device__ __forceinline__ int64_t row_nvalid(const int32_t* n_valid, int64_t row, int64_t n) {
   int64_t nv = n_valid ? (int64_t)n_valid[row] : n;
@@ -421,10 +422,13 @@ __device__ void write_selected(const uint32_t* key, int nc, const Threshold& th,
 // row: the largest bin b whose count from the top reaches target, the
 // count above it (above) and its own count (returned).  bin = 0 / above = 0
 // when the bins hold fewer than target entries.
+// SH: the bins are in shared memory (else global memory, read through L2).
+template <bool SH = false>
 __device__ uint32_t pick64(const uint32_t* bins, uint32_t target, uint32_t& bin,
                           uint32_t& above) {
   const int lane = threadIdx.x & 31;
-  const uint32_t hi = __ldcg(bins + 63 - 2 * lane), lo = __ldcg(bins + 62 - 2 * lane);
+  const uint32_t hi = SH ? bins[63 - 2 * lane] : __ldcg(bins + 63 - 2 * lane);
+  const uint32_t lo = SH ? bins[62 - 2 * lane] : __ldcg(bins + 62 - 2 * lane);
   uint32_t incl = hi + lo;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -477,9 +481,9 @@ __global__ void __launch_bounds__(kTkThreads, 2)
                      int32_t* __restrict__ idx_out, int64_t idx_ld, int vec,
                      const int32_t* __restrict__ remap, int64_t remap_ld, int clear) {
   extern __shared__ __align__(16) uint32_t dyn[];
-  uint32_t* hist = dyn;                                     // [kBins]
-  uint32_t* ckey = dyn + kBins;                             // [kCandCap] kept keys
-  int32_t* cidx = reinterpret_cast<int32_t*>(dyn + kBins + kCandCap);  // their indices
+  uint32_t* hist = dyn;                                     // [kTopkHistStride]
+  uint32_t* ckey = dyn + kTopkHistStride;                   // [kCandCap] kept keys
+  int32_t* cidx = reinterpret_cast<int32_t*>(ckey + kCandCap);  // their indices
   __shared__ TkTmp tmp;
   __shared__ uint32_t s_last, s_base[kMaxSlices + 1], s_cnt[kMaxSlices];
 
@@ -509,23 +513,22 @@ __global__ void __launch_bounds__(kTkThreads, 2)
   if (S > 1) {
     // ---- a slice: in each batch of kBatch scores warp w takes the
     // contiguous 512 from b0 + 512 w (lane l the float4 at 128 u + 4 l, u <
-    // kRounds).  Every warp issues its first loads before warp 0 reads the
-    // threshold bin (coarse, then fine bins: one reader per CTA, since a
-    // row's 32 or so CTAs all read the same histogram lines); the entries in
-    // bins >= T1 go straight to the slot in index order, the only block-wide
-    // step per batch being the prefix over the 16 warps' counts
-    // (double-buffered: one barrier per batch).
+    // kRounds).  The row's histogram and the first batch's scores are loaded
+    // together; warp 0 then finds the threshold bin in shared memory
+    // (coarse, then fine bins); the entries in bins >= T1 go straight to the
+    // slot in index order, the only block-wide step per batch being the
+    // prefix over the 16 warps' counts (double-buffered: one barrier per
+    // batch).
     uint32_t* sk = reinterpret_cast<uint32_t*>(slot + 16);
     int32_t* sj = reinterpret_cast<int32_t*>(slot + 16 + (size_t)kSlotCap * 4);
     uint32_t* wtot = tmp.wsum;  // [2][kTkWarps] per-warp counts of a batch
-    uint32_t base = 0;          // entries kept by earlier batches (block-uniform)
-    int par = 0;
-    bool first = true;
-    T1 = 0;
-    need = cnt1 = 0;
-    for (int64_t b0 = j0; b0 < j1; b0 += kBatch, first = false) {
+    // the row's level-1 histogram (fine and coarse bins) into shared memory
+    // in one round of cp.async, so the threshold bin costs one round trip
+    for (int i = tid; i < kTopkHistStride / 4; i += kTkThreads)
+      cp_async16(hist + 4 * i, hrow + 4 * i);
+    float4 x[kRounds];
+    auto load = [&](int64_t b0) {
       const int64_t wb = b0 + (int64_t)warp * (kBatch / kTkWarps);
-      float4 x[kRounds];
 #pragma unroll
       for (int u = 0; u < kRounds; ++u) {
         const int64_t j = wb + 128 * u + 4 * lane;
@@ -538,22 +541,30 @@ __global__ void __launch_bounds__(kTkThreads, 2)
           x[u].w = j + 3 < j1 ? s[j + 3] : 0.f;
         }
       }
-      if (first) {  // warp 0 reads the threshold bin (one reader per CTA)
-        if (warp == 0) {
-          uint32_t cbin, cabove, fbin, fabove;
-          pick64(hrow + kBins, m, cbin, cabove);
-          const uint32_t c1 = pick64(hrow + cbin * (kBins / kTopkCoarse), m - cabove, fbin, fabove);
-          if (lane == 0) {
-            tmp.t = (int)(cbin * (kBins / kTopkCoarse) + fbin);
-            tmp.above = cabove + fabove;
-            tmp.total = c1;
-          }
-        }
-        __syncthreads();
-        T1 = (uint32_t)tmp.t;
-        need = m - tmp.above;
-        cnt1 = tmp.total;
+    };
+    if (j0 < j1) load(j0);  // the first batch's scores are in flight during the pick
+    cp_async_wait_all();
+    __syncthreads();
+    if (warp == 0) {  // coarse, then fine bins
+      uint32_t cbin, cabove, fbin, fabove;
+      pick64<true>(hist + kBins, m, cbin, cabove);
+      const uint32_t c1 =
+          pick64<true>(hist + cbin * (kBins / kTopkCoarse), m - cabove, fbin, fabove);
+      if (lane == 0) {
+        tmp.t = (int)(cbin * (kBins / kTopkCoarse) + fbin);
+        tmp.above = cabove + fabove;
+        tmp.total = c1;
       }
+    }
+    __syncthreads();
+    T1 = (uint32_t)tmp.t;
+    need = m - tmp.above;
+    cnt1 = tmp.total;
+    uint32_t base = 0;  // entries kept by earlier batches (block-uniform)
+    int par = 0;
+    for (int64_t b0 = j0; b0 < j1; b0 += kBatch) {
+      if (b0 != j0) load(b0);
+      const int64_t wb = b0 + (int64_t)warp * (kBatch / kTkWarps);
       // 4 bits per float4: which of its scores are kept
       uint32_t bits[kRounds], cnt = 0;
 #pragma unroll
@@ -610,13 +621,6 @@ __global__ void __launch_bounds__(kTkThreads, 2)
       par ^= 1;
     }
     kept = base;
-    if (j0 >= j1) {  // an empty slice still reports the threshold
-      uint32_t cbin, cabove, fbin, fabove;
-      pick64(hrow + kBins, m, cbin, cabove);
-      cnt1 = pick64(hrow + cbin * (kBins / kTopkCoarse), m - cabove, fbin, fabove);
-      T1 = cbin * (kBins / kTopkCoarse) + fbin;
-      need = m - cabove - fabove;
-    }
   } else {
     // ---- one CTA per row: the row's first scores move into L1 (a prefetch
     // holds no registers) while warp 0 finds the threshold bin; the entries
@@ -800,17 +804,27 @@ __global__ void __launch_bounds__(kTkThreads)
   const int32_t* rm = remap ? remap + row * remap_ld : nullptr;
   int32_t* o = out + row * out_ld;
   for (int i = tid; i < kBins; i += kTkThreads) hist[i] = 0;
-  __syncthreads();
-  for (int i = tid; i < n; i += kTkThreads) {
-    uint32_t kk = 0;  // an empty slot
-    if (!gi) {
-      kk = score_key(s[i]);
-    } else {
-      const int32_t j = gi[i];
-      if (j >= 0) kk = score_key(s[j]);
+  // every position's source, then every score: the loads of each round are
+  // in flight together (a gathered score is two dependent loads)
+  constexpr int kPer = kSmallN / kTkThreads;
+  int32_t src[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = tid + u * kTkThreads;
+    src[u] = i < n ? (gi ? gi[i] : i) : -1;
+  }
+  float v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) v[u] = src[u] >= 0 ? s[src[u]] : 0.f;
+  __syncthreads();  // the histogram is cleared
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = tid + u * kTkThreads;
+    if (i < n) {
+      const uint32_t kk = src[u] >= 0 ? score_key(v[u]) : 0u;  // 0: an empty slot
+      key[i] = kk;
+      atomicAdd(&hist[kk >> 20], 1u);
     }
-    key[i] = kk;
-    atomicAdd(&hist[kk >> 20], 1u);
   }
   __syncthreads();
   const uint32_t m = (uint32_t)min(k, n);
