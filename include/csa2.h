@@ -477,7 +477,11 @@ csa2_status csa2_sparse_attn(const csa2_attn_args* args, csa2_stream_t stream);
  * codes  device u8 [rows, d/2] (even column in the low nibble), codes_ld
  * scales device u8 [rows, d/32] (UE8M0), scales_ld
  * out    optional device f32 [rows, d], out_ld
- * hidden a multiple of 32; d a multiple of 64.
+ * dev_status optional device int32 (see CSA2_DEVFLAG_*)
+ * hidden a multiple of 32; d a multiple of 64.  From 64 rows on, when hidden
+ * is a multiple of 256, the product runs on tcgen05 tensor cores; both
+ * paths sum each output in fp32 in a fixed order (the result does not
+ * depend on the launch).
  * Errors: INVALID_ARG, ALIGNMENT (h, w 16-byte aligned with h_ld, w_ld
  *         multiples of 8; out 8-byte aligned with out_ld even), CUDA.
  */
@@ -495,6 +499,7 @@ typedef struct csa2_project_args {
   int64_t scales_ld;
   float* out;
   int64_t out_ld;
+  int32_t* dev_status; /* optional: CSA2_DEVFLAG_TIMEOUT if a pipeline wait gave up */
 } csa2_project_args;
 
 csa2_status csa2_project_fp4(const csa2_project_args* args, csa2_stream_t stream);

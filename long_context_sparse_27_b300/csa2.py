@@ -77,7 +77,8 @@ class LayerDesc(ctypes.Structure):
 class ProjectArgs(ctypes.Structure):
     _fields_ = [("h", _c_p), ("w", _c_p), ("rows", _c_i64), ("hidden", _c_i32), ("d", _c_i32),
                 ("h_ld", _c_i64), ("w_ld", _c_i64), ("codes", _c_p), ("codes_ld", _c_i64),
-                ("scales", _c_p), ("scales_ld", _c_i64), ("out", _c_p), ("out_ld", _c_i64)]
+                ("scales", _c_p), ("scales_ld", _c_i64), ("out", _c_p), ("out_ld", _c_i64),
+                ("dev_status", _c_p)]
 
 
 class StackArgs(ctypes.Structure):
@@ -305,7 +306,7 @@ def index_candidates(q, w, k, theta, cand_cap, q_per_seq, n_valid=None, cand=Non
     return cand, cand_cnt
 
 
-def project_fp4(h, w, with_out=False):
+def project_fp4(h, w, with_out=False, dev_status=None):
     """The decoder's global KV of one layer: h bf16 [rows, hidden] (final
     encoder hidden state), w bf16 [d, hidden] (the layer's projection, one
     row per output column) -> (codes u8 [rows, d/2], scales u8 [rows, d/32],
@@ -320,7 +321,8 @@ def project_fp4(h, w, with_out=False):
     a = ProjectArgs(h=_ptr(h), w=_ptr(w), rows=rows, hidden=hidden, d=d, h_ld=h.stride(0),
                     w_ld=w.stride(0), codes=_ptr(codes), codes_ld=codes.stride(0),
                     scales=_ptr(scales), scales_ld=scales.stride(0), out=_ptr(out),
-                    out_ld=(out.stride(0) if out is not None else 0))
+                    out_ld=(out.stride(0) if out is not None else 0),
+                    dev_status=_ptr(dev_status))
     _check(lib.csa2_project_fp4(ctypes.byref(a), _stream()), "csa2_project_fp4")
     return codes, scales, out
 

@@ -790,23 +790,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
 
 // ---- host side: tensor maps ----
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
+EncodeTiledFn encode_fn() { return tensor_map_encoder(); }
 
 // CTAs of a launch over `total` tiles (at most CTAS_PER_SM per SM).
 template <int QG>
@@ -952,6 +936,24 @@ csa2_status launch_index_select_prefill(const csa2_index_args& a, const uint8_t*
   if (a.B * a.q_per_seq == 0 || a.n == 0) return CSA2_OK;
   return launch_tc<4>(a, q8, c, nullptr, IndexTuning{}, s, &sel);
 }
+
+EncodeTiledFn tensor_map_encoder() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (!f) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<EncodeTiledFn>(p);
+      fn.store(f, std::memory_order_release);
+    }
+  }
+  return f;
+}
+
+uint64_t wait_limit_ns() { return pipeline_wait_ns(); }
 
 bool index_fuses_topk_hist(const csa2_index_args& a) {
   return (a.q_dtype == CSA2_BF16 || a.q_dtype == CSA2_E4M3) && a.k_dtype == CSA2_E4M3 &&

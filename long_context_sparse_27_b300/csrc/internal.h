@@ -1,6 +1,7 @@
 // internal.h -- launchers shared between the C-ABI layer and the kernels.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only)
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -10,6 +11,15 @@
 #include "../../include/csa2.h"
 
 namespace csa2 {
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time (null if absent).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+// Limit of a tensor-core pipeline's waits: CSA2_WAIT_LIMIT_NS, else 2 s.
+uint64_t wait_limit_ns();
 
 // Round up to a multiple of 256 bytes (every workspace region starts aligned).
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -205,10 +205,252 @@ __global__ void __launch_bounds__(kPjThreads)
 
 std::atomic<uint64_t> g_project_attr{0};  // devices on which the kernel's attributes are set
 
+// ---------------------------------------------------------------------------
+// tensor-core path (from 64 rows): tcgen05 bf16 MMAs, accumulators in TMEM
+// ---------------------------------------------------------------------------
+//
+// A CTA owns (128 rows, 64 output columns, 1/4 of the hidden features); the
+// 4 CTAs of a cluster split the hidden dimension.  Warp 0 streams 128 x 64
+// tiles of h and 64 x 64 tiles of w by TMA (128-byte swizzle) through a
+// 4-stage mbarrier ring, warp 1 issues tcgen05.mma.kind::f16 (M = 128, N =
+// 64, K = 16; four per stage) into one TMEM accumulator, and warps 2 .. 5
+// (one TMEM lane quarter each) move the accumulator to a shared-memory
+// partial tile.  After one cluster barrier CTA r sums rows 32 r .. 32 r + 31
+// of the 4 partials in rank order over distributed shared memory and
+// quantises them, one thread per (row, 32-column block).  Every wait is
+// bounded; a wait that gives up sets CSA2_DEVFLAG_TIMEOUT and the CTA's
+// abort flag, and the CTA still takes part in both cluster barriers.
+constexpr int kTcM = 128;                  // rows per CTA (MMA M, TMEM lanes)
+constexpr int kTcN = 64;                   // output columns per CTA (MMA N)
+constexpr int kTcK = 64;                   // features per stage: 128-byte rows
+constexpr int kTcStages = 4;
+constexpr int kTcSplit = 4;                // CTAs of a cluster: shares of the hidden dimension
+constexpr int kTcThreads = 192;            // producer, MMA issuer, 4 epilogue warps
+constexpr int kTcATile = kTcM * kTcK * 2;  // 16 KB
+constexpr int kTcBTile = kTcN * kTcK * 2;  // 8 KB
+constexpr int kTcPartLd = kTcN + 4;        // padded fp32 row of the partial tile
+constexpr int kTcOffB = kTcStages * kTcATile;
+constexpr int kTcOffBar = kTcOffB + kTcStages * kTcBTile;
+constexpr int kTcSmem = kTcOffBar + 256;   // barriers, TMEM slot, abort flag
+constexpr int kTcSmemAlloc = kTcSmem + 1024;  // 1024-byte alignment of the tiles
+static_assert(kTcM * kTcPartLd * 4 <= kTcOffBar, "the partial tile reuses the rings");
+static_assert((kTcM / kTcSplit) * (kTcN / 32) <= kTcThreads, "one thread per (row, block)");
+static_assert(2 * (kTcSmemAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
+
+__global__ void __launch_bounds__(kTcThreads, 2)
+    project_tc_kernel(const __grid_constant__ CUtensorMap hmap,
+                      const __grid_constant__ CUtensorMap wmap, int64_t rows, int32_t hidden,
+                      uint8_t* __restrict__ codes, int64_t codes_ld,
+                      uint8_t* __restrict__ scales, int64_t scales_ld, float* __restrict__ out,
+                      int64_t out_ld, int32_t* dev_status, uint64_t wait_ns) {
+  extern __shared__ uint8_t tc_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcOffBar);
+  uint64_t* empty = full + kTcStages;
+  uint64_t* accb = empty + kTcStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* part = reinterpret_cast<float*>(smem);  // [kTcM][kTcPartLd], after the main loop
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = (int)(blockIdx.x % kTcSplit);
+  const int64_t r0 = (int64_t)(blockIdx.x / kTcSplit) * kTcM;
+  const int c0 = (int)blockIdx.y * kTcN;
+  const int nkb_all = hidden / kTcK;
+  const int per = (nkb_all + kTcSplit - 1) / kTcSplit;
+  const int kb0 = min(nkb_all, rank * per);
+  const int nkb = min(nkb_all, kb0 + per) - kb0;
+
+  if (tid == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(accb, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&hmap);
+    tma_prefetch_desc(&wmap);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTcN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && nkb > 0) {
+      const uint64_t pol = l2_policy_evict_normal();  // h and w tiles are read by several CTAs
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % kTcStages;
+        if (!mbar_wait(&empty[s], (uint32_t)(((i / kTcStages) & 1) ^ 1), abort_flag, dev_status,
+                       wait_ns))
+          break;
+        mbar_arrive_expect_tx(&full[s], kTcATile + kTcBTile);
+        const int32_t x = (kb0 + i) * kTcK;
+        tma_load_2d(&hmap, &full[s], smem + s * kTcATile, x, (int32_t)r0, pol);
+        tma_load_2d(&wmap, &full[s], smem + kTcOffB + s * kTcBTile, x, c0, pol);
+        ++issued;
+      }
+      // on an abort, let the copies in flight land before shared memory is reused
+      int dummy = 0;
+      for (int u = issued > kTcStages ? issued - kTcStages : 0; u < issued; ++u)
+        mbar_wait(&full[u % kTcStages], (uint32_t)((u / kTcStages) & 1), &dummy, nullptr,
+                  wait_ns);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && nkb > 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kTcM, kTcN);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % kTcStages;
+        if (!mbar_wait(&full[s], (uint32_t)((i / kTcStages) & 1), abort_flag, dev_status, wait_ns))
+          break;
+        tc_fence_after();
+        const uint64_t a = sdesc_k_sw128(smem_u32(smem + s * kTcATile));
+        const uint64_t b = sdesc_k_sw128(smem_u32(smem + kTcOffB + s * kTcBTile));
+#pragma unroll
+        for (int kk = 0; kk < kTcK / 16; ++kk)  // K = 16 bf16 = 32 bytes = 2 descriptor units
+          tc_mma_bf16(tmem_base, a + 2 * kk, b + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(accb);  // every MMA issued has completed
+    }
+  } else {
+    // ---------------- accumulator -> shared-memory partial ----------------
+    const int quarter = warp & 3;  // TMEM lanes 32 quarter .. (warp % 4 rule)
+    const int row = 32 * quarter + lane;
+    float v[kTcN];
+    if (nkb > 0) {
+      const bool got = mbar_wait(accb, 0, abort_flag, dev_status, wait_ns);
+      if (__all_sync(0xffffffffu, got)) {
+        tc_fence_after();
+        tmem_ld32(tmem_base + ((uint32_t)(32 * quarter) << 16), v);
+        tmem_ld32(tmem_base + ((uint32_t)(32 * quarter) << 16) + 32, v + 32);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < kTcN; ++i) v[i] = 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kTcN; ++i) v[i] = 0.f;
+    }
+    // the rings are free once the accumulator is complete (every stage's
+    // loads landed and its MMAs read it)
+    asm volatile("bar.sync 1, %0;" ::"n"(4 * 32) : "memory");
+    float* prow = part + row * kTcPartLd;
+#pragma unroll
+    for (int i = 0; i < kTcN; i += 4)
+      *reinterpret_cast<float4*>(prow + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+  }
+  // the producer's copies have landed (or were never issued) before the
+  // partial tile overwrites the rings: the epilogue wrote only after the
+  // accumulator barrier, which follows every stage's full barrier
+  tc_fence_before();
+  __syncthreads();
+  pdl_trigger();
+  cluster_arrive_release();
+  cluster_wait_acquire();
+
+  // ---- rows 32 rank .. 32 rank + 31: one thread per (row, 32-column block)
+  if (tid < (kTcM / kTcSplit) * (kTcN / 32)) {
+    const int lr = (kTcM / kTcSplit) * rank + tid / (kTcN / 32);
+    const int blk = tid % (kTcN / 32);
+    const int64_t grow = r0 + lr;
+    if (grow < rows) {
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = 0.f;
+      const uint32_t local = smem_u32(part + lr * kTcPartLd + 32 * blk);
+#pragma unroll
+      for (int q = 0; q < kTcSplit; ++q) {
+        const uint32_t ra = cluster_addr(local, (uint32_t)q);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 t = ld_cluster_f4(ra + 4 * i);
+          x[i] += t.x;
+          x[i + 1] += t.y;
+          x[i + 2] += t.z;
+          x[i + 3] += t.w;
+        }
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      uint32_t sbyte = 0, pk[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) pk[g] = fp4_encode8(x + 8 * g, amax, sbyte);
+      const int64_t col = c0 + 32 * blk;
+      *reinterpret_cast<uint4*>(codes + grow * codes_ld + col / 2) =
+          make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      scales[grow * scales_ld + col / 32] = (uint8_t)sbyte;
+      if (out) {
+        float* orow = out + grow * out_ld + col;
+#pragma unroll
+        for (int i = 0; i < 32; i += 2)
+          *reinterpret_cast<float2*>(orow + i) = make_float2(x[i], x[i + 1]);
+      }
+    }
+  }
+  // no CTA leaves (or frees its tensor memory) while another may still read its partial
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTcN);
+  }
+}
+
+std::atomic<uint64_t> g_project_tc_attr{0};
+
+
 }  // namespace
 
 csa2_status launch_project_fp4(const csa2_project_args& a, cudaStream_t s) {
   if (a.rows == 0) return CSA2_OK;
+  const bool tc = a.rows >= 64 && a.hidden % (kTcK * kTcSplit) == 0 &&
+                  (reinterpret_cast<uintptr_t>(a.codes) & 15) == 0 && a.codes_ld % 16 == 0;
+  if (tc) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return cuda_fail(cudaErrorNotSupported);
+    CUtensorMap hmap, wmap;
+    {
+      cuuint64_t dims[2] = {(cuuint64_t)a.hidden, (cuuint64_t)a.rows};
+      cuuint64_t strides[1] = {(cuuint64_t)a.h_ld * 2};
+      cuuint32_t box[2] = {kTcK, kTcM};
+      cuuint32_t es[2] = {1, 1};
+      if (enc(&hmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.h), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return CSA2_ERR_INVALID_ARG;
+    }
+    {
+      cuuint64_t dims[2] = {(cuuint64_t)a.hidden, (cuuint64_t)a.d};
+      cuuint64_t strides[1] = {(cuuint64_t)a.w_ld * 2};
+      cuuint32_t box[2] = {kTcK, kTcN};
+      cuuint32_t es[2] = {1, 1};
+      if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.w), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return CSA2_ERR_INVALID_ARG;
+    }
+    cudaError_t e = once_per_device(g_project_tc_attr, [] {
+      return cudaFuncSetAttribute(project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kTcSmemAlloc);
+    });
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int64_t row_tiles = (a.rows + kTcM - 1) / kTcM;
+    if (row_tiles * kTcSplit > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)(row_tiles * kTcSplit), (unsigned)(a.d / kTcN));
+    return launch_kernel(project_tc_kernel, grid, dim3(kTcThreads), (size_t)kTcSmemAlloc, s,
+                         kTcSplit, hmap, wmap, a.rows, a.hidden, a.codes, a.codes_ld, a.scales,
+                         a.scales_ld, a.out, a.out_ld, a.dev_status, wait_limit_ns());
+  }
   cudaError_t e = once_per_device(g_project_attr, [] {
     return cudaFuncSetAttribute(project_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kPjSmem);

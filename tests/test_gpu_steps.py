@@ -280,7 +280,8 @@ def test_index_score_pool_exact_small_integers(csa2, orc):
 # ------------------------------------ the decoder's global KV (projection + a1)
 
 @pytest.mark.parametrize("rows,hidden,d", [(8, 4096, 512), (100, 256, 128), (1, 64, 64),
-                                           (1024, 512, 512), (5, 416, 64), (65, 4096, 64)])
+                                           (1024, 512, 512), (5, 416, 64), (65, 4096, 64),
+                                           (300, 1024, 512), (64, 768, 192)])
 def test_project_fp4(csa2, orc, rows, hidden, d):
     h = synth.normal((rows, hidden), 210 + rows)
     w = synth.normal((d, hidden), 211 + rows) * 0.05
