@@ -130,9 +130,6 @@ bool stall_loads() {
   return e && e[0] == '1';
 }
 
-constexpr int kPageLookahead = 8;  // paged keys: tiles whose page ids are in flight ahead
-constexpr int kPageRing = 16;      // tiles in the page-id ring (two ids each)
-static_assert(kPageRing >= kPageLookahead + 1, "a ring slot is not rewritten while in use");
 
 template <int QG>
 struct TcCfg {
@@ -170,8 +167,7 @@ struct TcCfg {
   // barriers: full[S], empty[S], qfull[2], qempty[2], tfull[NACC], tempty[NACC], fin, nrdy
   static constexpr int NBAR = 2 * STAGES + 4 + 2 * NACC + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem slot, abort flag
-  static constexpr int OFF_PG = OFF_MISC + 16;                // int32 [kPageRing][2] page ids
-  static constexpr int SMEM = OFF_PG + kPageRing * 2 * 4;
+  static constexpr int SMEM = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
   static_assert(NACC % STREAMS == 0 && QG % SPLIT == 0,
                 "accumulator a is drained by the warpgroups of stream a % STREAMS");
@@ -205,6 +201,7 @@ struct TcParams {
   // boxes, each inside one page
   csa2_pages pages;
   int pg_box;
+  int pg_shift;            // log2(page_rows) when a power of two, else -1
   uint64_t wait_ns;        // limit of each pipeline wait (drain waits keep their own)
   int stall_loads;         // test hook: the producer issues no loads (waits run out)
   // sampled launches: the cursor's tile kt is key tile kt * tile_stride, and
@@ -308,7 +305,14 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0 && t_begin < t_end && !p.stall_loads) {
+    // Lane 0 issues the barrier operations and the copies.  Paged keys: the
+    // whole warp runs the loop and looks up the pool rows of the next 32
+    // tiles (lane l those of tile i0 + 32 + l, loads in flight while lane 0
+    // works through tiles i0 .. i0 + 31), and lane 0 takes tile i's rows from
+    // lane i % 32 by a shuffle: no lookup latency and no 64-bit division in
+    // the loop.
+    const bool paged_keys = p.pages.block_table != nullptr;
+    if (t_begin < t_end && !p.stall_loads && (paged_keys || lane == 0)) {
       const uint64_t pol_k = p.keep_in_l2 ? l2_policy_evict_normal() : l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
       int stage = 0;
@@ -317,47 +321,35 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       bool ok = true, nr_seen = false;
       const int64_t dir = p.reverse ? -1 : 1;
       TileCursor cur(p.reverse ? t_end - 1 : t_begin, p.ktiles);
-      // paged keys: the page ids of tile i (two 64-row halves) are copied by
-      // cp.async into ring slot i % kPageRing, kPageLookahead tiles before
-      // the tile's loads are issued (one commit group per tile)
-      const bool paged = p.pages.block_table != nullptr;
+      const bool paged = paged_keys;  // the whole warp runs the loop; else lane 0 alone
       const int64_t ntiles = t_end - t_begin;
-      int32_t* pg = reinterpret_cast<int32_t*>(smem + C::OFF_PG);
-      TileCursor ahead(p.reverse ? t_end - 1 : t_begin, p.ktiles);
-      int64_t ahead_i = 0;
-      // (the producer is one thread: no 64-bit divisions per tile; the
-      // sequence of a group changes rarely, and rows, page sizes and query
-      // counts fit 32 bits)
-      const uint32_t pr = paged ? (uint32_t)p.pages.page_rows : 1u;
       const uint32_t qps = (uint32_t)p.q_per_seq;
-      int64_t ahead_gprev = -1;
-      const int32_t* bt_row = nullptr;
-      auto page_ids_ahead = [&](int64_t upto) {  // issue tiles ahead_i .. upto - 1
-        for (; ahead_i < upto; ++ahead_i) {
-          if (ahead_i < ntiles) {
-            if (ahead.g != ahead_gprev) {
-              ahead_gprev = ahead.g;
-              bt_row = p.pages.block_table +
-                       (int64_t)((uint32_t)(ahead.g * QG) / qps) * p.pages.bt_ld;
-            }
+      const uint32_t pr = paged ? (uint32_t)p.pages.page_rows : 1u;
+      const int boxes = C::BM / (paged ? p.pg_box : C::BM);
+      // pool rows of the two 64-row halves of the CTA's tile i (-1: none)
+      auto rows_of = [&](int64_t i, int32_t* y) {
+        y[0] = y[1] = -1;
+        if (i >= ntiles) return;
+        const TileCursor c(p.reverse ? t_end - 1 - i : t_begin + i, p.ktiles);
+        const int64_t kt = c.kt * p.tile_stride;
+        const int32_t* bt = p.pages.block_table + (int64_t)((uint32_t)(c.g * QG) / qps) * p.pages.bt_ld;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int64_t j = ahead.kt * p.tile_stride * C::BM + 64 * h;
-              if (j < p.n && (h == 0 || p.pg_box == 64))
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                                 smem_u32(pg + (ahead_i % kPageRing) * 2 + h)),
-                             "l"(bt_row + (uint32_t)j / pr)
-                             : "memory");
-            }
-            ahead.advance(dir);
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t j = (uint32_t)(kt * C::BM + 64 * h);
+          if (h >= boxes || (int64_t)j >= p.n) continue;  // past the rows: masked
+          const uint32_t pi = p.pg_shift >= 0 ? j >> p.pg_shift : j / pr;
+          const int32_t page = __ldg(bt + pi);
+          if (page < 0 || page >= p.pages.num_pages) {
+            raise_flag(p.dev_status, CSA2_DEVFLAG_BOUNDS);
+            continue;
           }
-          asm volatile("cp.async.commit_group;" ::: "memory");
+          y[h] = (int32_t)((int64_t)page * pr + (j - pi * pr));
         }
       };
-      if (paged) page_ids_ahead(kPageLookahead);
       int64_t b_of = -1, b = 0;  // the sequence of group b_of
-      for (int64_t i = 0; i < ntiles; ++i, cur.advance(dir)) {
-        const int64_t g = cur.g, kt = cur.kt * p.tile_stride;  // the key tile
+      // lane 0: the barrier waits and copies of tile (g, kt); paged keys at
+      // pool rows y0 / y1 (-1: that half is not loaded).  False: a wait gave up.
+      auto issue_tile = [&](int64_t g, int64_t kt, int32_t y0, int32_t y1) -> bool {
         if (g != b_of) {
           b_of = g;
           b = (uint32_t)(g * QG) / qps;
@@ -365,27 +357,18 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         if (g != g_prev && !p.qbf) {
           const int qs = (int)(qcount & 1);
           const uint32_t qph = (uint32_t)((qcount >> 1) & 1);
-          if (!mbar_wait(&qempty[qs], qph ^ 1, abort_flag, p.dev_status, p.wait_ns)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(&qempty[qs], qph ^ 1, abort_flag, p.dev_status, p.wait_ns)) return false;
           mbar_arrive_expect_tx(&qfull[qs], C::QTILE);
           tma_load_2d(&qmap, &qfull[qs], qbuf + qs * C::QTILE, 0, (int32_t)(g * C::BN), pol_q);
           ++qcount;
           g_prev = g;
         }
-        if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, p.dev_status, p.wait_ns)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(&empty[stage], ph ^ 1, abort_flag, p.dev_status, p.wait_ns)) return false;
         if (p.nr.kv && !nr_seen && kt * C::BM < p.nr.row0 + p.nr.rows &&
             (kt + 1) * C::BM > p.nr.row0) {
           // this tile holds new rows: the epilogue warps have written them
           // (their proxy fence orders the stores before this TMA load)
-          if (!mbar_wait(nrdy, 0, abort_flag, p.dev_status, p.wait_ns)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(nrdy, 0, abort_flag, p.dev_status, p.wait_ns)) return false;
           nr_seen = true;
         }
         if (!paged) {
@@ -393,43 +376,43 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
           tma_load_3d(&kmap, &full[stage], kbuf + stage * C::KTILE, 0, (int32_t)(kt * C::BM),
                       (int32_t)b, pol_k);
         } else {
-          // tiles i .. i + kPageLookahead - 1 have their page ids in flight;
-          // the kPageLookahead - 1 groups after tile i's may stay pending
-          page_ids_ahead(i + kPageLookahead);
-          asm volatile("cp.async.wait_group %0;" ::"n"(kPageLookahead - 1) : "memory");
-          const int32_t* ids = pg + (i % kPageRing) * 2;
-          int32_t y[2];
-          uint32_t bytes = 0;
-          const int boxes = C::BM / p.pg_box;
           const uint32_t box_bytes = (uint32_t)p.pg_box * C::BK;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t j = kt * C::BM + 64 * h;
-            y[h] = -1;
-            if (h >= boxes || j >= p.n) continue;  // past the rows: never looked up (masked)
-            const int32_t page = ids[h];
-            if (page < 0 || page >= p.pages.num_pages) {
-              raise_flag(p.dev_status, CSA2_DEVFLAG_BOUNDS);
-              continue;
-            }
-            y[h] = (int32_t)((int64_t)page * pr + (uint32_t)j % pr);
-            bytes += box_bytes;
-          }
-          mbar_arrive_expect_tx(&full[stage], bytes);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            if (y[h] >= 0)
-              tma_load_2d(&kmap, &full[stage], kbuf + stage * C::KTILE + h * (C::KTILE / 2), 0,
-                          y[h], pol_k);
+          mbar_arrive_expect_tx(&full[stage],
+                                (y0 >= 0 ? box_bytes : 0u) + (y1 >= 0 ? box_bytes : 0u));
+          if (y0 >= 0) tma_load_2d(&kmap, &full[stage], kbuf + stage * C::KTILE, 0, y0, pol_k);
+          if (y1 >= 0)
+            tma_load_2d(&kmap, &full[stage], kbuf + stage * C::KTILE + C::KTILE / 2, 0, y1,
+                        pol_k);
         }
         ++issued;
         if (++stage == C::STAGES) {
           stage = 0;
           ph ^= 1;
         }
+        return true;
+      };
+      if (paged) {
+        // the whole warp: the rows of tiles i0 .. i0 + 31 in ycur (lane l:
+        // tile i0 + l), those of the next 32 in flight in ynext
+        int32_t ycur[2], ynext[2];
+        rows_of(lane, ycur);
+        rows_of(32 + lane, ynext);
+        for (int64_t i = 0; i < ntiles; ++i, cur.advance(dir)) {
+          if (i > 0 && (i & 31) == 0) {
+            ycur[0] = ynext[0];
+            ycur[1] = ynext[1];
+            rows_of(i + 32 + lane, ynext);
+          }
+          const int32_t y0 = __shfl_sync(0xffffffffu, ycur[0], (int)(i & 31));
+          const int32_t y1 = __shfl_sync(0xffffffffu, ycur[1], (int)(i & 31));
+          if (lane == 0) ok = issue_tile(cur.g, cur.kt * p.tile_stride, y0, y1);
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+        }
+      } else {
+        for (int64_t i = 0; i < ntiles && ok; ++i, cur.advance(dir))
+          ok = issue_tile(cur.g, cur.kt * p.tile_stride, -1, -1);
       }
-      if (paged) asm volatile("cp.async.wait_all;" ::: "memory");  // page ids in flight
-      if (!ok) {
+      if (lane == 0 && !ok) {
         // let the copies already in flight land before the CTA's shared
         // memory goes away: wait (bounded, ignoring the abort flag) for the
         // full barrier of every stage filled but possibly not consumed
@@ -861,6 +844,10 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   p.keep_in_l2 = tune.keep_in_l2 ? 1 : 0;
   p.pages = a.pages;
   p.pg_box = a.pages.page_rows % 128 == 0 ? 128 : 64;
+  p.pg_shift = -1;
+  if (a.pages.page_rows > 0 && (a.pages.page_rows & (a.pages.page_rows - 1)) == 0)
+    for (p.pg_shift = 0; (1 << p.pg_shift) < a.pages.page_rows; ++p.pg_shift) {
+    }
   p.wait_ns = pipeline_wait_ns();
   p.stall_loads = stall_loads() ? 1 : 0;
   p.tile_stride = sel && sel->tile_stride > 1 ? sel->tile_stride : 1;
