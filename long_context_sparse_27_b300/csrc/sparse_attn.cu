@@ -269,7 +269,13 @@ __device__ __noinline__ void dequant_block(uint4 cw, uint32_t sb, uint8_t* d0, u
 //     attn_combine_kernel merges.
 // pre: Q may be read before the programmatic-launch wait (the caller knows
 // the kernels still running on the stream do not write it).
-template <bool CLUSTER>
+// MODE: kModeCombine (chunk partials, merged by attn_combine_kernel),
+// kModeCluster (the chunks of a query and head group are a cluster and merge
+// their partials through L2) or kModeSeq (one CTA per query and head group
+// walks its chunks in order with a running softmax: no partials).
+constexpr int kModeCombine = 0, kModeCluster = 1, kModeSeq = 2;
+
+template <int MODE>
 __global__ void __launch_bounds__(kAttnThreads, 2)
     attn_bf16_kernel(const csa2_attn_args a, int nchunks, int fk, float* __restrict__ partial,
                      int pre) {
@@ -280,8 +286,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   uint8_t* sPl = sPh + kHG * kPRow;
   __shared__ ChunkRows rows;
   __shared__ float red_m[kPairs][kHG], red_l[kPairs][kHG];
+  // kModeSeq: the running softmax state of each head and this chunk's rescale
+  __shared__ float run_m[kHG], run_l[kHG], run_f[kHG];
 
-  const int chunk = blockIdx.x, hg = blockIdx.y;
+  const int hg = blockIdx.y;
   const int64_t qi = blockIdx.z;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
   const int ngroups = (a.hq + kHG - 1) / kHG;
@@ -308,24 +316,39 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   window_of(a, qi, ws, wl);
   const int64_t nkeys = a.k + wl;
 
+  // the key list index of row r of chunk c (-1: no key)
+  auto key_of = [&](int c, int r) -> int64_t {
+    if (fk > 0) {
+      if (r < fk) {
+        const int64_t i = (int64_t)c * fk + r;
+        return i < a.k ? i : -1;
+      }
+      const int64_t u = (int64_t)c * (kKC - fk) + (r - fk);
+      return u < wl ? a.k + u : -1;
+    }
+    const int64_t t = (int64_t)c * kKC + r;
+    return t < nkeys ? t : -1;
+  };
+  const int d0 = warp * kPVSlice;
+  const int r0 = lane >> 2;  // rows (heads) r0 and r0 + 8 of this thread's MMA fragments
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  if constexpr (MODE == kModeSeq) {
+    if (tid < kHG) {
+      run_m[tid] = -INFINITY;
+      run_l[tid] = 0.f;
+    }
+  }
+  for (int chunk = MODE == kModeSeq ? 0 : (int)blockIdx.x;
+       chunk < (MODE == kModeSeq ? nchunks : (int)blockIdx.x + 1); ++chunk) {
+    if constexpr (MODE == kModeSeq) __syncthreads();  // the previous chunk's tiles are read
   // ---- 1. key sources.  fk > 0: chunk c holds selected keys fk c .. fk c +
   // fk - 1 and window rows (kKC - fk) c .., so every chunk gathers the same
   // mix (the softmax is over the set of keys, in any order); fk = 0: keys
   // t = kKC c .. of the list (selected keys, then the window)
   if (tid < kKC) {
-    int64_t t = -1;  // no key
-    if (fk > 0) {
-      if (tid < fk) {
-        const int64_t i = (int64_t)chunk * fk + tid;
-        if (i < a.k) t = i;
-      } else {
-        const int64_t u = (int64_t)chunk * (kKC - fk) + (tid - fk);
-        if (u < wl) t = a.k + u;
-      }
-    } else {
-      t = (int64_t)chunk * kKC + tid;
-      if (t >= nkeys) t = -1;
-    }
+    const int64_t t = key_of(chunk, tid);
     KeySrc src{nullptr, nullptr, nullptr};
     if (t >= 0) src = key_source(a, qi, t, ws, wl);
     rows.codes[tid] = src.codes;
@@ -386,9 +409,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   }
   cp_async_wait_all();
   __syncthreads();
+  if constexpr (MODE == kModeSeq) {
+    // the next chunk's rows move into L2 while this chunk is computed
+    if (tid < kKC && chunk + 1 < nchunks) {
+      const int64_t t = key_of(chunk + 1, tid);
+      if (t >= 0) {
+        const KeySrc src = key_source(a, qi, t, ws, wl);
+        if (src.codes) {
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(src.codes));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(src.codes + 128));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(src.scales));
+        } else if (src.win) {
+#pragma unroll
+          for (int b = 0; b < kD * 2; b += 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(src.win) + b));
+        }
+      }
+    }
+  }
 
   // ---- 3. S = Q K^T and the chunk softmax (warps 0 .. kSWarps-1)
-  const int r0 = lane >> 2;
   if (warp < kSWarps) {
     const int pr = warp;
     // two independent accumulator chains per n-tile: dims 0..255 and 256..511
@@ -441,6 +481,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       m0 = fmaxf(m0, red_m[w][r0]);
       m1 = fmaxf(m1, red_m[w][r0 + 8]);
     }
+    if constexpr (MODE == kModeSeq) {  // P against the running maximum
+      m0 = fmaxf(m0, run_m[r0]);
+      m1 = fmaxf(m1, run_m[r0 + 8]);
+    }
     float l0 = 0.f, l1 = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -475,12 +519,34 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     }
   }
   __syncthreads();
+  if constexpr (MODE == kModeSeq) {
+    if (tid < kHG) {  // head tid: m_new = max(m_old, chunk max), l = l f + chunk sum
+      float mc = run_m[tid], l = 0.f;
+#pragma unroll
+      for (int w = 0; w < kPairs; ++w) {
+        mc = fmaxf(mc, red_m[w][tid]);
+        l += red_l[w][tid];
+      }
+      const float f = run_m[tid] == -INFINITY ? 0.f : __expf(run_m[tid] - mc);
+      run_f[tid] = f;
+      run_l[tid] = run_l[tid] * f + l;
+      run_m[tid] = mc;
+    }
+    __syncthreads();
+  }
 
   // ---- 4. O = P V: dims d0 .. d0+63 (8 n-tiles), keys as the K dimension
-  const int d0 = warp * kPVSlice;
-  float o[8][4];
+  if constexpr (MODE == kModeSeq) {
+    // the running state moves on: O and l scale by e^(m_old - m_new)
+    const float f0 = run_f[r0], f1 = run_f[r0 + 8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < 8; ++i) {
+      o[i][0] *= f0;
+      o[i][1] *= f0;
+      o[i][2] *= f1;
+      o[i][3] *= f1;
+    }
+  }
   {
     const uint32_t pbase_h = smem_u32(sPh) + (lane & 15) * kPRow + (lane >> 4) * 16;
     const uint32_t pbase_l = smem_u32(sPl) + (lane & 15) * kPRow + (lane >> 4) * 16;
@@ -503,6 +569,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     }
   }
 
+  }  // chunks
+
+  if constexpr (MODE == kModeSeq) {
+    // ---- 5. the output: O / l (no key: 0)
+    pdl_trigger();
+    const float i0 = run_l[r0] > 0.f ? 1.f / run_l[r0] : 0.f;
+    const float i1 = run_l[r0 + 8] > 0.f ? 1.f / run_l[r0 + 8] : 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = d0 + nt * 8 + 2 * (lane & 3);
+      if (r0 < hvalid)
+        *reinterpret_cast<float2*>(a.out + (qi * a.hq + (int64_t)hg * kHG + r0) * kD + col) =
+            make_float2(o[nt][0] * i0, o[nt][1] * i0);
+      if (r0 + 8 < hvalid)
+        *reinterpret_cast<float2*>(a.out + (qi * a.hq + (int64_t)hg * kHG + r0 + 8) * kD + col) =
+            make_float2(o[nt][2] * i1, o[nt][3] * i1);
+    }
+    return;
+  }
+  const int chunk = blockIdx.x;
   // ---- 5. this chunk's partial: O (unnormalised), then m and l per head
   float* part = partial + ((qi * ngroups + hg) * (int64_t)nchunks + chunk) *
                               PartialLayout::kFloats;
@@ -523,7 +609,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     part[kHG * kD + kHG + tid] = l;
   }
 
-  if constexpr (CLUSTER) {
+  if constexpr (MODE == kModeCluster) {
     // every chunk's partial is written (release) and visible (acquire)
     cluster_arrive_release();
     cluster_wait_acquire();
@@ -618,8 +704,16 @@ int attn_chunks(const csa2_attn_args& a) {
 
 }  // namespace
 
+// Many queries (a prefill chunk): one CTA per (query, head group) walking its
+// chunks fills the GPU at least twice over, and no partial goes through
+// memory; few queries (decode): one CTA per chunk, merged in a cluster.
+bool attn_sequential(const csa2_attn_args& a) {
+  const int64_t ctas = a.nq * ((a.hq + kHG - 1) / kHG);
+  return ctas >= 4 * (int64_t)sm_count();
+}
+
 size_t attn_workspace_bytes(const csa2_attn_args& a) {
-  if (a.q_dtype != CSA2_BF16) return 0;
+  if (a.q_dtype != CSA2_BF16 || attn_sequential(a)) return 0;
   // every chunk's partial (O, m, l) goes through the workspace
   const int64_t nchunks = attn_chunks(a);
   return (size_t)a.nq * ((a.hq + kHG - 1) / kHG) * nchunks * PartialLayout::kFloats *
@@ -643,15 +737,17 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s, bool q_
   }
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
-    cudaError_t r = cudaFuncSetAttribute(attn_bf16_kernel<true>,
+    cudaError_t r = cudaFuncSetAttribute(attn_bf16_kernel<kModeCluster>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(attn_bf16_kernel<false>,
+      r = cudaFuncSetAttribute(attn_bf16_kernel<kModeCombine>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(attn_bf16_kernel<kModeSeq>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
     return r;
   });
   if (e != cudaSuccess) return cuda_fail(e);
-  const dim3 grid((unsigned)nchunks, (unsigned)((a.hq + kHG - 1) / kHG), (unsigned)a.nq);
   float* partial = static_cast<float*>(a.workspace);
   const int pre = q_ready ? 1 : 0;
   // spread the selected keys and the window rows evenly over the chunks when
@@ -659,10 +755,16 @@ csa2_status launch_sparse_attn(const csa2_attn_args& in, cudaStream_t s, bool q_
   // an FP4 row's bytes: a chunk of window rows alone would finish last)
   int fk = (int)((a.k + nchunks - 1) / nchunks);
   if (fk > kKC || (int64_t)(kKC - fk) * nchunks < a.win_max) fk = 0;
+  const unsigned ngroups = (unsigned)((a.hq + kHG - 1) / kHG);
+  if (attn_sequential(a))
+    return launch_kernel(attn_bf16_kernel<kModeSeq>, dim3(1, ngroups, (unsigned)a.nq),
+                         dim3(kAttnThreads), (size_t)kAttnSmem, s, 1, a, nchunks, fk, partial,
+                         pre);
+  const dim3 grid((unsigned)nchunks, ngroups, (unsigned)a.nq);
   if (nchunks <= kMaxClusterChunks)
-    return launch_kernel(attn_bf16_kernel<true>, grid, dim3(kAttnThreads), (size_t)kAttnSmem, s,
-                         (unsigned)nchunks, a, nchunks, fk, partial, pre);
-  csa2_status st = launch_kernel(attn_bf16_kernel<false>, grid, dim3(kAttnThreads),
+    return launch_kernel(attn_bf16_kernel<kModeCluster>, grid, dim3(kAttnThreads),
+                         (size_t)kAttnSmem, s, (unsigned)nchunks, a, nchunks, fk, partial, pre);
+  csa2_status st = launch_kernel(attn_bf16_kernel<kModeCombine>, grid, dim3(kAttnThreads),
                                  (size_t)kAttnSmem, s, 1, a, nchunks, fk, partial, pre);
   if (st != CSA2_OK) return st;
   return launch_kernel(attn_combine_kernel, dim3((unsigned)a.hq, (unsigned)a.nq), dim3(128), 0, s,

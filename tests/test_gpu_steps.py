@@ -468,6 +468,34 @@ def test_attn_bf16_prefill_windows(csa2, orc):
     assert rel_l2(out.cpu().numpy(), ref) <= 2e-3
 
 
+def test_attn_bf16_many_queries_walk_their_chunks(csa2, orc):
+    # 160 queries x 64 heads: 640 CTAs of 16 heads, enough to fill the GPU,
+    # so each CTA takes one (query, head group) and walks its 8 chunks with a
+    # running softmax (no partials); per-query windows (some short, one
+    # empty) and ragged selections.  The same queries launched 8 at a time
+    # (one CTA per chunk, merged in a cluster) meet the same bar.
+    T, W, n, k, d, hq = 160, 128, 2000, 512, 512, 64
+    codes, scales = make_cache(csa2, 1, n, d, 130)
+    rc, rs = oracle_cache(orc, 1, n, d, 130)
+    q = synth.normal((T, hq, d), 131)
+    idx = synth.random_indices(T, k, n, 132, pad=37)
+    win = synth.normal((1, T + W - 1, d), 133)
+    ws = torch.arange(T, dtype=torch.int32)
+    wl = torch.full((T,), W, dtype=torch.int32)
+    wl[::7] = 3
+    wl[5] = 0
+    scale = 1 / math.sqrt(d)
+    out = csa2.sparse_attn(dev(q), codes, scales, dev(idx), dev(win), scale, q_per_seq=T,
+                           win_start=dev(ws), win_len=dev(wl), win_max=W)
+    ref = orc.sparse_attn(f64(q), rc, rs, idx.numpy(), f64(win), scale, q_per_seq=T,
+                          win_start=ws.numpy(), win_len=wl.numpy())
+    assert rel_l2(out.cpu().numpy(), ref) <= 2e-3
+    sub = slice(40, 48)
+    out8 = csa2.sparse_attn(dev(q[sub]), codes, scales, dev(idx[sub]), dev(win), scale,
+                            q_per_seq=8, win_start=dev(ws[sub]), win_len=dev(wl[sub]), win_max=W)
+    assert rel_l2(out8.cpu().numpy(), ref[sub]) <= 2e-3
+
+
 def test_attn_bounds_flag(csa2):
     d, n = 512, 100
     codes, scales = make_cache(csa2, 1, n, d, 99)
