@@ -222,7 +222,8 @@ csa2_status csa2_quantize_index_q(const void* q, const float* w, int64_t nq, int
  *         (elements); E4M3 needs k, k_ld, k_seq_stride 16-byte aligned.
  * n_valid optional device int32 [nq] (NULL = every entry visible).
  * scores  device f32, row q at scores + q * scores_ld.
- * Errors: INVALID_ARG, UNSUPPORTED (other shapes / dtypes), ALIGNMENT,
+ * Errors: INVALID_ARG, UNSUPPORTED (other shapes / dtypes; on the E4M3
+ *         path also n > 2^30 or nq * ceil(n / 128) >= 2^31), ALIGNMENT,
  *         WORKSPACE (csa2_index_score_workspace_bytes), CUDA.
  * Device: CSA2_DEVFLAG_TIMEOUT if the tensor-core pipeline stalled.
  */

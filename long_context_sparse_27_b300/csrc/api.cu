@@ -141,7 +141,9 @@ csa2_status check_index(const csa2_index_args* a) {
     if (!aligned(a->k, 16) || a->k_ld % 16 != 0 || a->k_seq_stride % 16 != 0)
       return CSA2_ERR_ALIGNMENT;
     if (!aligned(a->q, 16)) return CSA2_ERR_ALIGNMENT;
-    if (a->n > (int64_t)1 << 31 || nq * a->hi > (int64_t)1 << 31) return CSA2_ERR_UNSUPPORTED;
+    if (a->n > (int64_t)1 << 30 || nq * a->hi > (int64_t)1 << 31 ||
+        nq * ((a->n + 127) / 128) >= (int64_t)1 << 31)
+      return CSA2_ERR_UNSUPPORTED;
     if (a->q_dtype == CSA2_E4M3) return aligned(a->w, 16) ? CSA2_OK : CSA2_ERR_ALIGNMENT;
     if (!a->workspace || a->workspace_bytes < index_ws(a)) return CSA2_ERR_WORKSPACE;
     if (!aligned(a->workspace, 256)) return CSA2_ERR_ALIGNMENT;

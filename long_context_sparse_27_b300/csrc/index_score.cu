@@ -611,8 +611,11 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         if (lane == 0) mbar_arrive(nrdy);
       }
     }
-    int64_t nv[C::QPW];
+    // per query of the current group: entries visible (below n and
+    // n_valid), the candidate threshold and the score row
+    int32_t vis[C::QPW];
     uint32_t th[C::QPW];
+    float* srow[C::QPW];
     float wr[C::REG_W ? 16 : 1];  // REG_W: this thread's 16 head weights of its query
     // emitting launches: each (warp, query) stream reserves its candidate
     // slots 32 at a time (one atomic per 32 candidates); slots [cpos, cend)
@@ -630,13 +633,30 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         cpos[qq] = cend[qq] = 0;
       }
     };
-    // li counts tiles in processing order (from the range's end when reversed)
-    const int64_t dir = p.reverse ? -1 : 1;
-    TileCursor cur(p.reverse ? t_end - 1 - stream : t_begin + stream, p.ktiles);
-    for (int64_t li = stream; li < t_end - t_begin;
-         li += C::STREAMS, cur.advance(dir * C::STREAMS)) {
-      const int64_t g = cur.g, kt = cur.kt;
-      const int acc = (int)(li % C::NACC);
+    // li counts tiles in processing order (from the range's end when
+    // reversed); the cursor is (group g, tile kt).  The host keeps a
+    // launch's tiles and entries below 2^31, so the per-tile arithmetic is
+    // 32-bit.
+    const int32_t dir = p.reverse ? -1 : 1;
+    const int32_t ntiles = (int32_t)(t_end - t_begin), ktiles = (int32_t)p.ktiles;
+    const int32_t kstep = p.tile_stride * C::BM;  // entries from one cursor tile to the next
+    const int32_t n32 = (int32_t)p.n;
+    const int64_t tc0 = p.reverse ? t_end - 1 - stream : t_begin + stream;
+    int64_t g = tc0 / p.ktiles;
+    int32_t kt = (int32_t)(tc0 % p.ktiles);
+    auto advance = [&]() {
+      kt += dir * C::STREAMS;
+      while (kt >= ktiles) {
+        kt -= ktiles;
+        ++g;
+      }
+      while (kt < 0) {
+        kt += ktiles;
+        --g;
+      }
+    };
+    for (uint32_t li = stream; li < (uint32_t)ntiles; li += C::STREAMS, advance()) {
+      const int acc = li % C::NACC;
       const uint32_t aph = (uint32_t)((li / C::NACC) & 1);
       if (g != g_prev) {
         if (p.cand && g_prev >= 0) flush_chunks(g_prev);
@@ -657,10 +677,11 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         }
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < C::QPW; ++i)
-        {
-          nv[i] = p.n_valid ? (int64_t)p.n_valid[g * QG + q0 + i] : p.n;
-          th[i] = p.cand ? p.theta[g * QG + q0 + i] : 0u;
+        for (int i = 0; i < C::QPW; ++i) {
+          const int64_t qi = g * QG + q0 + i;
+          vis[i] = p.n_valid ? min(n32, p.n_valid[qi]) : n32;
+          th[i] = p.cand ? p.theta[qi] : 0u;
+          srow[i] = p.scores ? p.scores + qi * p.scores_ld : nullptr;
         }
         g_prev = g;
       }
@@ -737,17 +758,16 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         sc[qq] = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
       }
       }
-      const int64_t jc = kt * C::BM + row;          // score column (compact when sampled)
-      const int64_t j = jc + kt * (p.tile_stride - 1) * C::BM;  // the entry
+      const int32_t jc = kt * C::BM + row;  // score column (compact when sampled)
+      const int32_t j = kt * kstep + row;   // the entry
       if (p.cand) {
         // candidates of the exact selection: the warp's takes fill its
         // current chunk, then (one atomic) a new chunk of 32
         const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
         for (int qq = 0; qq < C::QPW; ++qq) {
-          const int64_t qi = g * QG + q0 + qq;
           const uint32_t key = score_key(sc[qq]);
-          const bool take = j < p.n && j < nv[qq] && key >= th[qq];
+          const bool take = j < vis[qq] && key >= th[qq];
           const uint32_t mask = __ballot_sync(0xffffffffu, take);
           if (mask) {
             const uint32_t cnt = __popc(mask), r = __popc(mask & lt);
@@ -757,29 +777,26 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
               cpos[qq] += cnt;
             } else {
               uint32_t nb = 0;
-              if (lane == 0) nb = atomicAdd(&p.cand_cnt[qi], 32u);
+              if (lane == 0) nb = atomicAdd(&p.cand_cnt[g * QG + q0 + qq], 32u);
               nb = __shfl_sync(0xffffffffu, nb, 0);
               if (r >= avail) pos = nb + (r - avail);
               cpos[qq] = nb + (cnt - avail);
               cend[qq] = nb + 32;
             }
             if (take && pos < (uint64_t)p.cand_cap)
-              p.cand[qi * p.cand_cap + pos] = make_uint2(key, (uint32_t)j);
+              p.cand[(g * QG + q0 + qq) * p.cand_cap + pos] = make_uint2(key, (uint32_t)j);
           }
         }
-      } else if (j < p.n || p.tile_stride > 1) {
+      } else if (j < n32 || p.tile_stride > 1) {
         // (a sampled row is compact: its columns past the entries read -inf)
 #pragma unroll
-        for (int qq = 0; qq < C::QPW; ++qq) {
-          const int64_t qi = g * QG + q0 + qq;
-          p.scores[qi * p.scores_ld + jc] = (j < p.n && j < nv[qq]) ? sc[qq] : -INFINITY;
-        }
+        for (int qq = 0; qq < C::QPW; ++qq) srow[qq][jc] = j < vis[qq] ? sc[qq] : -INFINITY;
       }
       if constexpr (QG == 1) {
         // first-level histogram of the visible keys (the top-k's level 1):
         // the CTA's first two groups in shared memory, any later one (short
         // rows) straight to global memory
-        if (p.hist1 && j < p.n && j < nv[0]) {
+        if (p.hist1 && j < vis[0]) {
           const uint32_t bin = score_key(sc[0]) >> 20;
           const int64_t slot = g - g_first;
           if (slot < C::HSLOTS)
@@ -878,6 +895,11 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return CSA2_ERR_INVALID_ARG;
   }
+  // the kernel's per-tile arithmetic is 32-bit: entries and tiles of a
+  // launch stay below 2^31
+  if (a.n > ((int64_t)1 << 30) || (nq / QG) * ((a.n + C::BM - 1) / C::BM) >= ((int64_t)1 << 31) ||
+      (sel && sel->tile_stride > 1024))
+    return CSA2_ERR_UNSUPPORTED;
   TcParams p;
   p.c = c;
   p.qbf = fuse_q ? static_cast<const uint16_t*>(a.q) : nullptr;

@@ -183,6 +183,14 @@ def test_index_validation(csa2, monkeypatch):
     a.k_seq_stride = 100
     assert L.csa2_index_score(ctypes.byref(a), None) == 1          # overlapping sequences
     a.k_seq_stride = 128 * 1000
+    # the tensor-core kernel's per-tile arithmetic is 32-bit: at most 2^30
+    # entries, fewer than 2^31 (query, 128-entry tile) pairs
+    a.n, a.scores_ld, a.k_seq_stride = (1 << 30) + 1, (1 << 30) + 1, 128 * ((1 << 30) + 1)
+    assert L.csa2_index_score(ctypes.byref(a), None) == 2
+    a.B, a.q_per_seq, a.n, a.scores_ld, a.k_seq_stride = 1, 1 << 20, 1 << 18, 1 << 18, 0
+    a.workspace_bytes = L.csa2_index_score_workspace_bytes(ctypes.byref(a))
+    assert L.csa2_index_score(ctypes.byref(a), None) == 2     # 2^20 queries x 2^11 tiles
+    a.B, a.q_per_seq, a.n, a.scores_ld, a.k_seq_stride = 2, 1, 1000, 1000, 128 * 1000
     monkeypatch.setenv("CSA2_FAULT_INJECT", "index_score:4")
     assert L.csa2_index_score(ctypes.byref(a), None) == 4
 
