@@ -139,14 +139,14 @@ struct TcCfg {
   static constexpr int CTAS_PER_SM = QG == 1 ? 2 : 1;
   static constexpr int STAGES = QG == 1 ? 3 : 8;
   // epilogue: STREAMS tiles drained at once, each by SPLIT warpgroups that
-  // share its queries.  A prefill tile holds 4 queries x 64 heads: one
-  // warpgroup per query.  Its threads read the accumulator in 16x256b
+  // share its queries.  A prefill tile holds 4 queries x 64 heads, two
+  // queries per warpgroup.  Its threads read the accumulator in 16x256b
   // shape (4 threads per entry, 16 heads each), so each thread keeps its
-  // 16 head weights in registers: read from shared memory for every
+  // 2 x 16 head weights in registers: read from shared memory for every
   // entry, the weights cost 512 B of load traffic per thread and tile,
   // more than the MMAs' time
-  static constexpr int SPLIT = QG == 1 ? 1 : QG;
-  static constexpr int STREAMS = QG == 1 ? 2 : 1;
+  static constexpr int SPLIT = QG == 1 ? 1 : 2;
+  static constexpr int STREAMS = 2;
   static constexpr bool REG_W = QG > 1;
   static constexpr int EPI_WGS = STREAMS * SPLIT;  // epilogue warpgroups
   static constexpr int QPW = QG / SPLIT;           // queries per epilogue warpgroup
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     int32_t vis[C::QPW];
     uint32_t th[C::QPW];
     float* srow[C::QPW];
-    float wr[C::REG_W ? 16 : 1];  // REG_W: this thread's 16 head weights of its query
+    float wr[C::REG_W ? 16 * C::QPW : 1];  // REG_W: this thread's 16 head weights per query
     // emitting launches: each (warp, query) stream reserves its candidate
     // slots 32 at a time (one atomic per 32 candidates); slots [cpos, cend)
     // of the current chunk are still free, and are filled with the empty
@@ -663,12 +663,15 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         cb ^= 1;
         __syncwarp();
         if constexpr (C::REG_W) {
-          // heads 8 k + 2 (lane % 4) + b of the warpgroup's query
+          // heads 8 k + 2 (lane % 4) + b of the warpgroup's queries
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+          for (int qq = 0; qq < C::QPW; ++qq)
 #pragma unroll
-            for (int b = 0; b < 2; ++b)
-              wr[2 * k + b] = __ldg(p.c + g * C::BN + q0 * 64 + 8 * k + 2 * (lane & 3) + b);
+            for (int k = 0; k < 8; ++k)
+#pragma unroll
+              for (int b = 0; b < 2; ++b)
+                wr[16 * qq + 2 * k + b] =
+                    __ldg(p.c + g * C::BN + (q0 + qq) * 64 + 8 * k + 2 * (lane & 3) + b);
         } else if (p.qbf) {
           for (int i = lane; i < C::BN; i += 32)
             my_c[cb * C::BN + i] = cq[(g == gq0 ? 0 : 1) * C::BN + i];
@@ -693,39 +696,43 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
       const uint32_t taddr = tmem_base + ((uint32_t)(lq * 32) << 16) + (uint32_t)(acc * C::BN);
       float sc[C::QPW];
       if constexpr (C::REG_W) {
-        // part[m]: this thread's 16 heads of entry lq * 32 + lane / 4 + 8 m
-        float part[4];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float v[32];
-          tmem_ld16x256b_x8(taddr + ((uint32_t)(16 * half) << 16) + q0 * 64, v);
-          tmem_ld_wait();
-          if (half == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
-          }
-          float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+        for (int qq = 0; qq < C::QPW; ++qq) {
+          // part[m]: this thread's 16 heads of entry lq * 32 + lane / 4 + 8 m
+          float part[4];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {  // heads 8 k + 2 (lane % 4) + {0, 1} of two entries
-            ffma2(a0, a1, wr[2 * k], wr[2 * k + 1], fmaxf(v[4 * k], 0.f), fmaxf(v[4 * k + 1], 0.f));
-            ffma2(b0, b1, wr[2 * k], wr[2 * k + 1], fmaxf(v[4 * k + 2], 0.f),
-                  fmaxf(v[4 * k + 3], 0.f));
+          for (int half = 0; half < 2; ++half) {
+            float v[32];
+            tmem_ld16x256b_x8(taddr + ((uint32_t)(16 * half) << 16) + (q0 + qq) * 64, v);
+            tmem_ld_wait();
+            if (qq == C::QPW - 1 && half == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            const float* w = wr + 16 * qq;
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {  // heads 8 k + 2 (lane % 4) + {0, 1} of two entries
+              ffma2(a0, a1, w[2 * k], w[2 * k + 1], fmaxf(v[4 * k], 0.f), fmaxf(v[4 * k + 1], 0.f));
+              ffma2(b0, b1, w[2 * k], w[2 * k + 1], fmaxf(v[4 * k + 2], 0.f),
+                    fmaxf(v[4 * k + 3], 0.f));
+            }
+            part[2 * half] = a0 + a1;
+            part[2 * half + 1] = b0 + b1;
           }
-          part[2 * half] = a0 + a1;
-          part[2 * half + 1] = b0 + b1;
+          // sum over the 4 threads of the entry's quad, thread j of the quad
+          // keeping entry m = j: two exchange steps (lane ^ 1, then lane ^ 2)
+          const int jq = lane & 3;
+          const bool odd = jq & 1;
+          float k0 = odd ? part[1] : part[0], k1 = odd ? part[3] : part[2];
+          k0 += __shfl_xor_sync(0xffffffffu, odd ? part[0] : part[1], 1);
+          k1 += __shfl_xor_sync(0xffffffffu, odd ? part[2] : part[3], 1);
+          const bool hi = jq & 2;
+          float kk = hi ? k1 : k0;
+          kk += __shfl_xor_sync(0xffffffffu, hi ? k0 : k1, 2);
+          sc[qq] = kk;
         }
-        // sum over the 4 threads of the entry's quad, thread j of the quad
-        // keeping entry m = j: two exchange steps (lane ^ 1, then lane ^ 2)
-        const int jq = lane & 3;
-        const bool odd = jq & 1;
-        float k0 = odd ? part[1] : part[0], k1 = odd ? part[3] : part[2];
-        k0 += __shfl_xor_sync(0xffffffffu, odd ? part[0] : part[1], 1);
-        k1 += __shfl_xor_sync(0xffffffffu, odd ? part[2] : part[3], 1);
-        const bool hi = jq & 2;
-        float kk = hi ? k1 : k0;
-        kk += __shfl_xor_sync(0xffffffffu, hi ? k0 : k1, 2);
-        sc[0] = kk;
       } else {
 #pragma unroll
       for (int qq = 0; qq < C::QPW; ++qq) {
