@@ -248,6 +248,24 @@ struct TileCursor {
   }
 };
 
+// ReLU on the FMA pipe: an accumulator value x = <q_h, k_j> of E4M3 codes
+// has |x| <= 128 * 448^2 < 2^25, so the saturating product x * 2^-25 is
+// max(x, 0) * 2^-25 exactly (a power-of-two scaling, far from the fp32
+// subnormals: the smallest nonzero |x| is 2^-18).  Each fused product-add
+// (w * 2^25) * that + s rounds the same real value as w max(x, 0) + s, so
+// the head sum is bit-identical to the one taken with a max.  Where
+// w * 2^25 could overflow (a weight of the warp's queries >= 2^100) the
+// kernel sums w * (x * 2^-25) and multiplies the sum by 2^25 instead: the
+// same sum, scaled, wherever its terms and partial sums stay above the fp32
+// subnormals (2^-101 before the scaling).  The epilogue's FMNMX
+// instructions would otherwise keep the ALU pipe the busiest.
+constexpr float kReluScale = 33554432.f;  // 2^25
+__device__ __forceinline__ float relu_scaled(float x) {
+  float y;
+  asm("mul.rn.sat.f32 %0, %1, 0f33000000;" : "=f"(y) : "f"(x));  // x * 2^-25 clamped to [0, 1]
+  return y;
+}
+
 template <int QG>
 __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     idx_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -616,7 +634,10 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     int32_t vis[C::QPW];
     uint32_t th[C::QPW];
     float* srow[C::QPW];
-    float wr[C::REG_W ? 16 * C::QPW : 1];  // REG_W: this thread's 16 head weights per query
+    // REG_W: this thread's 16 head weights per query, times kReluScale
+    // unless the head sums are scaled instead (relu_post = kReluScale)
+    float wr[C::REG_W ? 16 * C::QPW : 1];
+    float relu_post = 1.f;
     // emitting launches: each (warp, query) stream reserves its candidate
     // slots 32 at a time (one atomic per 32 candidates); slots [cpos, cend)
     // of the current chunk are still free, and are filled with the empty
@@ -672,6 +693,16 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
               for (int b = 0; b < 2; ++b)
                 wr[16 * qq + 2 * k + b] =
                     __ldg(p.c + g * C::BN + (q0 + qq) * 64 + 8 * k + 2 * (lane & 3) + b);
+          // the ReLU's 2^-25 is undone on the weights, or, where a weight
+          // of the warp's queries reaches 2^100 (times 2^25 it could
+          // overflow), on the head sums
+          bool big = false;
+#pragma unroll
+          for (int i = 0; i < 16 * C::QPW; ++i) big = big || !(fabsf(wr[i]) < 0x1p100f);
+          big = __any_sync(0xffffffffu, big);
+          relu_post = big ? kReluScale : 1.f;
+#pragma unroll
+          for (int i = 0; i < 16 * C::QPW; ++i) wr[i] *= big ? 1.f : kReluScale;
         } else if (p.qbf) {
           for (int i = lane; i < C::BN; i += 32)
             my_c[cb * C::BN + i] = cq[(g == gq0 ? 0 : 1) * C::BN + i];
@@ -714,9 +745,9 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
             float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {  // heads 8 k + 2 (lane % 4) + {0, 1} of two entries
-              ffma2(a0, a1, w[2 * k], w[2 * k + 1], fmaxf(v[4 * k], 0.f), fmaxf(v[4 * k + 1], 0.f));
-              ffma2(b0, b1, w[2 * k], w[2 * k + 1], fmaxf(v[4 * k + 2], 0.f),
-                    fmaxf(v[4 * k + 3], 0.f));
+              ffma2(a0, a1, w[2 * k], w[2 * k + 1], relu_scaled(v[4 * k]), relu_scaled(v[4 * k + 1]));
+              ffma2(b0, b1, w[2 * k], w[2 * k + 1], relu_scaled(v[4 * k + 2]),
+                    relu_scaled(v[4 * k + 3]));
             }
             part[2 * half] = a0 + a1;
             part[2 * half + 1] = b0 + b1;
@@ -731,7 +762,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
           const bool hi = jq & 2;
           float kk = hi ? k1 : k0;
           kk += __shfl_xor_sync(0xffffffffu, hi ? k0 : k1, 2);
-          sc[qq] = kk;
+          sc[qq] = kk * relu_post;
         }
       } else {
 #pragma unroll

@@ -171,6 +171,34 @@ def test_index_score_fp8_prefill_causal(csa2, orc):
     assert score_close(s.cpu().numpy(), ref) <= 1.0
 
 
+def test_index_score_prefill_relu_scalings_agree(csa2, orc):
+    # the prefill epilogue takes ReLU as a saturating multiply by 2^-25 and
+    # undoes the scale on the head weights, or, where a weight reaches 2^100,
+    # on the head sums; queries 4..7 repeat queries 0..3 with weights scaled
+    # by 2^110, so they take the second form and must give the same scores
+    # times 2^110, bit for bit (both are exact up to power-of-two scalings).
+    # Keys of magnitude <= 1 keep the scaled scores below the fp32 range.
+    n = 1000
+    g = torch.Generator().manual_seed(61)
+
+    def e4m3_bytes(shape, top):
+        b = torch.randint(0, top + 1, shape, generator=g, dtype=torch.int32)
+        return (b | (torch.randint(0, 2, shape, generator=g, dtype=torch.int32) << 7)).to(
+            torch.uint8)
+
+    q8 = e4m3_bytes((4, 64, 128), 0x7E).repeat(2, 1, 1)
+    c = (torch.rand(4, 64, generator=g, dtype=torch.float64) * 2 - 1) / 64
+    c = torch.cat([c, c * 2.0 ** 110]).float()
+    k8 = e4m3_bytes((1, n, 128), 0x38)
+    s = csa2.index_score(dev(q8), dev(c), dev(k8), q_per_seq=8).cpu()
+    assert torch.isfinite(s).all()
+    assert torch.equal((s[:4].double() * 2.0 ** 110).float().view(torch.int32),
+                       s[4:].view(torch.int32))
+    ref = orc.index_score(orc.e4m3_decode(q8.numpy()), c.double().numpy(),
+                          orc.e4m3_decode(k8.numpy()), q_per_seq=8)
+    assert score_close(s.numpy(), ref) <= 1.0
+
+
 def _score_keys(s):
     """Order-preserving uint32 keys of float32 scores (-0 counts as +0)."""
     u = np.ascontiguousarray(s, dtype=np.float32).view(np.uint32).copy()
