@@ -161,8 +161,10 @@ struct TcCfg {
   // shared memory carve-up (offsets from a 1024-byte aligned base)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_Q = OFF_K + STAGES * KTILE;
-  static constexpr int OFF_C = OFF_Q + 2 * QTILE;             // float [EPI_WARPS][2][BN]
-  static constexpr int OFF_CQ = OFF_C + EPI_WARPS * 2 * BN * 4;  // float [2][BN], fused Q
+  // float [EPI_WARPS][2][BN]: each epilogue warp's copy of its group's head
+  // weights (none when they live in registers)
+  static constexpr int OFF_C = OFF_Q + 2 * QTILE;
+  static constexpr int OFF_CQ = OFF_C + (REG_W ? 0 : EPI_WARPS * 2 * BN * 4);  // float [2][BN], fused Q
   // fused first-level top-k histogram (decode): two group slots of 4096 bins
   static constexpr int OFF_H = OFF_CQ + (QG == 1 ? 2 * BN * 4 : 0);
   // decode: the first HSLOTS groups of a CTA's range keep their histograms
