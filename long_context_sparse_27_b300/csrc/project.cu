@@ -206,6 +206,170 @@ __global__ void __launch_bounds__(kPjThreads)
 std::atomic<uint64_t> g_project_attr{0};  // devices on which the kernel's attributes are set
 
 // ---------------------------------------------------------------------------
+// few rows (at most 16, a decode step's new entries): the weight stream is
+// the whole cost, so every CTA issues all of its loads at once
+// ---------------------------------------------------------------------------
+//
+// A CTA owns (16 rows, one 32-column FP4 block, 1/8 of the hidden features);
+// the 8 CTAs of a cluster split the hidden dimension, so d / 32 x 8 CTAs
+// (128 for d = 512) stream the weights.  The CTA's h and w slices arrive in
+// one round of cp.async copies; its 4 warps take a quarter of the features
+// each (m16n8k16 bf16 MMAs, fp32 accumulators), their partials are summed in
+// shared memory, and after a cluster barrier CTA r sums rows 2r, 2r + 1 of
+// the 8 CTA partials in rank order over distributed shared memory (a fixed
+// order) and quantises them like the other projection kernels.
+
+constexpr int kPsRows = 16;
+constexpr int kPsCols = 32;         // one FP4 block
+constexpr int kPsThreads = 128;     // 4 warps
+constexpr int kPsSplit = 8;         // CTAs of a cluster
+constexpr int kPsWorkers = kPsSplit * kPsThreads / 32;  // warps over the hidden dimension
+constexpr int kPsPartLd = kPsCols + 4;
+constexpr int kPsMaxFeatures = 2048;  // per CTA: the slices fit in shared memory
+constexpr int kPsMaxHidden = kPsSplit * kPsMaxFeatures;
+
+// features of the CTA share / of one warp (multiples of 16)
+__host__ __device__ constexpr int ps_warp_steps(int hidden) {
+  return (hidden / 16 + kPsWorkers - 1) / kPsWorkers;
+}
+__host__ __device__ constexpr int ps_stride(int hidden) {  // padded smem row (bf16)
+  return 4 * 16 * ps_warp_steps(hidden) + 8;
+}
+__host__ __device__ constexpr int ps_smem(int hidden) {
+  return (kPsRows + kPsCols) * ps_stride(hidden) * 2 +
+         (kPsThreads / 32 + 1) * kPsRows * kPsPartLd * 4;
+}
+
+__global__ void __launch_bounds__(kPsThreads)
+    project_few_kernel(const uint16_t* __restrict__ h, int64_t h_ld,
+                       const uint16_t* __restrict__ w, int64_t w_ld, int32_t rows,
+                       int32_t hidden, uint8_t* __restrict__ codes, int64_t codes_ld,
+                       uint8_t* __restrict__ scales, int64_t scales_ld, float* __restrict__ out,
+                       int64_t out_ld) {
+  extern __shared__ __align__(16) uint16_t ps_smem_raw[];
+  const int stride = ps_stride(hidden);
+  uint16_t* sh = ps_smem_raw;                    // [16][stride]
+  uint16_t* sw = ps_smem_raw + kPsRows * stride;  // [32][stride]
+  // [4 warps + the CTA sum][16][kPsPartLd]
+  float* part = reinterpret_cast<float*>(ps_smem_raw + (kPsRows + kPsCols) * stride);
+  float* cpart = part + (kPsThreads / 32) * kPsRows * kPsPartLd;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = (int)(blockIdx.x % kPsSplit);
+  const int64_t c0 = (int64_t)blockIdx.y * kPsCols;
+  const int wsteps = ps_warp_steps(hidden);
+  const int ksteps = hidden / 16;
+  // the CTA's features [f0, f1): warps rank * 4 .. rank * 4 + 3 of the split
+  const int s0 = min(ksteps, rank * 4 * wsteps), s1 = min(ksteps, (rank + 1) * 4 * wsteps);
+  const int f0 = 16 * s0, nf = 16 * (s1 - s0);
+  pdl_wait();
+
+  // every copy of the CTA in flight at once: 8-element pieces of the 16 h
+  // rows (zeros past the last row) and of the 32 w rows
+  const int pieces = nf / 8;
+  for (int i = tid; i < (kPsRows + kPsCols) * pieces; i += kPsThreads) {
+    const int r = i / pieces, p = i % pieces;
+    if (r < kPsRows) {
+      uint16_t* d = sh + r * stride + p * 8;
+      if (r < rows)
+        cp_async16(d, h + (int64_t)r * h_ld + f0 + p * 8);
+      else
+        *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+    } else {
+      cp_async16(sw + (r - kPsRows) * stride + p * 8, w + (c0 + r - kPsRows) * w_ld + f0 + p * 8);
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // warp: k-steps [ws0, ws1) of the CTA's share
+  float acc[kPsCols / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < kPsCols / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  const int ws0 = min(s1 - s0, warp * wsteps), ws1 = min(s1 - s0, (warp + 1) * wsteps);
+  for (int kk = ws0; kk < ws1; ++kk) {
+    uint32_t a0, a1, a2, a3;
+    ldmatrix_x4(smem_u32(sh + (lane & 15) * stride + kk * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+#pragma unroll
+    for (int np = 0; np < kPsCols / 16; ++np) {
+      const int n = 16 * np + (lane & 7) + ((lane >> 4) << 3);
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4(smem_u32(sw + n * stride + kk * 16 + ((lane >> 3) & 1) * 8), b0, b1, b2, b3);
+      mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+      mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+    }
+  }
+  pdl_trigger();
+  {  // thread (g = lane / 4, t = lane % 4): rows g, g + 8, columns 8 nt + 2 t, + 1
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float* prow = part + (warp * kPsRows + g + 8 * half) * kPsPartLd + 2 * t;
+#pragma unroll
+      for (int nt = 0; nt < kPsCols / 8; ++nt)
+        *reinterpret_cast<float2*>(prow + 8 * nt) =
+            make_float2(acc[nt][2 * half], acc[nt][2 * half + 1]);
+    }
+  }
+  __syncthreads();
+  // the CTA's partial: the 4 warps' in warp order
+  for (int i = tid; i < kPsRows * kPsCols; i += kPsThreads) {
+    const int r = i / kPsCols, c = i % kPsCols;
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < kPsThreads / 32; ++q) v += part[(q * kPsRows + r) * kPsPartLd + c];
+    cpart[r * kPsPartLd + c] = v;
+  }
+  cluster_arrive_release();
+  cluster_wait_acquire();
+
+  // rows 2 rank, 2 rank + 1: thread tid < 16 takes row 2 rank + tid / 8,
+  // columns 4 (tid % 8) .. + 3 (the 8 lanes of a row hold its block)
+  if (tid < 2 * 8) {
+    const int lr = 2 * rank + tid / 8, col = 4 * (tid % 8);
+    if (lr < rows) {
+      const uint32_t local = smem_u32(cpart + lr * kPsPartLd + col);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kPsSplit; ++q) {
+        const float4 x = ld_cluster_f4(cluster_addr(local, (uint32_t)q));
+        v.x += x.x;
+        v.y += x.y;
+        v.z += x.z;
+        v.w += x.w;
+      }
+      float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+      const uint32_t grp = 0xFFu << (lane & 8);  // the 8 lanes of the row (both rows or none)
+      amax = fmaxf(amax, __shfl_xor_sync(grp, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(grp, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(grp, amax, 4));
+      uint32_t sbyte = 0, b0 = 0, b1 = 0;
+      if (amax > 0.f) {
+        int e = floor_log2_pos(amax) - 2;
+        e = max(-127, min(127, e));
+        sbyte = (uint32_t)(e + 127);
+        const float inv = exp2_int(-e);
+        b0 = e2m1_encode(v.x * inv) | (e2m1_encode(v.y * inv) << 4);
+        b1 = e2m1_encode(v.z * inv) | (e2m1_encode(v.w * inv) << 4);
+      }
+      uint8_t* crow = codes + (int64_t)lr * codes_ld + (c0 + col) / 2;
+      crow[0] = (uint8_t)b0;
+      crow[1] = (uint8_t)b1;
+      if ((tid & 7) == 0) scales[(int64_t)lr * scales_ld + c0 / 32] = (uint8_t)sbyte;
+      if (out) {
+        float* orow = out + (int64_t)lr * out_ld + c0 + col;
+        *reinterpret_cast<float2*>(orow) = make_float2(v.x, v.y);
+        *reinterpret_cast<float2*>(orow + 2) = make_float2(v.z, v.w);
+      }
+    }
+  }
+  // no CTA leaves while another may still read its partial
+  cluster_arrive_release();
+  cluster_wait_acquire();
+}
+
+std::atomic<uint64_t> g_project_few_attr{0};
+
+// ---------------------------------------------------------------------------
 // tensor-core path (from 64 rows): tcgen05 bf16 MMAs, accumulators in TMEM
 // ---------------------------------------------------------------------------
 //
@@ -450,6 +614,18 @@ csa2_status launch_project_fp4(const csa2_project_args& a, cudaStream_t s) {
     return launch_kernel(project_tc_kernel, grid, dim3(kTcThreads), (size_t)kTcSmemAlloc, s,
                          kTcSplit, hmap, wmap, a.rows, a.hidden, a.codes, a.codes_ld, a.scales,
                          a.scales_ld, a.out, a.out_ld, a.dev_status, wait_limit_ns());
+  }
+  if (a.rows <= kPsRows && a.hidden <= kPsMaxHidden) {
+    cudaError_t e = once_per_device(g_project_few_attr, [] {
+      return cudaFuncSetAttribute(project_few_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  ps_smem(kPsMaxHidden));
+    });
+    if (e != cudaSuccess) return cuda_fail(e);
+    const dim3 grid((unsigned)kPsSplit, (unsigned)(a.d / kPsCols));
+    return launch_kernel(project_few_kernel, grid, dim3(kPsThreads), (size_t)ps_smem(a.hidden), s,
+                         kPsSplit, static_cast<const uint16_t*>(a.h), a.h_ld,
+                         static_cast<const uint16_t*>(a.w), a.w_ld, (int32_t)a.rows, a.hidden,
+                         a.codes, a.codes_ld, a.scales, a.scales_ld, a.out, a.out_ld);
   }
   cudaError_t e = once_per_device(g_project_attr, [] {
     return cudaFuncSetAttribute(project_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

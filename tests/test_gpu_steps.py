@@ -309,7 +309,12 @@ def test_index_score_pool_exact_small_integers(csa2, orc):
 
 @pytest.mark.parametrize("rows,hidden,d", [(8, 4096, 512), (100, 256, 128), (1, 64, 64),
                                            (1024, 512, 512), (5, 416, 64), (65, 4096, 64),
-                                           (300, 1024, 512), (64, 768, 192)])
+                                           (300, 1024, 512), (64, 768, 192),
+                                           # at most 16 rows: one round of loads per CTA,
+                                           # uneven and empty shares of the hidden features,
+                                           # the largest hidden size of that path and past it
+                                           (16, 4096, 512), (3, 96, 128), (16, 16384, 64),
+                                           (12, 16416, 64), (17, 512, 64)])
 def test_project_fp4(csa2, orc, rows, hidden, d):
     h = synth.normal((rows, hidden), 210 + rows)
     w = synth.normal((d, hidden), 211 + rows) * 0.05
@@ -328,11 +333,12 @@ def test_project_fp4(csa2, orc, rows, hidden, d):
     assert int(scales[0].abs().sum()) == 0 and int(codes[0].sum()) == 0
 
 
-def test_project_fp4_exact_small_integers(csa2, orc):
+@pytest.mark.parametrize("rows", [70, 9])
+def test_project_fp4_exact_small_integers(csa2, orc, rows):
     # integer inputs keep every product and partial sum exact in fp32: the
     # projection and its codes match the oracle's fp64 path bit for bit
     g = torch.Generator().manual_seed(212)
-    h = torch.randint(-3, 4, (70, 256), generator=g).to(torch.bfloat16)
+    h = torch.randint(-3, 4, (rows, 256), generator=g).to(torch.bfloat16)
     w = torch.randint(-2, 3, (128, 256), generator=g).to(torch.bfloat16)
     codes, scales, out = csa2.project_fp4(dev(h), dev(w), with_out=True)
     assert np.array_equal(out.cpu().double().numpy(), orc.project_kv(f64(h), f64(w)))
