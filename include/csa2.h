@@ -480,9 +480,10 @@ csa2_status csa2_sparse_attn(const csa2_attn_args* args, csa2_stream_t stream);
  * out    optional device f32 [rows, d], out_ld
  * dev_status optional device int32 (see CSA2_DEVFLAG_*)
  * hidden a multiple of 32; d a multiple of 64.  From 64 rows on, when hidden
- * is a multiple of 256, the product runs on tcgen05 tensor cores; both
- * paths sum each output in fp32 in a fixed order (the result does not
- * depend on the launch).
+ * is a multiple of 256, the product runs on tcgen05 tensor cores; up to 16
+ * rows (hidden <= 16384) every CTA loads its whole share at once; other
+ * sizes stream through a ring.  Every path sums each output in fp32 in a
+ * fixed order (the result does not depend on the launch).
  * Errors: INVALID_ARG, ALIGNMENT (h, w 16-byte aligned with h_ld, w_ld
  *         multiples of 8; out 8-byte aligned with out_ld even), CUDA.
  */
