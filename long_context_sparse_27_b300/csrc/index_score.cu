@@ -768,35 +768,35 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         }
       } else {
 #pragma unroll
-      for (int qq = 0; qq < C::QPW; ++qq) {
-        float s8[8];
+        for (int qq = 0; qq < C::QPW; ++qq) {
+          float s8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s8[i] = 0.f;
-        // two halves of 32 heads: 32 accumulator values live at a time
+          for (int i = 0; i < 8; ++i) s8[i] = 0.f;
+          // two halves of 32 heads: 32 accumulator values live at a time
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float v[32];
-          tmem_ld32(taddr + (q0 + qq) * 64 + half * 32, v);
-          tmem_ld_wait();
-          if (qq == C::QPW - 1 && half == 1) {
-            // the accumulator is in registers: hand it back to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+          for (int half = 0; half < 2; ++half) {
+            float v[32];
+            tmem_ld32(taddr + (q0 + qq) * 64 + half * 32, v);
+            tmem_ld_wait();
+            if (qq == C::QPW - 1 && half == 1) {
+              // the accumulator is in registers: hand it back to the MMA warp
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            const float4* cw =
+                reinterpret_cast<const float4*>(my_c + cb * C::BN + (q0 + qq) * 64 + half * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = cw[i];
+              s8[(4 * i) & 7] = fmaf(f.x, fmaxf(v[4 * i], 0.f), s8[(4 * i) & 7]);
+              s8[(4 * i + 1) & 7] = fmaf(f.y, fmaxf(v[4 * i + 1], 0.f), s8[(4 * i + 1) & 7]);
+              s8[(4 * i + 2) & 7] = fmaf(f.z, fmaxf(v[4 * i + 2], 0.f), s8[(4 * i + 2) & 7]);
+              s8[(4 * i + 3) & 7] = fmaf(f.w, fmaxf(v[4 * i + 3], 0.f), s8[(4 * i + 3) & 7]);
+            }
           }
-          const float4* cw =
-              reinterpret_cast<const float4*>(my_c + cb * C::BN + (q0 + qq) * 64 + half * 32);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 f = cw[i];
-            s8[(4 * i) & 7] = fmaf(f.x, fmaxf(v[4 * i], 0.f), s8[(4 * i) & 7]);
-            s8[(4 * i + 1) & 7] = fmaf(f.y, fmaxf(v[4 * i + 1], 0.f), s8[(4 * i + 1) & 7]);
-            s8[(4 * i + 2) & 7] = fmaf(f.z, fmaxf(v[4 * i + 2], 0.f), s8[(4 * i + 2) & 7]);
-            s8[(4 * i + 3) & 7] = fmaf(f.w, fmaxf(v[4 * i + 3], 0.f), s8[(4 * i + 3) & 7]);
-          }
+          sc[qq] = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
         }
-        sc[qq] = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-      }
       }
       const int32_t jc = kt * C::BM + row;  // score column (compact when sampled)
       const int32_t j = kt * kstep + row;   // the entry
