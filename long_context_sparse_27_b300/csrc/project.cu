@@ -373,11 +373,12 @@ std::atomic<uint64_t> g_project_few_attr{0};
 // tensor-core path (from 64 rows): tcgen05 bf16 MMAs, accumulators in TMEM
 // ---------------------------------------------------------------------------
 //
-// A CTA owns (128 rows, 64 output columns, 1/4 of the hidden features); the
-// 4 CTAs of a cluster split the hidden dimension.  Warp 0 streams 128 x 64
-// tiles of h and 64 x 64 tiles of w by TMA (128-byte swizzle) through a
-// 4-stage mbarrier ring, warp 1 issues tcgen05.mma.kind::f16 (M = 128, N =
-// 64, K = 16; four per stage) into one TMEM accumulator, and warps 2 .. 5
+// A CTA owns (128 rows, N = 128 output columns (64 where d is not a multiple
+// of 128), 1/4 of the hidden features); the 4 CTAs of a cluster split the
+// hidden dimension.  Warp 0 streams 128 x 64 tiles of h and N x 64 tiles of
+// w by TMA (128-byte swizzle) through a 4-stage mbarrier ring, warp 1 issues
+// tcgen05.mma.kind::f16 (M = 128, N, K = 16; four per stage) into one TMEM
+// accumulator, and warps 2 .. 5
 // (one TMEM lane quarter each) move the accumulator to a shared-memory
 // partial tile.  After one cluster barrier CTA r sums rows 32 r .. 32 r + 31
 // of the 4 partials in rank order over distributed shared memory and
@@ -385,42 +386,50 @@ std::atomic<uint64_t> g_project_few_attr{0};
 // bounded; a wait that gives up sets CSA2_DEVFLAG_TIMEOUT and the CTA's
 // abort flag, and the CTA still takes part in both cluster barriers.
 constexpr int kTcM = 128;                  // rows per CTA (MMA M, TMEM lanes)
-constexpr int kTcN = 64;                   // output columns per CTA (MMA N)
 constexpr int kTcK = 64;                   // features per stage: 128-byte rows
 constexpr int kTcStages = 4;
 constexpr int kTcSplit = 4;                // CTAs of a cluster: shares of the hidden dimension
 constexpr int kTcThreads = 192;            // producer, MMA issuer, 4 epilogue warps
 constexpr int kTcATile = kTcM * kTcK * 2;  // 16 KB
-constexpr int kTcBTile = kTcN * kTcK * 2;  // 8 KB
-constexpr int kTcPartLd = kTcN + 4;        // padded fp32 row of the partial tile
-constexpr int kTcOffB = kTcStages * kTcATile;
-constexpr int kTcOffBar = kTcOffB + kTcStages * kTcBTile;
-constexpr int kTcSmem = kTcOffBar + 256;   // barriers, TMEM slot, abort flag
-constexpr int kTcSmemAlloc = kTcSmem + 1024;  // 1024-byte alignment of the tiles
-static_assert(kTcM * kTcPartLd * 4 <= kTcOffBar, "the partial tile reuses the rings");
-static_assert((kTcM / kTcSplit) * (kTcN / 32) <= kTcThreads, "one thread per (row, block)");
-static_assert(2 * (kTcSmemAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
 
-__global__ void __launch_bounds__(kTcThreads, 2)
+// N output columns per CTA (MMA N): 128 where d allows (each h tile then
+// serves twice the columns), else 64 (two CTAs per SM)
+template <int N>
+struct TcPj {
+  static constexpr int BTile = N * kTcK * 2;           // 8 or 16 KB
+  static constexpr int PartLd = N + 4;                 // padded fp32 row of the partial tile
+  static constexpr int OffB = kTcStages * kTcATile;
+  static constexpr int OffBar = OffB + kTcStages * BTile;
+  static constexpr int Smem = OffBar + 256;            // barriers, TMEM slot, abort flag
+  static constexpr int SmemAlloc = Smem + 1024;        // 1024-byte alignment of the tiles
+  static constexpr int CtasPerSm = N == 64 ? 2 : 1;
+  static_assert(kTcM * PartLd * 4 <= OffBar, "the partial tile reuses the rings");
+  static_assert((kTcM / kTcSplit) * (N / 32) <= kTcThreads, "one thread per (row, block)");
+  static_assert(CtasPerSm * (SmemAlloc + 1024) <= 228 * 1024, "CTAs per SM");
+};
+
+template <int N>
+__global__ void __launch_bounds__(kTcThreads, TcPj<N>::CtasPerSm)
     project_tc_kernel(const __grid_constant__ CUtensorMap hmap,
                       const __grid_constant__ CUtensorMap wmap, int64_t rows, int32_t hidden,
                       uint8_t* __restrict__ codes, int64_t codes_ld,
                       uint8_t* __restrict__ scales, int64_t scales_ld, float* __restrict__ out,
                       int64_t out_ld, int32_t* dev_status, uint64_t wait_ns) {
+  using C = TcPj<N>;
   extern __shared__ uint8_t tc_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcOffBar);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OffBar);
   uint64_t* empty = full + kTcStages;
   uint64_t* accb = empty + kTcStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* part = reinterpret_cast<float*>(smem);  // [kTcM][kTcPartLd], after the main loop
+  float* part = reinterpret_cast<float*>(smem);  // [kTcM][C::PartLd], after the main loop
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = (int)(blockIdx.x % kTcSplit);
   const int64_t r0 = (int64_t)(blockIdx.x / kTcSplit) * kTcM;
-  const int c0 = (int)blockIdx.y * kTcN;
+  const int c0 = (int)blockIdx.y * N;
   const int nkb_all = hidden / kTcK;
   const int per = (nkb_all + kTcSplit - 1) / kTcSplit;
   const int kb0 = min(nkb_all, rank * per);
@@ -437,7 +446,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     tma_prefetch_desc(&hmap);
     tma_prefetch_desc(&wmap);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTcN);
+  if (warp == 1) tmem_alloc(tmem_slot, N);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -454,10 +463,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (!mbar_wait(&empty[s], (uint32_t)(((i / kTcStages) & 1) ^ 1), abort_flag, dev_status,
                        wait_ns))
           break;
-        mbar_arrive_expect_tx(&full[s], kTcATile + kTcBTile);
+        mbar_arrive_expect_tx(&full[s], kTcATile + C::BTile);
         const int32_t x = (kb0 + i) * kTcK;
         tma_load_2d(&hmap, &full[s], smem + s * kTcATile, x, (int32_t)r0, pol);
-        tma_load_2d(&wmap, &full[s], smem + kTcOffB + s * kTcBTile, x, c0, pol);
+        tma_load_2d(&wmap, &full[s], smem + C::OffB + s * C::BTile, x, c0, pol);
         ++issued;
       }
       // on an abort, let the copies in flight land before shared memory is reused
@@ -469,14 +478,14 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && nkb > 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kTcM, kTcN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kTcM, N);
       for (int i = 0; i < nkb; ++i) {
         const int s = i % kTcStages;
         if (!mbar_wait(&full[s], (uint32_t)((i / kTcStages) & 1), abort_flag, dev_status, wait_ns))
           break;
         tc_fence_after();
         const uint64_t a = sdesc_k_sw128(smem_u32(smem + s * kTcATile));
-        const uint64_t b = sdesc_k_sw128(smem_u32(smem + kTcOffB + s * kTcBTile));
+        const uint64_t b = sdesc_k_sw128(smem_u32(smem + C::OffB + s * C::BTile));
 #pragma unroll
         for (int kk = 0; kk < kTcK / 16; ++kk)  // K = 16 bf16 = 32 bytes = 2 descriptor units
           tc_mma_bf16(tmem_base, a + 2 * kk, b + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
@@ -488,29 +497,27 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // ---------------- accumulator -> shared-memory partial ----------------
     const int quarter = warp & 3;  // TMEM lanes 32 quarter .. (warp % 4 rule)
     const int row = 32 * quarter + lane;
-    float v[kTcN];
-    if (nkb > 0) {
-      const bool got = mbar_wait(accb, 0, abort_flag, dev_status, wait_ns);
-      if (__all_sync(0xffffffffu, got)) {
-        tc_fence_after();
-        tmem_ld32(tmem_base + ((uint32_t)(32 * quarter) << 16), v);
-        tmem_ld32(tmem_base + ((uint32_t)(32 * quarter) << 16) + 32, v + 32);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int i = 0; i < kTcN; ++i) v[i] = 0.f;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kTcN; ++i) v[i] = 0.f;
-    }
+    bool got = false;
+    if (nkb > 0) got = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, dev_status, wait_ns));
+    if (got) tc_fence_after();
     // the rings are free once the accumulator is complete (every stage's
     // loads landed and its MMAs read it)
     asm volatile("bar.sync 1, %0;" ::"n"(4 * 32) : "memory");
-    float* prow = part + row * kTcPartLd;
+    float* prow = part + row * C::PartLd;
+#pragma unroll 1
+    for (int c = 0; c < N; c += 32) {  // 32 columns at a time
+      float v[32];
+      if (got) {
+        tmem_ld32(tmem_base + ((uint32_t)(32 * quarter) << 16) + c, v);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-    for (int i = 0; i < kTcN; i += 4)
-      *reinterpret_cast<float4*>(prow + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(prow + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
   }
   // the producer's copies have landed (or were never issued) before the
   // partial tile overwrites the rings: the epilogue wrote only after the
@@ -522,15 +529,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   cluster_wait_acquire();
 
   // ---- rows 32 rank .. 32 rank + 31: one thread per (row, 32-column block)
-  if (tid < (kTcM / kTcSplit) * (kTcN / 32)) {
-    const int lr = (kTcM / kTcSplit) * rank + tid / (kTcN / 32);
-    const int blk = tid % (kTcN / 32);
+  if (tid < (kTcM / kTcSplit) * (N / 32)) {
+    const int lr = (kTcM / kTcSplit) * rank + tid / (N / 32);
+    const int blk = tid % (N / 32);
     const int64_t grow = r0 + lr;
     if (grow < rows) {
       float x[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) x[i] = 0.f;
-      const uint32_t local = smem_u32(part + lr * kTcPartLd + 32 * blk);
+      const uint32_t local = smem_u32(part + lr * C::PartLd + 32 * blk);
 #pragma unroll
       for (int q = 0; q < kTcSplit; ++q) {
         const uint32_t ra = cluster_addr(local, (uint32_t)q);
@@ -566,12 +573,51 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   cluster_wait_acquire();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTcN);
+    tmem_dealloc(tmem_base, N);
   }
 }
 
-std::atomic<uint64_t> g_project_tc_attr{0};
+std::atomic<uint64_t> g_project_tc_attr[2] = {{0}, {0}};  // N = 64, 128
 
+
+template <int N>
+csa2_status launch_project_tc(const csa2_project_args& a, cudaStream_t s) {
+  using C = TcPj<N>;
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return cuda_fail(cudaErrorNotSupported);
+  CUtensorMap hmap, wmap;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)a.hidden, (cuuint64_t)a.rows};
+    cuuint64_t strides[1] = {(cuuint64_t)a.h_ld * 2};
+    cuuint32_t box[2] = {kTcK, kTcM};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&hmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.h), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return CSA2_ERR_INVALID_ARG;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)a.hidden, (cuuint64_t)a.d};
+    cuuint64_t strides[1] = {(cuuint64_t)a.w_ld * 2};
+    cuuint32_t box[2] = {kTcK, N};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.w), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return CSA2_ERR_INVALID_ARG;
+  }
+  cudaError_t e = once_per_device(g_project_tc_attr[N == 128 ? 1 : 0], [] {
+    return cudaFuncSetAttribute(project_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SmemAlloc);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int64_t row_tiles = (a.rows + kTcM - 1) / kTcM;
+  if (row_tiles * kTcSplit > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)(row_tiles * kTcSplit), (unsigned)(a.d / N));
+  return launch_kernel(project_tc_kernel<N>, grid, dim3(kTcThreads), (size_t)C::SmemAlloc, s,
+                       kTcSplit, hmap, wmap, a.rows, a.hidden, a.codes, a.codes_ld, a.scales,
+                       a.scales_ld, a.out, a.out_ld, a.dev_status, wait_limit_ns());
+}
 
 }  // namespace
 
@@ -579,42 +625,7 @@ csa2_status launch_project_fp4(const csa2_project_args& a, cudaStream_t s) {
   if (a.rows == 0) return CSA2_OK;
   const bool tc = a.rows >= 64 && a.hidden % (kTcK * kTcSplit) == 0 &&
                   (reinterpret_cast<uintptr_t>(a.codes) & 15) == 0 && a.codes_ld % 16 == 0;
-  if (tc) {
-    EncodeTiledFn enc = tensor_map_encoder();
-    if (!enc) return cuda_fail(cudaErrorNotSupported);
-    CUtensorMap hmap, wmap;
-    {
-      cuuint64_t dims[2] = {(cuuint64_t)a.hidden, (cuuint64_t)a.rows};
-      cuuint64_t strides[1] = {(cuuint64_t)a.h_ld * 2};
-      cuuint32_t box[2] = {kTcK, kTcM};
-      cuuint32_t es[2] = {1, 1};
-      if (enc(&hmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.h), dims, strides,
-              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return CSA2_ERR_INVALID_ARG;
-    }
-    {
-      cuuint64_t dims[2] = {(cuuint64_t)a.hidden, (cuuint64_t)a.d};
-      cuuint64_t strides[1] = {(cuuint64_t)a.w_ld * 2};
-      cuuint32_t box[2] = {kTcK, kTcN};
-      cuuint32_t es[2] = {1, 1};
-      if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.w), dims, strides,
-              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return CSA2_ERR_INVALID_ARG;
-    }
-    cudaError_t e = once_per_device(g_project_tc_attr, [] {
-      return cudaFuncSetAttribute(project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kTcSmemAlloc);
-    });
-    if (e != cudaSuccess) return cuda_fail(e);
-    const int64_t row_tiles = (a.rows + kTcM - 1) / kTcM;
-    if (row_tiles * kTcSplit > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED;
-    const dim3 grid((unsigned)(row_tiles * kTcSplit), (unsigned)(a.d / kTcN));
-    return launch_kernel(project_tc_kernel, grid, dim3(kTcThreads), (size_t)kTcSmemAlloc, s,
-                         kTcSplit, hmap, wmap, a.rows, a.hidden, a.codes, a.codes_ld, a.scales,
-                         a.scales_ld, a.out, a.out_ld, a.dev_status, wait_limit_ns());
-  }
+  if (tc) return a.d % 128 == 0 ? launch_project_tc<128>(a, s) : launch_project_tc<64>(a, s);
   if (a.rows <= kPsRows && a.hidden <= kPsMaxHidden) {
     cudaError_t e = once_per_device(g_project_few_attr, [] {
       return cudaFuncSetAttribute(project_few_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
