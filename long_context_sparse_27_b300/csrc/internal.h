@@ -178,9 +178,10 @@ csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int
                                const int32_t* remap = nullptr, int64_t remap_ld = 0,
                                bool clear_hist = true);
 // a5
-// q_ready: the attention queries may be read before the kernel's
-// programmatic-launch wait (no kernel still running on the stream writes
-// them); set by the layer stack, whose preceding kernels never do.
+// q_ready: the attention queries, the window rows and the window ranges may
+// be read before the kernel's programmatic-launch wait (no kernel still
+// running on the stream writes them); set by the layer stack, whose
+// preceding kernels never do.
 size_t attn_workspace_bytes(const csa2_attn_args& a);
 csa2_status launch_sparse_attn(const csa2_attn_args& a, cudaStream_t s, bool q_ready = false);
 

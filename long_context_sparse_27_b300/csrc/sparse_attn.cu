@@ -267,8 +267,10 @@ __device__ __noinline__ void dequant_block(uint4 cw, uint32_t sb, uint8_t* d0, u
 //     thread-block cluster; after one cluster barrier each CTA merges
 //     1/nchunks of the output from every chunk's partial.  Otherwise
 //     attn_combine_kernel merges.
-// pre: Q may be read before the programmatic-launch wait (the caller knows
-// the kernels still running on the stream do not write it).
+// pre: Q, the window rows and the window ranges may be read before the
+// programmatic-launch wait (the caller knows the kernels still running on the
+// stream do not write them): Q and the first chunk's window rows are copied
+// into shared memory while the previous kernel drains.
 // MODE: kModeCombine (chunk partials, merged by attn_combine_kernel),
 // kModeCluster (the chunks of a query and head group are a cluster and merge
 // their partials through L2) or kModeSeq (one CTA per query and head group
@@ -308,13 +310,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         *reinterpret_cast<uint4*>(sQ + r * kRowBytes + c * 16) = make_uint4(0, 0, 0, 0);
     }
   };
-  if (pre) load_q();
-  pdl_wait();
-  if (!pre) load_q();
-
-  int32_t ws, wl;
-  window_of(a, qi, ws, wl);
-  const int64_t nkeys = a.k + wl;
+  int32_t ws = 0, wl = 0;
+  int64_t nkeys = 0;
+  if (pre) {
+    load_q();
+    window_of(a, qi, ws, wl);
+    nkeys = a.k + wl;
+  }
 
   // the key list index of row r of chunk c (-1: no key)
   auto key_of = [&](int c, int r) -> int64_t {
@@ -329,6 +331,34 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const int64_t t = (int64_t)c * kKC + r;
     return t < nkeys ? t : -1;
   };
+  // the first chunk's window rows (inputs no earlier kernel writes, like Q)
+  // are copied before the programmatic-launch wait
+  const int c_first = MODE == kModeSeq ? 0 : (int)blockIdx.x;
+  if (pre) {
+    const int c = tid % kBlocks;
+    const int rot = (tid >> 1) & 3;
+#pragma unroll
+    for (int u = 0; u < kBItems; ++u) {
+      const int r = tid / kBlocks + u * (kAttnThreads / kBlocks);
+      const int64_t t = key_of(c_first, r);
+      if (t >= a.k) {
+        const KeySrc src = key_source(a, qi, t, ws, wl);
+        if (src.win) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int vv = (v + rot) & 3;
+            cp_async16(sK + r * kRowBytes + c * 64 + vv * 16, src.win + c * 32 + vv * 8);
+          }
+        }
+      }
+    }
+  }
+  pdl_wait();
+  if (!pre) {
+    load_q();
+    window_of(a, qi, ws, wl);
+    nkeys = a.k + wl;
+  }
   const int d0 = warp * kPVSlice;
   const int r0 = lane >> 2;  // rows (heads) r0 and r0 + 8 of this thread's MMA fragments
   float o[8][4];
@@ -375,7 +405,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const uint8_t* cp = rows.codes[r];
       cw[u] = cp ? __ldg(reinterpret_cast<const uint4*>(cp) + c) : make_uint4(0, 0, 0, 0);
       sb[u] = cp ? (uint32_t)__ldg(rows.scales[r] + c) : 0u;
-      if (const uint16_t* wrow = rows.win[r]) {
+      if (const uint16_t* wrow = rows.win[r]; wrow && !(pre && chunk == c_first)) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int vv = (v + rot) & 3;
