@@ -464,12 +464,12 @@ struct ScanLayout {
   __host__ __device__ static size_t align256_hd(size_t x) { return (x + 255) & ~(size_t)255; }
 };
 
-// Slices per row: about kSliceTarget CTAs per launch, each slice at least a
-// batch, at most kMaxSlices.  0 for short rows.
+// Slices per row: about kSliceTarget CTAs per launch (every CTA resident),
+// each slice at least 4096 scores, at most kMaxSlices.  0 for short rows.
 int scan_slices(int64_t rows, int64_t n) {
   if (n <= kSmallN || rows <= 0) return 0;
   const int64_t want = (kSliceTarget + rows - 1) / rows;
-  const int64_t most = std::min<int64_t>(kMaxSlices, (n + kBatch - 1) / kBatch);
+  const int64_t most = std::min<int64_t>(kMaxSlices, (n + 4095) / 4096);
   return (int)std::max<int64_t>(1, std::min(want, most));
 }
 
@@ -1048,9 +1048,11 @@ csa2_status launch_topk_select(const float* scores, int64_t rows, int64_t n, int
   });
   if (e != cudaSuccess) return cuda_fail(e);
   const int vec = (ld % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) % 16) == 0) ? 1 : 0;
-  // slices are whole rounds long, so every float4 of a slice is aligned
+  // slices are multiples of 4 scores long, so every float4 of a slice is
+  // aligned (a slice's last batch is partly past its end: those loads are
+  // bounded by the slice)
   const int64_t per = (n + L.S - 1) / L.S;
-  const int64_t slice = (per + kRound - 1) / kRound * kRound;
+  const int64_t slice = (per + 3) / 4 * 4;
   uint8_t* base = reinterpret_cast<uint8_t*>(hist1);
   return launch_kernel(topk_scan_kernel, dim3((unsigned)(rows * L.S)), dim3(kTkThreads),
                        (size_t)kScanSmem, s, 1, scores, n, ld, n_valid, k, hist1,
