@@ -342,7 +342,7 @@ csa2_status csa2_index_block_keys(const uint8_t* k8, int64_t B, int64_t n, int64
  * histogram per row of 4096 fine and 64 coarse bins (rows * 16,640 bytes)
  * and, for rows longer than 4096,
  * a counter per row and S candidate slots of 8 KiB per row (S = about 296 /
- * rows, at most 64, at most one per 8192 entries); the call clears what must
+ * rows, at most 64, at most one per 4096 entries); the call clears what must
  * start at zero.
  * Kernels: rows of at most 4096 entries run one CTA per row with every key
  * in shared memory; longer rows a histogram pass over the scores, then one

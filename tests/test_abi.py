@@ -86,11 +86,11 @@ def topk_ws(rows, n):
     # one u32 histogram of 4096 fine and 64 coarse bins per row; rows longer
     # than 4096 add a 16-byte counter per row (from a 256-byte boundary) and,
     # per row, S slices of a 16-byte count + 1024 (key, index) pairs, S =
-    # about 296 CTAs per launch, at most 64, at most one slice per 8192 entries
+    # about 296 CTAs per launch, at most 64, at most one slice per 4096 entries
     hist = rows * 4160 * 4
     if n <= 4096:
         return hist
-    S = max(1, min(-(-296 // rows), 64, -(-n // 8192)))
+    S = max(1, min(-(-296 // rows), 64, -(-n // 4096)))
     return -(-(hist + rows * 16) // 256) * 256 + rows * S * (16 + 1024 * 8)
 
 
@@ -98,7 +98,7 @@ def test_workspace_sizes(csa2):
     for rows, n, k in ((8, 262144, 512), (3, 100, 2048), (4096, 262144, 512), (20, 30000, 512),
                        (1, 4097, 1)):
         assert csa2.topk_workspace_bytes(rows, n, k) == topk_ws(rows, n)
-    assert topk_ws(8, 262144) == 133376 + 8 * 32 * 8208
+    assert topk_ws(8, 262144) == 133376 + 8 * 37 * 8208
     a = csa2.IndexArgs(q_dtype=csa2.BF16, k_dtype=csa2.E4M3, B=8, q_per_seq=1, hi=64, di=128,
                        n=262144)
     assert csa2.lib.csa2_index_score_workspace_bytes(ctypes.byref(a)) == 8 * 64 * 128 + 8 * 64 * 4
