@@ -64,7 +64,7 @@ __device__ __forceinline__ int64_t row_nvalid(const int32_t* n_valid, int64_t ro
 __global__ void __launch_bounds__(kHistThreads)
     topk_hist_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
                      const int32_t* __restrict__ n_valid, uint32_t* __restrict__ hist1,
-                     int64_t chunk, const uint32_t* __restrict__ within) {
+                     int64_t chunk, const uint32_t* __restrict__ within, int vec, int exclusive) {
   __shared__ uint32_t h[kBins];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < kBins; i += kHistThreads) h[i] = 0;
@@ -79,25 +79,62 @@ __global__ void __launch_bounds__(kHistThreads)
   // their next 12 bits
   const bool sub = within != nullptr;
   const uint32_t t1 = sub ? within[row] >> 20 : 0u;
+  auto count = [&](float x) {
+    const uint32_t key = score_key(x);
+    if (!sub || (key >> 20) == t1) atomicAdd(&h[sub ? (key >> 8) & (kBins - 1) : key >> 20], 1u);
+  };
   constexpr int U = 4;
-  for (int64_t base = j0 + warp * 32; base < j1; base += (int64_t)kHistThreads * U) {
-    float x[U];
+  if (vec) {
+    // 16 scores per thread in flight: float4 u of thread t at b + 2048 u + 4 t
+    // (chunks start on multiples of 4 scores)
+    for (int64_t b = j0; b < j1; b += (int64_t)kHistThreads * 4 * U) {
+      float4 x[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t j = base + u * kHistThreads + lane;
-      x[u] = j < j1 ? s[j] : 0.f;
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = b + (int64_t)u * kHistThreads * 4 + 4 * tid;
+        if (j + 3 < j1) {
+          x[u] = __ldcs(reinterpret_cast<const float4*>(s + j));
+        } else {
+          x[u].x = j < j1 ? s[j] : 0.f;
+          x[u].y = j + 1 < j1 ? s[j + 1] : 0.f;
+          x[u].z = j + 2 < j1 ? s[j + 2] : 0.f;
+          x[u].w = j + 3 < j1 ? s[j + 3] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = b + (int64_t)u * kHistThreads * 4 + 4 * tid;
+        if (j < j1) count(x[u].x);
+        if (j + 1 < j1) count(x[u].y);
+        if (j + 2 < j1) count(x[u].z);
+        if (j + 3 < j1) count(x[u].w);
+      }
     }
+  } else {
+    for (int64_t base = j0 + warp * 32; base < j1; base += (int64_t)kHistThreads * U) {
+      float x[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t j = base + u * kHistThreads + lane;
-      const uint32_t key = score_key(x[u]);
-      if (j < j1 && (!sub || (key >> 20) == t1))
-        atomicAdd(&h[sub ? (key >> 8) & (kBins - 1) : key >> 20], 1u);
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = base + u * kHistThreads + lane;
+        x[u] = j < j1 ? s[j] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (base + u * kHistThreads + lane < j1) count(x[u]);
     }
   }
   __syncthreads();
   pdl_trigger();
   uint32_t* hrow = hist1 + row * kTopkHistStride;
+  if (exclusive) {  // the row's only CTA: its counts are the row's (stores, no atomics)
+    for (int i = tid; i < kBins; i += kHistThreads) hrow[i] = h[i];
+    if (tid < kTopkCoarse) {
+      uint32_t v = 0;
+      for (int i = 0; i < kBins / kTopkCoarse; ++i) v += h[tid * (kBins / kTopkCoarse) + i];
+      hrow[kBins + tid] = v;
+    }
+    return;
+  }
   for (int i = tid; i < kBins; i += kHistThreads)
     if (h[i]) atomicAdd(&hrow[i], h[i]);
   if (tid < kTopkCoarse) {  // coarse bin t: fine bins 64t .. 64t + 63
@@ -1112,11 +1149,15 @@ csa2_status launch_topk_hist(const float* scores, int64_t rows, int64_t n, int64
   // enough CTAs to cover the GPU about twice
   const int64_t want = (2 * (int64_t)sm_count() + rows - 1) / rows;
   const int64_t max_chunks = (n + 4095) / 4096;
-  const int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(want, max_chunks));
-  const int64_t chunk = (n + chunks - 1) / chunks;
+  int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(want, max_chunks));
+  const int64_t chunk = ((n + chunks - 1) / chunks + 3) / 4 * 4;  // multiples of 4 scores
+  chunks = (n + chunk - 1) / chunk;
+  const int vec = (ld % 4 == 0 && (reinterpret_cast<uintptr_t>(scores) % 16) == 0) ? 1 : 0;
+  // with one CTA per row the row's histogram is that CTA's counts, written
+  // outright (every caller hands over rows at zero, which several CTAs add to)
   return launch_kernel(topk_hist_kernel, dim3((unsigned)chunks, (unsigned)rows),
                        dim3(kHistThreads), 0, s, 1, scores, n, ld, n_valid, hist1, chunk,
-                       within);
+                       within, vec, chunks == 1 ? 1 : 0);
 }
 
 csa2_status launch_topk(const float* scores, int64_t rows, int64_t n, int64_t ld,
