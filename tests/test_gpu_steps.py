@@ -351,7 +351,9 @@ def test_project_fp4_exact_small_integers(csa2, orc, rows):
 @pytest.mark.parametrize("rows,n,k,levels", [
     (3, 5000, 64, 0), (4, 4096, 512, 0), (5, 3000, 512, 40), (2, 262144, 512, 0),
     (2, 70000, 512, 3), (6, 1000, 2048, 0), (1, 100, 512, 0), (9, 1, 1, 0),
-    (4, 8000, 512, 1), (300, 5000, 256, 0), (37, 40000, 512, 0), (3, 262144, 2048, 5)])
+    (4, 8000, 512, 1), (300, 5000, 256, 0), (37, 40000, 512, 0), (3, 262144, 2048, 5),
+    # rows of an odd length: the histogram pass and the slices take scalar loads
+    (3, 30001, 512, 0), (1, 4097, 64, 2)])
 def test_topk_bit_exact(csa2, orc, rows, n, k, levels):
     s = synth.scores_with_ties(rows, n, seed=60 + rows + k, levels=levels)
     g = torch.Generator().manual_seed(61)
