@@ -225,6 +225,11 @@ struct TcParams {
   uint32_t* cand_cnt;
   uint2* cand;
   int64_t cand_cap;
+  // slots a (warp, query) stream reserves at a time: 32 (one atomic per 32
+  // candidates), or 0: exactly the slots a tile's takes need.  A stream's
+  // unused reserved slots count against cand_cap, so the host takes 0 when a
+  // query's tiles are spread over so many CTAs that they could add up
+  uint32_t cand_chunk;
   // decode Full layers (one query per sequence): the step's new rows, which
   // the epilogue warps quantise first; the producer waits for them (nrdy)
   // before loading a tile that holds one (nr.kv null: none)
@@ -816,12 +821,13 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
             if (cnt <= avail) {
               cpos[qq] += cnt;
             } else {
+              const uint32_t rsv = max(cnt - avail, p.cand_chunk);
               uint32_t nb = 0;
-              if (lane == 0) nb = atomicAdd(&p.cand_cnt[g * QG + q0 + qq], 32u);
+              if (lane == 0) nb = atomicAdd(&p.cand_cnt[g * QG + q0 + qq], rsv);
               nb = __shfl_sync(0xffffffffu, nb, 0);
               if (r >= avail) pos = nb + (r - avail);
               cpos[qq] = nb + (cnt - avail);
-              cend[qq] = nb + 32;
+              cend[qq] = nb + rsv;
             }
             if (take && pos < (uint64_t)p.cand_cap)
               p.cand[(g * QG + q0 + qq) * p.cand_cap + pos] = make_uint2(key, (uint32_t)j);
@@ -973,6 +979,16 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   if (nr) p.nr = *nr;
   const int64_t total = p.groups * p.ktiles;
   if (total == 0) return CSA2_OK;
+  {
+    // a query's (warp, query) streams: STREAMS tile streams x 4 warps in each CTA
+    // whose range meets the query's group; each may leave up to 31 reserved
+    // slots unused.  Chunks of 32 while that waste stays within a quarter of
+    // the buffer, else exact reservations.
+    const int64_t per_cta = (total + tc_grid<QG>(total) - 1) / tc_grid<QG>(total);
+    const int64_t ctas_per_group = (p.ktiles + per_cta - 1) / per_cta + 1;
+    const int64_t waste = (int64_t)C::STREAMS * 4 * ctas_per_group * 31;
+    p.cand_chunk = waste * 4 <= p.cand_cap ? 32u : 0u;
+  }
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [] {
     return cudaFuncSetAttribute(idx_score_tc_kernel<QG>,

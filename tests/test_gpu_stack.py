@@ -132,6 +132,18 @@ def test_stack_prefill_scaled(csa2, orc):
     compare(orc, W)
 
 
+@pytest.mark.parametrize("N", [1000, 20000])
+def test_stack_prefill_reindex_scaled(csa2, orc, N):
+    # a prefill chunk through Full, Reindex and Reuse layers: the Reindex
+    # layer's indexer walks its tiles from the end over the Full layer's keys;
+    # long rows (20000) select from the scoring pass's candidates
+    wl = synth.scaled(synth.PREFILL, q_per_seq=16, N=N, pos0=4 * N - 16,
+                      modes=(synth.FULL, synth.REINDEX, synth.REUSE))
+    W = build(wl, 6)
+    run_stack(W)
+    compare(orc, W)
+
+
 def test_stack_1m_pool_scaled(csa2, orc):
     # the Hierarchical Sparse Indexer: Reindex layers score only the top-1024
     # pool of their Full layer (pool < N, so the restriction matters)
