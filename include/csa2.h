@@ -281,7 +281,8 @@ csa2_status csa2_index_score_pool(const csa2_index_args* args, const int32_t* po
  * For every query q, every visible entry j whose score s[q, j] (exactly as
  * csa2_index_score computes it) has an order-preserving key >= theta[q] is
  * appended to q's candidates as cand[q * cand_cap + i] = key | (uint64_t)j
- * << 32.  The kernel reserves slots 32 at a time through cand_cnt[q]; a
+ * << 32.  The kernel reserves slots through cand_cnt[q], 32 at a time (or,
+ * when a query's tiles spread over many CTAs, exactly as needed); a
  * reserved slot it does not fill holds 0xFFFFFFFF00000000 (entry
  * 0xFFFFFFFF).  Candidates are in no particular order.  The key of a float
  * x with bits u is u ^ 0x80000000 for x >= 0 (-0 counts as +0) and ~u
