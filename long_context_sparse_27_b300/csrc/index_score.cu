@@ -979,12 +979,13 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
   if (nr) p.nr = *nr;
   const int64_t total = p.groups * p.ktiles;
   if (total == 0) return CSA2_OK;
+  const int grid = (int)tc_grid<QG>(total);
   {
     // a query's (warp, query) streams: STREAMS tile streams x 4 warps in each CTA
     // whose range meets the query's group; each may leave up to 31 reserved
     // slots unused.  Chunks of 32 while that waste stays within a quarter of
     // the buffer, else exact reservations.
-    const int64_t per_cta = (total + tc_grid<QG>(total) - 1) / tc_grid<QG>(total);
+    const int64_t per_cta = (total + grid - 1) / grid;
     const int64_t ctas_per_group = (p.ktiles + per_cta - 1) / per_cta + 1;
     const int64_t waste = (int64_t)C::STREAMS * 4 * ctas_per_group * 31;
     p.cand_chunk = waste * 4 <= p.cand_cap ? 32u : 0u;
@@ -995,7 +996,6 @@ csa2_status launch_tc(const csa2_index_args& a, const uint8_t* q8, const float* 
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   });
   if (e != cudaSuccess) return cuda_fail(e);
-  const int grid = (int)tc_grid<QG>(total);
   return launch_kernel(idx_score_tc_kernel<QG>, dim3(grid), dim3(C::THREADS),
                        (size_t)C::SMEM_ALLOC, s, 1, kmap, qmap, p);
 }
