@@ -273,6 +273,17 @@ __device__ __forceinline__ float relu_scaled(float x) {
   return y;
 }
 
+// The smallest score x with score_key(x) >= t: keys order the scores as
+// floats do (-0 counts as +0), so score_key(x) >= t exactly when x >= the
+// returned value.  Keys below every negative float's (t = 0 among them) give
+// -inf: every score; keys above every positive float's give a NaN, which no
+// score reaches.
+__device__ __forceinline__ float key_floor(uint32_t t) {
+  if (t & 0x80000000u) return __uint_as_float(t ^ 0x80000000u);  // +0 .. +inf, or NaN above
+  const float x = __uint_as_float(~t);                             // -0 .. -inf, or NaN below
+  return x != x ? -INFINITY : x;
+}
+
 template <int QG>
 __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     idx_score_tc_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -640,6 +651,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
     // n_valid), the candidate threshold and the score row
     int32_t vis[C::QPW];
     uint32_t th[C::QPW];
+    float thf[C::QPW];  // the smallest score whose key reaches th (see key_floor)
     float* srow[C::QPW];
     // REG_W: this thread's 16 head weights per query, times kReluScale
     // unless the head sums are scaled instead (relu_post = kReluScale)
@@ -722,6 +734,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
           const int64_t qi = g * QG + q0 + i;
           vis[i] = p.n_valid ? min(n32, p.n_valid[qi]) : n32;
           th[i] = p.cand ? p.theta[qi] : 0u;
+          thf[i] = key_floor(th[i]);
           srow[i] = p.scores ? p.scores + qi * p.scores_ld : nullptr;
         }
         g_prev = g;
@@ -811,8 +824,7 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
         const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
         for (int qq = 0; qq < C::QPW; ++qq) {
-          const uint32_t key = score_key(sc[qq]);
-          const bool take = j < vis[qq] && key >= th[qq];
+          const bool take = j < vis[qq] && sc[qq] >= thf[qq];
           const uint32_t mask = __ballot_sync(0xffffffffu, take);
           if (mask) {
             const uint32_t cnt = __popc(mask), r = __popc(mask & lt);
@@ -830,7 +842,8 @@ __global__ void __launch_bounds__(TcCfg<QG>::THREADS, TcCfg<QG>::CTAS_PER_SM)
               cend[qq] = nb + rsv;
             }
             if (take && pos < (uint64_t)p.cand_cap)
-              p.cand[(g * QG + q0 + qq) * p.cand_cap + pos] = make_uint2(key, (uint32_t)j);
+              p.cand[(g * QG + q0 + qq) * p.cand_cap + pos] =
+                  make_uint2(score_key(sc[qq]), (uint32_t)j);
           }
         }
       } else if (j < n32 || p.tile_stride > 1) {
